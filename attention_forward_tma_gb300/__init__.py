@@ -1,0 +1,214 @@
+"""Attention forward for NVIDIA GB300 (sm_103a): Python binding of libfa_gb300.so.
+
+This module only marshals arguments: it checks dtypes and shapes of torch
+tensors, passes their device pointers and the current CUDA stream to the C ABI
+declared in ``include/fa.h`` and ``include/fa_selftest.h``, and turns status
+codes into exceptions. Every step of the computation runs in the library's CUDA
+kernels; there is no CPU path. If the library cannot be built or loaded, or no
+sm_103 GPU is present, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import threading
+
+from . import _build
+
+__all__ = ["fa_fwd", "fa_fwd_varlen", "FaError", "set_option", "last_device_status", "library",
+           "selftest_mma_tile", "selftest_exp2", "selftest_wait_timeout", "varlen_schedule",
+           "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
+           "FA_ERR_NO_DEVICE"]
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_NO_DEVICE = range(6)
+_OPTIONS = {"tau": 1, "wait_timeout_ns": 2, "persistent": 3, "exp2_emulation": 4}
+
+_vp, _ci, _cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+_SIGNATURES = {
+    "fa_fwd": [_vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _cf, _ci, _vp],
+    "fa_fwd_varlen": [_vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _vp],
+    "fa_error_string": [_ci],
+    "fa_last_device_status": [_vp, ctypes.POINTER(ctypes.c_ulonglong)],
+    "fa_set_option": [_ci, ctypes.c_double],
+    "fa_version": [],
+    "fa_selftest_mma_tile": [_vp, _vp, _vp, _vp, _vp, _vp, _ci, _vp],
+    "fa_selftest_exp2": [_vp, _vp, _ci, _ci, _vp],
+    "fa_selftest_wait_timeout": [ctypes.c_ulonglong, _vp],
+    "fa_varlen_schedule": [_vp, _ci, _ci, _ci, _ci, _vp, _vp, _vp],
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {error_string(status)} (status {status})")
+
+
+def library() -> ctypes.CDLL:
+    """Load (building first if needed) the in-tree libfa_gb300.so."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            lib = ctypes.CDLL(path)
+            for name, args in _SIGNATURES.items():
+                f = getattr(lib, name)
+                f.argtypes = args
+                f.restype = ctypes.c_char_p if name == "fa_error_string" else ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def error_string(status: int) -> str:
+    return library().fa_error_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != FA_OK:
+        raise FaError(status, what)
+
+
+def set_option(name: str, value: float) -> None:
+    """Process-wide knobs: tau, wait_timeout_ns, persistent (-1/0/1), exp2_emulation (0..8)."""
+    _check(library().fa_set_option(_OPTIONS[name], float(value)), f"set_option({name})")
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream, device):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, name, dtype, ndim=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions")
+
+
+def fa_fwd(q, k, v, *, scale: float | None = None, causal: bool = False, out=None, lse=None,
+           return_lse: bool = True, stream=None):
+    """Attention forward on bf16 [B, N, H, d] tensors. Returns (o, lse) or o.
+
+    lse is fp32 [B, H, N] (natural log of the scaled logits' sum of exponentials).
+    scale defaults to 1/sqrt(d)."""
+    torch = _torch()
+    _need(q, "q", torch.bfloat16, 4)
+    B, N, H, d = q.shape
+    for name, t in (("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, 4)
+        if tuple(t.shape) != (B, N, H, d):
+            raise ValueError(f"{name} must have shape {(B, N, H, d)}")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", torch.bfloat16, 4)
+        if tuple(out.shape) != (B, N, H, d):
+            raise ValueError("out has the wrong shape")
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    elif lse is not None:
+        _need(lse, "lse", torch.float32, 3)
+        if tuple(lse.shape) != (B, H, N):
+            raise ValueError("lse must have shape (B, H, N)")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = library().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                          lse.data_ptr() if lse is not None else None, B, H, N, d, scale, int(bool(causal)),
+                          _stream_handle(stream, q.device))
+    _check(st, "fa_fwd")
+    return (out, lse) if lse is not None else out
+
+
+def fa_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, *, scale: float | None = None, causal: bool = False,
+                  out=None, lse=None, return_lse: bool = True, stream=None):
+    """Packed variable-length attention forward on bf16 [T, H, d]; cu_seqlens int32 [S+1] on the device.
+    Returns (o, lse) or o; lse is fp32 [H, T]."""
+    torch = _torch()
+    _need(q, "q", torch.bfloat16, 3)
+    T, H, d = q.shape
+    for name, t in (("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, 3)
+        if tuple(t.shape) != (T, H, d):
+            raise ValueError(f"{name} must have shape {(T, H, d)}")
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", torch.bfloat16, 3)
+    if lse is None and return_lse:
+        lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    elif lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = library().fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                 lse.data_ptr() if lse is not None else None, cu_seqlens.data_ptr(),
+                                 cu_seqlens.numel() - 1, T, int(max_seqlen), H, d, scale, int(bool(causal)),
+                                 _stream_handle(stream, q.device))
+    _check(st, "fa_fwd_varlen")
+    return (out, lse) if lse is not None else out
+
+
+def last_device_status(stream=None):
+    """Synchronize the stream; return (status, raw word) of the device-side status, and clear it."""
+    torch = _torch()
+    word = ctypes.c_ulonglong(0)
+    st = library().fa_last_device_status(_stream_handle(stream, torch.device("cuda")), ctypes.byref(word))
+    return st, word.value
+
+
+def selftest_mma_tile(q, k, v, p, stream=None):
+    """One tile through the MMA plumbing: returns (S = Q K^T fp32 [128,128], O = P V fp32 [128,d])."""
+    torch = _torch()
+    for name, t in (("q", q), ("k", k), ("v", v), ("p", p)):
+        _need(t, name, torch.bfloat16, 2)
+    d = q.shape[1]
+    s = torch.empty((128, 128), dtype=torch.float32, device=q.device)
+    o = torch.empty((128, d), dtype=torch.float32, device=q.device)
+    _check(library().fa_selftest_mma_tile(q.data_ptr(), k.data_ptr(), v.data_ptr(), p.data_ptr(), s.data_ptr(),
+                                          o.data_ptr(), d, _stream_handle(stream, q.device)),
+           "fa_selftest_mma_tile")
+    return s, o
+
+
+def selftest_exp2(x, use_poly: bool, stream=None):
+    torch = _torch()
+    _need(x, "x", torch.float32)
+    y = torch.empty_like(x)
+    _check(library().fa_selftest_exp2(x.data_ptr(), y.data_ptr(), x.numel(), int(bool(use_poly)),
+                                      _stream_handle(stream, x.device)), "fa_selftest_exp2")
+    return y
+
+
+def selftest_wait_timeout(timeout_ns: int, stream=None) -> int:
+    """Returns the status the never-completing wait recorded (FA_ERR_TIMEOUT when correct)."""
+    torch = _torch()
+    return library().fa_selftest_wait_timeout(int(timeout_ns), _stream_handle(stream, torch.device("cuda")))
+
+
+def varlen_schedule(cu_seqlens, H: int, causal: bool, capacity: int, stream=None):
+    """The longest-first varlen tile list: (tasks int32 [count, 4] of (seq, head, m_block, cost), count)."""
+    torch = _torch()
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    tasks = torch.full((max(capacity, 1), 4), -1, dtype=torch.int32, device=cu_seqlens.device)
+    count = torch.zeros(1, dtype=torch.int32, device=cu_seqlens.device)
+    _check(library().fa_varlen_schedule(cu_seqlens.data_ptr(), cu_seqlens.numel() - 1, H, int(bool(causal)),
+                                        capacity, tasks.data_ptr(), count.data_ptr(),
+                                        _stream_handle(stream, cu_seqlens.device)), "fa_varlen_schedule")
+    n = int(count.item())
+    return tasks[:n], n

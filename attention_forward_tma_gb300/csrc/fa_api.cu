@@ -1,0 +1,360 @@
+// fa_api.cu -- host side of the C ABI declared in include/fa.h: argument checks,
+// TMA tensor maps, the varlen longest-first schedule kernel, kernel launches and
+// the device status word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_fwd.cuh"
+#include "fa_selftest.h"
+
+namespace {
+
+// ------------------------------------------------------------------ options
+struct Options {
+  float tau = 8.0f;
+  unsigned long long timeout_ns = 2000000000ull;
+  int persistent = -1;   // -1: default per mask type
+  int emu_groups = 0;
+};
+Options g_opt;
+
+// ------------------------------------------------------------------ driver entry point
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// ------------------------------------------------------------------ per-device facts
+struct DevInfo {
+  bool init = false;
+  bool supported = false;
+  int sm_count = 0;
+  long long l2_bytes = 0;
+  bool attr_done[2][2] = {{false, false}, {false, false}};
+  int attr_status[2][2] = {{0, 0}, {0, 0}};
+};
+constexpr int kMaxDevices = 64;
+DevInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+int device_info(DevInfo** out) {
+  int dev = 0;
+  int n = 0;
+  if (cudaGetDeviceCount(&n) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return FA_ERR_NO_DEVICE;
+  }
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.init) {
+    int major = 0, minor = 0, sms = 0, l2 = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+      return FA_ERR_CUDA;
+    d.supported = (major == 10 && minor == 3);
+    d.sm_count = sms;
+    d.l2_bytes = l2;
+    d.init = true;
+  }
+  *out = &d;
+  return d.supported ? FA_OK : FA_ERR_UNSUPPORTED;
+}
+
+// 3-D map over a [tokens, H, d] bf16 tensor: x = d (contiguous), y = token, z = head.
+// Box = 64 x 128 x 1 (one 128-byte slab of 128 rows), 128-byte swizzle, OOB rows read 0.
+int make_map(CUtensorMap* m, const void* base, long long tokens, int H, int d) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return FA_ERR_CUDA;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)tokens, (cuuint64_t)H};
+  const cuuint64_t strides[2] = {(cuuint64_t)H * d * 2, (cuuint64_t)d * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)fa::kBlockM, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+template <int D, bool C>
+int launch_fwd(DevInfo* dev, const fa::FwdParams& p, int grid, cudaStream_t stream) {
+  using L = fa::Layout<D>;
+  auto kern = fa::fa_fwd_kernel<D, C>;
+  const int di = D == 128 ? 1 : 0, ci = C ? 1 : 0;
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!dev->attr_done[di][ci]) {
+      int st = FA_OK;
+      cudaFuncAttributes fa_attr;
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc) != cudaSuccess ||
+          cudaFuncGetAttributes(&fa_attr, kern) != cudaSuccess)
+        st = FA_ERR_CUDA;
+      // the warpgroup register split (192/192/48/80) needs exactly 128 registers
+      // per thread at launch
+      else if (fa_attr.numRegs != 128)
+        st = FA_ERR_UNSUPPORTED;
+      dev->attr_status[di][ci] = st;
+      dev->attr_done[di][ci] = true;
+    }
+    if (dev->attr_status[di][ci] != FA_OK) return dev->attr_status[di][ci];
+  }
+  kern<<<grid, fa::kThreads, L::kSmemAlloc, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int dispatch(DevInfo* dev, const fa::FwdParams& p, int d, bool causal, int grid, cudaStream_t s) {
+  if (d == 128) return causal ? launch_fwd<128, true>(dev, p, grid, s) : launch_fwd<128, false>(dev, p, grid, s);
+  return causal ? launch_fwd<64, true>(dev, p, grid, s) : launch_fwd<64, false>(dev, p, grid, s);
+}
+
+void fill_common(fa::FwdParams& p, float scale) {
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.tau = g_opt.tau;
+  p.emu_groups = g_opt.emu_groups;
+  p.timeout_ns = g_opt.timeout_ns;
+}
+
+bool use_persistent(bool causal) { return g_opt.persistent < 0 ? !causal : g_opt.persistent != 0; }
+
+}  // namespace
+
+// ------------------------------------------------------------------ varlen schedule kernel
+namespace fa {
+constexpr int kSchedBuckets = 4096;
+
+// One CTA: enumerate the (sequence, 256-row block) work tiles, bucket them by
+// their number of K/V blocks, and write them longest first, each followed by
+// all H heads ("FlashAttention-4（下）" (argus lesson 7), section "6. LPT 调度":
+// sort work tiles by their cost, write a virtual -> actual map).
+__global__ void __launch_bounds__(1024) fa_varlen_schedule_kernel(const int* cu, int num_seqs, int H, int causal,
+                                                                  int capacity, int4* tasks, int* count) {
+  __shared__ int hist[kSchedBuckets];
+  __shared__ int total_pairs;
+  for (int i = threadIdx.x; i < kSchedBuckets; i += blockDim.x) hist[i] = 0;
+  if (threadIdx.x == 0) total_pairs = 0;
+  __syncthreads();
+  auto cost_of = [&](int L, int m) {
+    const int kmax = causal ? min(m * kTaskRows + kTaskRows, L) : L;
+    return min((kmax + kBlockN - 1) / kBlockN, kSchedBuckets - 1);
+  };
+  for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
+    const int L = max(cu[s + 1] - cu[s], 0);
+    const int nm = (L + kTaskRows - 1) / kTaskRows;
+    for (int m = 0; m < nm; ++m) atomicAdd(&hist[cost_of(L, m)], 1);
+    atomicAdd(&total_pairs, nm);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // exclusive scan from the most expensive bucket down: hist[c] becomes the
+    // first slot of bucket c
+    int run = 0;
+    for (int c = kSchedBuckets - 1; c >= 0; --c) {
+      const int n = hist[c];
+      hist[c] = run;
+      run += n;
+    }
+    const long long n_tasks = (long long)total_pairs * H;
+    *count = (int)(n_tasks < capacity ? n_tasks : capacity);
+  }
+  __syncthreads();
+  for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
+    const int L = max(cu[s + 1] - cu[s], 0);
+    const int nm = (L + kTaskRows - 1) / kTaskRows;
+    for (int m = 0; m < nm; ++m) {
+      const int c = cost_of(L, m);
+      const int slot = atomicAdd(&hist[c], 1);
+      for (int h = 0; h < H; ++h) {
+        const long long ti = (long long)slot * H + h;
+        if (ti < capacity) tasks[ti] = make_int4(s, h, m, c);
+      }
+    }
+  }
+}
+}  // namespace fa
+
+// ------------------------------------------------------------------ C ABI
+extern "C" {
+
+int fa_version(void) { return 100; }
+
+const char* fa_error_string(int status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported (head dim, device or kernel resources)";
+    case FA_ERR_CUDA: return "CUDA runtime/driver error";
+    case FA_ERR_TIMEOUT: return "device-side wait timed out";
+    case FA_ERR_NO_DEVICE: return "no CUDA device";
+    default: return "unknown status";
+  }
+}
+
+int fa_set_option(int option, double value) {
+  switch (option) {
+    case FA_OPT_TAU:
+      if (!(value >= 0.0)) return FA_ERR_INVALID_ARG;  // also rejects NaN
+      g_opt.tau = value > 3.0e38 ? INFINITY : (float)value;
+      return FA_OK;
+    case FA_OPT_WAIT_TIMEOUT_NS:
+      if (!(value >= 1000.0 && value <= 6.0e11)) return FA_ERR_INVALID_ARG;
+      g_opt.timeout_ns = (unsigned long long)value;
+      return FA_OK;
+    case FA_OPT_PERSISTENT:
+      if (value != -1.0 && value != 0.0 && value != 1.0) return FA_ERR_INVALID_ARG;
+      g_opt.persistent = (int)value;
+      return FA_OK;
+    case FA_OPT_EXP2_EMULATION:
+      if (!(value >= 0.0 && value <= 8.0) || value != std::floor(value)) return FA_ERR_INVALID_ARG;
+      g_opt.emu_groups = (int)value;
+      return FA_OK;
+    default:
+      return FA_ERR_INVALID_ARG;
+  }
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+           float scale, int causal, void* stream) {
+  if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || (lse && !aligned(lse, 4)))
+    return FA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long tokens = (long long)B * N;
+  if (tokens * H > INT_MAX) return FA_ERR_INVALID_ARG;  // 32-bit row and LSE indexing
+  DevInfo* dev = nullptr;
+  int st = device_info(&dev);
+  if (st != FA_OK) return st;
+
+  fa::FwdParams p;
+  std::memset(&p, 0, sizeof p);
+  if ((st = make_map(&p.tm_q, q, tokens, H, d)) != FA_OK || (st = make_map(&p.tm_k, k, tokens, H, d)) != FA_OK ||
+      (st = make_map(&p.tm_v, v, tokens, H, d)) != FA_OK)
+    return st;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.B = B; p.H = H; p.N = N;
+  p.total_tokens = (int)tokens;
+  p.num_m = (N + fa::kTaskRows - 1) / fa::kTaskRows;
+  const long long ntask = (long long)B * H * p.num_m;
+  if (ntask > INT_MAX) return FA_ERR_INVALID_ARG;
+  p.num_tasks = (int)ntask;
+  const long long kv_bytes = 4LL * N * d;                       // K + V of one (b, h)
+  long long group = (dev->l2_bytes / 2) / (kv_bytes > 0 ? kv_bytes : 1);
+  if (group < 1) group = 1;
+  if (group > (long long)B * H) group = (long long)B * H;
+  p.lpt_group = (int)group;
+  p.varlen = 0;
+  fill_common(p, scale);
+  int grid = p.num_tasks;
+  if (use_persistent(causal != 0) && grid > dev->sm_count) grid = dev->sm_count;
+  return dispatch(dev, p, d, causal != 0, grid, static_cast<cudaStream_t>(stream));
+}
+
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
+                  int num_seqs, int total_tokens, int max_seqlen, int H, int d, float scale, int causal,
+                  void* stream) {
+  if (!q || !k || !v || !o || !cu_seqlens) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || (lse && !aligned(lse, 4)) ||
+      !aligned(cu_seqlens, 4))
+    return FA_ERR_INVALID_ARG;
+  if (num_seqs <= 0 || total_tokens <= 0 || max_seqlen <= 0 || H <= 0) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if ((long long)total_tokens * H > INT_MAX) return FA_ERR_INVALID_ARG;
+  const long long cap = (long long)H * ((total_tokens + fa::kTaskRows - 1) / fa::kTaskRows + num_seqs);
+  if (cap > INT_MAX) return FA_ERR_INVALID_ARG;
+  DevInfo* dev = nullptr;
+  int st = device_info(&dev);
+  if (st != FA_OK) return st;
+
+  fa::FwdParams p;
+  std::memset(&p, 0, sizeof p);
+  if ((st = make_map(&p.tm_q, q, total_tokens, H, d)) != FA_OK ||
+      (st = make_map(&p.tm_k, k, total_tokens, H, d)) != FA_OK ||
+      (st = make_map(&p.tm_v, v, total_tokens, H, d)) != FA_OK)
+    return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  const size_t ws_bytes = (size_t)cap * sizeof(int4) + 16;
+  if (cudaMallocAsync(&ws, ws_bytes, s) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  int4* tasks = static_cast<int4*>(ws);
+  int* count = reinterpret_cast<int*>(static_cast<char*>(ws) + (size_t)cap * sizeof(int4));
+  fa::fa_varlen_schedule_kernel<<<1, 1024, 0, s>>>(cu_seqlens, num_seqs, H, causal, (int)cap, tasks, count);
+  if (cudaGetLastError() != cudaSuccess) {
+    cudaFreeAsync(ws, s);
+    return FA_ERR_CUDA;
+  }
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.cu_seqlens = cu_seqlens;
+  p.tasks = tasks;
+  p.task_count = count;
+  p.H = H;
+  p.total_tokens = total_tokens;
+  p.num_tasks = (int)cap;
+  p.varlen = 1;
+  fill_common(p, scale);
+  int grid = (int)cap;
+  if (use_persistent(causal != 0) && grid > dev->sm_count) grid = dev->sm_count;
+  st = dispatch(dev, p, d, causal != 0, grid, s);
+  if (cudaFreeAsync(ws, s) != cudaSuccess && st == FA_OK) st = FA_ERR_CUDA;
+  return st;
+}
+
+int fa_varlen_schedule(const int* cu_seqlens, int num_seqs, int H, int causal, int capacity, void* tasks,
+                       int* count, void* stream) {
+  if (!cu_seqlens || !tasks || !count || num_seqs <= 0 || H <= 0 || capacity < 0 || (causal != 0 && causal != 1))
+    return FA_ERR_INVALID_ARG;
+  if (!aligned(tasks, 16) || !aligned(count, 4) || !aligned(cu_seqlens, 4)) return FA_ERR_INVALID_ARG;
+  DevInfo* dev = nullptr;
+  int st = device_info(&dev);
+  if (st != FA_OK) return st;
+  fa::fa_varlen_schedule_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(
+      cu_seqlens, num_seqs, H, causal, capacity, static_cast<int4*>(tasks), count);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_last_device_status(void* stream, unsigned long long* detail) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  unsigned long long word = 0;
+  if (cudaMemcpyFromSymbol(&word, fa::g_fa_status, sizeof word) != cudaSuccess) return FA_ERR_CUDA;
+  if (detail) *detail = word;
+  if (word != 0) {
+    const unsigned long long zero = 0;
+    if (cudaMemcpyToSymbol(fa::g_fa_status, &zero, sizeof zero) != cudaSuccess) return FA_ERR_CUDA;
+    return (int)(word & 0xff);
+  }
+  return FA_OK;
+}
+
+}  // extern "C"

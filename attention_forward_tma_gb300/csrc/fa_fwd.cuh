@@ -1,0 +1,616 @@
+// fa_fwd.cuh -- the attention forward kernel for GB300 (sm_103a).
+//
+// One CTA of 512 threads works on tasks of 256 query rows of one (sequence,
+// head): two Q tiles of 128 rows that share every streamed K/V block. The four
+// warpgroups have fixed roles ("Flash Attention 4", section "Warp 角色与 Scope"):
+//
+//   WG0, WG1  softmax of Q tile 0 / Q tile 1 (thread r owns row r of its tile)
+//   WG2       correction (rescale of O in tensor memory) and the epilogue
+//             (O / row_sum -> bf16 -> global memory)
+//   WG3       warp 12: tcgen05 MMA issue (one thread); warp 13: TMA loads (one
+//             thread); warps 14-15 idle
+//
+// Per K/V block j (visited from the last block down to block 0, section
+// "Pipeline 时间线"):   S_t = Q_t K_j^T  (tcgen05, smem x smem -> TMEM fp32)
+//                      P_t = exp2(S_t * scale_log2 - ref_t * scale_log2)  (registers,
+//                            written back to TMEM as bf16 over the upper half of S_t)
+//                      O_t (+)= P_t V_j  (tcgen05, A from TMEM, B from smem)
+// with the delayed-rescale rule of section "算法结构": the reference ref_t of a
+// row moves to the new maximum only when that maximum exceeds it by more than
+// tau (base-2 exponent units); then O and row_sum are multiplied by
+// acc_scale = 2^delta. The rescale of O is done by WG2, which skips a warp's 32
+// rows when none of them needs it (section "重缩放与结果写回").
+//
+// Tensor memory (512 columns x 128 lanes x 32 bit, section "TMEM 布局与复用"):
+//   S_0 [0,128)   S_1 [128,256)   O_0 [256,256+D)   O_1 [384,384+D)
+//   P_t = bf16 pairs over columns [64,128) of S_t.
+//
+// Shared memory: Q tiles (2), a ring of K/V stages (K and V blocks alternate
+// through the same ring), mbarriers, and a 2x128 float mailbox that carries
+// acc_scale (and finally row_sum) from the softmax warpgroups to WG2.
+//
+// Every wait is bounded: after FwdParams::timeout_ns a waiter records
+// FA_ERR_TIMEOUT in g_fa_status, raises a CTA-wide abort flag and unwinds;
+// the CTA then drains its own TMA copies and MMAs (again with a bound), frees
+// its tensor memory and exits.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+
+namespace fa {
+
+constexpr int kBlockM = 128;          // rows of one Q tile
+constexpr int kBlockN = 128;          // keys of one K/V block
+constexpr int kTaskRows = 2 * kBlockM;
+constexpr int kThreads = 512;
+constexpr uint32_t kTmemCols = 512;
+
+// Device status word: 0 = OK; else code | role << 8 | barrier << 16 | block << 32.
+static __device__ unsigned long long g_fa_status;  // one copy per translation unit
+
+enum : uint32_t { kRoleMma = 1, kRoleLoad = 2, kRoleSoftmax0 = 3, kRoleSoftmax1 = 4, kRoleCorr = 5,
+                  kRoleDrain = 6 };
+constexpr unsigned long long kStatusTimeout = 4;  // == FA_ERR_TIMEOUT
+
+struct FwdParams {
+  CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps of [tokens, H, d]: x = d, y = token, z = head
+  __nv_bfloat16* o;              // [tokens, H, d]
+  float* lse;                    // fixed length [B, H, N]; varlen [H, tokens]; may be null
+  const int* cu_seqlens;         // varlen only
+  const int4* tasks;             // varlen only: {seq, head, m_block, cost}, longest first
+  const int* task_count;         // varlen only
+  int B, H, N;                   // fixed length: batch, heads, sequence length
+  int total_tokens;
+  int num_tasks;                 // fixed length: exact; varlen: upper bound (grid sizing)
+  int num_m;                     // fixed length: 256-row blocks per (b, h)
+  int lpt_group;                 // causal fixed length: (b, h) pairs per L2 section
+  int varlen;
+  float scale_log2;              // scale * log2(e)
+  float tau;                     // delayed-rescale threshold
+  int emu_groups;                // 16-column groups per row evaluated with the polynomial exp2
+  unsigned long long timeout_ns;
+};
+
+template <int D>
+struct Layout {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kHalves = D / 64;                   // 128-byte (64 x bf16) column slabs
+  static constexpr int kSlabBytes = kBlockM * 128;          // one slab: 128 rows x 128 bytes
+  static constexpr int kTileBytes = kHalves * kSlabBytes;   // one Q, K or V tile
+  static constexpr int kStages = D == 128 ? 3 : 6;          // K/V ring depth
+  static constexpr int kQOff = 0;
+  static constexpr int kKVOff = kQOff + 2 * kTileBytes;
+  static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+  // barrier indices
+  static constexpr int bQFull = 0, bQEmpty = 2, bKVFull = 4, bKVEmpty = 4 + kStages;
+  static constexpr int bSFull = 4 + 2 * kStages, bPO = bSFull + 2, bCorrFull = bPO + 2,
+                       bCorrEmpty = bCorrFull + 2, bOFinal = bCorrEmpty + 2, bDrain = bOFinal + 2;
+  static constexpr int kNumBars = bDrain + 1;
+  static constexpr int kMailOff = kBarOff + ((kNumBars * 8 + 127) / 128) * 128;
+  static constexpr int kMiscOff = kMailOff + 2 * kBlockM * 4;  // tmem slot, abort flag
+  static constexpr int kSmemBytes = kMiscOff + 64;
+  static constexpr int kSmemAlloc = kSmemBytes + 1024;         // slack for 1024-byte alignment
+  // tensor memory columns of S_t and O_t
+  static __device__ __forceinline__ uint32_t col_s(int t) { return (uint32_t)t * 128u; }
+  static __device__ __forceinline__ uint32_t col_o(int t) { return 256u + (uint32_t)t * 128u; }
+};
+
+// ------------------------------------------------------------------ tasks
+struct Task {
+  int h, tok0, len, m;   // head, first token of the sequence, its length, 256-row block
+  int lse_base;          // lse index of row 0 of the sequence for this head
+};
+
+__device__ __forceinline__ bool get_task(const FwdParams& p, bool causal, int idx, Task& t) {
+  if (p.varlen) {
+    if (idx >= *p.task_count) return false;
+    const int4 e = p.tasks[idx];
+    const int s0 = p.cu_seqlens[e.x], s1 = p.cu_seqlens[e.x + 1];
+    t.h = e.y; t.m = e.z; t.tok0 = s0; t.len = s1 - s0;
+    t.lse_base = t.h * p.total_tokens + s0;
+    return true;
+  }
+  if (idx >= p.num_tasks) return false;
+  int bh, m;
+  if (causal) {
+    // Longest-processing-time order: heavy m-blocks first, inside sections of
+    // lpt_group (b, h) pairs so that a section's K/V stays resident in L2
+    // ("Flash Attention 4", section "Tile 调度"; "FlashAttention-4（下）", section "6. LPT 调度").
+    const int bh_total = p.B * p.H;
+    const int per_group = p.lpt_group * p.num_m;
+    const int g = idx / per_group;
+    const int r = idx - g * per_group;
+    const int gsize = min(p.lpt_group, bh_total - g * p.lpt_group);
+    m = p.num_m - 1 - r / gsize;
+    bh = g * p.lpt_group + r % gsize;
+  } else {
+    bh = idx / p.num_m;
+    m = idx - bh * p.num_m;
+  }
+  const int b = bh / p.H;
+  t.h = bh - b * p.H; t.m = m; t.tok0 = b * p.N; t.len = p.N;
+  t.lse_base = bh * p.N;
+  return true;
+}
+
+// Number of K/V blocks a task visits: keys [0, n*128) (causal stops at the last
+// key the bottom row of the task may see; "Flash Attention 4", section "Causal Mask").
+__device__ __forceinline__ int task_blocks(const Task& t, bool causal) {
+  int kmax = t.len;
+  if (causal) kmax = min(t.m * kTaskRows + kTaskRows, t.len);
+  return (kmax + kBlockN - 1) / kBlockN;
+}
+
+// ------------------------------------------------------------------ bounded waits
+struct Waiter {
+  volatile int* abort_flag;
+  unsigned long long timeout_ns;
+  uint32_t role;
+
+  __device__ __forceinline__ bool wait(uint32_t bar_addr, uint32_t parity, uint32_t bar_id, int block) {
+    if (mbar_try_wait(bar_addr, parity)) return true;
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+      if (mbar_try_wait(bar_addr, parity)) return true;
+      if ((it & 63) == 63) {
+        if (*abort_flag) return false;
+        const uint64_t now = globaltimer();
+        if (t0 == 0) t0 = now;
+        else if (now - t0 > timeout_ns) {
+          *abort_flag = 1;
+          const unsigned long long word = kStatusTimeout | ((unsigned long long)role << 8) |
+                                          ((unsigned long long)bar_id << 16) |
+                                          ((unsigned long long)(uint32_t)block << 32);
+          atomicCAS(&g_fa_status, 0ull, word);
+          return false;
+        }
+      }
+    }
+  }
+};
+
+// ------------------------------------------------------------------ exp2 on the FMA pipe
+// 2^x = 2^floor(x) * p(x - floor(x)) with p a cubic fitted to 2^f on [0, 1) by
+// the Remez exchange algorithm (minimax relative error 1.52e-4, p(0) = 1; see
+// fit_exp2_poly.py). The integer part is added to the exponent field.
+// ("Flash Attention 4", section "算法结构": part of the exponentials run as a
+// cubic polynomial on FMA units so the hardware ex2 unit is not the only path.)
+__device__ __forceinline__ float exp2_poly(float x) {
+  x = fmaxf(x, -127.0f);
+  const float fl = floorf(x);
+  const float f = x - fl;
+  float p = fmaf(f, 0.07908560335636139f, 0.22537171840667725f);
+  p = fmaf(p, f, 0.6955426931381226f);
+  p = fmaf(p, f, 1.0f);
+  const int e = static_cast<int>(fl);
+  return __int_as_float(__float_as_int(p) + (e << 23));
+}
+
+// ------------------------------------------------------------------ MMA issue helpers
+// S = Q K^T : M = 128 rows, N = 128 keys, K = D (16 per instruction). Both
+// operands K-major with 128-byte swizzle; a K step of 16 bf16 is a 32-byte
+// advance inside a 128-byte row; D = 128 spans two 64-column slabs.
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, kBlockN, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk / 4) * Layout<D>::kSlabBytes + (kk % 4) * 32;
+    const uint64_t a = smem_desc_sw128(q_smem + off, 16, 1024);
+    const uint64_t b = smem_desc_sw128(k_smem + off, 16, 1024);
+    mma_ss(d_tmem, a, b, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+// O (+)= P V : M = 128 rows, N = D, K = 128 keys. P (bf16 pairs) from TMEM,
+// 8 columns per 16 keys. V is [keys, d] in smem = MN-major for the B operand:
+// 64-wide d slabs LBO = 16 KiB apart, 8-key groups SBO = 1 KiB apart; a K step
+// of 16 keys is a 2 KiB advance.
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, D, true);
+#pragma unroll
+  for (int kk = 0; kk < kBlockN / 16; ++kk) {
+    const uint64_t b = smem_desc_sw128(v_smem + kk * 2048, Layout<D>::kSlabBytes, 1024);
+    mma_ts(d_tmem, p_tmem + kk * 8, b, idesc, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using L = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sQ = sbase + L::kQOff;
+  const uint32_t sKV = sbase + L::kKVOff;
+  const uint32_t sBar = sbase + L::kBarOff;
+  float* mail = reinterpret_cast<float*>(smem + L::kMailOff);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  volatile int* never_abort = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 8);  // stays 0
+  auto bar = [&](int i) -> uint32_t { return sBar + 8u * (uint32_t)i; };
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  // ---- setup
+  if (tid == 0) {
+    *abort_flag = 0;
+    *never_abort = 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(L::bQFull + i), 1);
+      mbar_init(bar(L::bQEmpty + i), 1);
+      mbar_init(bar(L::bSFull + i), 1);
+      mbar_init(bar(L::bPO + i), 2 * kBlockM);      // softmax WG + correction WG
+      mbar_init(bar(L::bCorrFull + i), kBlockM);
+      mbar_init(bar(L::bCorrEmpty + i), kBlockM);
+      mbar_init(bar(L::bOFinal + i), 1);
+    }
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(bar(L::bKVFull + s), 1);
+      mbar_init(bar(L::bKVEmpty + s), 1);
+    }
+    mbar_init(bar(L::bDrain), 1);
+    fence_mbar_init();
+  }
+  if (warp == 13 && lane == 0) {
+    prefetch_tmap(&p.tm_q);
+    prefetch_tmap(&p.tm_k);
+    prefetch_tmap(&p.tm_v);
+  }
+  if (warp == 12) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int first_task = blockIdx.x;
+  const int task_stride = gridDim.x;
+
+  // Register split 192/192/48/80 per thread for WG0/WG1/WG2/WG3 (sum = 4 x 128,
+  // the launch allocation). Each setmaxnreg sits inside its role's branch so the
+  // compiler allocates that role's code with the new limit.
+  if (warp >= 12) setmaxnreg_dec<80>();
+  if (warp == 13) {
+    // ================================================================ TMA producer
+    if (lane == 0) {
+      Waiter w{abort_flag, p.timeout_ns, kRoleLoad};
+      uint32_t stage = 0, phase = 0;
+      // armed full barriers and the parity of their last arm, for the drain on abort
+      uint32_t q_armed = 0, q_par = 0, kv_armed = 0, kv_par = 0;
+      bool ok = true;
+      int it = 0;
+      auto load_tile = [&](const CUtensorMap* m, uint32_t dst, int tok, int h, uint32_t b) {
+#pragma unroll
+        for (int c = 0; c < L::kHalves; ++c) tma_load_3d(dst + c * L::kSlabBytes, m, c * 64, tok, h, b);
+      };
+      auto load_kv = [&](const CUtensorMap* m, int tok, int h, int blk) -> bool {
+        if (!w.wait(bar(L::bKVEmpty + stage), phase ^ 1, L::bKVEmpty + stage, blk)) return false;
+        mbar_arrive_expect_tx(bar(L::bKVFull + stage), L::kTileBytes);
+        load_tile(m, sKV + stage * L::kTileBytes, tok, h, bar(L::bKVFull + stage));
+        kv_armed |= 1u << stage;
+        kv_par = (kv_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == L::kStages) { stage = 0; phase ^= 1; }
+        return true;
+      };
+      auto load_q = [&](int t, int tok, int h, int blk) -> bool {
+        if (!w.wait(bar(L::bQEmpty + t), (it & 1) ^ 1, L::bQEmpty + t, blk)) return false;
+        mbar_arrive_expect_tx(bar(L::bQFull + t), L::kTileBytes);
+        load_tile(&p.tm_q, sQ + t * L::kTileBytes, tok, h, bar(L::bQFull + t));
+        q_armed |= 1u << t;
+        q_par = (q_par & ~(1u << t)) | ((uint32_t)(it & 1) << t);
+        return true;
+      };
+      Task tk;
+      for (int idx = first_task; ok && get_task(p, CAUSAL, idx, tk); idx += task_stride, ++it) {
+        const int nb = task_blocks(tk, CAUSAL);
+        const int row0 = tk.tok0 + tk.m * kTaskRows;
+        int j = nb - 1;
+        ok = load_q(0, row0, tk.h, j) && load_kv(&p.tm_k, tk.tok0 + j * kBlockN, tk.h, j) &&
+             load_q(1, row0 + kBlockM, tk.h, j) && load_kv(&p.tm_v, tk.tok0 + j * kBlockN, tk.h, j);
+        for (j = nb - 2; ok && j >= 0; --j)
+          ok = load_kv(&p.tm_k, tk.tok0 + j * kBlockN, tk.h, j) &&
+               load_kv(&p.tm_v, tk.tok0 + j * kBlockN, tk.h, j);
+      }
+      if (!ok) {
+        // drain: every armed full barrier completes once its bytes have landed
+        Waiter d{never_abort, p.timeout_ns, kRoleDrain};
+        for (int t = 0; t < 2; ++t)
+          if (q_armed & (1u << t)) d.wait(bar(L::bQFull + t), (q_par >> t) & 1, L::bQFull + t, -1);
+        for (int s = 0; s < L::kStages; ++s)
+          if (kv_armed & (1u << s)) d.wait(bar(L::bKVFull + s), (kv_par >> s) & 1, L::bKVFull + s, -1);
+      }
+    }
+  } else if (warp == 12) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      Waiter w{abort_flag, p.timeout_ns, kRoleMma};
+      uint32_t stage = 0, phase = 0;
+      uint32_t po_par = 0;  // bit t: parity of the next wait on p_o[t]
+      bool ok = true;
+      int it = 0;
+      const uint32_t S0 = tmem + L::col_s(0), S1 = tmem + L::col_s(1);
+      const uint32_t O0 = tmem + L::col_o(0), O1 = tmem + L::col_o(1);
+      const uint32_t P0 = S0 + 64, P1 = S1 + 64;
+      const uint32_t Q0 = sQ, Q1 = sQ + L::kTileBytes;
+      Task tk;
+      for (int idx = first_task; ok && get_task(p, CAUSAL, idx, tk); idx += task_stride, ++it) {
+        const int nb = task_blocks(tk, CAUSAL);
+        const uint32_t qpar = it & 1;
+        // prologue: S_0 and S_1 for the last block
+        uint32_t ks = stage;
+        ok = w.wait(bar(L::bQFull + 0), qpar, L::bQFull, nb - 1) &&
+             w.wait(bar(L::bKVFull + ks), phase, L::bKVFull + ks, nb - 1);
+        if (!ok) break;
+        if (++stage == L::kStages) { stage = 0; phase ^= 1; }
+        tc_fence_after();
+        issue_qk<D>(S0, Q0, sKV + ks * L::kTileBytes);
+        mma_commit(bar(L::bSFull + 0));
+        if (!w.wait(bar(L::bQFull + 1), qpar, L::bQFull + 1, nb - 1)) { ok = false; break; }
+        tc_fence_after();
+        issue_qk<D>(S1, Q1, sKV + ks * L::kTileBytes);
+        mma_commit(bar(L::bSFull + 1));
+        mma_commit(bar(L::bKVEmpty + ks));
+        for (int i = 0; i < nb; ++i) {
+          const int j = nb - 1 - i;
+          const bool last = (i == nb - 1);
+          const uint32_t vs = stage;
+          if (!w.wait(bar(L::bKVFull + vs), phase, L::bKVFull + vs, j)) { ok = false; break; }
+          if (++stage == L::kStages) { stage = 0; phase ^= 1; }
+          // ---- tile 0: O_0 (+)= P_0 V_j, then S_0 for block j-1
+          if (!w.wait(bar(L::bPO + 0), po_par & 1, L::bPO, j)) { ok = false; break; }
+          po_par ^= 1;
+          tc_fence_after();
+          issue_pv<D>(O0, P0, sKV + vs * L::kTileBytes, i > 0);
+          if (!last) {
+            ks = stage;
+            if (!w.wait(bar(L::bKVFull + ks), phase, L::bKVFull + ks, j - 1)) { ok = false; break; }
+            if (++stage == L::kStages) { stage = 0; phase ^= 1; }
+            tc_fence_after();
+            issue_qk<D>(S0, Q0, sKV + ks * L::kTileBytes);
+            mma_commit(bar(L::bSFull + 0));
+          } else {
+            mma_commit(bar(L::bOFinal + 0));
+            mma_commit(bar(L::bQEmpty + 0));
+          }
+          // ---- tile 1: O_1 (+)= P_1 V_j, then S_1 for block j-1
+          if (!w.wait(bar(L::bPO + 1), (po_par >> 1) & 1, L::bPO + 1, j)) { ok = false; break; }
+          po_par ^= 2;
+          tc_fence_after();
+          issue_pv<D>(O1, P1, sKV + vs * L::kTileBytes, i > 0);
+          mma_commit(bar(L::bKVEmpty + vs));
+          if (!last) {
+            issue_qk<D>(S1, Q1, sKV + ks * L::kTileBytes);
+            mma_commit(bar(L::bSFull + 1));
+            mma_commit(bar(L::bKVEmpty + ks));
+          } else {
+            mma_commit(bar(L::bOFinal + 1));
+            mma_commit(bar(L::bQEmpty + 1));
+          }
+        }
+      }
+      // all issued MMAs must finish before the tensor memory is released
+      mma_commit(bar(L::bDrain));
+      Waiter d{never_abort, p.timeout_ns, kRoleDrain};
+      d.wait(bar(L::bDrain), 0, L::bDrain, -1);
+    }
+  } else if (warp < 8) {
+    // ================================================================ softmax WG0 / WG1
+    setmaxnreg_inc<192>();
+    const int t = warp >> 2;                 // Q tile of this warpgroup
+    const int r = tid & 127;                 // row within the tile == TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + L::col_s(t);
+    const uint32_t tP = tS + 64;
+    Waiter w{abort_flag, p.timeout_ns, t == 0 ? kRoleSoftmax0 : kRoleSoftmax1};
+    const float sl2 = p.scale_log2;
+    uint32_t s_par = 0, ce_par = 0;
+    bool ok = true;
+    Task tk;
+    for (int idx = first_task; ok && get_task(p, CAUSAL, idx, tk); idx += task_stride) {
+      const int nb = task_blocks(tk, CAUSAL);
+      const int row = tk.m * kTaskRows + t * kBlockM + r;       // row within the sequence
+      const int tile_row0 = tk.m * kTaskRows + t * kBlockM;
+      const int row_limit = CAUSAL ? min(row + 1, tk.len) : tk.len;  // keys [0, row_limit) visible
+      float row_max = -INFINITY, row_sum = 0.f;
+      for (int i = 0; i < nb; ++i) {
+        const int j = nb - 1 - i;
+        if (!w.wait(bar(L::bSFull + t), s_par, L::bSFull + t, j)) { ok = false; break; }
+        s_par ^= 1;
+        tc_fence_after();
+        float s[kBlockN];
+        {
+          uint32_t u[kBlockN];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&u[c * 32]));
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < kBlockN; ++e) s[e] = __uint_as_float(u[e]);
+        }
+        const int k0 = j * kBlockN;
+        const bool need_mask = (k0 + kBlockN > tk.len) || (CAUSAL && k0 + kBlockN - 1 > tile_row0);
+        if (need_mask) {
+          const int lim = row_limit - k0;
+#pragma unroll
+          for (int c = 0; c < kBlockN; ++c)
+            if (c >= lim) s[c] = -INFINITY;
+        }
+        // block maximum (tree)
+        float m4[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float a = s[q * 32];
+#pragma unroll
+          for (int e = 1; e < 32; ++e) a = fmaxf(a, s[q * 32 + e]);
+          m4[q] = a;
+        }
+        const float blk_max = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        // delayed-rescale rule
+        float ref, acc;
+        if (i == 0) {
+          ref = blk_max;
+          acc = 1.f;
+        } else {
+          const float cand = fmaxf(row_max, blk_max);
+          const float cand_safe = cand == -INFINITY ? 0.f : cand;
+          const float delta = (row_max - cand_safe) * sl2;
+          // a row with no valid score yet (reference -inf) always adopts the candidate
+          if (delta >= -p.tau && row_max != -INFINITY) {
+            ref = row_max;
+            acc = 1.f;
+          } else {
+            ref = cand;
+            acc = ex2_approx(delta);
+          }
+        }
+        row_max = ref;
+        const float ref_safe = ref == -INFINITY ? 0.f : ref;
+        const float nbias = -ref_safe * sl2;
+        // P = exp2(S * sl2 - ref * sl2); the first emu_groups 16-column groups
+        // use the polynomial (only in blocks without masked columns)
+        const int emu = need_mask ? 0 : p.emu_groups;
+        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[kBlockN / 2];
+#pragma unroll
+        for (int g = 0; g < kBlockN / 16; ++g) {
+          if (g < emu) {
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+              const int c = g * 16 + e;
+              const float p0 = exp2_poly(fmaf(s[c], sl2, nbias));
+              const float p1 = exp2_poly(fmaf(s[c + 1], sl2, nbias));
+              sum4[(c >> 1) & 3] += p0 + p1;
+              pk[c >> 1] = pack_bf16x2(p0, p1);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+              const int c = g * 16 + e;
+              const float p0 = ex2_approx(fmaf(s[c], sl2, nbias));
+              const float p1 = ex2_approx(fmaf(s[c + 1], sl2, nbias));
+              sum4[(c >> 1) & 3] += p0 + p1;
+              pk[c >> 1] = pack_bf16x2(p0, p1);
+            }
+          }
+        }
+        // P over the upper half of S_t (S has been read completely above)
+        tmem_st32(tP, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(tP + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+        tmem_wait_st();
+        if (i > 0) {
+          if (!w.wait(bar(L::bCorrEmpty + t), ce_par ^ 1, L::bCorrEmpty + t, j)) { ok = false; break; }
+          ce_par ^= 1;
+          mail[t * kBlockM + r] = acc;
+          mbar_arrive(bar(L::bCorrFull + t));
+        }
+        tc_fence_before();
+        mbar_arrive(bar(L::bPO + t));
+        row_sum = row_sum * acc + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+      }
+      if (!ok) break;
+      // final statistics to WG2 (row_sum), LSE straight to global memory
+      if (!w.wait(bar(L::bCorrEmpty + t), ce_par ^ 1, L::bCorrEmpty + t, -1)) { ok = false; break; }
+      ce_par ^= 1;
+      mail[t * kBlockM + r] = row_sum;
+      mbar_arrive(bar(L::bCorrFull + t));
+      if (p.lse != nullptr && row < tk.len && tk.tok0 + row < p.total_tokens) {
+        const float ref_safe = row_max == -INFINITY ? 0.f : row_max;
+        const float lse = row_sum > 0.f ? (lg2_approx(row_sum) + ref_safe * sl2) * 0.69314718055994531f
+                                        : -INFINITY;
+        p.lse[tk.lse_base + row] = lse;
+      }
+    }
+  } else if (warp < 12) {
+    // ================================================================ correction + epilogue (WG2)
+    setmaxnreg_dec<48>();
+    const int r = tid & 127;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    Waiter w{abort_flag, p.timeout_ns, kRoleCorr};
+    uint32_t cf_par = 0, of_par = 0;  // bit t: parity of the next wait on corr_full[t] / o_final[t]
+    bool ok = true;
+    Task tk;
+    for (int idx = first_task; ok && get_task(p, CAUSAL, idx, tk); idx += task_stride) {
+      const int nb = task_blocks(tk, CAUSAL);
+      // first block of this task: O_t is free (previous epilogue finished)
+      mbar_arrive(bar(L::bPO + 0));
+      mbar_arrive(bar(L::bPO + 1));
+      for (int i = 1; ok && i < nb; ++i) {
+        const int j = nb - 1 - i;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!w.wait(bar(L::bCorrFull + t), (cf_par >> t) & 1, L::bCorrFull + t, j)) { ok = false; break; }
+          cf_par ^= 1u << t;
+          const float a = mail[t * kBlockM + r];
+          mbar_arrive(bar(L::bCorrEmpty + t));
+          if (__any_sync(0xffffffffu, a < 1.f)) {
+            tc_fence_after();
+            const uint32_t tO = tmem + lane_base + L::col_o(t);
+#pragma unroll
+            for (int c = 0; c < D / 16; ++c) {
+              uint32_t u[16];
+              tmem_ld16(tO + c * 16, u);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * a);
+              tmem_st16(tO + c * 16, u);
+            }
+            tmem_wait_st();
+          }
+          tc_fence_before();
+          mbar_arrive(bar(L::bPO + t));
+        }
+      }
+      if (!ok) break;
+      // epilogue: O_t / row_sum -> bf16 -> global
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (!w.wait(bar(L::bCorrFull + t), (cf_par >> t) & 1, L::bCorrFull + t, -1)) { ok = false; break; }
+        cf_par ^= 1u << t;
+        const float l = mail[t * kBlockM + r];
+        mbar_arrive(bar(L::bCorrEmpty + t));
+        if (!w.wait(bar(L::bOFinal + t), (of_par >> t) & 1, L::bOFinal + t, -1)) { ok = false; break; }
+        of_par ^= 1u << t;
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const int row = tk.m * kTaskRows + t * kBlockM + r;
+        const bool valid = row < tk.len && tk.tok0 + row < p.total_tokens;
+        __nv_bfloat16* orow = p.o + ((size_t)(tk.tok0 + row) * p.H + tk.h) * D;
+        const uint32_t tO = tmem + lane_base + L::col_o(t);
+#pragma unroll
+        for (int c = 0; c < D / 16; ++c) {
+          uint32_t u[16];
+          tmem_ld16(tO + c * 16, u);
+          tmem_wait_ld();
+          uint32_t pk[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(u[2 * e]) * inv, __uint_as_float(u[2 * e + 1]) * inv);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 16);
+            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
+        }
+        tc_fence_before();
+      }
+    }
+  }
+
+  // ---- teardown: every role has returned; release tensor memory
+  __syncwarp();  // lanes that skipped a single-thread role wait for lane 0
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 12) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace fa

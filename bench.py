@@ -1,0 +1,421 @@
+"""Benchmark: attention forward TFLOP/s (bf16, d=128) and fraction of the GB300 dense bf16 peak.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step is one call of the library's attention forward over one batch of the
+workload (inputs already resident in HBM): the scheduler, TMA loads, both
+tcgen05 MMAs, the softmax with delayed rescaling, the correction and the
+epilogue all run inside that call. The default workload is the causal
+B=4, H=16, N=4096, d=128 problem (Q, K, V iid N(0,1) in bf16, scale 1/sqrt(128)).
+FLOPs per step follow the usual convention 4*B*H*N^2*d, halved for causal.
+
+With N > 1 (torchrun), every rank runs its own replica of the workload on its
+own GPU (independent problems, no collective on the data path; weak scaling);
+a barrier brackets the timed region and the slowest rank's time is used.
+
+``--impl reference`` times the fp64 CPU oracle (the test oracle under
+oracle/, as it stands) on a bounded sample of the same workload and prints the
+same JSON line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import fa_inputs  # noqa: E402
+
+METRIC = "attention fwd TFLOPS (bf16, d=128) and % of GB300 dense BF16 tensor peak"
+DEFAULT_WORKLOAD = "c3_b4h16n4096d128_causal"
+FALLBACK_PEAK_TFLOPS = 1900.0
+FLOP_PER_CLK_PER_SM = 8192  # dense bf16 tcgen05 rate per SM per clock
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(fa_inputs.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    a = ap.parse_args()
+    if a.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    return a
+
+
+# --------------------------------------------------------------------------- distributed plumbing
+class Dist:
+    def __init__(self, n):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if os.environ.get("FA_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        dev = "cuda" if self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# --------------------------------------------------------------------------- helpers
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["bf16_tflops"]), float(j.get("bf16_tflops_sustained", j["bf16_tflops"])), \
+            float(j.get("hbm_gbs", 0.0)), "measured"
+    except Exception:
+        return FALLBACK_PEAK_TFLOPS, 1700.0, 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "attention_forward_tma_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", f"fa_fwd_{workload}_dram.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha256_16") != kernel_source_hash():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def workload_flops(w, x=None):
+    if w.varlen:
+        return fa_inputs.varlen_flops(x["lengths"], w.H, w.d, w.causal)
+    return fa_inputs.attention_flops(w.B, w.H, w.N, w.d, w.causal)
+
+
+def oracle_sample(w, x, budget_rows: int, seed: int):
+    """A bounded row sample of the workload for the CPU oracle, with its exact FLOPs."""
+    rng = np.random.default_rng(seed)
+    if w.varlen:
+        cu = x["cu_seqlens"]
+        T = int(cu[-1])
+        toks = rng.integers(0, T, budget_rows)
+        heads = rng.integers(0, w.H, budget_rows)
+        rows = np.stack([heads, toks], 1).astype(np.int64)
+        seq = np.searchsorted(cu, toks, side="right") - 1
+        pos = toks - cu[seq]
+        L = cu[seq + 1] - cu[seq]
+        nkeys = np.minimum(pos + 1, L) if w.causal else L
+    else:
+        b = rng.integers(0, w.B, budget_rows)
+        h = rng.integers(0, w.H, budget_rows)
+        i = rng.integers(0, w.N, budget_rows)
+        rows = np.stack([b, h, i], 1).astype(np.int64)
+        nkeys = np.minimum(i + 1, w.N) if w.causal else np.full(budget_rows, w.N)
+    flops = float((4.0 * w.d * nkeys).sum())
+    return rows, flops
+
+
+def run_oracle_rows(w, x, rows, threads):
+    import oracle
+    if w.varlen:
+        return oracle.attention_rows_varlen(x["q"], x["k"], x["v"], x["cu_seqlens"], rows, w.scale, w.causal,
+                                            threads=threads)
+    return oracle.attention_rows(x["q"], x["k"], x["v"], rows, w.scale, w.causal, threads=threads)
+
+
+def cpu_baseline(w, x, target_s: float = 10.0):
+    """The oracle (as it stands) on a bounded row sample; TFLOP/s of the work it did."""
+    import oracle
+    threads = oracle.default_threads()
+    rows, flops = oracle_sample(w, x, 256, seed=1)
+    t0 = time.perf_counter()
+    run_oracle_rows(w, x, rows, threads)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    n = int(min(max(256, 256 * target_s / dt), 1 << 20))
+    rows, flops = oracle_sample(w, x, n, seed=2)
+    t0 = time.perf_counter()
+    run_oracle_rows(w, x, rows, threads)
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} random query rows of {w.name} (fp64 two-pass softmax per row, "
+                      f"{flops / 1e9:.1f} GFLOP by the 4*d*keys count), {dt:.1f} s"}
+
+
+# --------------------------------------------------------------------------- the reference arm
+def run_reference(a, dist):
+    w = fa_inputs.WORKLOADS[a.workload]
+    if dist.rank != 0:
+        return
+    import oracle
+    x = fa_inputs.make_workload(w)
+    threads = oracle.default_threads()
+    # size one step so that warmup + steps take about a minute in total
+    rows, flops = oracle_sample(w, x, 64, seed=0)
+    t0 = time.perf_counter()
+    run_oracle_rows(w, x, rows, threads)
+    per_row = max(time.perf_counter() - t0, 1e-6) / 64
+    total_steps = a.steps + a.warmup
+    n_rows = int(max(1, min(4096, 60.0 / total_steps / per_row)))
+    samples = [oracle_sample(w, x, n_rows, seed=100 + i) for i in range(total_steps)]
+    for i in range(a.warmup):
+        run_oracle_rows(w, x, samples[i][0], threads)
+    flops = sum(s[1] for s in samples[a.warmup:])
+    t0 = time.perf_counter()
+    for i in range(a.warmup, total_steps):
+        run_oracle_rows(w, x, samples[i][0], threads)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    cfg = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal}
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "impl": "reference", "n_gpus": a.gpus,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": dt / a.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{n_rows} random query rows of {w.name} per step"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- our arm
+def run_ours(a, dist):
+    import torch
+    import attention_forward_tma_gb300 as fa
+
+    torch.cuda.set_device(dist.local)
+    dev = torch.device("cuda", dist.local)
+    w = fa_inputs.WORKLOADS[a.workload]
+    x = fa_inputs.make_workload(w)
+    flops = workload_flops(w, x)
+
+    def to_dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q, k, v = to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"])
+    o = torch.empty_like(q)
+    if w.varlen:
+        cu = torch.from_numpy(x["cu_seqlens"]).to(dev)
+        maxL = int(x["lengths"].max())
+        lse = torch.empty((w.H, q.shape[0]), dtype=torch.float32, device=dev)
+
+        def step(s=None):
+            fa.fa_fwd_varlen(q, k, v, cu, maxL, scale=w.scale, causal=w.causal, out=o, lse=lse, stream=s)
+        launches_per_step = 2
+    else:
+        lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+
+        def step(s=None):
+            fa.fa_fwd(q, k, v, scale=w.scale, causal=w.causal, out=o, lse=lse, stream=s)
+        launches_per_step = 1
+
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(a.warmup):
+        step(stream)
+    torch.cuda.synchronize(dev)
+    st, word = fa.last_device_status(stream)
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device status {st} ({word:#x}) after warm-up")
+
+    # timed region: K steps, per-launch CUDA events on the launching stream
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dist.local) as clocks:
+        t0 = time.perf_counter()
+        for i in range(a.steps):
+            ev[i][0].record(stream)
+            step(stream)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+    dist.barrier()
+    st, word = fa.last_device_status(stream)
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device status {st} ({word:#x}) in the timed region")
+    per_launch_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    region_ms = ev[0][0].elapsed_time(ev[-1][1])
+    region_s = dist.max(region_ms / 1e3)
+    value = dist.world * flops * a.steps / region_s / 1e12
+    avg_launch_s = sum(per_launch_ms) / len(per_launch_ms) / 1e3
+
+    # end to end through the public API with host buffers (pinned), copies inside the region
+    hq, hk, hv = (t.to("cpu").pin_memory() for t in (q, k, v))
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    n_e2e = max(1, min(a.e2e_steps, a.steps))
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        if w.varlen:
+            fa.fa_fwd_varlen(dq, dk, dv, cu, maxL, scale=w.scale, causal=w.causal, out=o, lse=lse)
+        else:
+            fa.fa_fwd(dq, dk, dv, scale=w.scale, causal=w.causal, out=o, lse=lse)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_s = dist.max(e0.elapsed_time(e1) / 1e3)
+    h2d = 3 * q.numel() * 2 + (0 if not w.varlen else 0)
+    d2h = o.numel() * 2 + lse.numel() * 4
+
+    if dist.rank != 0:
+        return
+    peak, peak_sust, hbm, peak_src = measured_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    clk = clocks.summary()
+    max_mhz = clk["sm_max_mhz"] or 2070.0
+    theoretical = props.multi_processor_count * FLOP_PER_CLK_PER_SM * max_mhz * 1e6 / 1e12
+    achieved = flops / avg_launch_s / 1e12
+    traffic = profiled_traffic(w.name)
+    cfg = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+           "scale": w.scale, "seed": w.seed, "l2": "inputs larger than L2 (Q+K+V+O = %.0f MiB), no flush"
+           % ((4 * q.numel() * 2) / 2 ** 20),
+           "flops_per_step": flops}
+    if w.varlen:
+        cfg["lengths"] = [int(L) for L in x["lengths"]]
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": dist.world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": region_s / a.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+        "pct_of_measured_peak": 100.0 * value / dist.world / peak,
+        "pct_of_theoretical_peak": 100.0 * value / dist.world / theoretical,
+        "theoretical_peak_tflops": theoretical,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)" if peak_src == "measured"
+                     else "fallback 1.9 PFLOP/s bf16 burst",
+                     "kernel": "fa_fwd_kernel", "avg_launch_ms": avg_launch_s * 1e3,
+                     "min_launch_ms": min(per_launch_ms), "wall_s": wall},
+        "e2e": {"value": dist.world * flops * n_e2e / e2e_s / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e},
+        "gpu_launches": launches_per_step * a.steps,
+        "clocks": clk,
+    }
+    if not a.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, x)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    a = parse()
+    dist = Dist(a.gpus)
+    try:
+        if a.impl == "reference":
+            run_reference(a, dist)
+        else:
+            run_ours(a, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,121 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) attention forward library
+ *         (libfa_gb300.so, built from attention_forward_tma_gb300/csrc).
+ *
+ * The library computes, for every batch b, head h and query row i,
+ *
+ *     O_i   = sum_j softmax_j(scale * q_i . k_j) * v_j
+ *     LSE_i = ln sum_j exp(scale * q_i . k_j)
+ *
+ * over the keys j the mask allows, streaming K/V blocks through shared memory
+ * and keeping the score tile, the weight tile and the output accumulator in
+ * tensor memory, so the score matrix never reaches global memory.
+ *
+ * Sources: "Flash Attention 4" (mlc.ai, Modern GPU Programming for MLSys),
+ * sections "概览" (overview: O = softmax(QK^T/sqrt(d))V computed block by
+ * block with per-row online-softmax state), "算法结构" (the update rule with
+ * delayed rescaling at threshold 8), "重缩放与结果写回" (LSE = ln(row_sum) +
+ * reference * scale, -inf for rows without a valid key) and "Causal Mask"
+ * (bottom-right alignment). The explicit scale argument follows
+ * "FlashAttention：一次前向计算" (qingsen), section "先看 attention 最后要得到什么",
+ * which writes softmax(s * S) with s passed in rather than fixed.
+ *
+ * Conventions for every entry point below:
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    never frees them and keeps no reference after the call returns.
+ *  - bf16 tensors are row-major with the head dimension d innermost and must be
+ *    16-byte aligned (TMA). d must be 64 or 128.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Work is
+ *    enqueued asynchronously; argument errors are reported synchronously by the
+ *    return value and enqueue nothing.
+ *  - Nothing is printed and nothing is thrown across the ABI.
+ *  - A device-side wait that exceeds its time limit makes the kernel give up
+ *    cleanly (no trap, no hang) and records FA_ERR_TIMEOUT; read it with
+ *    fa_last_device_status().
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, bad scale, bad cu_seqlens */
+  FA_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, device is not sm_103, kernel resources */
+  FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed (launch, tensor map, ...) */
+  FA_ERR_TIMEOUT = 4,      /* a device-side wait gave up (reported by fa_last_device_status) */
+  FA_ERR_NO_DEVICE = 5     /* no CUDA device visible */
+} fa_status;
+
+/*
+ * Fixed-length attention forward.
+ *   q, k, v : bf16 [B, N, H, d]      (device, read only)
+ *   o       : bf16 [B, N, H, d]      (device, written; rounded to nearest even)
+ *   lse     : fp32 [B, H, N] or NULL (device, written: natural-log LSE of the
+ *                                     scaled logits; -inf for a row with no key)
+ *   B, H, N : >= 1;  d in {64, 128};  scale finite and > 0 (e.g. 1/sqrt(d))
+ *   causal  : 0 = full attention; 1 = query i sees keys j <= i (bottom-right
+ *             alignment, which is the usual lower-triangular mask since N_q = N_kv)
+ * Returns FA_OK or an error code; the call is asynchronous on `stream`.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int N, int d, float scale, int causal, void* stream);
+
+/*
+ * Variable-length (packed) attention forward: sequence s owns the rows
+ * [cu_seqlens[s], cu_seqlens[s+1]) of q, k, v and o; each sequence attends only
+ * to itself (self-attention, causal mask aligned per sequence).
+ *   q, k, v, o  : bf16 [total_tokens, H, d]  (device)
+ *   lse         : fp32 [H, total_tokens] or NULL (device)
+ *   cu_seqlens  : int32 [num_seqs + 1] (device), cu_seqlens[0] = 0,
+ *                 non-decreasing, cu_seqlens[num_seqs] = total_tokens,
+ *                 every length <= max_seqlen (zero-length sequences allowed)
+ *   num_seqs >= 1, total_tokens >= 1, max_seqlen >= 1
+ * Work tiles are ordered longest-first by a small schedule kernel launched on
+ * the same stream ("FlashAttention-4（下）" (argus lesson 7), section "6. LPT 调度":
+ * a pre-kernel sorts work tiles by their cost). Its tile list lives in a
+ * temporary device buffer taken from the stream-ordered allocator
+ * (cudaMallocAsync / cudaFreeAsync on `stream`).
+ * The contents of cu_seqlens are trusted (they are on the device): lengths
+ * above max_seqlen or a total other than total_tokens are not detected.
+ */
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                  const int* cu_seqlens, int num_seqs, int total_tokens, int max_seqlen,
+                  int H, int d, float scale, int causal, void* stream);
+
+/* Text for a status code (static storage; never NULL). */
+const char* fa_error_string(int status);
+
+/*
+ * Synchronizes `stream`, then returns and clears the device-side status word of
+ * the current device: FA_OK, or FA_ERR_TIMEOUT if a kernel of this library gave
+ * up on a wait since the last call (FA_ERR_CUDA if the synchronization failed).
+ * If `detail` is not NULL it receives the raw word (role, barrier, block).
+ */
+int fa_last_device_status(void* stream, unsigned long long* detail);
+
+/*
+ * Process-wide tuning knobs (not thread-safe; meant for tests and benchmarks).
+ *   FA_OPT_TAU             : rescale threshold tau in base-2 exponent units (default 8)
+ *   FA_OPT_WAIT_TIMEOUT_NS : device wait limit in nanoseconds (default 2e9)
+ *   FA_OPT_PERSISTENT      : 1 = persistent CTAs (one per SM, static task stride),
+ *                            0 = one CTA per task (default: 1 for non-causal, 0 for causal)
+ *                            -1 = restore the default
+ *   FA_OPT_EXP2_EMULATION  : number of 16-element groups per 128-wide row (0..8)
+ *                            whose exp2 is evaluated with the FMA polynomial instead
+ *                            of the hardware ex2 unit (default 0)
+ * Returns FA_OK or FA_ERR_INVALID_ARG.
+ */
+enum { FA_OPT_TAU = 1, FA_OPT_WAIT_TIMEOUT_NS = 2, FA_OPT_PERSISTENT = 3, FA_OPT_EXP2_EMULATION = 4 };
+int fa_set_option(int option, double value);
+
+/* Library version, as major*10000 + minor*100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

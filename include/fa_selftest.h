@@ -1,0 +1,50 @@
+/*
+ * fa_selftest.h -- diagnostic entry points of libfa_gb300.so.
+ *
+ * These calls exercise single pieces of the attention kernel on the GPU so a
+ * test can check each against a plain host computation: the tcgen05 MMA
+ * plumbing on one tile, the exponential paths, the bounded waits, and the
+ * varlen longest-first schedule. They are not needed to run attention.
+ * Conventions as in fa.h: device pointers owned by the caller, `stream` is a
+ * cudaStream_t, return value is an fa_status code.
+ */
+#ifndef FA_GB300_SELFTEST_H
+#define FA_GB300_SELFTEST_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * One tile through the kernel's own TMA maps, shared-memory descriptors and
+ * tcgen05 instructions:
+ *   s_out = Q K^T          (fp32 [128, 128])    q, k : bf16 [128, d]
+ *   o_out = P V            (fp32 [128, d])      p : bf16 [128, 128], v : bf16 [128, d]
+ * d in {64, 128}. Synchronizes the stream before returning.
+ */
+int fa_selftest_mma_tile(const void* q, const void* k, const void* v, const void* p,
+                         float* s_out, float* o_out, int d, void* stream);
+
+/* y[i] = 2^x[i] with the hardware ex2 unit (use_poly = 0) or with the FMA
+ * polynomial used for part of the softmax exponentials (use_poly = 1).
+ * x, y: fp32 [n] device. Asynchronous. */
+int fa_selftest_exp2(const float* x, float* y, int n, int use_poly, void* stream);
+
+/* Launches a kernel whose only mbarrier wait can never complete, with the given
+ * wait limit; the wait must give up without trapping or hanging. Synchronizes
+ * the stream and returns the recorded status: FA_ERR_TIMEOUT is the expected
+ * (correct) outcome, FA_OK would mean the wait did not time out. */
+int fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream);
+
+/* The varlen longest-first tile schedule that fa_fwd_varlen computes, written
+ * to caller buffers: tasks = int32 [capacity, 4] of {sequence, head, m_block,
+ * cost in K/V blocks}, sorted by non-increasing cost; *count = number written.
+ * cu_seqlens: device int32 [num_seqs + 1]. Asynchronous. */
+int fa_varlen_schedule(const int* cu_seqlens, int num_seqs, int H, int causal, int capacity,
+                       void* tasks, int* count, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_SELFTEST_H */

@@ -1,0 +1,111 @@
+"""The C ABI without a GPU: the library builds, loads, exports every declared
+symbol, and rejects bad arguments before touching a device."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import attention_forward_tma_gb300 as fa
+from attention_forward_tma_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for h in ("fa.h", "fa_selftest.h"):
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(fa_\w+)\s*\(", text, flags=re.M))
+    return names
+
+
+def test_headers_declare_the_boundary():
+    names = declared_functions()
+    assert {"fa_fwd", "fa_fwd_varlen", "fa_error_string", "fa_last_device_status"} <= names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(_build.build())
+    for name in sorted(declared_functions()):
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_binding_signatures_cover_the_headers():
+    assert declared_functions() == set(fa._SIGNATURES)
+
+
+def test_error_strings_and_version():
+    lib = fa.library()
+    for code in range(6):
+        assert fa.error_string(code)
+    assert fa.error_string(99) == "unknown status"
+    assert lib.fa_version() >= 100
+
+
+NULL = None
+
+
+def fwd(**kw):
+    args = dict(q=16, k=16, v=16, o=16, lse=NULL, B=1, H=1, N=128, d=128, scale=0.125, causal=0, stream=NULL)
+    args.update(kw)
+    return fa.library().fa_fwd(args["q"], args["k"], args["v"], args["o"], args["lse"], args["B"], args["H"],
+                               args["N"], args["d"], args["scale"], args["causal"], args["stream"])
+
+
+@pytest.mark.parametrize("kw", [dict(q=NULL), dict(k=NULL), dict(v=NULL), dict(o=NULL), dict(q=8),
+                                dict(o=24), dict(lse=2), dict(B=0), dict(H=-1), dict(N=0),
+                                dict(scale=0.0), dict(scale=-1.0), dict(scale=math.inf), dict(scale=math.nan),
+                                dict(causal=2), dict(B=1 << 16, N=1 << 16)])
+def test_fwd_rejects_invalid_arguments(kw):
+    assert fwd(**kw) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("d", [0, 32, 96, 256])
+def test_fwd_rejects_unsupported_head_dim(d):
+    assert fwd(d=d) == fa.FA_ERR_UNSUPPORTED
+
+
+def varlen(**kw):
+    args = dict(q=16, k=16, v=16, o=16, lse=NULL, cu=16, S=2, T=256, maxL=200, H=2, d=64, scale=0.125,
+                causal=1, stream=NULL)
+    args.update(kw)
+    return fa.library().fa_fwd_varlen(args["q"], args["k"], args["v"], args["o"], args["lse"], args["cu"],
+                                      args["S"], args["T"], args["maxL"], args["H"], args["d"], args["scale"],
+                                      args["causal"], args["stream"])
+
+
+@pytest.mark.parametrize("kw", [dict(cu=NULL), dict(cu=2), dict(q=NULL), dict(S=0), dict(T=0), dict(maxL=0),
+                                dict(H=0), dict(scale=0.0), dict(causal=-1), dict(T=1 << 30, H=8)])
+def test_varlen_rejects_invalid_arguments(kw):
+    assert varlen(**kw) == fa.FA_ERR_INVALID_ARG
+
+
+def test_varlen_rejects_unsupported_head_dim():
+    assert varlen(d=80) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_valid_arguments_without_gpu_report_no_device():
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert fwd() == fa.FA_ERR_NO_DEVICE
+    assert varlen() == fa.FA_ERR_NO_DEVICE
+
+
+@pytest.mark.parametrize("opt,val,ok", [(1, 8.0, True), (1, 0.0, True), (1, 1e30, True), (1, -1.0, False),
+                                        (1, math.nan, False), (2, 1e9, True), (2, 10.0, False),
+                                        (3, 1, True), (3, 0, True), (3, -1, True), (3, 2, False),
+                                        (4, 0, True), (4, 8, True), (4, 9, False), (4, 2.5, False),
+                                        (99, 1, False)])
+def test_set_option_validation(opt, val, ok):
+    lib = fa.library()
+    st = lib.fa_set_option(opt, val)
+    assert (st == fa.FA_OK) == ok
+    # restore defaults
+    lib.fa_set_option(1, 8.0)
+    lib.fa_set_option(2, 2e9)
+    lib.fa_set_option(3, -1)
+    lib.fa_set_option(4, 0)
