@@ -186,11 +186,12 @@ def selftest_mma_tile(q, k, v, p, stream=None):
     return s, o
 
 
-def selftest_exp2(x, use_poly: bool, stream=None):
+def selftest_exp2(x, use_poly: int, stream=None):
+    """2^x on the device: use_poly 0 = hardware ex2, 1 = FMA polynomial, 2 = its packed-pair form."""
     torch = _torch()
     _need(x, "x", torch.float32)
     y = torch.empty_like(x)
-    _check(library().fa_selftest_exp2(x.data_ptr(), y.data_ptr(), x.numel(), int(bool(use_poly)),
+    _check(library().fa_selftest_exp2(x.data_ptr(), y.data_ptr(), x.numel(), int(use_poly),
                                       _stream_handle(stream, x.device)), "fa_selftest_exp2")
     return y
 

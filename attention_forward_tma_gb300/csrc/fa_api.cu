@@ -50,8 +50,8 @@ struct DevInfo {
   bool supported = false;
   int sm_count = 0;
   long long l2_bytes = 0;
-  bool attr_done[2][2] = {{false, false}, {false, false}};
-  int attr_status[2][2] = {{0, 0}, {0, 0}};
+  bool attr_done[2][2][2] = {};
+  int attr_status[2][2][2] = {};
 };
 constexpr int kMaxDevices = 64;
 DevInfo g_dev[kMaxDevices];
@@ -100,14 +100,14 @@ int make_map(CUtensorMap* m, const void* base, long long tokens, int H, int d) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-template <int D, bool C>
+template <int D, bool C, bool E>
 int launch_fwd(DevInfo* dev, const fa::FwdParams& p, int grid, cudaStream_t stream) {
   using L = fa::Layout<D>;
-  auto kern = fa::fa_fwd_kernel<D, C>;
-  const int di = D == 128 ? 1 : 0, ci = C ? 1 : 0;
+  auto kern = fa::fa_fwd_kernel<D, C, E>;
+  const int di = D == 128 ? 1 : 0, ci = C ? 1 : 0, ei = E ? 1 : 0;
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (!dev->attr_done[di][ci]) {
+    if (!dev->attr_done[di][ci][ei]) {
       int st = FA_OK;
       cudaFuncAttributes fa_attr;
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc) != cudaSuccess ||
@@ -117,18 +117,23 @@ int launch_fwd(DevInfo* dev, const fa::FwdParams& p, int grid, cudaStream_t stre
       // per thread at launch
       else if (fa_attr.numRegs != 128)
         st = FA_ERR_UNSUPPORTED;
-      dev->attr_status[di][ci] = st;
-      dev->attr_done[di][ci] = true;
+      dev->attr_status[di][ci][ei] = st;
+      dev->attr_done[di][ci][ei] = true;
     }
-    if (dev->attr_status[di][ci] != FA_OK) return dev->attr_status[di][ci];
+    if (dev->attr_status[di][ci][ei] != FA_OK) return dev->attr_status[di][ci][ei];
   }
   kern<<<grid, fa::kThreads, L::kSmemAlloc, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+template <int D, bool C>
+int dispatch_emu(DevInfo* dev, const fa::FwdParams& p, int grid, cudaStream_t s) {
+  return p.emu_groups > 0 ? launch_fwd<D, C, true>(dev, p, grid, s) : launch_fwd<D, C, false>(dev, p, grid, s);
+}
+
 int dispatch(DevInfo* dev, const fa::FwdParams& p, int d, bool causal, int grid, cudaStream_t s) {
-  if (d == 128) return causal ? launch_fwd<128, true>(dev, p, grid, s) : launch_fwd<128, false>(dev, p, grid, s);
-  return causal ? launch_fwd<64, true>(dev, p, grid, s) : launch_fwd<64, false>(dev, p, grid, s);
+  if (d == 128) return causal ? dispatch_emu<128, true>(dev, p, grid, s) : dispatch_emu<128, false>(dev, p, grid, s);
+  return causal ? dispatch_emu<64, true>(dev, p, grid, s) : dispatch_emu<64, false>(dev, p, grid, s);
 }
 
 void fill_common(fa::FwdParams& p, float scale) {

@@ -44,6 +44,7 @@ namespace fa {
 constexpr int kBlockM = 128;          // rows of one Q tile
 constexpr int kBlockN = 128;          // keys of one K/V block
 constexpr int kTaskRows = 2 * kBlockM;
+constexpr int kSplitP = 64;           // P is handed to the PV MMA in two column halves
 constexpr int kThreads = 512;
 constexpr uint32_t kTmemCols = 512;
 
@@ -85,7 +86,7 @@ struct Layout {
   static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
   // barrier indices
   static constexpr int bQFull = 0, bQEmpty = 2, bKVFull = 4, bKVEmpty = 4 + kStages;
-  static constexpr int bSFull = 4 + 2 * kStages, bPO = bSFull + 2, bCorrFull = bPO + 2,
+  static constexpr int bSFull = 4 + 2 * kStages, bPO = bSFull + 2, bP2 = bPO + 2, bCorrFull = bP2 + 2,
                        bCorrEmpty = bCorrFull + 2, bOFinal = bCorrEmpty + 2, bDrain = bOFinal + 2;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kMailOff = kBarOff + ((kNumBars * 8 + 127) / 128) * 128;
@@ -188,6 +189,53 @@ __device__ __forceinline__ float exp2_poly(float x) {
   return __int_as_float(__float_as_int(p) + (e << 23));
 }
 
+// ------------------------------------------------------------------ packed fp32 pairs (f32x2)
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t pack_bf16x2_u64(uint64_t v) {
+  float lo, hi;
+  unpack2(v, lo, hi);
+  return pack_bf16x2(lo, hi);
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float m;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+  return m;
+}
+// The polynomial exponential on a pair, with the Horner steps as f32x2 FMAs.
+__device__ __forceinline__ uint64_t exp2_poly2(uint64_t x2) {
+  float x0, x1;
+  unpack2(x2, x0, x1);
+  x0 = fmaxf(x0, -127.0f);
+  x1 = fmaxf(x1, -127.0f);
+  const float fl0 = floorf(x0), fl1 = floorf(x1);
+  const uint64_t f = pack2(x0 - fl0, x1 - fl1);
+  uint64_t q = fma2(f, pack2(0.07908560335636139f, 0.07908560335636139f),
+                    pack2(0.22537171840667725f, 0.22537171840667725f));
+  q = fma2(q, f, pack2(0.6955426931381226f, 0.6955426931381226f));
+  q = fma2(q, f, pack2(1.0f, 1.0f));
+  float q0, q1;
+  unpack2(q, q0, q1);
+  return pack2(__int_as_float(__float_as_int(q0) + (static_cast<int>(fl0) << 23)),
+               __int_as_float(__float_as_int(q1) + (static_cast<int>(fl1) << 23)));
+}
+
 // ------------------------------------------------------------------ MMA issue helpers
 // S = Q K^T : M = 128 rows, N = 128 keys, K = D (16 per instruction). Both
 // operands K-major with 128-byte swizzle; a K step of 16 bf16 is a 32-byte
@@ -207,18 +255,18 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint3
 // 8 columns per 16 keys. V is [keys, d] in smem = MN-major for the B operand:
 // 64-wide d slabs LBO = 16 KiB apart, 8-key groups SBO = 1 KiB apart; a K step
 // of 16 keys is a 2 KiB advance.
-template <int D>
+template <int D, int K0, int K1>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, bool accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, D, true);
 #pragma unroll
-  for (int kk = 0; kk < kBlockN / 16; ++kk) {
+  for (int kk = K0 / 16; kk < K1 / 16; ++kk) {
     const uint64_t b = smem_desc_sw128(v_smem + kk * 2048, Layout<D>::kSlabBytes, 1024);
     mma_ts(d_tmem, p_tmem + kk * 8, b, idesc, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool EMU>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -245,7 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       mbar_init(bar(L::bQFull + i), 1);
       mbar_init(bar(L::bQEmpty + i), 1);
       mbar_init(bar(L::bSFull + i), 1);
-      mbar_init(bar(L::bPO + i), 2 * kBlockM);      // softmax WG + correction WG
+      mbar_init(bar(L::bPO + i), 2 * kBlockM);      // P[:, :64] stored (softmax WG) + O ready (WG2)
+      mbar_init(bar(L::bP2 + i), kBlockM);          // P[:, 64:] stored (softmax WG)
       mbar_init(bar(L::bCorrFull + i), kBlockM);
       mbar_init(bar(L::bCorrEmpty + i), kBlockM);
       mbar_init(bar(L::bOFinal + i), 1);
@@ -333,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     if (lane == 0) {
       Waiter w{abort_flag, p.timeout_ns, kRoleMma};
       uint32_t stage = 0, phase = 0;
-      uint32_t po_par = 0;  // bit t: parity of the next wait on p_o[t]
+      uint32_t po_par = 0, p2_par = 0;  // bit t: parity of the next wait on p_o[t] / p2[t]
       bool ok = true;
       int it = 0;
       const uint32_t S0 = tmem + L::col_s(0), S1 = tmem + L::col_s(1);
@@ -368,7 +417,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           if (!w.wait(bar(L::bPO + 0), po_par & 1, L::bPO, j)) { ok = false; break; }
           po_par ^= 1;
           tc_fence_after();
-          issue_pv<D>(O0, P0, sKV + vs * L::kTileBytes, i > 0);
+          issue_pv<D, 0, kSplitP>(O0, P0, sKV + vs * L::kTileBytes, i > 0);
+          if (!w.wait(bar(L::bP2 + 0), p2_par & 1, L::bP2, j)) { ok = false; break; }
+          p2_par ^= 1;
+          tc_fence_after();
+          issue_pv<D, kSplitP, kBlockN>(O0, P0, sKV + vs * L::kTileBytes, true);
           if (!last) {
             ks = stage;
             if (!w.wait(bar(L::bKVFull + ks), phase, L::bKVFull + ks, j - 1)) { ok = false; break; }
@@ -384,7 +437,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           if (!w.wait(bar(L::bPO + 1), (po_par >> 1) & 1, L::bPO + 1, j)) { ok = false; break; }
           po_par ^= 2;
           tc_fence_after();
-          issue_pv<D>(O1, P1, sKV + vs * L::kTileBytes, i > 0);
+          issue_pv<D, 0, kSplitP>(O1, P1, sKV + vs * L::kTileBytes, i > 0);
+          if (!w.wait(bar(L::bP2 + 1), (p2_par >> 1) & 1, L::bP2 + 1, j)) { ok = false; break; }
+          p2_par ^= 2;
+          tc_fence_after();
+          issue_pv<D, kSplitP, kBlockN>(O1, P1, sKV + vs * L::kTileBytes, true);
           mma_commit(bar(L::bKVEmpty + vs));
           if (!last) {
             issue_qk<D>(S1, Q1, sKV + ks * L::kTileBytes);
@@ -425,33 +482,34 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         if (!w.wait(bar(L::bSFull + t), s_par, L::bSFull + t, j)) { ok = false; break; }
         s_par ^= 1;
         tc_fence_after();
-        float s[kBlockN];
-        {
-          uint32_t u[kBlockN];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&u[c * 32]));
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < kBlockN; ++e) s[e] = __uint_as_float(u[e]);
-        }
         const int k0 = j * kBlockN;
         const bool need_mask = (k0 + kBlockN > tk.len) || (CAUSAL && k0 + kBlockN - 1 > tile_row0);
-        if (need_mask) {
-          const int lim = row_limit - k0;
+        const int lim = need_mask ? row_limit - k0 : kBlockN;   // columns [lim, 128) are masked
+        // S in two halves: the second half's TMEM load overlaps the first half's max
+        float s[kBlockN];
+        uint32_t u[kBlockN];
+        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+        tmem_wait_ld();
+        tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&u[64]));
+        tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&u[96]));
+        float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < kBlockN; ++c)
-            if (c >= lim) s[c] = -INFINITY;
+        for (int c = 0; c < 64; c += 4) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) s[c + e] = (c + e < lim) ? __uint_as_float(u[c + e]) : -INFINITY;
+          mx0 = max3(mx0, s[c], s[c + 1]);
+          mx1 = max3(mx1, s[c + 2], s[c + 3]);
         }
-        // block maximum (tree)
-        float m4[4];
+        tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float a = s[q * 32];
+        for (int c = 64; c < kBlockN; c += 4) {
 #pragma unroll
-          for (int e = 1; e < 32; ++e) a = fmaxf(a, s[q * 32 + e]);
-          m4[q] = a;
+          for (int e = 0; e < 4; ++e) s[c + e] = (c + e < lim) ? __uint_as_float(u[c + e]) : -INFINITY;
+          mx0 = max3(mx0, s[c], s[c + 1]);
+          mx1 = max3(mx1, s[c + 2], s[c + 3]);
         }
-        const float blk_max = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        const float blk_max = fmaxf(mx0, mx1);
         // delayed-rescale rule
         float ref, acc;
         if (i == 0) {
@@ -471,48 +529,54 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           }
         }
         row_max = ref;
-        const float ref_safe = ref == -INFINITY ? 0.f : ref;
-        const float nbias = -ref_safe * sl2;
-        // P = exp2(S * sl2 - ref * sl2); the first emu_groups 16-column groups
-        // use the polynomial (only in blocks without masked columns)
-        const int emu = need_mask ? 0 : p.emu_groups;
-        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t pk[kBlockN / 2];
-#pragma unroll
-        for (int g = 0; g < kBlockN / 16; ++g) {
-          if (g < emu) {
-#pragma unroll
-            for (int e = 0; e < 16; e += 2) {
-              const int c = g * 16 + e;
-              const float p0 = exp2_poly(fmaf(s[c], sl2, nbias));
-              const float p1 = exp2_poly(fmaf(s[c + 1], sl2, nbias));
-              sum4[(c >> 1) & 3] += p0 + p1;
-              pk[c >> 1] = pack_bf16x2(p0, p1);
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 16; e += 2) {
-              const int c = g * 16 + e;
-              const float p0 = ex2_approx(fmaf(s[c], sl2, nbias));
-              const float p1 = ex2_approx(fmaf(s[c + 1], sl2, nbias));
-              sum4[(c >> 1) & 3] += p0 + p1;
-              pk[c >> 1] = pack_bf16x2(p0, p1);
-            }
-          }
-        }
-        // P over the upper half of S_t (S has been read completely above)
-        tmem_st32(tP, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(tP + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
-        tmem_wait_st();
+        // hand acc_scale to WG2 now, so the O rescale runs while P is computed
         if (i > 0) {
           if (!w.wait(bar(L::bCorrEmpty + t), ce_par ^ 1, L::bCorrEmpty + t, j)) { ok = false; break; }
           ce_par ^= 1;
           mail[t * kBlockM + r] = acc;
           mbar_arrive(bar(L::bCorrFull + t));
         }
-        tc_fence_before();
-        mbar_arrive(bar(L::bPO + t));
-        row_sum = row_sum * acc + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+        const float ref_safe = ref == -INFINITY ? 0.f : ref;
+        const uint64_t scale2 = pack2(sl2, sl2);
+        const uint64_t bias2 = pack2(-ref_safe * sl2, -ref_safe * sl2);
+        // P = exp2(S * sl2 - ref * sl2) -> bf16 pairs; with EMU the first emu_groups
+        // 16-column groups use the FMA polynomial (blocks without masked columns only)
+        const int emu = (EMU && !need_mask) ? p.emu_groups : 0;
+        uint64_t sum2a = 0, sum2b = 0;
+        uint32_t pk[kBlockN / 2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int g = h * 4; g < h * 4 + 4; ++g) {
+            if (EMU && g < emu) {
+#pragma unroll
+              for (int e = 0; e < 16; e += 2) {
+                const int c = g * 16 + e;
+                const uint64_t pp = exp2_poly2(fma2(pack2(s[c], s[c + 1]), scale2, bias2));
+                if (e & 2) sum2b = add2(sum2b, pp); else sum2a = add2(sum2a, pp);
+                pk[c >> 1] = pack_bf16x2_u64(pp);
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; e += 2) {
+                const int c = g * 16 + e;
+                float x0, x1;
+                unpack2(fma2(pack2(s[c], s[c + 1]), scale2, bias2), x0, x1);
+                const uint64_t pp = pack2(ex2_approx(x0), ex2_approx(x1));
+                if (e & 2) sum2b = add2(sum2b, pp); else sum2a = add2(sum2a, pp);
+                pk[c >> 1] = pack_bf16x2_u64(pp);
+              }
+            }
+          }
+          // this half of P over the upper half of S_t (all of S was read above)
+          tmem_st32(tP + h * 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[h * 32]));
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar(h == 0 ? L::bPO + t : L::bP2 + t));
+        }
+        float sa, sb;
+        unpack2(add2(sum2a, sum2b), sa, sb);
+        row_sum = row_sum * acc + (sa + sb);
       }
       if (!ok) break;
       // final statistics to WG2 (row_sum), LSE straight to global memory

@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(128, 1) mma_tile_kernel(const __grid_constant_
   __syncthreads();
   tc_fence_after();
   if (tid == 0) {
-    if (ok) issue_pv<D>(tmem + L::col_o(0), tmem + L::col_s(0) + 64, sV, false);
+    if (ok) issue_pv<D, 0, kBlockN>(tmem + L::col_o(0), tmem + L::col_s(0) + 64, sV, false);
     mma_commit(bMma);
   }
   __syncwarp();
@@ -126,7 +126,15 @@ __global__ void __launch_bounds__(128, 1) mma_tile_kernel(const __grid_constant_
 
 __global__ void exp2_kernel(const float* x, float* y, int n, int use_poly) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n) y[i] = use_poly ? fa::exp2_poly(x[i]) : fa::ex2_approx(x[i]);
+  if (i < n) {
+    if (use_poly == 2) {  // the packed pair form used inside the softmax
+      float lo, hi;
+      fa::unpack2(fa::exp2_poly2(fa::pack2(x[i], x[i])), lo, hi);
+      y[i] = lo;
+    } else {
+      y[i] = use_poly ? fa::exp2_poly(x[i]) : fa::ex2_approx(x[i]);
+    }
+  }
 }
 
 __global__ void wait_timeout_kernel(unsigned long long timeout_ns) {

@@ -25,8 +25,9 @@ extern "C" {
 int fa_selftest_mma_tile(const void* q, const void* k, const void* v, const void* p,
                          float* s_out, float* o_out, int d, void* stream);
 
-/* y[i] = 2^x[i] with the hardware ex2 unit (use_poly = 0) or with the FMA
- * polynomial used for part of the softmax exponentials (use_poly = 1).
+/* y[i] = 2^x[i] with the hardware ex2 unit (use_poly = 0), with the FMA
+ * polynomial used for part of the softmax exponentials (use_poly = 1), or with
+ * the packed-pair (f32x2) form of that polynomial the softmax runs (use_poly = 2).
  * x, y: fp32 [n] device. Asynchronous. */
 int fa_selftest_exp2(const float* x, float* y, int n, int use_poly, void* stream);
 

@@ -87,6 +87,8 @@ def test_exp2_paths():
     poly = host(fa.selftest_exp2(x, True))
     assert np.abs(hw / ref - 1).max() < 1e-6
     assert np.abs(poly / ref - 1).max() < 2e-4
+    poly2 = host(fa.selftest_exp2(x, 2))
+    assert np.array_equal(poly2, poly)
     # very negative and -inf inputs: hardware path gives 0, polynomial a value below 2^-126
     y = host(fa.selftest_exp2(torch.tensor([-float("inf"), -200.0, -127.0], device="cuda"), False))
     assert y[0] == 0.0 and y[1] == 0.0
