@@ -172,23 +172,6 @@ struct Waiter {
   }
 };
 
-// ------------------------------------------------------------------ exp2 on the FMA pipe
-// 2^x = 2^floor(x) * p(x - floor(x)) with p a cubic fitted to 2^f on [0, 1) by
-// the Remez exchange algorithm (minimax relative error 1.52e-4, p(0) = 1; see
-// fit_exp2_poly.py). The integer part is added to the exponent field.
-// ("Flash Attention 4", section "算法结构": part of the exponentials run as a
-// cubic polynomial on FMA units so the hardware ex2 unit is not the only path.)
-__device__ __forceinline__ float exp2_poly(float x) {
-  x = fmaxf(x, -127.0f);
-  const float fl = floorf(x);
-  const float f = x - fl;
-  float p = fmaf(f, 0.07908560335636139f, 0.22537171840667725f);
-  p = fmaf(p, f, 0.6955426931381226f);
-  p = fmaf(p, f, 1.0f);
-  const int e = static_cast<int>(fl);
-  return __int_as_float(__float_as_int(p) + (e << 23));
-}
-
 // ------------------------------------------------------------------ packed fp32 pairs (f32x2)
 __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
   uint64_t r;
@@ -218,22 +201,46 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
   return m;
 }
-// The polynomial exponential on a pair, with the Horner steps as f32x2 FMAs.
+// ------------------------------------------------------------------ exp2 on the FMA pipe
+// 2^x = 2^j * p(f) with j = round(x), f = x - j in [-1/2, 1/2] and p a cubic
+// fitted to 2^f by the Remez exchange algorithm (all four coefficients free,
+// max relative error 7.5e-5; see fit_exp2_poly.py). Rounding uses the 1.5*2^23
+// trick: in x + 1.5*2^23 the low mantissa bits hold round(x), and shifting that
+// word left by 23 moves j into the exponent field. No instruction of this path
+// runs on the transcendental (XU) pipe. x is clamped to [-126, 126] so the
+// exponent field stays in range: inputs below -126 give a non-negative value
+// under 2^-125 instead of 0, inputs above 126 give 2^126 * p(f) instead of inf.
+// ("Flash Attention 4", section "算法结构": part of the exponentials run as a
+// cubic polynomial on FMA units so the hardware ex2 unit is not the only path.)
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+constexpr float kP0 = 0.9999280571937561f, kP1 = 0.6932609677314758f, kP2 = 0.2426111251115799f,
+                kP3 = 0.0551716685295105f;
+
+__device__ __forceinline__ float exp2_poly(float x) {
+  x = fminf(fmaxf(x, -126.0f), 126.0f);
+  const float r = __fadd_rn(x, kRoundMagic);
+  const float f = __fsub_rn(x, __fsub_rn(r, kRoundMagic));
+  float q = fmaf(f, kP3, kP2);
+  q = fmaf(q, f, kP1);
+  q = fmaf(q, f, kP0);
+  return __int_as_float(__float_as_int(q) + (__float_as_int(r) << 23));
+}
+
+// The same steps on a pair, with the adds and the Horner steps as f32x2 ops.
 __device__ __forceinline__ uint64_t exp2_poly2(uint64_t x2) {
   float x0, x1;
   unpack2(x2, x0, x1);
-  x0 = fmaxf(x0, -127.0f);
-  x1 = fmaxf(x1, -127.0f);
-  const float fl0 = floorf(x0), fl1 = floorf(x1);
-  const uint64_t f = pack2(x0 - fl0, x1 - fl1);
-  uint64_t q = fma2(f, pack2(0.07908560335636139f, 0.07908560335636139f),
-                    pack2(0.22537171840667725f, 0.22537171840667725f));
-  q = fma2(q, f, pack2(0.6955426931381226f, 0.6955426931381226f));
-  q = fma2(q, f, pack2(1.0f, 1.0f));
-  float q0, q1;
+  const uint64_t x = pack2(fminf(fmaxf(x0, -126.0f), 126.0f), fminf(fmaxf(x1, -126.0f), 126.0f));
+  const uint64_t r = add2(x, pack2(kRoundMagic, kRoundMagic));
+  const uint64_t f = fma2(add2(r, pack2(-kRoundMagic, -kRoundMagic)), pack2(-1.0f, -1.0f), x);
+  uint64_t q = fma2(f, pack2(kP3, kP3), pack2(kP2, kP2));
+  q = fma2(q, f, pack2(kP1, kP1));
+  q = fma2(q, f, pack2(kP0, kP0));
+  float q0, q1, r0, r1;
   unpack2(q, q0, q1);
-  return pack2(__int_as_float(__float_as_int(q0) + (static_cast<int>(fl0) << 23)),
-               __int_as_float(__float_as_int(q1) + (static_cast<int>(fl1) << 23)));
+  unpack2(r, r0, r1);
+  return pack2(__int_as_float(__float_as_int(q0) + (__float_as_int(r0) << 23)),
+               __int_as_float(__float_as_int(q1) + (__float_as_int(r1) << 23)));
 }
 
 // ------------------------------------------------------------------ MMA issue helpers
@@ -494,20 +501,39 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&u[64]));
         tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&u[96]));
         float mx0 = -INFINITY, mx1 = -INFINITY;
+        if (need_mask) {
+          // diagonal / tail block: columns >= lim become -inf before the max
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
+          for (int c = 0; c < 64; c += 4) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) s[c + e] = (c + e < lim) ? __uint_as_float(u[c + e]) : -INFINITY;
-          mx0 = max3(mx0, s[c], s[c + 1]);
-          mx1 = max3(mx1, s[c + 2], s[c + 3]);
-        }
-        tmem_wait_ld();
+            for (int e = 0; e < 4; ++e) s[c + e] = (c + e < lim) ? __uint_as_float(u[c + e]) : -INFINITY;
+            mx0 = max3(mx0, s[c], s[c + 1]);
+            mx1 = max3(mx1, s[c + 2], s[c + 3]);
+          }
+          tmem_wait_ld();
 #pragma unroll
-        for (int c = 64; c < kBlockN; c += 4) {
+          for (int c = 64; c < kBlockN; c += 4) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) s[c + e] = (c + e < lim) ? __uint_as_float(u[c + e]) : -INFINITY;
-          mx0 = max3(mx0, s[c], s[c + 1]);
-          mx1 = max3(mx1, s[c + 2], s[c + 3]);
+            for (int e = 0; e < 4; ++e) s[c + e] = (c + e < lim) ? __uint_as_float(u[c + e]) : -INFINITY;
+            mx0 = max3(mx0, s[c], s[c + 1]);
+            mx1 = max3(mx1, s[c + 2], s[c + 3]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; c += 4) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[c + e] = __uint_as_float(u[c + e]);
+            mx0 = max3(mx0, s[c], s[c + 1]);
+            mx1 = max3(mx1, s[c + 2], s[c + 3]);
+          }
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 64; c < kBlockN; c += 4) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[c + e] = __uint_as_float(u[c + e]);
+            mx0 = max3(mx0, s[c], s[c + 1]);
+            mx1 = max3(mx1, s[c + 2], s[c + 3]);
+          }
         }
         const float blk_max = fmaxf(mx0, mx1);
         // delayed-rescale rule
