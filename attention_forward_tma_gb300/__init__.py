@@ -11,6 +11,7 @@ from __future__ import annotations
 
 import ctypes
 import math
+import os
 import threading
 
 from . import _build
@@ -35,6 +36,8 @@ _SIGNATURES = {
     "fa_selftest_exp2": [_vp, _vp, _ci, _ci, _vp],
     "fa_selftest_wait_timeout": [ctypes.c_ulonglong, _vp],
     "fa_varlen_schedule": [_vp, _ci, _ci, _ci, _ci, _vp, _vp, _vp],
+    "fa_trace_configure": [_vp, _ci],
+    "fa_trace_layout": [ctypes.POINTER(_ci), ctypes.POINTER(_ci)],
 }
 
 _lock = threading.Lock()
@@ -48,11 +51,12 @@ class FaError(RuntimeError):
 
 
 def library() -> ctypes.CDLL:
-    """Load (building first if needed) the in-tree libfa_gb300.so."""
+    """Load (building first if needed) the in-tree libfa_gb300.so, or its tracing
+    build libfa_gb300_trace.so when the environment sets FA_GB300_TRACE=1."""
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.build()
+            path = _build.build(trace=os.environ.get("FA_GB300_TRACE", "0") == "1")
             lib = ctypes.CDLL(path)
             for name, args in _SIGNATURES.items():
                 f = getattr(lib, name)

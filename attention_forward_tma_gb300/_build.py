@@ -17,6 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libfa_gb300.so")
+LIB_TRACE = os.path.join(PKG, "libfa_gb300_trace.so")   # -DFA_TRACE: clock stamps at pipeline hand-offs
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          f"-I{INCLUDE}", f"-I{CSRC}"]
@@ -35,23 +36,24 @@ def _sources():
             glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(s) <= t for s in _sources())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
+def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
+    lib = LIB_TRACE if trace else LIB
+    if not force and up_to_date(lib):
+        return lib
     exe = nvcc()
     out_dir = os.path.join(PKG, "_build")
     os.makedirs(out_dir, exist_ok=True)
 
     def compile_one(unit):
-        obj = os.path.join(out_dir, unit.replace(".cu", f".{os.getpid()}.o"))
-        cmd = [exe, *ARCH, *FLAGS, "-c", os.path.join(CSRC, unit), "-o", obj]
+        obj = os.path.join(out_dir, unit.replace(".cu", f".{'t' if trace else 'n'}{os.getpid()}.o"))
+        cmd = [exe, *ARCH, *FLAGS, *(["-DFA_TRACE"] if trace else []), "-c", os.path.join(CSRC, unit), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -62,20 +64,19 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with cf.ThreadPoolExecutor(max_workers=len(UNITS)) as ex:
         results = list(ex.map(compile_one, UNITS))
     objs = [o for o, _ in results]
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     r = subprocess.run([exe, *ARCH, "-shared", *objs, "-o", tmp], capture_output=True, text=True)
     for o in objs:
         os.remove(o)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     if verbose:
         for _, log in results:
             print(log)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
     import sys
-    build(force="--force" in sys.argv, verbose="-v" in sys.argv)
-    print(LIB)
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, trace="--trace" in sys.argv))

@@ -25,6 +25,10 @@ struct Options {
 };
 Options g_opt;
 
+// tracing builds: where fa_fwd / fa_fwd_varlen write their clock stamps
+unsigned long long* g_trace_buf = nullptr;
+int g_trace_ctas = 0;
+
 // ------------------------------------------------------------------ driver entry point
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -137,6 +141,8 @@ int dispatch(DevInfo* dev, const fa::FwdParams& p, int d, bool causal, int grid,
 }
 
 void fill_common(fa::FwdParams& p, float scale) {
+  p.trace = g_trace_buf;
+  p.trace_ctas = g_trace_ctas;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.tau = g_opt.tau;
   p.emu_groups = g_opt.emu_groups;
@@ -334,6 +340,26 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
   st = dispatch(dev, p, d, causal != 0, grid, s);
   if (cudaFreeAsync(ws, s) != cudaSuccess && st == FA_OK) st = FA_ERR_CUDA;
   return st;
+}
+
+int fa_trace_configure(void* buf, int ctas) {
+#ifdef FA_TRACE
+  if (ctas < 0 || (ctas > 0 && (buf == nullptr || !aligned(buf, 8)))) return FA_ERR_INVALID_ARG;
+  g_trace_buf = ctas > 0 ? static_cast<unsigned long long*>(buf) : nullptr;
+  g_trace_ctas = ctas;
+  return FA_OK;
+#else
+  (void)buf;
+  (void)ctas;
+  return FA_ERR_UNSUPPORTED;
+#endif
+}
+
+int fa_trace_layout(int* roles, int* slots_per_role) {
+  if (!roles || !slots_per_role) return FA_ERR_INVALID_ARG;
+  *roles = fa::kTraceRoles;
+  *slots_per_role = fa::kTraceSlots;
+  return FA_OK;
 }
 
 int fa_varlen_schedule(const int* cu_seqlens, int num_seqs, int H, int causal, int capacity, void* tasks,

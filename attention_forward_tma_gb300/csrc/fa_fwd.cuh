@@ -39,6 +39,10 @@
 
 #include "ptx.cuh"
 
+#ifndef FA_KV_STAGES_D128
+#define FA_KV_STAGES_D128 4
+#endif
+
 namespace fa {
 
 constexpr int kBlockM = 128;          // rows of one Q tile
@@ -72,6 +76,43 @@ struct FwdParams {
   float tau;                     // delayed-rescale threshold
   int emu_groups;                // 16-column groups per row evaluated with the polynomial exp2
   unsigned long long timeout_ns;
+  unsigned long long* trace;     // tracing build only: clock stamps per CTA and role (else null)
+  int trace_ctas;
+};
+
+// ------------------------------------------------------------------ tracing (FA_TRACE builds)
+// A tracing build stamps clock64 at every hand-off of the pipeline for the first
+// trace_ctas CTAs: one leader thread per role writes (clock, event code, block)
+// pairs into trace[(cta * kTraceRoles + role) * kTraceSlots ...]; slot 0 holds
+// the event count. Normal builds compile the stamps away.
+constexpr int kTraceRoles = 5;      // producer, MMA, softmax 0, softmax 1, correction
+constexpr int kTraceSlots = 8192;   // 64-bit words per role: count + 2 per event
+enum : uint32_t {
+  kEvQ0 = 1, kEvK = 2, kEvQ1 = 3, kEvV = 4,
+  kEvS0 = 10, kEvS1 = 11, kEvPO0 = 12, kEvPV0a = 13, kEvP20 = 14, kEvPV0b = 15, kEvPO1 = 16,
+  kEvPV1a = 17, kEvP21 = 18, kEvPV1b = 19, kEvKVV = 20, kEvKVK = 21,
+  kEvSFull = 30, kEvSMax = 31, kEvMail = 32, kEvHalf1 = 33, kEvHalf2 = 34, kEvStats = 35,
+  kEvCorrFull = 40, kEvCorrDone = 42, kEvEpiStart = 44, kEvEpiEnd = 46, kEvTask = 48
+};
+struct Tracer {
+#ifdef FA_TRACE
+  unsigned long long* buf = nullptr;
+  uint32_t n = 0;
+  __device__ __forceinline__ void init(const FwdParams& p, int role, bool leader) {
+    if (leader && p.trace != nullptr && (int)blockIdx.x < p.trace_ctas)
+      buf = p.trace + ((size_t)blockIdx.x * kTraceRoles + role) * kTraceSlots;
+  }
+  __device__ __forceinline__ void rec(uint32_t code, int blk) {
+    if (buf != nullptr && 2 * n + 2 < (uint32_t)kTraceSlots) {
+      buf[1 + 2 * n] = clock64();
+      buf[2 + 2 * n] = ((unsigned long long)code << 32) | (uint32_t)blk;
+      buf[0] = ++n;
+    }
+  }
+#else
+  __device__ __forceinline__ void init(const FwdParams&, int, bool) {}
+  __device__ __forceinline__ void rec(uint32_t, int) {}
+#endif
 };
 
 template <int D>
@@ -80,7 +121,7 @@ struct Layout {
   static constexpr int kHalves = D / 64;                   // 128-byte (64 x bf16) column slabs
   static constexpr int kSlabBytes = kBlockM * 128;          // one slab: 128 rows x 128 bytes
   static constexpr int kTileBytes = kHalves * kSlabBytes;   // one Q, K or V tile
-  static constexpr int kStages = D == 128 ? 3 : 6;          // K/V ring depth
+  static constexpr int kStages = D == 128 ? FA_KV_STAGES_D128 : 8;  // K/V ring depth
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kQOff + 2 * kTileBytes;
   static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
@@ -150,14 +191,16 @@ struct Waiter {
   unsigned long long timeout_ns;
   uint32_t role;
 
+  // Called by all 32 lanes of a warp together; the result is warp-uniform (every
+  // lane has observed the phase, so each has its own acquire).
   __device__ __forceinline__ bool wait(uint32_t bar_addr, uint32_t parity, uint32_t bar_id, int block) {
-    if (mbar_try_wait(bar_addr, parity)) return true;
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar_addr, parity))) return true;
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
-      if (mbar_try_wait(bar_addr, parity)) return true;
+      if (__all_sync(0xffffffffu, mbar_try_wait(bar_addr, parity))) return true;
       if ((it & 63) == 63) {
-        if (*abort_flag) return false;
-        const uint64_t now = globaltimer();
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
+        const uint64_t now = __shfl_sync(0xffffffffu, globaltimer(), 0);
         if (t0 == 0) t0 = now;
         else if (now - t0 > timeout_ns) {
           *abort_flag = 1;
@@ -247,29 +290,29 @@ __device__ __forceinline__ uint64_t exp2_poly2(uint64_t x2) {
 // S = Q K^T : M = 128 rows, N = 128 keys, K = D (16 per instruction). Both
 // operands K-major with 128-byte swizzle; a K step of 16 bf16 is a 32-byte
 // advance inside a 128-byte row; D = 128 spans two 64-column slabs.
+// qdesc / kdesc: descriptors of the tiles' first byte; the per-step offsets are
+// added to the 16-byte start-address field (shared-memory addresses stay below
+// 256 KiB, so the 14-bit field never carries).
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t qdesc, uint64_t kdesc) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, kBlockN, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk / 4) * Layout<D>::kSlabBytes + (kk % 4) * 32;
-    const uint64_t a = smem_desc_sw128(q_smem + off, 16, 1024);
-    const uint64_t b = smem_desc_sw128(k_smem + off, 16, 1024);
-    mma_ss(d_tmem, a, b, idesc, kk > 0 ? 1u : 0u);
+    const uint32_t off = ((kk / 4) * Layout<D>::kSlabBytes + (kk % 4) * 32) >> 4;
+    mma_ss(d_tmem, qdesc + off, kdesc + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 // O (+)= P V : M = 128 rows, N = D, K = 128 keys. P (bf16 pairs) from TMEM,
 // 8 columns per 16 keys. V is [keys, d] in smem = MN-major for the B operand:
 // 64-wide d slabs LBO = 16 KiB apart, 8-key groups SBO = 1 KiB apart; a K step
 // of 16 keys is a 2 KiB advance.
+// vdesc: MN-major descriptor of the V tile's first byte (LBO = one 64-column slab).
 template <int D, int K0, int K1>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t vdesc, bool accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, D, true);
 #pragma unroll
-  for (int kk = K0 / 16; kk < K1 / 16; ++kk) {
-    const uint64_t b = smem_desc_sw128(v_smem + kk * 2048, Layout<D>::kSlabBytes, 1024);
-    mma_ts(d_tmem, p_tmem + kk * 8, b, idesc, (accumulate || kk > 0) ? 1u : 0u);
-  }
+  for (int kk = K0 / 16; kk < K1 / 16; ++kk)
+    mma_ts(d_tmem, p_tmem + kk * 8, vdesc + ((kk * 2048) >> 4), idesc, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -336,8 +379,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   if (warp >= 12) setmaxnreg_dec<80>();
   if (warp == 13) {
     // ================================================================ TMA producer
-    if (lane == 0) {
+    // The whole warp runs the loop (its state stays warp-uniform); one elected
+    // lane issues the copies.
+    {
       Waiter w{abort_flag, p.timeout_ns, kRoleLoad};
+      Tracer tr;
+      tr.init(p, 0, lane == 0);
+      const bool leader = elect_one();
       uint32_t stage = 0, phase = 0;
       // armed full barriers and the parity of their last arm, for the drain on abort
       uint32_t q_armed = 0, q_par = 0, kv_armed = 0, kv_par = 0;
@@ -349,8 +397,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       };
       auto load_kv = [&](const CUtensorMap* m, int tok, int h, int blk) -> bool {
         if (!w.wait(bar(L::bKVEmpty + stage), phase ^ 1, L::bKVEmpty + stage, blk)) return false;
-        mbar_arrive_expect_tx(bar(L::bKVFull + stage), L::kTileBytes);
-        load_tile(m, sKV + stage * L::kTileBytes, tok, h, bar(L::bKVFull + stage));
+        if (leader) {
+          mbar_arrive_expect_tx(bar(L::bKVFull + stage), L::kTileBytes);
+          load_tile(m, sKV + stage * L::kTileBytes, tok, h, bar(L::bKVFull + stage));
+        }
+        __syncwarp();
+        tr.rec(m == &p.tm_k ? kEvK : kEvV, blk);
         kv_armed |= 1u << stage;
         kv_par = (kv_par & ~(1u << stage)) | (phase << stage);
         if (++stage == L::kStages) { stage = 0; phase ^= 1; }
@@ -358,8 +410,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       };
       auto load_q = [&](int t, int tok, int h, int blk) -> bool {
         if (!w.wait(bar(L::bQEmpty + t), (it & 1) ^ 1, L::bQEmpty + t, blk)) return false;
-        mbar_arrive_expect_tx(bar(L::bQFull + t), L::kTileBytes);
-        load_tile(&p.tm_q, sQ + t * L::kTileBytes, tok, h, bar(L::bQFull + t));
+        if (leader) {
+          mbar_arrive_expect_tx(bar(L::bQFull + t), L::kTileBytes);
+          load_tile(&p.tm_q, sQ + t * L::kTileBytes, tok, h, bar(L::bQFull + t));
+        }
+        __syncwarp();
+        tr.rec(t == 0 ? kEvQ0 : kEvQ1, blk);
         q_armed |= 1u << t;
         q_par = (q_par & ~(1u << t)) | ((uint32_t)(it & 1) << t);
         return true;
@@ -386,8 +442,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     }
   } else if (warp == 12) {
     // ================================================================ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop so stages, phases and descriptors stay in
+    // uniform registers; one elected lane (the same one throughout, so its
+    // tcgen05.commit covers its own MMAs) issues the tcgen05 instructions.
+    {
       Waiter w{abort_flag, p.timeout_ns, kRoleMma};
+      Tracer tr;
+      tr.init(p, 1, lane == 0);
+      const bool leader = elect_one();
       uint32_t stage = 0, phase = 0;
       uint32_t po_par = 0, p2_par = 0;  // bit t: parity of the next wait on p_o[t] / p2[t]
       bool ok = true;
@@ -395,7 +457,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       const uint32_t S0 = tmem + L::col_s(0), S1 = tmem + L::col_s(1);
       const uint32_t O0 = tmem + L::col_o(0), O1 = tmem + L::col_o(1);
       const uint32_t P0 = S0 + 64, P1 = S1 + 64;
-      const uint32_t Q0 = sQ, Q1 = sQ + L::kTileBytes;
+      const uint64_t Q0 = smem_desc_sw128(sQ, 16, 1024), Q1 = smem_desc_sw128(sQ + L::kTileBytes, 16, 1024);
+      const uint64_t Kd = smem_desc_sw128(sKV, 16, 1024);              // K tile of stage 0 (K-major)
+      const uint64_t Vd = smem_desc_sw128(sKV, L::kSlabBytes, 1024);   // V tile of stage 0 (MN-major)
+      constexpr uint32_t kStageStep = L::kTileBytes >> 4;
       Task tk;
       for (int idx = first_task; ok && get_task(p, CAUSAL, idx, tk); idx += task_stride, ++it) {
         const int nb = task_blocks(tk, CAUSAL);
@@ -407,61 +472,75 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         if (!ok) break;
         if (++stage == L::kStages) { stage = 0; phase ^= 1; }
         tc_fence_after();
-        issue_qk<D>(S0, Q0, sKV + ks * L::kTileBytes);
-        mma_commit(bar(L::bSFull + 0));
+        if (leader) issue_qk<D>(S0, Q0, Kd + ks * kStageStep);
+        if (leader) mma_commit(bar(L::bSFull + 0));
+        tr.rec(kEvS0, nb - 1);
         if (!w.wait(bar(L::bQFull + 1), qpar, L::bQFull + 1, nb - 1)) { ok = false; break; }
         tc_fence_after();
-        issue_qk<D>(S1, Q1, sKV + ks * L::kTileBytes);
-        mma_commit(bar(L::bSFull + 1));
-        mma_commit(bar(L::bKVEmpty + ks));
+        if (leader) issue_qk<D>(S1, Q1, Kd + ks * kStageStep);
+        tr.rec(kEvS1, nb - 1);
+        if (leader) mma_commit(bar(L::bSFull + 1));
+        if (leader) mma_commit(bar(L::bKVEmpty + ks));
         for (int i = 0; i < nb; ++i) {
           const int j = nb - 1 - i;
           const bool last = (i == nb - 1);
           const uint32_t vs = stage;
           if (!w.wait(bar(L::bKVFull + vs), phase, L::bKVFull + vs, j)) { ok = false; break; }
+          tr.rec(kEvKVV, j);
           if (++stage == L::kStages) { stage = 0; phase ^= 1; }
           // ---- tile 0: O_0 (+)= P_0 V_j, then S_0 for block j-1
           if (!w.wait(bar(L::bPO + 0), po_par & 1, L::bPO, j)) { ok = false; break; }
           po_par ^= 1;
+          tr.rec(kEvPO0, j);
           tc_fence_after();
-          issue_pv<D, 0, kSplitP>(O0, P0, sKV + vs * L::kTileBytes, i > 0);
+          if (leader) issue_pv<D, 0, kSplitP>(O0, P0, Vd + vs * kStageStep, i > 0);
+          tr.rec(kEvPV0a, j);
           if (!w.wait(bar(L::bP2 + 0), p2_par & 1, L::bP2, j)) { ok = false; break; }
           p2_par ^= 1;
+          tr.rec(kEvP20, j);
           tc_fence_after();
-          issue_pv<D, kSplitP, kBlockN>(O0, P0, sKV + vs * L::kTileBytes, true);
+          if (leader) issue_pv<D, kSplitP, kBlockN>(O0, P0, Vd + vs * kStageStep, true);
+          tr.rec(kEvPV0b, j);
           if (!last) {
             ks = stage;
             if (!w.wait(bar(L::bKVFull + ks), phase, L::bKVFull + ks, j - 1)) { ok = false; break; }
+            tr.rec(kEvKVK, j - 1);
             if (++stage == L::kStages) { stage = 0; phase ^= 1; }
             tc_fence_after();
-            issue_qk<D>(S0, Q0, sKV + ks * L::kTileBytes);
-            mma_commit(bar(L::bSFull + 0));
+            if (leader) issue_qk<D>(S0, Q0, Kd + ks * kStageStep);
+            if (leader) mma_commit(bar(L::bSFull + 0));
+            tr.rec(kEvS0, j - 1);
           } else {
-            mma_commit(bar(L::bOFinal + 0));
-            mma_commit(bar(L::bQEmpty + 0));
+            if (leader) mma_commit(bar(L::bOFinal + 0));
+            if (leader) mma_commit(bar(L::bQEmpty + 0));
           }
           // ---- tile 1: O_1 (+)= P_1 V_j, then S_1 for block j-1
           if (!w.wait(bar(L::bPO + 1), (po_par >> 1) & 1, L::bPO + 1, j)) { ok = false; break; }
           po_par ^= 2;
+          tr.rec(kEvPO1, j);
           tc_fence_after();
-          issue_pv<D, 0, kSplitP>(O1, P1, sKV + vs * L::kTileBytes, i > 0);
+          if (leader) issue_pv<D, 0, kSplitP>(O1, P1, Vd + vs * kStageStep, i > 0);
+          tr.rec(kEvPV1a, j);
           if (!w.wait(bar(L::bP2 + 1), (p2_par >> 1) & 1, L::bP2 + 1, j)) { ok = false; break; }
           p2_par ^= 2;
+          tr.rec(kEvP21, j);
           tc_fence_after();
-          issue_pv<D, kSplitP, kBlockN>(O1, P1, sKV + vs * L::kTileBytes, true);
-          mma_commit(bar(L::bKVEmpty + vs));
+          if (leader) issue_pv<D, kSplitP, kBlockN>(O1, P1, Vd + vs * kStageStep, true);
+          tr.rec(kEvPV1b, j);
+          if (leader) mma_commit(bar(L::bKVEmpty + vs));
           if (!last) {
-            issue_qk<D>(S1, Q1, sKV + ks * L::kTileBytes);
-            mma_commit(bar(L::bSFull + 1));
-            mma_commit(bar(L::bKVEmpty + ks));
+            if (leader) issue_qk<D>(S1, Q1, Kd + ks * kStageStep);
+            if (leader) mma_commit(bar(L::bSFull + 1));
+            if (leader) mma_commit(bar(L::bKVEmpty + ks));
+            tr.rec(kEvS1, j - 1);
           } else {
-            mma_commit(bar(L::bOFinal + 1));
-            mma_commit(bar(L::bQEmpty + 1));
+            if (leader) mma_commit(bar(L::bOFinal + 1));
+            if (leader) mma_commit(bar(L::bQEmpty + 1));
           }
         }
       }
       // all issued MMAs must finish before the tensor memory is released
-      mma_commit(bar(L::bDrain));
+      if (leader) mma_commit(bar(L::bDrain));
       Waiter d{never_abort, p.timeout_ns, kRoleDrain};
       d.wait(bar(L::bDrain), 0, L::bDrain, -1);
     }
@@ -474,6 +553,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     const uint32_t tS = tmem + lane_base + L::col_s(t);
     const uint32_t tP = tS + 64;
     Waiter w{abort_flag, p.timeout_ns, t == 0 ? kRoleSoftmax0 : kRoleSoftmax1};
+    Tracer tr;
+    tr.init(p, 2 + t, r == 0);
     const float sl2 = p.scale_log2;
     uint32_t s_par = 0, ce_par = 0;
     bool ok = true;
@@ -488,6 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         const int j = nb - 1 - i;
         if (!w.wait(bar(L::bSFull + t), s_par, L::bSFull + t, j)) { ok = false; break; }
         s_par ^= 1;
+        tr.rec(kEvSFull, j);
         tc_fence_after();
         const int k0 = j * kBlockN;
         const bool need_mask = (k0 + kBlockN > tk.len) || (CAUSAL && k0 + kBlockN - 1 > tile_row0);
@@ -536,6 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           }
         }
         const float blk_max = fmaxf(mx0, mx1);
+        tr.rec(kEvSMax, j);
         // delayed-rescale rule
         float ref, acc;
         if (i == 0) {
@@ -561,6 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           ce_par ^= 1;
           mail[t * kBlockM + r] = acc;
           mbar_arrive(bar(L::bCorrFull + t));
+          tr.rec(kEvMail, j);
         }
         const float ref_safe = ref == -INFINITY ? 0.f : ref;
         const uint64_t scale2 = pack2(sl2, sl2);
@@ -599,6 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(bar(h == 0 ? L::bPO + t : L::bP2 + t));
+          tr.rec(h == 0 ? kEvHalf1 : kEvHalf2, j);
         }
         float sa, sb;
         unpack2(add2(sum2a, sum2b), sa, sb);
@@ -610,6 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       ce_par ^= 1;
       mail[t * kBlockM + r] = row_sum;
       mbar_arrive(bar(L::bCorrFull + t));
+      tr.rec(kEvStats, -1);
       if (p.lse != nullptr && row < tk.len && tk.tok0 + row < p.total_tokens) {
         const float ref_safe = row_max == -INFINITY ? 0.f : row_max;
         const float lse = row_sum > 0.f ? (lg2_approx(row_sum) + ref_safe * sl2) * 0.69314718055994531f
@@ -623,11 +709,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     const int r = tid & 127;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     Waiter w{abort_flag, p.timeout_ns, kRoleCorr};
+    Tracer tr;
+    tr.init(p, 4, r == 0);
     uint32_t cf_par = 0, of_par = 0;  // bit t: parity of the next wait on corr_full[t] / o_final[t]
     bool ok = true;
     Task tk;
     for (int idx = first_task; ok && get_task(p, CAUSAL, idx, tk); idx += task_stride) {
       const int nb = task_blocks(tk, CAUSAL);
+      tr.rec(kEvTask, nb);
       // first block of this task: O_t is free (previous epilogue finished)
       mbar_arrive(bar(L::bPO + 0));
       mbar_arrive(bar(L::bPO + 1));
@@ -637,6 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         for (int t = 0; t < 2; ++t) {
           if (!w.wait(bar(L::bCorrFull + t), (cf_par >> t) & 1, L::bCorrFull + t, j)) { ok = false; break; }
           cf_par ^= 1u << t;
+          tr.rec(kEvCorrFull + t, j);
           const float a = mail[t * kBlockM + r];
           mbar_arrive(bar(L::bCorrEmpty + t));
           if (__any_sync(0xffffffffu, a < 1.f)) {
@@ -655,6 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           }
           tc_fence_before();
           mbar_arrive(bar(L::bPO + t));
+          tr.rec(kEvCorrDone + t, j);
         }
       }
       if (!ok) break;
@@ -667,6 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         mbar_arrive(bar(L::bCorrEmpty + t));
         if (!w.wait(bar(L::bOFinal + t), (of_par >> t) & 1, L::bOFinal + t, -1)) { ok = false; break; }
         of_par ^= 1u << t;
+        tr.rec(kEvEpiStart + t, -1);
         tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const int row = tk.m * kTaskRows + t * kBlockM + r;
@@ -688,6 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           }
         }
+        tr.rec(kEvEpiEnd + t, -1);
         tc_fence_before();
       }
     }

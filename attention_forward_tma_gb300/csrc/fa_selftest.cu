@@ -69,21 +69,27 @@ __global__ void __launch_bounds__(128, 1) mma_tile_kernel(const __grid_constant_
   const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
   Waiter w{abort_flag, timeout_ns, 7};
   bool ok = true;
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bLoad, 3 * L::kTileBytes);
-    for (int c = 0; c < L::kHalves; ++c) {
-      tma_load_3d(sQ + c * L::kSlabBytes, &maps.q, c * 64, 0, 0, bLoad);
-      tma_load_3d(sK + c * L::kSlabBytes, &maps.k, c * 64, 0, 0, bLoad);
-      tma_load_3d(sV + c * L::kSlabBytes, &maps.v, c * 64, 0, 0, bLoad);
+  if (warp == 0) {  // whole warp waits; one elected lane issues
+    const bool leader = elect_one();
+    if (leader) {
+      mbar_arrive_expect_tx(bLoad, 3 * L::kTileBytes);
+      for (int c = 0; c < L::kHalves; ++c) {
+        tma_load_3d(sQ + c * L::kSlabBytes, &maps.q, c * 64, 0, 0, bLoad);
+        tma_load_3d(sK + c * L::kSlabBytes, &maps.k, c * 64, 0, 0, bLoad);
+        tma_load_3d(sV + c * L::kSlabBytes, &maps.v, c * 64, 0, 0, bLoad);
+      }
     }
+    __syncwarp();
     ok = w.wait(bLoad, 0, 0, 0);
-    if (ok) {
-      tc_fence_after();
-      issue_qk<D>(tmem + L::col_s(0), sQ, sK);
+    if (leader) {
+      if (ok) {
+        tc_fence_after();
+        issue_qk<D>(tmem + L::col_s(0), smem_desc_sw128(sQ, 16, 1024), smem_desc_sw128(sK, 16, 1024));
+      }
+      mma_commit(bMma);
     }
-    mma_commit(bMma);
+    __syncwarp();
   }
-  __syncwarp();
   ok = w.wait(bMma, 0, 1, 0) && !*abort_flag;
   tc_fence_after();
   const int r = tid;
@@ -101,11 +107,14 @@ __global__ void __launch_bounds__(128, 1) mma_tile_kernel(const __grid_constant_
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (tid == 0) {
-    if (ok) issue_pv<D, 0, kBlockN>(tmem + L::col_o(0), tmem + L::col_s(0) + 64, sV, false);
-    mma_commit(bMma);
+  if (warp == 0) {
+    if (elect_one()) {
+      if (ok) issue_pv<D, 0, kBlockN>(tmem + L::col_o(0), tmem + L::col_s(0) + 64,
+                                      smem_desc_sw128(sV, L::kSlabBytes, 1024), false);
+      mma_commit(bMma);
+    }
+    __syncwarp();
   }
-  __syncwarp();
   ok = w.wait(bMma, 1, 1, 1) && ok;
   tc_fence_after();
   if (ok) {
@@ -146,10 +155,8 @@ __global__ void wait_timeout_kernel(unsigned long long timeout_ns) {
     fa::fence_mbar_init();
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    fa::Waiter w{&abort_flag, timeout_ns, 7};
-    w.wait(fa::smem_u32(&bar), 0, 99, -1);
-  }
+  fa::Waiter w{&abort_flag, timeout_ns, 7};  // all 32 lanes wait together
+  w.wait(fa::smem_u32(&bar), 0, 99, -1);
 }
 
 int read_and_clear_status() {

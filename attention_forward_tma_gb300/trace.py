@@ -1,0 +1,150 @@
+"""Pipeline traces from the tracing build of the library (libfa_gb300_trace.so).
+
+python -m attention_forward_tma_gb300.trace [--workload NAME] [--ctas N] [--json FILE]
+
+Runs one attention forward of a synthetic workload with clock stamps at every
+hand-off of the pipeline (TMA issue, MMA issue, softmax phases, correction and
+epilogue) for the first N CTAs, then prints per-role cycle statistics: the
+softmax latency per K/V block, how long the MMA issuer waited for each tile's
+P, the MMA issue period per block pair, and the epilogue time.
+Stamps are SM clock cycles (clock64) of the CTA's own SM.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import sys
+
+os.environ["FA_GB300_TRACE"] = "1"
+
+EVENTS = {1: "Q0", 2: "K", 3: "Q1", 4: "V", 10: "S0", 11: "S1", 12: "PO0", 13: "PV0a", 14: "P2_0", 15: "PV0b",
+          16: "PO1", 17: "PV1a", 18: "P2_1", 19: "PV1b", 20: "KVfull_V", 21: "KVfull_K", 30: "SFull", 31: "SMax",
+          32: "Mail", 33: "Half1", 34: "Half2", 35: "Stats", 40: "CorrFull0", 41: "CorrFull1", 42: "CorrDone0",
+          43: "CorrDone1", 44: "EpiStart0", 45: "EpiStart1", 46: "EpiEnd0", 47: "EpiEnd1", 48: "Task"}
+ROLES = ["producer", "mma", "softmax0", "softmax1", "correction"]
+
+
+def capture(run, ctas: int = 2):
+    """Call run() (which launches fa_fwd / fa_fwd_varlen) with tracing on; return decoded events
+    as {cta: {role: [(clock, event, block), ...]}}."""
+    import ctypes
+
+    import numpy as np
+    import torch
+
+    from . import library
+    lib = library()
+    roles, slots = ctypes.c_int(), ctypes.c_int()
+    lib.fa_trace_layout(ctypes.byref(roles), ctypes.byref(slots))
+    buf = torch.zeros(ctas * roles.value * slots.value, dtype=torch.int64, device="cuda")
+    st = lib.fa_trace_configure(buf.data_ptr(), ctas)
+    if st != 0:
+        raise RuntimeError(f"fa_trace_configure failed with status {st} (not a tracing build?)")
+    try:
+        run()
+        torch.cuda.synchronize()
+    finally:
+        lib.fa_trace_configure(None, 0)
+    raw = buf.cpu().numpy().view(np.uint64).reshape(ctas, roles.value, slots.value)
+    out = {}
+    for c in range(ctas):
+        out[c] = {}
+        for r in range(roles.value):
+            n = int(raw[c, r, 0])
+            ev = []
+            for i in range(n):
+                clk = int(raw[c, r, 1 + 2 * i])
+                word = int(raw[c, r, 2 + 2 * i])
+                code, blk = word >> 32, word & 0xFFFFFFFF
+                if blk >= 1 << 31:
+                    blk -= 1 << 32
+                ev.append((clk, EVENTS.get(code, str(code)), blk))
+            out[c][ROLES[r]] = ev
+    return out
+
+
+def _pairs(events, a, b):
+    """Cycle gaps from each event a to the next event b."""
+    out, start = [], None
+    for clk, name, _ in events:
+        if name == a:
+            start = clk
+        elif name == b and start is not None:
+            out.append(clk - start)
+            start = None
+    return out
+
+
+def summarize(trace) -> dict:
+    res = {}
+    for c, roles in trace.items():
+        t0 = min((ev[0][0] for ev in roles.values() if ev), default=0)
+        d = {"span_cycles": max((ev[-1][0] for ev in roles.values() if ev), default=0) - t0}
+        for t in (0, 1):
+            ev = roles[f"softmax{t}"]
+            d[f"softmax{t}_sfull_to_half2"] = _pairs(ev, "SFull", "Half2")
+            d[f"softmax{t}_sfull_to_max"] = _pairs(ev, "SFull", "SMax")
+            d[f"softmax{t}_half1_to_half2"] = _pairs(ev, "Half1", "Half2")
+            d[f"softmax{t}_half2_to_next_sfull"] = _pairs(ev, "Half2", "SFull")
+        m = roles["mma"]
+        d["mma_wait_po0"] = _pairs(m, "PV1b", "PO0")
+        d["mma_wait_po1"] = _pairs(m, "S0", "PO1")
+        d["mma_wait_p2_0"] = _pairs(m, "PV0a", "P2_0")
+        d["mma_wait_p2_1"] = _pairs(m, "PV1a", "P2_1")
+        s0 = [clk for clk, name, _ in m if name == "S0"]
+        d["mma_s0_period"] = [b - a for a, b in zip(s0, s0[1:])]
+        cor = roles["correction"]
+        d["epilogue"] = _pairs(cor, "EpiStart0", "EpiEnd1")
+        res[c] = d
+    return res
+
+
+def _fmt(v):
+    if isinstance(v, list):
+        if not v:
+            return "-"
+        return f"n={len(v):3d} median={statistics.median(v):8.0f} min={min(v):7d} max={max(v):8d}"
+    return str(v)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="c4_b1h32n16384d128_causal_spiky")
+    ap.add_argument("--ctas", type=int, default=2)
+    ap.add_argument("--json", default=None)
+    a = ap.parse_args()
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import numpy as np
+    import torch
+
+    import fa_inputs
+
+    from . import fa_fwd, fa_fwd_varlen
+    w = fa_inputs.WORKLOADS[a.workload]
+    x = fa_inputs.make_workload(w)
+
+    def dev(b):
+        return torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
+
+    q, k, v = dev(x["q"]), dev(x["k"]), dev(x["v"])
+    if w.varlen:
+        cu = torch.from_numpy(x["cu_seqlens"]).cuda()
+        run = lambda: fa_fwd_varlen(q, k, v, cu, int(x["lengths"].max()), scale=w.scale, causal=w.causal)  # noqa: E731
+    else:
+        run = lambda: fa_fwd(q, k, v, scale=w.scale, causal=w.causal)  # noqa: E731
+    run()
+    torch.cuda.synchronize()
+    tr = capture(run, a.ctas)
+    if a.json:
+        with open(a.json, "w") as f:
+            json.dump({str(c): r for c, r in tr.items()}, f)
+    for c, d in summarize(tr).items():
+        print(f"CTA {c}")
+        for key, val in d.items():
+            print(f"  {key:28s} {_fmt(val)}")
+
+
+if __name__ == "__main__":
+    main()

@@ -44,6 +44,22 @@ int fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream);
 int fa_varlen_schedule(const int* cu_seqlens, int num_seqs, int H, int causal, int capacity,
                        void* tasks, int* count, void* stream);
 
+/*
+ * Pipeline tracing. Only the tracing build of the library (compiled with
+ * -DFA_TRACE, libfa_gb300_trace.so) records; the normal build returns
+ * FA_ERR_UNSUPPORTED from fa_trace_configure.
+ * fa_trace_configure(buf, ctas): later fa_fwd / fa_fwd_varlen calls make one
+ * leader thread per role of CTAs 0..ctas-1 stamp clock64 at each pipeline
+ * hand-off into buf (device, uint64 [ctas][roles][slots]); ctas = 0 turns it
+ * off. Per role, word 0 is the number of events, then each event is two
+ * words: the SM clock and (event code << 32 | K/V block index). Roles:
+ * 0 TMA producer, 1 MMA issuer, 2 softmax of Q tile 0, 3 softmax of Q tile 1,
+ * 4 correction/epilogue. The buffer must hold ctas * roles * slots words.
+ * fa_trace_layout reports roles and slots per role (works in both builds).
+ */
+int fa_trace_configure(void* buf, int ctas);
+int fa_trace_layout(int* roles, int* slots_per_role);
+
 #ifdef __cplusplus
 }
 #endif
