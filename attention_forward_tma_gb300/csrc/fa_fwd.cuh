@@ -92,7 +92,8 @@ enum : uint32_t {
   kEvS0 = 10, kEvS1 = 11, kEvPO0 = 12, kEvPV0a = 13, kEvP20 = 14, kEvPV0b = 15, kEvPO1 = 16,
   kEvPV1a = 17, kEvP21 = 18, kEvPV1b = 19, kEvKVV = 20, kEvKVK = 21,
   kEvSFull = 30, kEvSMax = 31, kEvMail = 32, kEvHalf1 = 33, kEvHalf2 = 34, kEvStats = 35,
-  kEvCorrFull = 40, kEvCorrDone = 42, kEvEpiStart = 44, kEvEpiEnd = 46, kEvTask = 48
+  kEvCorrFull = 40, kEvCorrDone = 42, kEvEpiStart = 44, kEvEpiEnd = 46, kEvTask = 48,
+  kEvIssueBegin = 50
 };
 struct Tracer {
 #ifdef FA_TRACE
@@ -194,7 +195,6 @@ struct Waiter {
   // Called by all 32 lanes of a warp together; the result is warp-uniform (every
   // lane has observed the phase, so each has its own acquire).
   __device__ __forceinline__ bool wait(uint32_t bar_addr, uint32_t parity, uint32_t bar_id, int block) {
-    if (__all_sync(0xffffffffu, mbar_try_wait(bar_addr, parity))) return true;
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
       if (__all_sync(0xffffffffu, mbar_try_wait(bar_addr, parity))) return true;
@@ -203,15 +203,19 @@ struct Waiter {
         const uint64_t now = __shfl_sync(0xffffffffu, globaltimer(), 0);
         if (t0 == 0) t0 = now;
         else if (now - t0 > timeout_ns) {
-          *abort_flag = 1;
-          const unsigned long long word = kStatusTimeout | ((unsigned long long)role << 8) |
-                                          ((unsigned long long)bar_id << 16) |
-                                          ((unsigned long long)(uint32_t)block << 32);
-          atomicCAS(&g_fa_status, 0ull, word);
+          give_up(bar_id, block);
           return false;
         }
       }
     }
+  }
+  // Cold path: raise the CTA's abort flag and record the first timeout.
+  __device__ __noinline__ void give_up(uint32_t bar_id, int block) {
+    *abort_flag = 1;
+    const unsigned long long word = kStatusTimeout | ((unsigned long long)role << 8) |
+                                    ((unsigned long long)bar_id << 16) |
+                                    ((unsigned long long)(uint32_t)block << 32);
+    atomicCAS(&g_fa_status, 0ull, word);
   }
 };
 
@@ -424,18 +428,25 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       for (int idx = first_task; ok && get_task(p, CAUSAL, idx, tk); idx += task_stride, ++it) {
         const int nb = task_blocks(tk, CAUSAL);
         const int row0 = tk.tok0 + tk.m * kTaskRows;
-        int j = nb - 1;
-        ok = load_q(0, row0, tk.h, j) && load_kv(&p.tm_k, tk.tok0 + j * kBlockN, tk.h, j) &&
-             load_q(1, row0 + kBlockM, tk.h, j) && load_kv(&p.tm_v, tk.tok0 + j * kBlockN, tk.h, j);
-        for (j = nb - 2; ok && j >= 0; --j)
-          ok = load_kv(&p.tm_k, tk.tok0 + j * kBlockN, tk.h, j) &&
-               load_kv(&p.tm_v, tk.tok0 + j * kBlockN, tk.h, j);
+        // load order: Q_0, K_{nb-1}, Q_1, V_{nb-1}, K_{nb-2}, V_{nb-2}, ..., K_0, V_0
+#pragma unroll 1
+        for (int e = 0; ok && e < 2 * nb + 2; ++e) {
+          if (e == 0 || e == 2) {
+            ok = load_q(e >> 1, row0 + (e >> 1) * kBlockM, tk.h, nb - 1);
+          } else {
+            const int kvi = e == 1 ? 0 : e - 2;          // even: K, odd: V
+            const int j = nb - 1 - (kvi >> 1);
+            ok = load_kv((kvi & 1) ? &p.tm_v : &p.tm_k, tk.tok0 + j * kBlockN, tk.h, j);
+          }
+        }
       }
       if (!ok) {
         // drain: every armed full barrier completes once its bytes have landed
         Waiter d{never_abort, p.timeout_ns, kRoleDrain};
+#pragma unroll 1
         for (int t = 0; t < 2; ++t)
           if (q_armed & (1u << t)) d.wait(bar(L::bQFull + t), (q_par >> t) & 1, L::bQFull + t, -1);
+#pragma unroll 1
         for (int s = 0; s < L::kStages; ++s)
           if (kv_armed & (1u << s)) d.wait(bar(L::bKVFull + s), (kv_par >> s) & 1, L::bKVFull + s, -1);
       }
@@ -467,20 +478,22 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         const uint32_t qpar = it & 1;
         // prologue: S_0 and S_1 for the last block
         uint32_t ks = stage;
-        ok = w.wait(bar(L::bQFull + 0), qpar, L::bQFull, nb - 1) &&
-             w.wait(bar(L::bKVFull + ks), phase, L::bKVFull + ks, nb - 1);
-        if (!ok) break;
+        if (!w.wait(bar(L::bKVFull + ks), phase, L::bKVFull + ks, nb - 1)) { ok = false; break; }
         if (++stage == L::kStages) { stage = 0; phase ^= 1; }
-        tc_fence_after();
-        if (leader) issue_qk<D>(S0, Q0, Kd + ks * kStageStep);
-        if (leader) mma_commit(bar(L::bSFull + 0));
-        tr.rec(kEvS0, nb - 1);
-        if (!w.wait(bar(L::bQFull + 1), qpar, L::bQFull + 1, nb - 1)) { ok = false; break; }
-        tc_fence_after();
-        if (leader) issue_qk<D>(S1, Q1, Kd + ks * kStageStep);
-        tr.rec(kEvS1, nb - 1);
-        if (leader) mma_commit(bar(L::bSFull + 1));
-        if (leader) mma_commit(bar(L::bKVEmpty + ks));
+#pragma unroll 1
+        for (int t = 0; t < 2; ++t) {
+          if (!w.wait(bar(L::bQFull + t), qpar, L::bQFull + t, nb - 1)) { ok = false; break; }
+          tc_fence_after();
+          tr.rec(kEvIssueBegin, 0);
+          if (leader) {
+            issue_qk<D>(t ? S1 : S0, t ? Q1 : Q0, Kd + ks * kStageStep);
+            mma_commit(bar(L::bSFull + t));
+            if (t == 1) mma_commit(bar(L::bKVEmpty + ks));
+          }
+          __syncwarp();
+          tr.rec(kEvS0 + t, nb - 1);
+        }
+        if (!ok) break;
         for (int i = 0; i < nb; ++i) {
           const int j = nb - 1 - i;
           const bool last = (i == nb - 1);
@@ -488,55 +501,48 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           if (!w.wait(bar(L::bKVFull + vs), phase, L::bKVFull + vs, j)) { ok = false; break; }
           tr.rec(kEvKVV, j);
           if (++stage == L::kStages) { stage = 0; phase ^= 1; }
-          // ---- tile 0: O_0 (+)= P_0 V_j, then S_0 for block j-1
-          if (!w.wait(bar(L::bPO + 0), po_par & 1, L::bPO, j)) { ok = false; break; }
-          po_par ^= 1;
-          tr.rec(kEvPO0, j);
-          tc_fence_after();
-          if (leader) issue_pv<D, 0, kSplitP>(O0, P0, Vd + vs * kStageStep, i > 0);
-          tr.rec(kEvPV0a, j);
-          if (!w.wait(bar(L::bP2 + 0), p2_par & 1, L::bP2, j)) { ok = false; break; }
-          p2_par ^= 1;
-          tr.rec(kEvP20, j);
-          tc_fence_after();
-          if (leader) issue_pv<D, kSplitP, kBlockN>(O0, P0, Vd + vs * kStageStep, true);
-          tr.rec(kEvPV0b, j);
-          if (!last) {
-            ks = stage;
-            if (!w.wait(bar(L::bKVFull + ks), phase, L::bKVFull + ks, j - 1)) { ok = false; break; }
-            tr.rec(kEvKVK, j - 1);
-            if (++stage == L::kStages) { stage = 0; phase ^= 1; }
+          // per Q tile t: O_t (+)= P_t V_j in two halves, then S_t for block j-1
+#pragma unroll 1
+          for (int t = 0; t < 2; ++t) {
+            const uint32_t Ot = t ? O1 : O0, Pt = t ? P1 : P0, St = t ? S1 : S0;
+            const uint64_t Qt = t ? Q1 : Q0;
+            if (!w.wait(bar(L::bPO + t), (po_par >> t) & 1, L::bPO + t, j)) { ok = false; break; }
+            po_par ^= 1u << t;
+            tr.rec(kEvPO0 + 4 * t, j);
             tc_fence_after();
-            if (leader) issue_qk<D>(S0, Q0, Kd + ks * kStageStep);
-            if (leader) mma_commit(bar(L::bSFull + 0));
-            tr.rec(kEvS0, j - 1);
-          } else {
-            if (leader) mma_commit(bar(L::bOFinal + 0));
-            if (leader) mma_commit(bar(L::bQEmpty + 0));
+            tr.rec(kEvIssueBegin, 0);
+            if (leader) issue_pv<D, 0, kSplitP>(Ot, Pt, Vd + vs * kStageStep, i > 0);
+            tr.rec(kEvPV0a + 4 * t, j);
+            if (!w.wait(bar(L::bP2 + t), (p2_par >> t) & 1, L::bP2 + t, j)) { ok = false; break; }
+            p2_par ^= 1u << t;
+            tr.rec(kEvP20 + 4 * t, j);
+            tc_fence_after();
+            tr.rec(kEvIssueBegin, 0);
+            if (leader) issue_pv<D, kSplitP, kBlockN>(Ot, Pt, Vd + vs * kStageStep, true);
+            tr.rec(kEvPV0b + 4 * t, j);
+            if (t == 1 && leader) mma_commit(bar(L::bKVEmpty + vs));   // V_j read by both tiles
+            if (!last) {
+              if (t == 0) {
+                ks = stage;
+                if (!w.wait(bar(L::bKVFull + ks), phase, L::bKVFull + ks, j - 1)) { ok = false; break; }
+                tr.rec(kEvKVK, j - 1);
+                if (++stage == L::kStages) { stage = 0; phase ^= 1; }
+                tc_fence_after();
+              }
+              tr.rec(kEvIssueBegin, 0);
+              if (leader) {
+                issue_qk<D>(St, Qt, Kd + ks * kStageStep);
+                mma_commit(bar(L::bSFull + t));
+                if (t == 1) mma_commit(bar(L::bKVEmpty + ks));           // K_{j-1} read by both tiles
+              }
+              tr.rec(kEvS0 + t, j - 1);
+            } else if (leader) {
+              mma_commit(bar(L::bOFinal + t));
+              mma_commit(bar(L::bQEmpty + t));
+            }
+            __syncwarp();
           }
-          // ---- tile 1: O_1 (+)= P_1 V_j, then S_1 for block j-1
-          if (!w.wait(bar(L::bPO + 1), (po_par >> 1) & 1, L::bPO + 1, j)) { ok = false; break; }
-          po_par ^= 2;
-          tr.rec(kEvPO1, j);
-          tc_fence_after();
-          if (leader) issue_pv<D, 0, kSplitP>(O1, P1, Vd + vs * kStageStep, i > 0);
-          tr.rec(kEvPV1a, j);
-          if (!w.wait(bar(L::bP2 + 1), (p2_par >> 1) & 1, L::bP2 + 1, j)) { ok = false; break; }
-          p2_par ^= 2;
-          tr.rec(kEvP21, j);
-          tc_fence_after();
-          if (leader) issue_pv<D, kSplitP, kBlockN>(O1, P1, Vd + vs * kStageStep, true);
-          tr.rec(kEvPV1b, j);
-          if (leader) mma_commit(bar(L::bKVEmpty + vs));
-          if (!last) {
-            if (leader) issue_qk<D>(S1, Q1, Kd + ks * kStageStep);
-            if (leader) mma_commit(bar(L::bSFull + 1));
-            if (leader) mma_commit(bar(L::bKVEmpty + ks));
-            tr.rec(kEvS1, j - 1);
-          } else {
-            if (leader) mma_commit(bar(L::bOFinal + 1));
-            if (leader) mma_commit(bar(L::bQEmpty + 1));
-          }
+          if (!ok) break;
         }
       }
       // all issued MMAs must finish before the tensor memory is released
@@ -722,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       mbar_arrive(bar(L::bPO + 1));
       for (int i = 1; ok && i < nb; ++i) {
         const int j = nb - 1 - i;
-#pragma unroll
+#pragma unroll 1
         for (int t = 0; t < 2; ++t) {
           if (!w.wait(bar(L::bCorrFull + t), (cf_par >> t) & 1, L::bCorrFull + t, j)) { ok = false; break; }
           cf_par ^= 1u << t;
@@ -732,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           if (__any_sync(0xffffffffu, a < 1.f)) {
             tc_fence_after();
             const uint32_t tO = tmem + lane_base + L::col_o(t);
-#pragma unroll
+#pragma unroll 1
             for (int c = 0; c < D / 16; ++c) {
               uint32_t u[16];
               tmem_ld16(tO + c * 16, u);
@@ -750,7 +756,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       }
       if (!ok) break;
       // epilogue: O_t / row_sum -> bf16 -> global
-#pragma unroll
+#pragma unroll 1
       for (int t = 0; t < 2; ++t) {
         if (!w.wait(bar(L::bCorrFull + t), (cf_par >> t) & 1, L::bCorrFull + t, -1)) { ok = false; break; }
         cf_par ^= 1u << t;
@@ -765,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         const bool valid = row < tk.len && tk.tok0 + row < p.total_tokens;
         __nv_bfloat16* orow = p.o + ((size_t)(tk.tok0 + row) * p.H + tk.h) * D;
         const uint32_t tO = tmem + lane_base + L::col_o(t);
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < D / 16; ++c) {
           uint32_t u[16];
           tmem_ld16(tO + c * 16, u);

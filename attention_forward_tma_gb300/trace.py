@@ -22,7 +22,8 @@ os.environ["FA_GB300_TRACE"] = "1"
 EVENTS = {1: "Q0", 2: "K", 3: "Q1", 4: "V", 10: "S0", 11: "S1", 12: "PO0", 13: "PV0a", 14: "P2_0", 15: "PV0b",
           16: "PO1", 17: "PV1a", 18: "P2_1", 19: "PV1b", 20: "KVfull_V", 21: "KVfull_K", 30: "SFull", 31: "SMax",
           32: "Mail", 33: "Half1", 34: "Half2", 35: "Stats", 40: "CorrFull0", 41: "CorrFull1", 42: "CorrDone0",
-          43: "CorrDone1", 44: "EpiStart0", 45: "EpiStart1", 46: "EpiEnd0", 47: "EpiEnd1", 48: "Task"}
+          43: "CorrDone1", 44: "EpiStart0", 45: "EpiStart1", 46: "EpiEnd0", 47: "EpiEnd1", 48: "Task",
+          50: "IssueBegin"}
 ROLES = ["producer", "mma", "softmax0", "softmax1", "correction"]
 
 
