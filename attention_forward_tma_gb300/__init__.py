@@ -19,15 +19,16 @@ from . import _build
 __all__ = ["fa_fwd", "fa_fwd_varlen", "FaError", "set_option", "last_device_status", "library",
            "selftest_mma_tile", "selftest_exp2", "selftest_wait_timeout", "varlen_schedule",
            "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
-           "FA_ERR_NO_DEVICE"]
+           "FA_ERR_NO_DEVICE", "FA_ERR_CAPACITY"]
 
-FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_NO_DEVICE = range(6)
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_NO_DEVICE, FA_ERR_CAPACITY = range(7)
 _OPTIONS = {"tau": 1, "wait_timeout_ns": 2, "persistent": 3, "exp2_emulation": 4}
 
 _vp, _ci, _cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 _SIGNATURES = {
     "fa_fwd": [_vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _cf, _ci, _vp],
     "fa_fwd_varlen": [_vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _vp],
+    "fa_fwd_varlen_noalloc": [_vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _vp],
     "fa_error_string": [_ci],
     "fa_last_device_status": [_vp, ctypes.POINTER(ctypes.c_ulonglong)],
     "fa_set_option": [_ci, ctypes.c_double],

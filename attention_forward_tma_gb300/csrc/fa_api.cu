@@ -207,6 +207,34 @@ __global__ void __launch_bounds__(1024) fa_varlen_schedule_kernel(const int* cu,
 }
 }  // namespace fa
 
+// ------------------------------------------------------------------ allocation-free scratch
+namespace {
+// Scratch of fa_fwd_varlen_noalloc: kNoAllocMaxTasks work tiles (int4 each)
+// followed by one int4 whose first word is the tile count. A file-scope device
+// array, so it exists on every GPU that loads this library until the process
+// exits. Host code must not use the symbol as an address: noalloc_scratch()
+// looks the device address up (once per device, with that device current).
+constexpr int kNoAllocMaxTasks = 1 << 17;
+static __device__ __align__(256) int4 g_noalloc_scratch[kNoAllocMaxTasks + 1];
+int4* g_noalloc_ptr[kMaxDevices] = {};
+
+int noalloc_scratch(int4** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+      cudaGetLastError();
+      return FA_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = static_cast<int4*>(ptr);
+  }
+  *out = g_noalloc_ptr[dev];
+  return FA_OK;
+}
+}  // namespace
+
 // ------------------------------------------------------------------ C ABI
 extern "C" {
 
@@ -220,6 +248,7 @@ const char* fa_error_string(int status) {
     case FA_ERR_CUDA: return "CUDA runtime/driver error";
     case FA_ERR_TIMEOUT: return "device-side wait timed out";
     case FA_ERR_NO_DEVICE: return "no CUDA device";
+    case FA_ERR_CAPACITY: return "problem larger than the fixed scratch of the allocation-free entry point";
     default: return "unknown status";
   }
 }
@@ -373,6 +402,52 @@ int fa_varlen_schedule(const int* cu_seqlens, int num_seqs, int H, int causal, i
   fa::fa_varlen_schedule_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(
       cu_seqlens, num_seqs, H, causal, capacity, static_cast<int4*>(tasks), count);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_fwd_varlen_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
+                          int num_seqs, int total_tokens, int max_seqlen, int H, int d, float scale, int causal,
+                          void* stream) {
+  if (!q || !k || !v || !o || !cu_seqlens) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || (lse && !aligned(lse, 4)) ||
+      !aligned(cu_seqlens, 4))
+    return FA_ERR_INVALID_ARG;
+  if (num_seqs <= 0 || total_tokens <= 0 || max_seqlen <= 0 || H <= 0) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if ((long long)total_tokens * H > INT_MAX) return FA_ERR_INVALID_ARG;
+  const long long cap = (long long)H * ((total_tokens + fa::kTaskRows - 1) / fa::kTaskRows + num_seqs);
+  if (cap > kNoAllocMaxTasks) return FA_ERR_CAPACITY;
+  DevInfo* dev = nullptr;
+  int st = device_info(&dev);
+  if (st != FA_OK) return st;
+  int4* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != FA_OK) return st;
+
+  fa::FwdParams p;
+  std::memset(&p, 0, sizeof p);
+  if ((st = make_map(&p.tm_q, q, total_tokens, H, d)) != FA_OK ||
+      (st = make_map(&p.tm_k, k, total_tokens, H, d)) != FA_OK ||
+      (st = make_map(&p.tm_v, v, total_tokens, H, d)) != FA_OK)
+    return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int4* tasks = scratch;
+  int* count = reinterpret_cast<int*>(scratch + kNoAllocMaxTasks);
+  fa::fa_varlen_schedule_kernel<<<1, 1024, 0, s>>>(cu_seqlens, num_seqs, H, causal, (int)cap, tasks, count);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.cu_seqlens = cu_seqlens;
+  p.tasks = tasks;
+  p.task_count = count;
+  p.H = H;
+  p.total_tokens = total_tokens;
+  p.num_tasks = (int)cap;
+  p.varlen = 1;
+  fill_common(p, scale);
+  int grid = (int)cap;
+  if (use_persistent(causal != 0) && grid > dev->sm_count) grid = dev->sm_count;
+  return dispatch(dev, p, d, causal != 0, grid, s);
 }
 
 int fa_last_device_status(void* stream, unsigned long long* detail) {

@@ -46,7 +46,8 @@ typedef enum {
   FA_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, device is not sm_103, kernel resources */
   FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed (launch, tensor map, ...) */
   FA_ERR_TIMEOUT = 4,      /* a device-side wait gave up (reported by fa_last_device_status) */
-  FA_ERR_NO_DEVICE = 5     /* no CUDA device visible */
+  FA_ERR_NO_DEVICE = 5,    /* no CUDA device visible */
+  FA_ERR_CAPACITY = 6      /* problem larger than the fixed scratch of fa_fwd_varlen_noalloc */
 } fa_status;
 
 /*
@@ -84,6 +85,34 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
 int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                   const int* cu_seqlens, int num_seqs, int total_tokens, int max_seqlen,
                   int H, int d, float scale, int causal, void* stream);
+
+/*
+ * fa_fwd_varlen_noalloc: the same computation, arguments and results as
+ * fa_fwd_varlen, for callers that cannot allocate device memory at call time:
+ * for example a serving process that hands all of the GPU's memory to its own
+ * pool at start-up (so a later cudaMalloc fails), or a latency-critical loop
+ * that must not run allocator calls, which can block on other work of the
+ * device. The paper has no counterpart; this entry point exists only for
+ * such callers.
+ *
+ * It allocates nothing. Its work-tile list lives in a fixed array of this
+ * library (2 MiB + 16 bytes of device memory, taken on every GPU that loads
+ * the library and kept until the process exits), so:
+ *  - the problem must satisfy H * (ceil(total_tokens / 256) + num_seqs) <= 131072
+ *    (tiles of 256 query rows of one head), else it returns FA_ERR_CAPACITY
+ *    and enqueues nothing;
+ *  - all calls on a device share that array: calls whose work overlaps on the
+ *    GPU (for example on two streams at once) race and may return wrong
+ *    results; order them on one stream or with events;
+ *  - nothing in the array needs clearing between calls: each call's schedule
+ *    kernel overwrites the tile count and every tile it reports;
+ *  - the first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ */
+int fa_fwd_varlen_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                          const int* cu_seqlens, int num_seqs, int total_tokens, int max_seqlen,
+                          int H, int d, float scale, int causal, void* stream);
 
 /* Text for a status code (static storage; never NULL). */
 const char* fa_error_string(int status);
