@@ -77,7 +77,7 @@ def _check(status: int, what: str):
 
 
 def set_option(name: str, value: float) -> None:
-    """Process-wide knobs: tau, wait_timeout_ns, persistent (-1/0/1), exp2_emulation (0..8)."""
+    """Process-wide knobs: tau, wait_timeout_ns, persistent (-1/0/1/2), exp2_emulation (0..8)."""
     _check(library().fa_set_option(_OPTIONS[name], float(value)), f"set_option({name})")
 
 

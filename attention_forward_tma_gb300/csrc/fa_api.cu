@@ -20,7 +20,7 @@ namespace {
 struct Options {
   float tau = 8.0f;
   unsigned long long timeout_ns = 2000000000ull;
-  int persistent = -1;   // -1: default per mask type
+  int persistent = -1;   // -1: default (work stealing)
   int emu_groups = 0;
 };
 Options g_opt;
@@ -141,6 +141,7 @@ int dispatch(DevInfo* dev, const fa::FwdParams& p, int d, bool causal, int grid,
 }
 
 void fill_common(fa::FwdParams& p, float scale) {
+  p.sched = g_opt.persistent < 0 ? 2 : g_opt.persistent;
   p.trace = g_trace_buf;
   p.trace_ctas = g_trace_ctas;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -149,7 +150,10 @@ void fill_common(fa::FwdParams& p, float scale) {
   p.timeout_ns = g_opt.timeout_ns;
 }
 
-bool use_persistent(bool causal) { return g_opt.persistent < 0 ? !causal : g_opt.persistent != 0; }
+// Grid size: one CTA per task, except the static-stride mode (one CTA per SM).
+int grid_for(const fa::FwdParams& p, const DevInfo* dev, int n_tasks) {
+  return (p.sched == 1 && n_tasks > dev->sm_count) ? dev->sm_count : n_tasks;
+}
 
 }  // namespace
 
@@ -264,7 +268,7 @@ int fa_set_option(int option, double value) {
       g_opt.timeout_ns = (unsigned long long)value;
       return FA_OK;
     case FA_OPT_PERSISTENT:
-      if (value != -1.0 && value != 0.0 && value != 1.0) return FA_ERR_INVALID_ARG;
+      if (value != -1.0 && value != 0.0 && value != 1.0 && value != 2.0) return FA_ERR_INVALID_ARG;
       g_opt.persistent = (int)value;
       return FA_OK;
     case FA_OPT_EXP2_EMULATION:
@@ -311,8 +315,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.lpt_group = (int)group;
   p.varlen = 0;
   fill_common(p, scale);
-  int grid = p.num_tasks;
-  if (use_persistent(causal != 0) && grid > dev->sm_count) grid = dev->sm_count;
+  const int grid = grid_for(p, dev, p.num_tasks);
   return dispatch(dev, p, d, causal != 0, grid, static_cast<cudaStream_t>(stream));
 }
 
@@ -364,8 +367,7 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
   p.num_tasks = (int)cap;
   p.varlen = 1;
   fill_common(p, scale);
-  int grid = (int)cap;
-  if (use_persistent(causal != 0) && grid > dev->sm_count) grid = dev->sm_count;
+  const int grid = grid_for(p, dev, (int)cap);
   st = dispatch(dev, p, d, causal != 0, grid, s);
   if (cudaFreeAsync(ws, s) != cudaSuccess && st == FA_OK) st = FA_ERR_CUDA;
   return st;
@@ -445,8 +447,7 @@ int fa_fwd_varlen_noalloc(const void* q, const void* k, const void* v, void* o, 
   p.num_tasks = (int)cap;
   p.varlen = 1;
   fill_common(p, scale);
-  int grid = (int)cap;
-  if (use_persistent(causal != 0) && grid > dev->sm_count) grid = dev->sm_count;
+  const int grid = grid_for(p, dev, (int)cap);
   return dispatch(dev, p, d, causal != 0, grid, s);
 }
 

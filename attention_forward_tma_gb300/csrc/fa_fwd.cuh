@@ -7,8 +7,8 @@
 //   WG0, WG1  softmax of Q tile 0 / Q tile 1 (thread r owns row r of its tile)
 //   WG2       correction (rescale of O in tensor memory) and the epilogue
 //             (O / row_sum -> bf16 -> global memory)
-//   WG3       warp 12: tcgen05 MMA issue (one thread); warp 13: TMA loads (one
-//             thread); warps 14-15 idle
+//   WG3       warp 12: tcgen05 MMA issue; warp 13: TMA loads and task claims
+//             (work stealing by cluster launch control); warps 14-15 idle
 //
 // Per K/V block j (visited from the last block down to block 0, section
 // "Pipeline 时间线"):   S_t = Q_t K_j^T  (tcgen05, smem x smem -> TMEM fp32)
@@ -75,6 +75,7 @@ struct FwdParams {
   float scale_log2;              // scale * log2(e)
   float tau;                     // delayed-rescale threshold
   int emu_groups;                // 16-column groups per row evaluated with the polynomial exp2
+  int sched;                     // 0: one task per CTA; 1: static stride; 2: work stealing (launch control)
   unsigned long long timeout_ns;
   unsigned long long* trace;     // tracing build only: clock stamps per CTA and role (else null)
   int trace_ctas;
@@ -129,11 +130,13 @@ struct Layout {
   // barrier indices
   static constexpr int bQFull = 0, bQEmpty = 2, bKVFull = 4, bKVEmpty = 4 + kStages;
   static constexpr int bSFull = 4 + 2 * kStages, bPO = bSFull + 2, bP2 = bPO + 2, bCorrFull = bP2 + 2,
-                       bCorrEmpty = bCorrFull + 2, bOFinal = bCorrEmpty + 2, bDrain = bOFinal + 2;
-  static constexpr int kNumBars = bDrain + 1;
+                       bCorrEmpty = bCorrFull + 2, bOFinal = bCorrEmpty + 2, bDrain = bOFinal + 2,
+                       bTaskFull = bDrain + 1, bTaskEmpty = bTaskFull + 2, bClc = bTaskEmpty + 2;
+  static constexpr int kNumBars = bClc + 1;
   static constexpr int kMailOff = kBarOff + ((kNumBars * 8 + 127) / 128) * 128;
-  static constexpr int kMiscOff = kMailOff + 2 * kBlockM * 4;  // tmem slot, abort flag
-  static constexpr int kSmemBytes = kMiscOff + 64;
+  static constexpr int kMiscOff = kMailOff + 2 * kBlockM * 4;  // tmem slot, abort flags, task ring
+  static constexpr int kClcOff = kMiscOff + 64;                 // 16-byte launch-control response
+  static constexpr int kSmemBytes = kClcOff + 16;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;         // slack for 1024-byte alignment
   // tensor memory columns of S_t and O_t
   static __device__ __forceinline__ uint32_t col_s(int t) { return (uint32_t)t * 128u; }
@@ -185,6 +188,13 @@ __device__ __forceinline__ int task_blocks(const Task& t, bool causal) {
   if (causal) kmax = min(t.m * kTaskRows + kTaskRows, t.len);
   return (kmax + kBlockN - 1) / kBlockN;
 }
+
+// ------------------------------------------------------------------ task ring
+// The producer warp claims task indices and publishes them (or -1 = no more
+// work) through a two-slot ring in shared memory. The MMA warp, the 8 softmax
+// warps and the 4 correction warps take the k-th task from slot k % 2 and give
+// the slot back with one arrival per warp.
+constexpr int kTaskConsumerWarps = 13;
 
 // ------------------------------------------------------------------ bounded waits
 struct Waiter {
@@ -333,6 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
   volatile int* never_abort = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 8);  // stays 0
+  volatile int* task_slot = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 16);   // [2]
+  const uint32_t clc_resp = sbase + L::kClcOff;
   auto bar = [&](int i) -> uint32_t { return sBar + 8u * (uint32_t)i; };
 
   const int tid = threadIdx.x;
@@ -358,6 +370,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       mbar_init(bar(L::bKVEmpty + s), 1);
     }
     mbar_init(bar(L::bDrain), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(L::bTaskFull + i), 1);
+      mbar_init(bar(L::bTaskEmpty + i), kTaskConsumerWarps);
+    }
+    mbar_init(bar(L::bClc), 1);
     fence_mbar_init();
   }
   if (warp == 13 && lane == 0) {
@@ -374,8 +391,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int first_task = blockIdx.x;
-  const int task_stride = gridDim.x;
+  // consumers: the k-th task of this CTA from the ring (warp-uniform; -1 = done)
+  auto take_task = [&](Waiter& w, int k) -> int {
+    const int slot = k & 1;
+    if (!w.wait(bar(L::bTaskFull + slot), (k >> 1) & 1, L::bTaskFull + slot, -1)) return -1;
+    const int idx = task_slot[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(L::bTaskEmpty + slot));
+    return idx;
+  };
 
   // Register split 192/192/48/80 per thread for WG0/WG1/WG2/WG3 (sum = 4 x 128,
   // the launch allocation). Each setmaxnreg sits inside its role's branch so the
@@ -424,8 +448,48 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         q_par = (q_par & ~(1u << t)) | ((uint32_t)(it & 1) << t);
         return true;
       };
+      // The producer also claims this CTA's tasks and publishes them to the other
+      // warps: sched 2 takes over the task of a CTA that has not been launched
+      // yet (cluster launch control), which turns the launch order (longest task
+      // first for causal work) into a dynamic work queue; it does so only after
+      // issuing the last load of the current task, so a task is claimed shortly
+      // before an SM is free for it. sched 1 strides by the grid size; sched 0
+      // runs only blockIdx.x.
+      const int limit = p.varlen ? *p.task_count : p.num_tasks;
+      uint32_t clc_par = 0;
+      auto claim_next = [&](int cur) -> int {
+        for (;;) {
+          int n;
+          if (p.sched == 2) {
+            if (leader) {
+              mbar_arrive_expect_tx(bar(L::bClc), 16);
+              clc_try_cancel(clc_resp, bar(L::bClc));
+            }
+            __syncwarp();
+            if (!w.wait(bar(L::bClc), clc_par, L::bClc, -1)) return -1;
+            clc_par ^= 1;
+            n = clc_cancelled_ctaid_x(clc_resp);
+          } else {
+            n = p.sched == 1 ? cur + (int)gridDim.x : -1;
+          }
+          if (n < limit) return n;       // includes n = -1: no more work
+          if (p.sched != 2) return -1;   // static orders only grow
+          cur = n;                       // a grid-padding CTA without work: keep claiming
+        }
+      };
+      int idx = (int)blockIdx.x;
       Task tk;
-      for (int idx = first_task; ok && get_task(p, CAUSAL, idx, tk); idx += task_stride, ++it) {
+      for (int k = 0; ok; ++k, ++it) {
+        if (k > 0 || idx >= limit) idx = claim_next(idx);
+        const int slot = k & 1;
+        if (!w.wait(bar(L::bTaskEmpty + slot), ((k >> 1) & 1) ^ 1, L::bTaskEmpty + slot, -1)) { ok = false; break; }
+        if (leader) {
+          task_slot[slot] = idx;
+          mbar_arrive(bar(L::bTaskFull + slot));
+        }
+        __syncwarp();
+        if (idx < 0) break;
+        get_task(p, CAUSAL, idx, tk);
         const int nb = task_blocks(tk, CAUSAL);
         const int row0 = tk.tok0 + tk.m * kTaskRows;
         // load order: Q_0, K_{nb-1}, Q_1, V_{nb-1}, K_{nb-2}, V_{nb-2}, ..., K_0, V_0
@@ -473,7 +537,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       const uint64_t Vd = smem_desc_sw128(sKV, L::kSlabBytes, 1024);   // V tile of stage 0 (MN-major)
       constexpr uint32_t kStageStep = L::kTileBytes >> 4;
       Task tk;
-      for (int idx = first_task; ok && get_task(p, CAUSAL, idx, tk); idx += task_stride, ++it) {
+      for (int k = 0; ok; ++k, ++it) {
+        const int idx = take_task(w, k);
+        if (idx < 0) break;
+        get_task(p, CAUSAL, idx, tk);
         const int nb = task_blocks(tk, CAUSAL);
         const uint32_t qpar = it & 1;
         // prologue: S_0 and S_1 for the last block
@@ -489,6 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             issue_qk<D>(t ? S1 : S0, t ? Q1 : Q0, Kd + ks * kStageStep);
             mma_commit(bar(L::bSFull + t));
             if (t == 1) mma_commit(bar(L::bKVEmpty + ks));
+            if (nb == 1) mma_commit(bar(L::bQEmpty + t));   // Q_t's last use: the next task's Q may load
           }
           __syncwarp();
           tr.rec(kEvS0 + t, nb - 1);
@@ -534,11 +602,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                 issue_qk<D>(St, Qt, Kd + ks * kStageStep);
                 mma_commit(bar(L::bSFull + t));
                 if (t == 1) mma_commit(bar(L::bKVEmpty + ks));           // K_{j-1} read by both tiles
+                if (j == 1) mma_commit(bar(L::bQEmpty + t));             // last use of Q_t in this task
               }
               tr.rec(kEvS0 + t, j - 1);
             } else if (leader) {
               mma_commit(bar(L::bOFinal + t));
-              mma_commit(bar(L::bQEmpty + t));
             }
             __syncwarp();
           }
@@ -565,7 +633,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     uint32_t s_par = 0, ce_par = 0;
     bool ok = true;
     Task tk;
-    for (int idx = first_task; ok && get_task(p, CAUSAL, idx, tk); idx += task_stride) {
+    for (int k = 0; ok; ++k) {
+      const int idx = take_task(w, k);
+      if (idx < 0) break;
+      get_task(p, CAUSAL, idx, tk);
       const int nb = task_blocks(tk, CAUSAL);
       const int row = tk.m * kTaskRows + t * kBlockM + r;       // row within the sequence
       const int tile_row0 = tk.m * kTaskRows + t * kBlockM;
@@ -720,12 +791,17 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     uint32_t cf_par = 0, of_par = 0;  // bit t: parity of the next wait on corr_full[t] / o_final[t]
     bool ok = true;
     Task tk;
-    for (int idx = first_task; ok && get_task(p, CAUSAL, idx, tk); idx += task_stride) {
+    // O_0 and O_1 are free for the first task's first PV; later tasks get this
+    // arrival right after the epilogue of the same tile (below), so the next
+    // task's PV can start while the other tile is still being written out.
+    mbar_arrive(bar(L::bPO + 0));
+    mbar_arrive(bar(L::bPO + 1));
+    for (int k = 0; ok; ++k) {
+      const int idx = take_task(w, k);
+      if (idx < 0) break;
+      get_task(p, CAUSAL, idx, tk);
       const int nb = task_blocks(tk, CAUSAL);
       tr.rec(kEvTask, nb);
-      // first block of this task: O_t is free (previous epilogue finished)
-      mbar_arrive(bar(L::bPO + 0));
-      mbar_arrive(bar(L::bPO + 1));
       for (int i = 1; ok && i < nb; ++i) {
         const int j = nb - 1 - i;
 #pragma unroll 1
@@ -788,6 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         }
         tr.rec(kEvEpiEnd + t, -1);
         tc_fence_before();
+        mbar_arrive(bar(L::bPO + t));   // O_t is free for the next task's first PV
       }
     }
   }

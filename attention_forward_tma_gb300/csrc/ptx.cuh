@@ -76,6 +76,31 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- cluster launch control
+// Ask the hardware to cancel one not-yet-launched CTA of this grid; the 16-byte
+// response lands in shared memory and completes `bar` (expect 16 bytes first).
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp_smem, uint32_t bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+          resp_smem),
+      "r"(bar)
+      : "memory");
+}
+// blockIdx.x of the cancelled CTA, or -1 when no CTA was left to cancel.
+__device__ __forceinline__ int clc_cancelled_ctaid_x(uint32_t resp_smem) {
+  uint32_t cancelled, x;
+  asm volatile(
+      "{\n\t.reg .b128 h;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 h, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, h;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, h;\n\t}"
+      : "=r"(cancelled), "=r"(x)
+      : "r"(resp_smem)
+      : "memory");
+  return cancelled ? static_cast<int>(x) : -1;
+}
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),

@@ -129,9 +129,11 @@ int fa_last_device_status(void* stream, unsigned long long* detail);
  * Process-wide tuning knobs (not thread-safe; meant for tests and benchmarks).
  *   FA_OPT_TAU             : rescale threshold tau in base-2 exponent units (default 8)
  *   FA_OPT_WAIT_TIMEOUT_NS : device wait limit in nanoseconds (default 2e9)
- *   FA_OPT_PERSISTENT      : 1 = persistent CTAs (one per SM, static task stride),
- *                            0 = one CTA per task (default: 1 for non-causal, 0 for causal)
- *                            -1 = restore the default
+ *   FA_OPT_PERSISTENT      : task scheduling. 2 = one CTA per task in launch order, and
+ *                            each running CTA takes over the tasks of CTAs not yet
+ *                            launched (cluster launch control; the default);
+ *                            1 = one CTA per SM with a static task stride;
+ *                            0 = one CTA per task, no take-over; -1 = restore the default
  *   FA_OPT_EXP2_EMULATION  : number of 16-element groups per 128-wide row (0..8)
  *                            whose exp2 is evaluated with the FMA polynomial instead
  *                            of the hardware ex2 unit (default 0)

@@ -97,7 +97,7 @@ def test_valid_arguments_without_gpu_report_no_device():
 
 @pytest.mark.parametrize("opt,val,ok", [(1, 8.0, True), (1, 0.0, True), (1, 1e30, True), (1, -1.0, False),
                                         (1, math.nan, False), (2, 1e9, True), (2, 10.0, False),
-                                        (3, 1, True), (3, 0, True), (3, -1, True), (3, 2, False),
+                                        (3, 1, True), (3, 0, True), (3, -1, True), (3, 2, True), (3, 3, False),
                                         (4, 0, True), (4, 8, True), (4, 9, False), (4, 2.5, False),
                                         (99, 1, False)])
 def test_set_option_validation(opt, val, ok):
