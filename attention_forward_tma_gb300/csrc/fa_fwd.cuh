@@ -196,6 +196,12 @@ __device__ __forceinline__ int task_blocks(const Task& t, bool causal) {
 // the slot back with one arrival per warp.
 constexpr int kTaskConsumerWarps = 13;
 
+// Causal tasks: the top K/V block lies entirely above Q tile 0's last row, so
+// tile 0 skips it (its scores there would all be masked). Returns 1 or 0.
+__device__ __forceinline__ int task_skip0(const Task& t, int nb, bool causal) {
+  return (causal && nb >= 2 && (nb - 1) * kBlockN > t.m * kTaskRows + kBlockM - 1) ? 1 : 0;
+}
+
 // ------------------------------------------------------------------ bounded waits
 struct Waiter {
   volatile int* abort_flag;
@@ -542,8 +548,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         if (idx < 0) break;
         get_task(p, CAUSAL, idx, tk);
         const int nb = task_blocks(tk, CAUSAL);
+        const int skip0 = task_skip0(tk, nb, CAUSAL);   // tile 0 starts one block lower
         const uint32_t qpar = it & 1;
-        // prologue: S_0 and S_1 for the last block
+        // prologue: S_0 and S_1 for the last block (S_0 only if tile 0 sees it)
         uint32_t ks = stage;
         if (!w.wait(bar(L::bKVFull + ks), phase, L::bKVFull + ks, nb - 1)) { ok = false; break; }
         if (++stage == L::kStages) { stage = 0; phase ^= 1; }
@@ -553,8 +560,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           tc_fence_after();
           tr.rec(kEvIssueBegin, 0);
           if (leader) {
-            issue_qk<D>(t ? S1 : S0, t ? Q1 : Q0, Kd + ks * kStageStep);
-            mma_commit(bar(L::bSFull + t));
+            if (t == 1 || !skip0) {
+              issue_qk<D>(t ? S1 : S0, t ? Q1 : Q0, Kd + ks * kStageStep);
+              mma_commit(bar(L::bSFull + t));
+            }
             if (t == 1) mma_commit(bar(L::bKVEmpty + ks));
             if (nb == 1) mma_commit(bar(L::bQEmpty + t));   // Q_t's last use: the next task's Q may load
           }
@@ -574,20 +583,23 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           for (int t = 0; t < 2; ++t) {
             const uint32_t Ot = t ? O1 : O0, Pt = t ? P1 : P0, St = t ? S1 : S0;
             const uint64_t Qt = t ? Q1 : Q0;
-            if (!w.wait(bar(L::bPO + t), (po_par >> t) & 1, L::bPO + t, j)) { ok = false; break; }
-            po_par ^= 1u << t;
-            tr.rec(kEvPO0 + 4 * t, j);
-            tc_fence_after();
-            tr.rec(kEvIssueBegin, 0);
-            if (leader) issue_pv<D, 0, kSplitP>(Ot, Pt, Vd + vs * kStageStep, i > 0);
-            tr.rec(kEvPV0a + 4 * t, j);
-            if (!w.wait(bar(L::bP2 + t), (p2_par >> t) & 1, L::bP2 + t, j)) { ok = false; break; }
-            p2_par ^= 1u << t;
-            tr.rec(kEvP20 + 4 * t, j);
-            tc_fence_after();
-            tr.rec(kEvIssueBegin, 0);
-            if (leader) issue_pv<D, kSplitP, kBlockN>(Ot, Pt, Vd + vs * kStageStep, true);
-            tr.rec(kEvPV0b + 4 * t, j);
+            const int first_i = t == 0 ? skip0 : 0;   // this tile's first block
+            if (i >= first_i) {
+              if (!w.wait(bar(L::bPO + t), (po_par >> t) & 1, L::bPO + t, j)) { ok = false; break; }
+              po_par ^= 1u << t;
+              tr.rec(kEvPO0 + 4 * t, j);
+              tc_fence_after();
+              tr.rec(kEvIssueBegin, 0);
+              if (leader) issue_pv<D, 0, kSplitP>(Ot, Pt, Vd + vs * kStageStep, i > first_i);
+              tr.rec(kEvPV0a + 4 * t, j);
+              if (!w.wait(bar(L::bP2 + t), (p2_par >> t) & 1, L::bP2 + t, j)) { ok = false; break; }
+              p2_par ^= 1u << t;
+              tr.rec(kEvP20 + 4 * t, j);
+              tc_fence_after();
+              tr.rec(kEvIssueBegin, 0);
+              if (leader) issue_pv<D, kSplitP, kBlockN>(Ot, Pt, Vd + vs * kStageStep, true);
+              tr.rec(kEvPV0b + 4 * t, j);
+            }
             if (t == 1 && leader) mma_commit(bar(L::bKVEmpty + vs));   // V_j read by both tiles
             if (!last) {
               if (t == 0) {
@@ -637,7 +649,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       const int idx = take_task(w, k);
       if (idx < 0) break;
       get_task(p, CAUSAL, idx, tk);
-      const int nb = task_blocks(tk, CAUSAL);
+      const int nb_all = task_blocks(tk, CAUSAL);
+      const int nb = nb_all - (t == 0 ? task_skip0(tk, nb_all, CAUSAL) : 0);   // this tile's blocks
       const int row = tk.m * kTaskRows + t * kBlockM + r;       // row within the sequence
       const int tile_row0 = tk.m * kTaskRows + t * kBlockM;
       const int row_limit = CAUSAL ? min(row + 1, tk.len) : tk.len;  // keys [0, row_limit) visible
@@ -801,11 +814,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       if (idx < 0) break;
       get_task(p, CAUSAL, idx, tk);
       const int nb = task_blocks(tk, CAUSAL);
+      const int skip0 = task_skip0(tk, nb, CAUSAL);
       tr.rec(kEvTask, nb);
       for (int i = 1; ok && i < nb; ++i) {
         const int j = nb - 1 - i;
 #pragma unroll 1
         for (int t = 0; t < 2; ++t) {
+          if (t == 0 && i - skip0 < 1) continue;   // tile 0's first block needs no correction
           if (!w.wait(bar(L::bCorrFull + t), (cf_par >> t) & 1, L::bCorrFull + t, j)) { ok = false; break; }
           cf_par ^= 1u << t;
           tr.rec(kEvCorrFull + t, j);
