@@ -298,7 +298,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   fa::FwdParams p;
   std::memset(&p, 0, sizeof p);
   if ((st = make_map(&p.tm_q, q, tokens, H, d)) != FA_OK || (st = make_map(&p.tm_k, k, tokens, H, d)) != FA_OK ||
-      (st = make_map(&p.tm_v, v, tokens, H, d)) != FA_OK)
+      (st = make_map(&p.tm_v, v, tokens, H, d)) != FA_OK ||
+      (st = make_map(&p.tm_o, o, tokens, H, d)) != FA_OK)
     return st;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
@@ -341,7 +342,8 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
   std::memset(&p, 0, sizeof p);
   if ((st = make_map(&p.tm_q, q, total_tokens, H, d)) != FA_OK ||
       (st = make_map(&p.tm_k, k, total_tokens, H, d)) != FA_OK ||
-      (st = make_map(&p.tm_v, v, total_tokens, H, d)) != FA_OK)
+      (st = make_map(&p.tm_v, v, total_tokens, H, d)) != FA_OK ||
+      (st = make_map(&p.tm_o, o, total_tokens, H, d)) != FA_OK)
     return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* ws = nullptr;
@@ -430,7 +432,8 @@ int fa_fwd_varlen_noalloc(const void* q, const void* k, const void* v, void* o, 
   std::memset(&p, 0, sizeof p);
   if ((st = make_map(&p.tm_q, q, total_tokens, H, d)) != FA_OK ||
       (st = make_map(&p.tm_k, k, total_tokens, H, d)) != FA_OK ||
-      (st = make_map(&p.tm_v, v, total_tokens, H, d)) != FA_OK)
+      (st = make_map(&p.tm_v, v, total_tokens, H, d)) != FA_OK ||
+      (st = make_map(&p.tm_o, o, total_tokens, H, d)) != FA_OK)
     return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int4* tasks = scratch;

@@ -40,7 +40,7 @@
 #include "ptx.cuh"
 
 #ifndef FA_KV_STAGES_D128
-#define FA_KV_STAGES_D128 4
+#define FA_KV_STAGES_D128 3
 #endif
 
 namespace fa {
@@ -61,6 +61,7 @@ constexpr unsigned long long kStatusTimeout = 4;  // == FA_ERR_TIMEOUT
 
 struct FwdParams {
   CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps of [tokens, H, d]: x = d, y = token, z = head
+  CUtensorMap tm_o;              // the same view of O, for the TMA store of full tiles
   __nv_bfloat16* o;              // [tokens, H, d]
   float* lse;                    // fixed length [B, H, N]; varlen [H, tokens]; may be null
   const int* cu_seqlens;         // varlen only
@@ -126,13 +127,15 @@ struct Layout {
   static constexpr int kStages = D == 128 ? FA_KV_STAGES_D128 : 8;  // K/V ring depth
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kQOff + 2 * kTileBytes;
-  static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+  static constexpr int kOstOff = kKVOff + kStages * kTileBytes;  // O staging tile for the TMA store
+  static constexpr int kBarOff = kOstOff + kTileBytes;
   // barrier indices
   static constexpr int bQFull = 0, bQEmpty = 2, bKVFull = 4, bKVEmpty = 4 + kStages;
   static constexpr int bSFull = 4 + 2 * kStages, bPO = bSFull + 2, bP2 = bPO + 2, bCorrFull = bP2 + 2,
                        bCorrEmpty = bCorrFull + 2, bOFinal = bCorrEmpty + 2, bDrain = bOFinal + 2,
-                       bTaskFull = bDrain + 1, bTaskEmpty = bTaskFull + 2, bClc = bTaskEmpty + 2;
-  static constexpr int kNumBars = bClc + 1;
+                       bTaskFull = bDrain + 1, bTaskEmpty = bTaskFull + 2, bClc = bTaskEmpty + 2,
+                       bOstReady = bClc + 1, bOstFree = bOstReady + 1;
+  static constexpr int kNumBars = bOstFree + 1;
   static constexpr int kMailOff = kBarOff + ((kNumBars * 8 + 127) / 128) * 128;
   static constexpr int kMiscOff = kMailOff + 2 * kBlockM * 4;  // tmem slot, abort flags, task ring
   static constexpr int kClcOff = kMiscOff + 64;                 // 16-byte launch-control response
@@ -344,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase + L::kQOff;
   const uint32_t sKV = sbase + L::kKVOff;
+  const uint32_t sOst = sbase + L::kOstOff;
   const uint32_t sBar = sbase + L::kBarOff;
   float* mail = reinterpret_cast<float*>(smem + L::kMailOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
@@ -381,12 +385,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       mbar_init(bar(L::bTaskEmpty + i), kTaskConsumerWarps);
     }
     mbar_init(bar(L::bClc), 1);
+    mbar_init(bar(L::bOstReady), kBlockM);
+    mbar_init(bar(L::bOstFree), 1);
     fence_mbar_init();
   }
   if (warp == 13 && lane == 0) {
     prefetch_tmap(&p.tm_q);
     prefetch_tmap(&p.tm_k);
     prefetch_tmap(&p.tm_v);
+    prefetch_tmap(&p.tm_o);
   }
   if (warp == 12) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -802,6 +809,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     Tracer tr;
     tr.init(p, 4, r == 0);
     uint32_t cf_par = 0, of_par = 0;  // bit t: parity of the next wait on corr_full[t] / o_final[t]
+    uint32_t ost_n = 0;               // uses of the O staging tile so far
     bool ok = true;
     Task tk;
     // O_0 and O_1 are free for the first task's first PV; later tasks get this
@@ -858,23 +866,64 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         tr.rec(kEvEpiStart + t, -1);
         tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        const int row = tk.m * kTaskRows + t * kBlockM + r;
-        const bool valid = row < tk.len && tk.tok0 + row < p.total_tokens;
-        __nv_bfloat16* orow = p.o + ((size_t)(tk.tok0 + row) * p.H + tk.h) * D;
+        const int tile_row0 = tk.m * kTaskRows + t * kBlockM;
+        const int row = tile_row0 + r;
         const uint32_t tO = tmem + lane_base + L::col_o(t);
+        const bool full_tile = tile_row0 + kBlockM <= tk.len && tk.tok0 + tile_row0 + kBlockM <= p.total_tokens;
+        if (full_tile) {
+          // Stage the tile in shared memory in the TMA's 128-byte-swizzled layout
+          // (16-byte unit k of row r sits at unit k ^ (r % 8)), then one thread
+          // stores it with the TMA ("Flash Attention 4", section "Tile Primitive 数据流":
+          // O -> registers -> SMEM -> TMA store).
+          if (!w.wait(bar(L::bOstFree), (ost_n & 1) ^ 1, L::bOstFree, -1)) { ok = false; break; }
+          const uint32_t row_base = sOst + (uint32_t)r * 128u;
 #pragma unroll 1
-        for (int c = 0; c < D / 16; ++c) {
-          uint32_t u[16];
-          tmem_ld16(tO + c * 16, u);
-          tmem_wait_ld();
-          uint32_t pk[8];
+          for (int c = 0; c < D / 16; ++c) {
+            uint32_t u[16];
+            tmem_ld16(tO + c * 16, u);
+            tmem_wait_ld();
+            uint32_t pk[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            pk[e] = pack_bf16x2(__uint_as_float(u[2 * e]) * inv, __uint_as_float(u[2 * e + 1]) * inv);
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 16);
-            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            for (int e = 0; e < 8; ++e)
+              pk[e] = pack_bf16x2(__uint_as_float(u[2 * e]) * inv, __uint_as_float(u[2 * e + 1]) * inv);
+            const uint32_t slab = row_base + (uint32_t)(c >> 2) * L::kSlabBytes;
+            const uint32_t k0 = (uint32_t)(c & 3) * 2;
+            st_shared_v4(slab + (((k0 + 0) ^ (r & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
+            st_shared_v4(slab + (((k0 + 1) ^ (r & 7)) << 4), pk[4], pk[5], pk[6], pk[7]);
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(bar(L::bOstReady));
+          if (warp == 8) {
+            if (!w.wait(bar(L::bOstReady), ost_n & 1, L::bOstReady, -1)) { ok = false; break; }
+            if (lane == 0) {
+#pragma unroll
+              for (int c = 0; c < L::kHalves; ++c)
+                tma_store_3d(&p.tm_o, sOst + c * L::kSlabBytes, c * 64, tk.tok0 + tile_row0, tk.h);
+              bulk_commit();
+              bulk_wait_read_all();
+              mbar_arrive(bar(L::bOstFree));
+            }
+            __syncwarp();
+          }
+          ++ost_n;
+        } else {
+          // ragged tile: per-row stores, nothing past the sequence or the tensor
+          const bool valid = row < tk.len && tk.tok0 + row < p.total_tokens;
+          __nv_bfloat16* orow = p.o + ((size_t)(tk.tok0 + row) * p.H + tk.h) * D;
+#pragma unroll 1
+          for (int c = 0; c < D / 16; ++c) {
+            uint32_t u[16];
+            tmem_ld16(tO + c * 16, u);
+            tmem_wait_ld();
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              pk[e] = pack_bf16x2(__uint_as_float(u[2 * e]) * inv, __uint_as_float(u[2 * e + 1]) * inv);
+            if (valid) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + c * 16);
+              dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
           }
         }
         tr.rec(kEvEpiEnd + t, -1);
@@ -883,6 +932,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       }
     }
   }
+
+  // the TMA stores of O must complete (and stop reading shared memory) before exit
+  if (warp == 8 && lane == 0) bulk_wait_all();
 
   // ---- teardown: every role has returned; release tensor memory
   __syncwarp();  // lanes that skipped a single-thread role wait for lane 0
