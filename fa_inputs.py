@@ -1,7 +1,7 @@
-"""Seeded synthetic inputs for attention forward: Q, K, V as bf16 bit patterns.
+"""Seeded synthetic inputs for attention forward: Q, K, V as bf16 or fp16 bit patterns.
 
 This module is shared by the tests, ``bench.py`` and ``__graft_entry__.smoke()``.
-It draws random numbers, rounds them to bf16 and builds ``cu_seqlens``; it holds
+It draws random numbers, rounds them to bf16 or fp16 and builds ``cu_seqlens``; it holds
 none of the attention arithmetic, so both the CUDA path and the oracle can take
 their inputs from here without sharing any of the method's code.
 
@@ -15,7 +15,11 @@ Recipe (the same bytes go to the GPU and to the oracle):
   key rows, drawn without replacement, are multiplied by 8. Both factors are
   powers of two, so the scaled values are still exact bf16 numbers;
 * varlen: sequence lengths are uniform integers in [lo, hi] (inclusive) drawn
-  before Q, K, V from the same generator, packed as [T, H, d].
+  before Q, K, V from the same generator, packed as [T, H, d];
+* grouped-query attention: K and V have H_kv heads (H a multiple of H_kv); the
+  draws are the same with the K/V shapes changed;
+* fp16 inputs: the same float32 draws rounded to IEEE binary16 (numpy's
+  correctly rounded float32 -> float16 conversion, ties to even).
 """
 from __future__ import annotations
 
@@ -48,8 +52,30 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (b.astype(np.uint32) << 16).view(np.float32)
 
 
+def f32_to_f16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to IEEE fp16 (round to nearest, ties to even); return uint16 bits."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def f16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """Widen fp16 bit patterns (uint16) to float32 exactly."""
+    return np.ascontiguousarray(b, dtype=np.uint16).view(np.float16).astype(np.float32)
+
+
+def bits_to_f32(b: np.ndarray, dtype: str) -> np.ndarray:
+    return f16_bits_to_f32(b) if dtype == "f16" else bf16_bits_to_f32(b)
+
+
+def f32_to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
+    return f32_to_f16_bits(x) if dtype == "f16" else f32_to_bf16_bits(x)
+
+
+def _normal(rng: np.random.Generator, shape, dtype: str = "bf16") -> np.ndarray:
+    return f32_to_bits(rng.standard_normal(size=shape, dtype=np.float32), dtype)
+
+
 def _normal_bf16(rng: np.random.Generator, shape) -> np.ndarray:
-    return f32_to_bf16_bits(rng.standard_normal(size=shape, dtype=np.float32))
+    return _normal(rng, shape, "bf16")
 
 
 @dataclass
@@ -67,10 +93,14 @@ class Workload:
     varlen_lo: int = 0
     varlen_hi: int = 0
     scale: float = field(default=float("nan"))
+    Hkv: int = 0                  # K/V heads (0: the same as H)
+    dtype: str = "bf16"           # element type of Q, K, V and O: "bf16" or "f16"
 
     def __post_init__(self):
         if math.isnan(self.scale):
             self.scale = 1.0 / math.sqrt(self.d)
+        if self.Hkv == 0:
+            self.Hkv = self.H
 
     @property
     def varlen(self) -> bool:
@@ -89,56 +119,74 @@ WORKLOADS = {
                                           seed=20265, varlen_seqs=8, varlen_lo=512, varlen_hi=8192),
 }
 
+# Grouped-query attention and fp16 inputs ("Flash Attention 4", sections "GQA 支持"
+# and "编译与验证": 32 query heads over 8 K/V heads, fp16, non-causal, N = 1024), and
+# the same grouping at the size of the long causal workloads.
+WORKLOADS.update({
+    "g1_gqa_b1h32kv8n1024d128_f16": Workload("g1_gqa_b1h32kv8n1024d128_f16", B=1, H=32, N=1024, d=128,
+                                             causal=False, seed=20266, Hkv=8, dtype="f16"),
+    "g2_gqa_b4h32kv8n4096d128_causal": Workload("g2_gqa_b4h32kv8n4096d128_causal", B=4, H=32, N=4096, d=128,
+                                                causal=True, seed=20267, Hkv=8),
+    "g3_gqa_varlen8_h32kv4d128_causal_f16": Workload("g3_gqa_varlen8_h32kv4d128_causal_f16", B=1, H=32, N=0,
+                                                     d=128, causal=True, seed=20268, varlen_seqs=8,
+                                                     varlen_lo=512, varlen_hi=8192, Hkv=4, dtype="f16"),
+})
+
 
 def make_qkv(B: int, N: int, H: int, d: int, seed: int, spiky: bool = False,
-             Nkv: int | None = None):
-    """Q [B,N,H,d], K and V [B,Nkv,H,d] as bf16 bit patterns (uint16)."""
+             Nkv: int | None = None, Hkv: int | None = None, dtype: str = "bf16"):
+    """Q [B,N,H,d], K and V [B,Nkv,Hkv,d] as bf16 or fp16 bit patterns (uint16)."""
     Nkv = N if Nkv is None else Nkv
+    Hkv = H if Hkv is None else Hkv
     rng = np.random.Generator(np.random.PCG64(seed))
-    q = _normal_bf16(rng, (B, N, H, d))
-    k = _normal_bf16(rng, (B, Nkv, H, d))
-    v = _normal_bf16(rng, (B, Nkv, H, d))
+    q = _normal(rng, (B, N, H, d), dtype)
+    k = _normal(rng, (B, Nkv, Hkv, d), dtype)
+    v = _normal(rng, (B, Nkv, Hkv, d), dtype)
     if spiky:
-        q = f32_to_bf16_bits(bf16_bits_to_f32(q) * np.float32(4.0))
-        kf = bf16_bits_to_f32(k)
+        q = f32_to_bits(bits_to_f32(q, dtype) * np.float32(4.0), dtype)
+        kf = bits_to_f32(k, dtype)
         n_spike = int(math.ceil(0.01 * Nkv))
         for b in range(B):
-            for h in range(H):
+            for h in range(Hkv):
                 rows = rng.choice(Nkv, size=n_spike, replace=False)
                 kf[b, rows, h, :] *= np.float32(8.0)
-        k = f32_to_bf16_bits(kf)
+        k = f32_to_bits(kf, dtype)
     return q, k, v
 
 
-def make_varlen(num_seqs: int, lo: int, hi: int, H: int, d: int, seed: int):
-    """Packed variable-length batch: (lengths, cu_seqlens int32 [S+1], q, k, v [T,H,d])."""
+def make_varlen(num_seqs: int, lo: int, hi: int, H: int, d: int, seed: int, Hkv: int | None = None,
+                dtype: str = "bf16"):
+    """Packed variable-length batch: (lengths, cu_seqlens int32 [S+1], q [T,H,d], k, v [T,Hkv,d])."""
     rng = np.random.Generator(np.random.PCG64(seed))
     lengths = rng.integers(lo, hi + 1, size=num_seqs).astype(np.int64)
-    return _pack_varlen(rng, lengths, H, d)
+    return _pack_varlen(rng, lengths, H, d, Hkv, dtype)
 
 
-def make_varlen_from_lengths(lengths, H: int, d: int, seed: int):
+def make_varlen_from_lengths(lengths, H: int, d: int, seed: int, Hkv: int | None = None,
+                             dtype: str = "bf16"):
     """Packed batch with the given sequence lengths (zero-length sequences allowed)."""
     rng = np.random.Generator(np.random.PCG64(seed))
-    return _pack_varlen(rng, np.asarray(lengths, dtype=np.int64), H, d)
+    return _pack_varlen(rng, np.asarray(lengths, dtype=np.int64), H, d, Hkv, dtype)
 
 
-def _pack_varlen(rng, lengths, H, d):
+def _pack_varlen(rng, lengths, H, d, Hkv=None, dtype="bf16"):
+    Hkv = H if Hkv is None else Hkv
     cu = np.zeros(len(lengths) + 1, dtype=np.int32)
     cu[1:] = np.cumsum(lengths)
     T = int(cu[-1])
-    q = _normal_bf16(rng, (T, H, d))
-    k = _normal_bf16(rng, (T, H, d))
-    v = _normal_bf16(rng, (T, H, d))
+    q = _normal(rng, (T, H, d), dtype)
+    k = _normal(rng, (T, Hkv, d), dtype)
+    v = _normal(rng, (T, Hkv, d), dtype)
     return lengths, cu, q, k, v
 
 
 def make_workload(w: Workload):
     """Inputs of a named workload: dict with q, k, v (and lengths, cu_seqlens for varlen)."""
     if w.varlen:
-        lengths, cu, q, k, v = make_varlen(w.varlen_seqs, w.varlen_lo, w.varlen_hi, w.H, w.d, w.seed)
+        lengths, cu, q, k, v = make_varlen(w.varlen_seqs, w.varlen_lo, w.varlen_hi, w.H, w.d, w.seed,
+                                           Hkv=w.Hkv, dtype=w.dtype)
         return {"q": q, "k": k, "v": v, "lengths": lengths, "cu_seqlens": cu}
-    q, k, v = make_qkv(w.B, w.N, w.H, w.d, w.seed, spiky=w.spiky)
+    q, k, v = make_qkv(w.B, w.N, w.H, w.d, w.seed, spiky=w.spiky, Hkv=w.Hkv, dtype=w.dtype)
     return {"q": q, "k": k, "v": v}
 
 

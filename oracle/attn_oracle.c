@@ -30,6 +30,14 @@
  *    "FlashAttention：一次前向计算" (qingsen), section on causal masking, fig. 12.
  *  - "FlashAttention：一次前向计算", section "先看 attention 最后要得到什么":
  *    S = QK^T, P = softmax_row(s*S), O = PV, with an explicit scale s.
+ *  - "Flash Attention 4", section "GQA 支持" (grouped-query attention): with
+ *    H query heads and H_kv key/value heads (H a multiple of H_kv), query head h
+ *    reads key/value head h / (H / H_kv): the group of H / H_kv consecutive
+ *    query heads kv*G .. kv*G + G - 1 shares K/V head kv. H_kv = H is plain
+ *    multi-head attention.
+ *  - Element types: inputs are bf16 or IEEE fp16 bit patterns ("Flash
+ *    Attention 4", section "编译与验证", runs the kernel on fp16 tensors);
+ *    each is widened exactly to double before any arithmetic.
  *
  * The computation is two passes per row (max, then the exponentials and the
  * weighted sum of V); no blocking, no delayed rescaling, no reordering. Work
@@ -37,10 +45,11 @@
  * nothing in any row's arithmetic.
  *
  * Layouts (row-major, elements):
- *   fixed length:  q [B, Nq, H, d], k and v [B, Nkv, H, d]  (bf16 bit patterns)
+ *   fixed length:  q [B, Nq, H, d], k and v [B, Nkv, H_kv, d]  (16-bit patterns)
  *                  o [B, Nq, H, d] (double), lse [B, H, Nq] (double)
- *   varlen:        q, k, v [T, H, d] packed by cu_seqlens (bf16 bit patterns)
+ *   varlen:        q [T, H, d], k and v [T, H_kv, d] packed by cu_seqlens
  *                  o [T, H, d] (double), lse [H, T] (double)
+ * dtype: ORACLE_BF16 (0) or ORACLE_F16 (1), the type of all of q, k, v.
  */
 #include <math.h>
 #include <pthread.h>
@@ -48,12 +57,32 @@
 #include <stdlib.h>
 #include <string.h>
 
+enum { ORACLE_BF16 = 0, ORACLE_F16 = 1 };
+
+/* bf16 is the upper half of an IEEE binary32 word. */
 static double bf16_to_double(uint16_t h)
 {
     uint32_t u = (uint32_t)h << 16;
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* IEEE binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+ * Subnormals are fraction * 2^-24; normal numbers (1024 + fraction) * 2^(e-25). */
+static double f16_to_double(uint16_t h)
+{
+    const int sign = h >> 15, e = (h >> 10) & 31, f = h & 1023;
+    double x;
+    if (e == 0) x = ldexp((double)f, -24);
+    else if (e == 31) x = f ? NAN : INFINITY;
+    else x = ldexp((double)(1024 + f), e - 25);
+    return sign ? -x : x;
+}
+
+static double to_double(uint16_t h, int dtype)
+{
+    return dtype == ORACLE_F16 ? f16_to_double(h) : bf16_to_double(h);
 }
 
 /* One query row against the key/value rows [0, nvalid) of one head.
@@ -108,8 +137,9 @@ static int64_t valid_keys(int64_t i, int64_t nkv, int causal, int64_t off)
 /* A "head problem" is one (sequence, head): rows of Q, K, V addressed by a
  * base pointer and a row stride (elements).                                 */
 typedef struct {
-    const uint16_t *q, *k, *v;   /* first row of this head                   */
-    int64_t row_stride;          /* elements between consecutive rows        */
+    const uint16_t *q, *k, *v;   /* first row of this head (k, v: its K/V head) */
+    int64_t row_stride;          /* elements between consecutive q / o rows  */
+    int64_t kv_row_stride;       /* elements between consecutive k / v rows */
     int64_t nq, nkv, off;
     double *o;                   /* first output row (same stride as q)      */
     double *lse;                 /* lse of row 0; rows are contiguous        */
@@ -122,11 +152,13 @@ typedef struct {
     int64_t d;
     double scale;
     int causal;
+    int dtype;
     int64_t next;                /* atomic work counter                      */
     int failed;
 } pool_t;
 
-static void run_item(const work_item *w, int64_t d, double scale, int causal, int *failed)
+static void run_item(const work_item *w, int64_t d, double scale, int causal, int dtype,
+                     int *failed)
 {
     int64_t i, c, j;
     /* keys needed by the last row of the item */
@@ -146,11 +178,11 @@ static void run_item(const work_item *w, int64_t d, double scale, int causal, in
     }
     for (j = 0; j < need; ++j)
         for (c = 0; c < d; ++c) {
-            kd[j * d + c] = bf16_to_double(w->k[j * w->row_stride + c]);
-            vd[j * d + c] = bf16_to_double(w->v[j * w->row_stride + c]);
+            kd[j * d + c] = to_double(w->k[j * w->kv_row_stride + c], dtype);
+            vd[j * d + c] = to_double(w->v[j * w->kv_row_stride + c], dtype);
         }
     for (i = w->row_begin; i < w->row_end; ++i) {
-        for (c = 0; c < d; ++c) qd[c] = bf16_to_double(w->q[i * w->row_stride + c]);
+        for (c = 0; c < d; ++c) qd[c] = to_double(w->q[i * w->row_stride + c], dtype);
         attend_row(qd, kd, vd, valid_keys(i, w->nkv, causal, w->off), d, scale, t,
                    w->o + i * w->row_stride, w->lse + i);
     }
@@ -163,17 +195,17 @@ static void *pool_worker(void *arg)
     for (;;) {
         int64_t idx = __atomic_fetch_add(&p->next, 1, __ATOMIC_RELAXED);
         if (idx >= p->n_items) break;
-        run_item(&p->items[idx], p->d, p->scale, p->causal, &p->failed);
+        run_item(&p->items[idx], p->d, p->scale, p->causal, p->dtype, &p->failed);
     }
     return NULL;
 }
 
 static int run_pool(const work_item *items, int64_t n_items, int64_t d, double scale,
-                    int causal, int nthreads)
+                    int causal, int dtype, int nthreads)
 {
     pool_t p;
     p.items = items; p.n_items = n_items; p.d = d; p.scale = scale;
-    p.causal = causal; p.next = 0; p.failed = 0;
+    p.causal = causal; p.dtype = dtype; p.next = 0; p.failed = 0;
     if (nthreads < 1) nthreads = 1;
     if (nthreads > 1024) nthreads = 1024;
     if ((int64_t)nthreads > n_items) nthreads = (int)(n_items > 0 ? n_items : 1);
@@ -192,15 +224,24 @@ static int run_pool(const work_item *items, int64_t n_items, int64_t d, double s
 
 #define ROWS_PER_ITEM 64
 
+/* Valid head counts and element type. */
+static int heads_ok(int64_t H, int64_t Hkv, int dtype)
+{
+    return H >= 0 && Hkv >= 1 && (H == 0 || H % Hkv == 0) &&
+           (dtype == ORACLE_BF16 || dtype == ORACLE_F16);
+}
+
 /* Fixed-length batch. Returns 0 on success, -1 on bad arguments, -2 on
  * allocation failure. off = Nkv - Nq gives the bottom-right aligned mask. */
 int oracle_attention_bshd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                          int64_t B, int64_t H, int64_t Nq, int64_t Nkv, int64_t d,
-                          double scale, int causal, int64_t off,
+                          int64_t B, int64_t H, int64_t Hkv, int64_t Nq, int64_t Nkv, int64_t d,
+                          int dtype, double scale, int causal, int64_t off,
                           double *o, double *lse, int nthreads)
 {
-    if (!q || !k || !v || !o || !lse || B < 0 || H < 0 || Nq < 0 || Nkv < 0 || d <= 0)
+    if (!q || !k || !v || !o || !lse || B < 0 || !heads_ok(H, Hkv, dtype) || Nq < 0 ||
+        Nkv < 0 || d <= 0)
         return -1;
+    const int64_t G = H > 0 ? H / Hkv : 1;
     int64_t chunks = (Nq + ROWS_PER_ITEM - 1) / ROWS_PER_ITEM;
     int64_t n_items = B * H * chunks;
     if (n_items == 0) return 0;
@@ -212,16 +253,17 @@ int oracle_attention_bshd(const uint16_t *q, const uint16_t *k, const uint16_t *
             for (int64_t ch = 0; ch < chunks; ++ch) {
                 work_item *w = &items[n++];
                 w->q = q + (b * Nq * H + h) * d;
-                w->k = k + (b * Nkv * H + h) * d;
-                w->v = v + (b * Nkv * H + h) * d;
+                w->k = k + (b * Nkv * Hkv + h / G) * d;
+                w->v = v + (b * Nkv * Hkv + h / G) * d;
                 w->row_stride = H * d;
+                w->kv_row_stride = Hkv * d;
                 w->nq = Nq; w->nkv = Nkv; w->off = off;
                 w->o = o + (b * Nq * H + h) * d;
                 w->lse = lse + (b * H + h) * Nq;
                 w->row_begin = ch * ROWS_PER_ITEM;
                 w->row_end = w->row_begin + ROWS_PER_ITEM < Nq ? w->row_begin + ROWS_PER_ITEM : Nq;
             }
-    int rc = run_pool(items, n_items, d, scale, causal, nthreads);
+    int rc = run_pool(items, n_items, d, scale, causal, dtype, nthreads);
     free(items);
     return rc;
 }
@@ -230,11 +272,13 @@ int oracle_attention_bshd(const uint16_t *q, const uint16_t *k, const uint16_t *
  * (self-attention, N_q = N_kv = length, so off = 0). lse is [H, T]. */
 int oracle_attention_varlen(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                             const int32_t *cu_seqlens, int64_t num_seqs,
-                            int64_t H, int64_t d, double scale, int causal,
+                            int64_t H, int64_t Hkv, int64_t d, int dtype, double scale, int causal,
                             double *o, double *lse, int nthreads)
 {
-    if (!q || !k || !v || !o || !lse || !cu_seqlens || num_seqs < 0 || H < 0 || d <= 0)
+    if (!q || !k || !v || !o || !lse || !cu_seqlens || num_seqs < 0 || !heads_ok(H, Hkv, dtype) ||
+        d <= 0)
         return -1;
+    const int64_t G = H > 0 ? H / Hkv : 1;
     if (cu_seqlens[0] != 0) return -1;
     int64_t T = cu_seqlens[num_seqs];
     int64_t n_items = 0;
@@ -255,9 +299,10 @@ int oracle_attention_varlen(const uint16_t *q, const uint16_t *k, const uint16_t
             for (int64_t ch = 0; ch < chunks; ++ch) {
                 work_item *w = &items[n++];
                 w->q = q + (start * H + h) * d;
-                w->k = k + (start * H + h) * d;
-                w->v = v + (start * H + h) * d;
+                w->k = k + (start * Hkv + h / G) * d;
+                w->v = v + (start * Hkv + h / G) * d;
                 w->row_stride = H * d;
+                w->kv_row_stride = Hkv * d;
                 w->nq = L; w->nkv = L; w->off = 0;
                 w->o = o + (start * H + h) * d;
                 w->lse = lse + h * T + start;
@@ -265,7 +310,7 @@ int oracle_attention_varlen(const uint16_t *q, const uint16_t *k, const uint16_t
                 w->row_end = w->row_begin + ROWS_PER_ITEM < L ? w->row_begin + ROWS_PER_ITEM : L;
             }
     }
-    int rc = run_pool(items, n_items, d, scale, causal, nthreads);
+    int rc = run_pool(items, n_items, d, scale, causal, dtype, nthreads);
     free(items);
     return rc;
 }
@@ -276,9 +321,10 @@ int oracle_attention_varlen(const uint16_t *q, const uint16_t *k, const uint16_t
  * o_rows [n_rows, d], lse_rows [n_rows].                                     */
 typedef struct {
     const uint16_t *q, *k, *v;
-    int64_t H, Nq, Nkv, d, off;
+    int64_t H, Hkv, Nq, Nkv, d, off;
     double scale;
     int causal;
+    int dtype;
     const int64_t *rows;   /* triples (b,h,i), or (seq-start, h, local row, L) quads for varlen */
     int varlen;
     const int32_t *cu;
@@ -300,13 +346,13 @@ static void *rows_worker(void *arg)
         int64_t r = __atomic_fetch_add(&J->next, 1, __ATOMIC_RELAXED);
         if (r >= J->n_rows) break;
         const uint16_t *qb, *kb, *vb;
-        int64_t i, nvalid, stride = J->H * d;
+        int64_t i, nvalid, stride = J->H * d, kv_stride = J->Hkv * d, G = J->H / J->Hkv;
         if (!J->varlen) {
             int64_t b = J->rows[3 * r], h = J->rows[3 * r + 1];
             i = J->rows[3 * r + 2];
             qb = J->q + (b * J->Nq * J->H + h) * d;
-            kb = J->k + (b * J->Nkv * J->H + h) * d;
-            vb = J->v + (b * J->Nkv * J->H + h) * d;
+            kb = J->k + (b * J->Nkv * J->Hkv + h / G) * d;
+            vb = J->v + (b * J->Nkv * J->Hkv + h / G) * d;
             nvalid = valid_keys(i, J->Nkv, J->causal, J->off);
         } else {
             /* rows: pairs (h, token); find the token's sequence */
@@ -319,8 +365,8 @@ static void *rows_worker(void *arg)
             int64_t start = J->cu[lo], L = (int64_t)J->cu[lo + 1] - start;
             i = tok - start;
             qb = J->q + (start * J->H + h) * d;
-            kb = J->k + (start * J->H + h) * d;
-            vb = J->v + (start * J->H + h) * d;
+            kb = J->k + (start * J->Hkv + h / G) * d;
+            vb = J->v + (start * J->Hkv + h / G) * d;
             nvalid = valid_keys(i, L, J->causal, 0);
         }
         if (nvalid > cap) {
@@ -333,10 +379,10 @@ static void *rows_worker(void *arg)
         }
         for (int64_t j = 0; j < nvalid; ++j)
             for (int64_t c = 0; c < d; ++c) {
-                kd[j * d + c] = bf16_to_double(kb[j * stride + c]);
-                vd[j * d + c] = bf16_to_double(vb[j * stride + c]);
+                kd[j * d + c] = to_double(kb[j * kv_stride + c], J->dtype);
+                vd[j * d + c] = to_double(vb[j * kv_stride + c], J->dtype);
             }
-        for (int64_t c = 0; c < d; ++c) qd[c] = bf16_to_double(qb[i * stride + c]);
+        for (int64_t c = 0; c < d; ++c) qd[c] = to_double(qb[i * stride + c], J->dtype);
         attend_row(qd, kd, vd, nvalid, d, J->scale, t ? t : qd, J->o_rows + r * d, J->lse_rows + r);
     }
     free(qd); free(kd); free(vd); free(t);
@@ -361,20 +407,22 @@ static int run_rows(rows_job *J, int nthreads)
 }
 
 int oracle_attention_rows_bshd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                               int64_t B, int64_t H, int64_t Nq, int64_t Nkv, int64_t d,
-                               double scale, int causal, int64_t off,
+                               int64_t B, int64_t H, int64_t Hkv, int64_t Nq, int64_t Nkv,
+                               int64_t d, int dtype, double scale, int causal, int64_t off,
                                const int64_t *rows, int64_t n_rows,
                                double *o_rows, double *lse_rows, int nthreads)
 {
-    if (!q || !k || !v || !rows || !o_rows || !lse_rows || d <= 0 || n_rows < 0) return -1;
+    if (!q || !k || !v || !rows || !o_rows || !lse_rows || d <= 0 || n_rows < 0 ||
+        !heads_ok(H, Hkv, dtype))
+        return -1;
     for (int64_t r = 0; r < n_rows; ++r) {
         int64_t b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
         if (b < 0 || b >= B || h < 0 || h >= H || i < 0 || i >= Nq) return -1;
     }
     rows_job J;
     memset(&J, 0, sizeof J);
-    J.q = q; J.k = k; J.v = v; J.H = H; J.Nq = Nq; J.Nkv = Nkv; J.d = d; J.off = off;
-    J.scale = scale; J.causal = causal; J.rows = rows; J.varlen = 0;
+    J.q = q; J.k = k; J.v = v; J.H = H; J.Hkv = Hkv; J.Nq = Nq; J.Nkv = Nkv; J.d = d; J.off = off;
+    J.scale = scale; J.causal = causal; J.dtype = dtype; J.rows = rows; J.varlen = 0;
     J.n_rows = n_rows; J.o_rows = o_rows; J.lse_rows = lse_rows;
     return run_rows(&J, nthreads);
 }
@@ -382,12 +430,12 @@ int oracle_attention_rows_bshd(const uint16_t *q, const uint16_t *k, const uint1
 /* rows: n_rows pairs (h, token) of the packed layout. */
 int oracle_attention_rows_varlen(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                  const int32_t *cu_seqlens, int64_t num_seqs,
-                                 int64_t H, int64_t d, double scale, int causal,
-                                 const int64_t *rows, int64_t n_rows,
+                                 int64_t H, int64_t Hkv, int64_t d, int dtype, double scale,
+                                 int causal, const int64_t *rows, int64_t n_rows,
                                  double *o_rows, double *lse_rows, int nthreads)
 {
     if (!q || !k || !v || !cu_seqlens || !rows || !o_rows || !lse_rows || d <= 0 ||
-        num_seqs <= 0 || n_rows < 0)
+        num_seqs <= 0 || n_rows < 0 || !heads_ok(H, Hkv, dtype))
         return -1;
     int64_t T = cu_seqlens[num_seqs];
     for (int64_t r = 0; r < n_rows; ++r) {
@@ -396,8 +444,9 @@ int oracle_attention_rows_varlen(const uint16_t *q, const uint16_t *k, const uin
     }
     rows_job J;
     memset(&J, 0, sizeof J);
-    J.q = q; J.k = k; J.v = v; J.H = H; J.Nq = num_seqs; J.d = d;
-    J.scale = scale; J.causal = causal; J.rows = rows; J.varlen = 1; J.cu = cu_seqlens;
+    J.q = q; J.k = k; J.v = v; J.H = H; J.Hkv = Hkv; J.Nq = num_seqs; J.d = d;
+    J.scale = scale; J.causal = causal; J.dtype = dtype; J.rows = rows; J.varlen = 1;
+    J.cu = cu_seqlens;
     J.n_rows = n_rows; J.o_rows = o_rows; J.lse_rows = lse_rows;
     return run_rows(&J, nthreads);
 }

@@ -266,3 +266,97 @@ def test_invalid_arguments_raise():
         oracle.attention_rows(q, q, q, np.array([[0, 0, 4]]), 0.5, False)
     with pytest.raises(TypeError):
         oracle.attention(q.astype(np.float32), q, q, 0.5, False)
+
+
+# --------------------------------------------------------------------------- element types
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_every_16bit_pattern_widens_exactly(dtype):
+    """With a single key the weights are exactly 1, so O is V widened to double:
+    every one of the 65536 bit patterns (zeros, subnormals, normals, infinities,
+    NaNs) must come back as numpy's own widening of that pattern."""
+    pat = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    v = pat.reshape(1, 1, 1, -1)
+    z = np.zeros_like(v)
+    o, lse = oracle.attention(z, z, v, 0.5, False, dtype=dtype)
+    with np.errstate(invalid="ignore"):   # signalling NaN patterns widen to quiet NaNs
+        if dtype == "f16":
+            want = pat.view(np.float16).astype(np.float64)
+        else:
+            want = (pat.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    np.testing.assert_array_equal(o.reshape(-1), want)
+    assert lse.reshape(-1)[0] == 0.0
+
+
+def rand_bits_dtype(shape, seed, dtype):
+    rng = np.random.default_rng(seed)
+    return fa_inputs.f32_to_bits(rng.standard_normal(shape).astype(np.float32), dtype)
+
+
+# --------------------------------------------------------------------------- grouped-query attention
+@pytest.mark.parametrize("H,Hkv", [(6, 2), (4, 1), (8, 8)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_equals_mha_with_each_kv_head_shared_by_its_group(H, Hkv, causal):
+    """"Flash Attention 4", section "GQA 支持": the G = H / H_kv consecutive query
+    heads kv*G .. kv*G+G-1 all read K/V head kv. Giving every query head its own
+    copy of that K/V head must change nothing, bit for bit."""
+    B, N, d = 2, 37, 16
+    q = rand_bits_dtype((B, N, H, d), 50, "bf16")
+    k = rand_bits_dtype((B, N, Hkv, d), 51, "bf16")
+    v = rand_bits_dtype((B, N, Hkv, d), 52, "bf16")
+    G = H // Hkv
+    o, lse = oracle.attention(q, k, v, 0.3, causal)
+    o2, lse2 = oracle.attention(q, np.repeat(k, G, axis=2), np.repeat(v, G, axis=2), 0.3, causal)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(lse, lse2)
+    rows = np.array([[0, 0, 0], [1, H - 1, N - 1], [0, H // 2, 20]], np.int64)
+    orow, lrow = oracle.attention_rows(q, k, v, rows, 0.3, causal)
+    for r, (b, h, i) in enumerate(rows):
+        np.testing.assert_array_equal(orow[r], o[b, i, h])
+        assert lrow[r] == lse[b, h, i]
+
+
+def test_gqa_varlen_equals_mha_varlen():
+    lengths = [9, 0, 70, 1]
+    H, Hkv, d = 6, 3, 8
+    _, cu, q, k, v = fa_inputs.make_varlen_from_lengths(lengths, H, d, seed=53, Hkv=Hkv)
+    assert k.shape == (sum(lengths), Hkv, d)
+    for causal in (False, True):
+        o, lse = oracle.attention_varlen(q, k, v, cu, 0.25, causal)
+        o2, lse2 = oracle.attention_varlen(q, np.repeat(k, 2, axis=1), np.repeat(v, 2, axis=1), cu, 0.25, causal)
+        np.testing.assert_array_equal(o, o2)
+        np.testing.assert_array_equal(lse, lse2)
+        rows = np.array([[0, 0], [5, 8], [4, 9], [1, 79]], np.int64)
+        orow, lrow = oracle.attention_rows_varlen(q, k, v, cu, rows, 0.25, causal)
+        for r, (h, t) in enumerate(rows):
+            np.testing.assert_array_equal(orow[r], o[t, h])
+            assert lrow[r] == lse[h, t]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_matches_float64_sdpa(dtype, causal):
+    """The pages' own check ("编译与验证"): PyTorch SDPA with enable_gqa, here in float64."""
+    torch = pytest.importorskip("torch")
+    B, N, H, Hkv, d = 1, 96, 8, 2, 64
+    q = rand_bits_dtype((B, N, H, d), 60, dtype)
+    k = rand_bits_dtype((B, N, Hkv, d), 61, dtype)
+    v = rand_bits_dtype((B, N, Hkv, d), 62, dtype)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = oracle.attention(q, k, v, scale, causal, dtype=dtype)
+    t = lambda b: torch.from_numpy(fa_inputs.bits_to_f32(b, dtype).astype(np.float64)).permute(0, 2, 1, 3)  # noqa: E731
+    ref = torch.nn.functional.scaled_dot_product_attention(t(q), t(k), t(v), scale=scale, is_causal=causal,
+                                                           enable_gqa=True)
+    np.testing.assert_allclose(o, ref.permute(0, 2, 1, 3).numpy(), atol=1e-12, rtol=0)
+    s = torch.einsum("bhid,bhjd->bhij", t(q), t(k).repeat_interleave(H // Hkv, dim=1)) * scale
+    if causal:
+        s = s.masked_fill(torch.ones(N, N, dtype=torch.bool).triu(1), float("-inf"))
+    np.testing.assert_allclose(lse, torch.logsumexp(s, dim=-1).numpy(), atol=1e-12, rtol=0)
+
+
+def test_gqa_and_dtype_arguments_are_checked():
+    q = np.zeros((1, 4, 6, 8), np.uint16)
+    k = np.zeros((1, 4, 4, 8), np.uint16)
+    with pytest.raises(ValueError):
+        oracle.attention(q, k, k, 0.5, False)          # 6 query heads over 4 K/V heads
+    with pytest.raises(ValueError):
+        oracle.attention(q, q, q, 0.5, False, dtype="f32")
