@@ -17,26 +17,30 @@ import threading
 from . import _build
 
 __all__ = ["fa_fwd", "fa_fwd_varlen", "FaError", "set_option", "last_device_status", "library",
+           "FA_DTYPE_BF16", "FA_DTYPE_FP16",
            "selftest_mma_tile", "selftest_exp2", "selftest_wait_timeout", "varlen_schedule",
            "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
            "FA_ERR_NO_DEVICE", "FA_ERR_CAPACITY"]
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_NO_DEVICE, FA_ERR_CAPACITY = range(7)
+FA_DTYPE_BF16, FA_DTYPE_FP16 = 0, 1
 _OPTIONS = {"tau": 1, "wait_timeout_ns": 2, "persistent": 3, "exp2_emulation": 4}
 
 _vp, _ci, _cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 _SIGNATURES = {
     "fa_fwd": [_vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _cf, _ci, _vp],
+    "fa_fwd_gqa": [_vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _ci, _vp],
     "fa_fwd_varlen": [_vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _vp],
+    "fa_fwd_varlen_gqa": [_vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _ci, _vp],
     "fa_fwd_varlen_noalloc": [_vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _vp],
     "fa_error_string": [_ci],
     "fa_last_device_status": [_vp, ctypes.POINTER(ctypes.c_ulonglong)],
     "fa_set_option": [_ci, ctypes.c_double],
     "fa_version": [],
-    "fa_selftest_mma_tile": [_vp, _vp, _vp, _vp, _vp, _vp, _ci, _vp],
+    "fa_selftest_mma_tile": [_vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _vp],
     "fa_selftest_exp2": [_vp, _vp, _ci, _ci, _vp],
     "fa_selftest_wait_timeout": [ctypes.c_ulonglong, _vp],
-    "fa_varlen_schedule": [_vp, _ci, _ci, _ci, _ci, _vp, _vp, _vp],
+    "fa_varlen_schedule": [_vp, _ci, _ci, _ci, _ci, _ci, _vp, _vp, _vp],
     "fa_trace_configure": [_vp, _ci],
     "fa_trace_layout": [ctypes.POINTER(_ci), ctypes.POINTER(_ci)],
 }
@@ -97,8 +101,9 @@ def _need(t, name, dtype, ndim=None):
     torch = _torch()
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.dtype != dtype:
-        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    allowed = dtype if isinstance(dtype, tuple) else (dtype,)
+    if t.dtype not in allowed:
+        raise TypeError(f"{name} must be {' or '.join(map(str, allowed))}, got {t.dtype}")
     if not t.is_cuda:
         raise ValueError(f"{name} must be on a CUDA device")
     if not t.is_contiguous():
@@ -107,23 +112,33 @@ def _need(t, name, dtype, ndim=None):
         raise ValueError(f"{name} must have {ndim} dimensions")
 
 
+def _dtype_code(q):
+    torch = _torch()
+    _need(q, "q", (torch.bfloat16, torch.float16))
+    return FA_DTYPE_FP16 if q.dtype == torch.float16 else FA_DTYPE_BF16
+
+
 def fa_fwd(q, k, v, *, scale: float | None = None, causal: bool = False, out=None, lse=None,
            return_lse: bool = True, stream=None):
-    """Attention forward on bf16 [B, N, H, d] tensors. Returns (o, lse) or o.
+    """Attention forward: q [B, N, H, d], k and v [B, N, H_kv, d], all bf16 or all fp16.
+    Returns (o, lse) or o; o has q's shape and type.
 
-    lse is fp32 [B, H, N] (natural log of the scaled logits' sum of exponentials).
-    scale defaults to 1/sqrt(d)."""
+    H_kv < H is grouped-query attention (query head h uses K/V head h // (H // H_kv));
+    H // H_kv must be a power of two up to 128. lse is fp32 [B, H, N] (natural log
+    of the scaled logits' sum of exponentials). scale defaults to 1/sqrt(d)."""
     torch = _torch()
-    _need(q, "q", torch.bfloat16, 4)
+    code = _dtype_code(q)
+    _need(q, "q", q.dtype, 4)
     B, N, H, d = q.shape
+    Hkv = k.shape[2] if isinstance(k, torch.Tensor) and k.dim() == 4 else H
     for name, t in (("k", k), ("v", v)):
-        _need(t, name, torch.bfloat16, 4)
-        if tuple(t.shape) != (B, N, H, d):
-            raise ValueError(f"{name} must have shape {(B, N, H, d)}")
+        _need(t, name, q.dtype, 4)
+        if tuple(t.shape) != (B, N, Hkv, d):
+            raise ValueError(f"{name} must have shape {(B, N, Hkv, d)}")
     if out is None:
         out = torch.empty_like(q)
     else:
-        _need(out, "out", torch.bfloat16, 4)
+        _need(out, "out", q.dtype, 4)
         if tuple(out.shape) != (B, N, H, d):
             raise ValueError("out has the wrong shape")
     if lse is None and return_lse:
@@ -133,38 +148,40 @@ def fa_fwd(q, k, v, *, scale: float | None = None, causal: bool = False, out=Non
         if tuple(lse.shape) != (B, H, N):
             raise ValueError("lse must have shape (B, H, N)")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    st = library().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                          lse.data_ptr() if lse is not None else None, B, H, N, d, scale, int(bool(causal)),
-                          _stream_handle(stream, q.device))
+    st = library().fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                              lse.data_ptr() if lse is not None else None, B, H, Hkv, N, d, scale,
+                              int(bool(causal)), code, _stream_handle(stream, q.device))
     _check(st, "fa_fwd")
     return (out, lse) if lse is not None else out
 
 
 def fa_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, *, scale: float | None = None, causal: bool = False,
                   out=None, lse=None, return_lse: bool = True, stream=None):
-    """Packed variable-length attention forward on bf16 [T, H, d]; cu_seqlens int32 [S+1] on the device.
-    Returns (o, lse) or o; lse is fp32 [H, T]."""
+    """Packed variable-length attention forward: q [T, H, d], k and v [T, H_kv, d] (bf16 or fp16);
+    cu_seqlens int32 [S+1] on the device. Returns (o, lse) or o; lse is fp32 [H, T]."""
     torch = _torch()
-    _need(q, "q", torch.bfloat16, 3)
+    code = _dtype_code(q)
+    _need(q, "q", q.dtype, 3)
     T, H, d = q.shape
+    Hkv = k.shape[1] if isinstance(k, torch.Tensor) and k.dim() == 3 else H
     for name, t in (("k", k), ("v", v)):
-        _need(t, name, torch.bfloat16, 3)
-        if tuple(t.shape) != (T, H, d):
-            raise ValueError(f"{name} must have shape {(T, H, d)}")
+        _need(t, name, q.dtype, 3)
+        if tuple(t.shape) != (T, Hkv, d):
+            raise ValueError(f"{name} must have shape {(T, Hkv, d)}")
     _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
     if out is None:
         out = torch.empty_like(q)
     else:
-        _need(out, "out", torch.bfloat16, 3)
+        _need(out, "out", q.dtype, 3)
     if lse is None and return_lse:
         lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
     elif lse is not None:
         _need(lse, "lse", torch.float32, 2)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    st = library().fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                                 lse.data_ptr() if lse is not None else None, cu_seqlens.data_ptr(),
-                                 cu_seqlens.numel() - 1, T, int(max_seqlen), H, d, scale, int(bool(causal)),
-                                 _stream_handle(stream, q.device))
+    st = library().fa_fwd_varlen_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                     lse.data_ptr() if lse is not None else None, cu_seqlens.data_ptr(),
+                                     cu_seqlens.numel() - 1, T, int(max_seqlen), H, Hkv, d, scale,
+                                     int(bool(causal)), code, _stream_handle(stream, q.device))
     _check(st, "fa_fwd_varlen")
     return (out, lse) if lse is not None else out
 
@@ -178,15 +195,17 @@ def last_device_status(stream=None):
 
 
 def selftest_mma_tile(q, k, v, p, stream=None):
-    """One tile through the MMA plumbing: returns (S = Q K^T fp32 [128,128], O = P V fp32 [128,d])."""
+    """One tile through the MMA plumbing: returns (S = Q K^T fp32 [128,128], O = P V fp32 [128,d]).
+    q, k, v, p: all bf16 or all fp16."""
     torch = _torch()
+    code = _dtype_code(q)
     for name, t in (("q", q), ("k", k), ("v", v), ("p", p)):
-        _need(t, name, torch.bfloat16, 2)
+        _need(t, name, q.dtype, 2)
     d = q.shape[1]
     s = torch.empty((128, 128), dtype=torch.float32, device=q.device)
     o = torch.empty((128, d), dtype=torch.float32, device=q.device)
     _check(library().fa_selftest_mma_tile(q.data_ptr(), k.data_ptr(), v.data_ptr(), p.data_ptr(), s.data_ptr(),
-                                          o.data_ptr(), d, _stream_handle(stream, q.device)),
+                                          o.data_ptr(), d, code, _stream_handle(stream, q.device)),
            "fa_selftest_mma_tile")
     return s, o
 
@@ -207,13 +226,15 @@ def selftest_wait_timeout(timeout_ns: int, stream=None) -> int:
     return library().fa_selftest_wait_timeout(int(timeout_ns), _stream_handle(stream, torch.device("cuda")))
 
 
-def varlen_schedule(cu_seqlens, H: int, causal: bool, capacity: int, stream=None):
-    """The longest-first varlen tile list: (tasks int32 [count, 4] of (seq, head, m_block, cost), count)."""
+def varlen_schedule(cu_seqlens, H: int, causal: bool, capacity: int, stream=None, group: int = 1):
+    """The longest-first varlen tile list: (tasks int32 [count, 4] of (seq, kv head, m_block, cost), count).
+    H is the number of K/V heads; group the query heads per K/V head."""
     torch = _torch()
     _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
     tasks = torch.full((max(capacity, 1), 4), -1, dtype=torch.int32, device=cu_seqlens.device)
     count = torch.zeros(1, dtype=torch.int32, device=cu_seqlens.device)
-    _check(library().fa_varlen_schedule(cu_seqlens.data_ptr(), cu_seqlens.numel() - 1, H, int(bool(causal)),
+    _check(library().fa_varlen_schedule(cu_seqlens.data_ptr(), cu_seqlens.numel() - 1, H, int(group),
+                                        int(bool(causal)),
                                         capacity, tasks.data_ptr(), count.data_ptr(),
                                         _stream_handle(stream, cu_seqlens.device)), "fa_varlen_schedule")
     n = int(count.item())

@@ -54,8 +54,8 @@ struct DevInfo {
   bool supported = false;
   int sm_count = 0;
   long long l2_bytes = 0;
-  bool attr_done[2][2][2] = {};
-  int attr_status[2][2][2] = {};
+  bool attr_done[2][2][2][2] = {};   // [d == 128][causal][emulation][fp16]
+  int attr_status[2][2][2][2] = {};
 };
 constexpr int kMaxDevices = 64;
 DevInfo g_dev[kMaxDevices];
@@ -87,31 +87,59 @@ int device_info(DevInfo** out) {
   return d.supported ? FA_OK : FA_ERR_UNSUPPORTED;
 }
 
-// 3-D map over a [tokens, H, d] bf16 tensor: x = d (contiguous), y = token, z = head.
-// Box = 64 x 128 x 1 (one 128-byte slab of 128 rows), 128-byte swizzle, OOB rows read 0.
-int make_map(CUtensorMap* m, const void* base, long long tokens, int H, int d) {
+// 3-D map over a [tokens, heads, d] tensor of 16-bit elements: x = d (contiguous),
+// y = head, z = token. Box = 64 x box_heads x (128 / box_heads): one 128-byte
+// slab of a 128-row tile whose row r is token r / box_heads, head r % box_heads
+// (box_heads = G packs the query heads of one K/V group; K and V use 1).
+// 128-byte swizzle; rows outside the tensor read as 0.
+int make_map(CUtensorMap* m, const void* base, long long tokens, int heads, int d, int box_heads, bool f16) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return FA_ERR_CUDA;
-  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)tokens, (cuuint64_t)H};
-  const cuuint64_t strides[2] = {(cuuint64_t)H * d * 2, (cuuint64_t)d * 2};
-  const cuuint32_t box[3] = {64, (cuuint32_t)fa::kBlockM, 1};
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)tokens};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_heads, (cuuint32_t)(fa::kBlockM / box_heads)};
   const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+// The four maps of one call: Q and O with H heads in boxes of G, K and V with H_kv heads.
+int make_maps(fa::FwdParams& p, const void* q, const void* k, const void* v, void* o, long long tokens, int H,
+              int Hkv, int d, bool f16) {
+  const int G = H / Hkv;
+  int st;
+  if ((st = make_map(&p.tm_q, q, tokens, H, d, G, f16)) != FA_OK ||
+      (st = make_map(&p.tm_k, k, tokens, Hkv, d, 1, f16)) != FA_OK ||
+      (st = make_map(&p.tm_v, v, tokens, Hkv, d, 1, f16)) != FA_OK ||
+      (st = make_map(&p.tm_o, o, tokens, H, d, G, f16)) != FA_OK)
+    return st;
+  return FA_OK;
+}
+
+// H_kv must divide H, and the group size G = H / H_kv must divide the 128 rows of
+// a Q tile (a power of two up to 128). Sets gshift = log2(G).
+int check_heads(int H, int Hkv, int* gshift) {
+  if (H <= 0 || Hkv <= 0 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
+  const int G = H / Hkv;
+  if (G > fa::kBlockM || (G & (G - 1)) != 0) return FA_ERR_UNSUPPORTED;
+  int sh = 0;
+  while ((1 << sh) < G) ++sh;
+  *gshift = sh;
+  return FA_OK;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-template <int D, bool C, bool E>
+template <int D, bool C, bool E, bool F>
 int launch_fwd(DevInfo* dev, const fa::FwdParams& p, int grid, cudaStream_t stream) {
   using L = fa::Layout<D>;
-  auto kern = fa::fa_fwd_kernel<D, C, E>;
-  const int di = D == 128 ? 1 : 0, ci = C ? 1 : 0, ei = E ? 1 : 0;
+  auto kern = fa::fa_fwd_kernel<D, C, E, F>;
+  const int di = D == 128 ? 1 : 0, ci = C ? 1 : 0, ei = E ? 1 : 0, fi = F ? 1 : 0;
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (!dev->attr_done[di][ci][ei]) {
+    if (!dev->attr_done[di][ci][ei][fi]) {
       int st = FA_OK;
       cudaFuncAttributes fa_attr;
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc) != cudaSuccess ||
@@ -121,31 +149,41 @@ int launch_fwd(DevInfo* dev, const fa::FwdParams& p, int grid, cudaStream_t stre
       // per thread at launch
       else if (fa_attr.numRegs != 128)
         st = FA_ERR_UNSUPPORTED;
-      dev->attr_status[di][ci][ei] = st;
-      dev->attr_done[di][ci][ei] = true;
+      dev->attr_status[di][ci][ei][fi] = st;
+      dev->attr_done[di][ci][ei][fi] = true;
     }
-    if (dev->attr_status[di][ci][ei] != FA_OK) return dev->attr_status[di][ci][ei];
+    if (dev->attr_status[di][ci][ei][fi] != FA_OK) return dev->attr_status[di][ci][ei][fi];
   }
   kern<<<grid, fa::kThreads, L::kSmemAlloc, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-template <int D, bool C>
+template <int D, bool C, bool F>
 int dispatch_emu(DevInfo* dev, const fa::FwdParams& p, int grid, cudaStream_t s) {
-  return p.emu_groups > 0 ? launch_fwd<D, C, true>(dev, p, grid, s) : launch_fwd<D, C, false>(dev, p, grid, s);
+  return p.emu_groups > 0 ? launch_fwd<D, C, true, F>(dev, p, grid, s) : launch_fwd<D, C, false, F>(dev, p, grid, s);
 }
 
-int dispatch(DevInfo* dev, const fa::FwdParams& p, int d, bool causal, int grid, cudaStream_t s) {
-  if (d == 128) return causal ? dispatch_emu<128, true>(dev, p, grid, s) : dispatch_emu<128, false>(dev, p, grid, s);
-  return causal ? dispatch_emu<64, true>(dev, p, grid, s) : dispatch_emu<64, false>(dev, p, grid, s);
+template <bool F>
+int dispatch_t(DevInfo* dev, const fa::FwdParams& p, int d, bool causal, int grid, cudaStream_t s) {
+  if (d == 128)
+    return causal ? dispatch_emu<128, true, F>(dev, p, grid, s) : dispatch_emu<128, false, F>(dev, p, grid, s);
+  return causal ? dispatch_emu<64, true, F>(dev, p, grid, s) : dispatch_emu<64, false, F>(dev, p, grid, s);
 }
 
-void fill_common(fa::FwdParams& p, float scale) {
+int dispatch(DevInfo* dev, const fa::FwdParams& p, int d, bool causal, bool f16, int grid, cudaStream_t s) {
+  return f16 ? dispatch_t<true>(dev, p, d, causal, grid, s) : dispatch_t<false>(dev, p, d, causal, grid, s);
+}
+
+// fp16 weights P = 2^(s - ref) stay below 2^tau; fp16 holds up to 65504, so its
+// threshold is capped at 15.
+constexpr float kTauMaxF16 = 15.0f;
+
+void fill_common(fa::FwdParams& p, float scale, bool f16) {
   p.sched = g_opt.persistent < 0 ? 2 : g_opt.persistent;
   p.trace = g_trace_buf;
   p.trace_ctas = g_trace_ctas;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.tau = g_opt.tau;
+  p.tau = f16 && g_opt.tau > kTauMaxF16 ? kTauMaxF16 : g_opt.tau;
   p.emu_groups = g_opt.emu_groups;
   p.timeout_ns = g_opt.timeout_ns;
 }
@@ -163,22 +201,24 @@ constexpr int kSchedBuckets = 4096;
 
 // One CTA: enumerate the (sequence, 256-row block) work tiles, bucket them by
 // their number of K/V blocks, and write them longest first, each followed by
-// all H heads ("FlashAttention-4（下）" (argus lesson 7), section "6. LPT 调度":
-// sort work tiles by their cost, write a virtual -> actual map).
-__global__ void __launch_bounds__(1024) fa_varlen_schedule_kernel(const int* cu, int num_seqs, int H, int causal,
-                                                                  int capacity, int4* tasks, int* count) {
+// all Hkv K/V heads ("FlashAttention-4（下）" (argus lesson 7), section "6. LPT 调度":
+// sort work tiles by their cost, write a virtual -> actual map). Rows are packed
+// (sequence position, query head of the group): a sequence of length L has
+// L << gshift rows, and row r of a block sits at position r >> gshift.
+__global__ void __launch_bounds__(1024) fa_varlen_schedule_kernel(const int* cu, int num_seqs, int Hkv, int gshift,
+                                                                  int causal, int capacity, int4* tasks, int* count) {
   __shared__ int hist[kSchedBuckets];
   __shared__ int total_pairs;
   for (int i = threadIdx.x; i < kSchedBuckets; i += blockDim.x) hist[i] = 0;
   if (threadIdx.x == 0) total_pairs = 0;
   __syncthreads();
   auto cost_of = [&](int L, int m) {
-    const int kmax = causal ? min(m * kTaskRows + kTaskRows, L) : L;
+    const int kmax = causal ? min(((m * kTaskRows + kTaskRows - 1) >> gshift) + 1, L) : L;
     return min((kmax + kBlockN - 1) / kBlockN, kSchedBuckets - 1);
   };
   for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
     const int L = max(cu[s + 1] - cu[s], 0);
-    const int nm = (L + kTaskRows - 1) / kTaskRows;
+    const int nm = ((L << gshift) + kTaskRows - 1) / kTaskRows;
     for (int m = 0; m < nm; ++m) atomicAdd(&hist[cost_of(L, m)], 1);
     atomicAdd(&total_pairs, nm);
   }
@@ -192,18 +232,18 @@ __global__ void __launch_bounds__(1024) fa_varlen_schedule_kernel(const int* cu,
       hist[c] = run;
       run += n;
     }
-    const long long n_tasks = (long long)total_pairs * H;
+    const long long n_tasks = (long long)total_pairs * Hkv;
     *count = (int)(n_tasks < capacity ? n_tasks : capacity);
   }
   __syncthreads();
   for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
     const int L = max(cu[s + 1] - cu[s], 0);
-    const int nm = (L + kTaskRows - 1) / kTaskRows;
+    const int nm = ((L << gshift) + kTaskRows - 1) / kTaskRows;
     for (int m = 0; m < nm; ++m) {
       const int c = cost_of(L, m);
       const int slot = atomicAdd(&hist[c], 1);
-      for (int h = 0; h < H; ++h) {
-        const long long ti = (long long)slot * H + h;
+      for (int h = 0; h < Hkv; ++h) {
+        const long long ti = (long long)slot * Hkv + h;
         if (ti < capacity) tasks[ti] = make_int4(s, h, m, c);
       }
     }
@@ -280,71 +320,121 @@ int fa_set_option(int option, double value) {
   }
 }
 
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
-           float scale, int causal, void* stream) {
+int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
+               int d, float scale, int causal, int dtype, void* stream) {
   if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || (lse && !aligned(lse, 4)))
     return FA_ERR_INVALID_ARG;
-  if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || H_kv <= 0 || N <= 0) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_INVALID_ARG;
+  int gshift = 0;
+  int st = check_heads(H, H_kv, &gshift);
+  if (st != FA_OK) return st;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   const long long tokens = (long long)B * N;
   if (tokens * H > INT_MAX) return FA_ERR_INVALID_ARG;  // 32-bit row and LSE indexing
   DevInfo* dev = nullptr;
-  int st = device_info(&dev);
-  if (st != FA_OK) return st;
+  if ((st = device_info(&dev)) != FA_OK) return st;
+  const bool f16 = dtype == FA_DTYPE_FP16;
 
   fa::FwdParams p;
   std::memset(&p, 0, sizeof p);
-  if ((st = make_map(&p.tm_q, q, tokens, H, d)) != FA_OK || (st = make_map(&p.tm_k, k, tokens, H, d)) != FA_OK ||
-      (st = make_map(&p.tm_v, v, tokens, H, d)) != FA_OK ||
-      (st = make_map(&p.tm_o, o, tokens, H, d)) != FA_OK)
-    return st;
-  p.o = static_cast<__nv_bfloat16*>(o);
+  if ((st = make_maps(p, q, k, v, o, tokens, H, H_kv, d, f16)) != FA_OK) return st;
+  p.o = static_cast<uint16_t*>(o);
   p.lse = lse;
   p.B = B; p.H = H; p.N = N;
+  p.Hkv = H_kv;
+  p.gshift = gshift;
   p.total_tokens = (int)tokens;
-  p.num_m = (N + fa::kTaskRows - 1) / fa::kTaskRows;
-  const long long ntask = (long long)B * H * p.num_m;
+  // tasks of 256 packed rows; a (b, kv head) has N * G rows
+  p.num_m = (int)((((long long)N << gshift) + fa::kTaskRows - 1) / fa::kTaskRows);
+  const long long ntask = (long long)B * H_kv * p.num_m;
   if (ntask > INT_MAX) return FA_ERR_INVALID_ARG;
   p.num_tasks = (int)ntask;
-  const long long kv_bytes = 4LL * N * d;                       // K + V of one (b, h)
+  const long long kv_bytes = 4LL * N * d;                       // K + V of one (b, kv head)
   long long group = (dev->l2_bytes / 2) / (kv_bytes > 0 ? kv_bytes : 1);
   if (group < 1) group = 1;
-  if (group > (long long)B * H) group = (long long)B * H;
+  if (group > (long long)B * H_kv) group = (long long)B * H_kv;
   p.lpt_group = (int)group;
   p.varlen = 0;
-  fill_common(p, scale);
+  fill_common(p, scale, f16);
   const int grid = grid_for(p, dev, p.num_tasks);
-  return dispatch(dev, p, d, causal != 0, grid, static_cast<cudaStream_t>(stream));
+  return dispatch(dev, p, d, causal != 0, f16, grid, static_cast<cudaStream_t>(stream));
 }
 
-int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
-                  int num_seqs, int total_tokens, int max_seqlen, int H, int d, float scale, int causal,
-                  void* stream) {
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+           float scale, int causal, void* stream) {
+  return fa_fwd_gqa(q, k, v, o, lse, B, H, H, N, d, scale, causal, FA_DTYPE_BF16, stream);
+}
+
+}  // extern "C"
+
+namespace {
+// Argument checks shared by the varlen entry points; *cap = the task-list
+// capacity: H_kv * (ceil(T * G / 256) + num_seqs) tiles of 256 packed rows.
+int varlen_check(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
+                 int num_seqs, int total_tokens, int max_seqlen, int H, int H_kv, int d, float scale, int causal,
+                 int dtype, int* gshift, long long* cap) {
   if (!q || !k || !v || !o || !cu_seqlens) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || (lse && !aligned(lse, 4)) ||
       !aligned(cu_seqlens, 4))
     return FA_ERR_INVALID_ARG;
-  if (num_seqs <= 0 || total_tokens <= 0 || max_seqlen <= 0 || H <= 0) return FA_ERR_INVALID_ARG;
+  if (num_seqs <= 0 || total_tokens <= 0 || max_seqlen <= 0 || H <= 0 || H_kv <= 0) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_INVALID_ARG;
+  int st = check_heads(H, H_kv, gshift);
+  if (st != FA_OK) return st;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if ((long long)total_tokens * H > INT_MAX) return FA_ERR_INVALID_ARG;
-  const long long cap = (long long)H * ((total_tokens + fa::kTaskRows - 1) / fa::kTaskRows + num_seqs);
-  if (cap > INT_MAX) return FA_ERR_INVALID_ARG;
-  DevInfo* dev = nullptr;
-  int st = device_info(&dev);
-  if (st != FA_OK) return st;
+  *cap = (long long)H_kv *
+         ((((long long)total_tokens << *gshift) + fa::kTaskRows - 1) / fa::kTaskRows + num_seqs);
+  return FA_OK;
+}
 
+// Maps, schedule kernel and attention kernel of a varlen call whose task list
+// lives in tasks[0, cap) with its count at *count.
+int varlen_launch(DevInfo* dev, const void* q, const void* k, const void* v, void* o, float* lse,
+                  const int* cu_seqlens, int num_seqs, int total_tokens, int H, int H_kv, int gshift, int d,
+                  float scale, int causal, bool f16, int4* tasks, int* count, int cap, cudaStream_t s) {
   fa::FwdParams p;
   std::memset(&p, 0, sizeof p);
-  if ((st = make_map(&p.tm_q, q, total_tokens, H, d)) != FA_OK ||
-      (st = make_map(&p.tm_k, k, total_tokens, H, d)) != FA_OK ||
-      (st = make_map(&p.tm_v, v, total_tokens, H, d)) != FA_OK ||
-      (st = make_map(&p.tm_o, o, total_tokens, H, d)) != FA_OK)
-    return st;
+  int st = make_maps(p, q, k, v, o, total_tokens, H, H_kv, d, f16);
+  if (st != FA_OK) return st;
+  fa::fa_varlen_schedule_kernel<<<1, 1024, 0, s>>>(cu_seqlens, num_seqs, H_kv, gshift, causal, cap, tasks, count);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  p.o = static_cast<uint16_t*>(o);
+  p.lse = lse;
+  p.cu_seqlens = cu_seqlens;
+  p.tasks = tasks;
+  p.task_count = count;
+  p.H = H;
+  p.Hkv = H_kv;
+  p.gshift = gshift;
+  p.total_tokens = total_tokens;
+  p.num_tasks = cap;
+  p.varlen = 1;
+  fill_common(p, scale, f16);
+  const int grid = grid_for(p, dev, cap);
+  return dispatch(dev, p, d, causal != 0, f16, grid, s);
+}
+}  // namespace
+
+extern "C" {
+
+int fa_fwd_varlen_gqa(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
+                      int num_seqs, int total_tokens, int max_seqlen, int H, int H_kv, int d, float scale,
+                      int causal, int dtype, void* stream) {
+  int gshift = 0;
+  long long cap = 0;
+  int st = varlen_check(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, max_seqlen, H, H_kv, d, scale, causal,
+                        dtype, &gshift, &cap);
+  if (st != FA_OK) return st;
+  if (cap > INT_MAX) return FA_ERR_INVALID_ARG;
+  DevInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != FA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* ws = nullptr;
   const size_t ws_bytes = (size_t)cap * sizeof(int4) + 16;
@@ -354,25 +444,17 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
   }
   int4* tasks = static_cast<int4*>(ws);
   int* count = reinterpret_cast<int*>(static_cast<char*>(ws) + (size_t)cap * sizeof(int4));
-  fa::fa_varlen_schedule_kernel<<<1, 1024, 0, s>>>(cu_seqlens, num_seqs, H, causal, (int)cap, tasks, count);
-  if (cudaGetLastError() != cudaSuccess) {
-    cudaFreeAsync(ws, s);
-    return FA_ERR_CUDA;
-  }
-  p.o = static_cast<__nv_bfloat16*>(o);
-  p.lse = lse;
-  p.cu_seqlens = cu_seqlens;
-  p.tasks = tasks;
-  p.task_count = count;
-  p.H = H;
-  p.total_tokens = total_tokens;
-  p.num_tasks = (int)cap;
-  p.varlen = 1;
-  fill_common(p, scale);
-  const int grid = grid_for(p, dev, (int)cap);
-  st = dispatch(dev, p, d, causal != 0, grid, s);
+  st = varlen_launch(dev, q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, H, H_kv, gshift, d, scale, causal,
+                     dtype == FA_DTYPE_FP16, tasks, count, (int)cap, s);
   if (cudaFreeAsync(ws, s) != cudaSuccess && st == FA_OK) st = FA_ERR_CUDA;
   return st;
+}
+
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
+                  int num_seqs, int total_tokens, int max_seqlen, int H, int d, float scale, int causal,
+                  void* stream) {
+  return fa_fwd_varlen_gqa(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, max_seqlen, H, H, d, scale, causal,
+                           FA_DTYPE_BF16, stream);
 }
 
 int fa_trace_configure(void* buf, int ctas) {
@@ -395,63 +477,39 @@ int fa_trace_layout(int* roles, int* slots_per_role) {
   return FA_OK;
 }
 
-int fa_varlen_schedule(const int* cu_seqlens, int num_seqs, int H, int causal, int capacity, void* tasks,
-                       int* count, void* stream) {
-  if (!cu_seqlens || !tasks || !count || num_seqs <= 0 || H <= 0 || capacity < 0 || (causal != 0 && causal != 1))
+int fa_varlen_schedule(const int* cu_seqlens, int num_seqs, int H_kv, int group, int causal, int capacity,
+                       void* tasks, int* count, void* stream) {
+  if (!cu_seqlens || !tasks || !count || num_seqs <= 0 || H_kv <= 0 || capacity < 0 || (causal != 0 && causal != 1))
     return FA_ERR_INVALID_ARG;
   if (!aligned(tasks, 16) || !aligned(count, 4) || !aligned(cu_seqlens, 4)) return FA_ERR_INVALID_ARG;
-  DevInfo* dev = nullptr;
-  int st = device_info(&dev);
+  int gshift = 0;
+  if (group <= 0) return FA_ERR_INVALID_ARG;
+  int st = check_heads(H_kv * group, H_kv, &gshift);
   if (st != FA_OK) return st;
+  DevInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != FA_OK) return st;
   fa::fa_varlen_schedule_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(
-      cu_seqlens, num_seqs, H, causal, capacity, static_cast<int4*>(tasks), count);
+      cu_seqlens, num_seqs, H_kv, gshift, causal, capacity, static_cast<int4*>(tasks), count);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_fwd_varlen_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
                           int num_seqs, int total_tokens, int max_seqlen, int H, int d, float scale, int causal,
                           void* stream) {
-  if (!q || !k || !v || !o || !cu_seqlens) return FA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || (lse && !aligned(lse, 4)) ||
-      !aligned(cu_seqlens, 4))
-    return FA_ERR_INVALID_ARG;
-  if (num_seqs <= 0 || total_tokens <= 0 || max_seqlen <= 0 || H <= 0) return FA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
-  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if ((long long)total_tokens * H > INT_MAX) return FA_ERR_INVALID_ARG;
-  const long long cap = (long long)H * ((total_tokens + fa::kTaskRows - 1) / fa::kTaskRows + num_seqs);
+  int gshift = 0;
+  long long cap = 0;
+  int st = varlen_check(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, max_seqlen, H, H, d, scale, causal,
+                        FA_DTYPE_BF16, &gshift, &cap);
+  if (st != FA_OK) return st;
   if (cap > kNoAllocMaxTasks) return FA_ERR_CAPACITY;
   DevInfo* dev = nullptr;
-  int st = device_info(&dev);
-  if (st != FA_OK) return st;
+  if ((st = device_info(&dev)) != FA_OK) return st;
   int4* scratch = nullptr;
   if ((st = noalloc_scratch(&scratch)) != FA_OK) return st;
-
-  fa::FwdParams p;
-  std::memset(&p, 0, sizeof p);
-  if ((st = make_map(&p.tm_q, q, total_tokens, H, d)) != FA_OK ||
-      (st = make_map(&p.tm_k, k, total_tokens, H, d)) != FA_OK ||
-      (st = make_map(&p.tm_v, v, total_tokens, H, d)) != FA_OK ||
-      (st = make_map(&p.tm_o, o, total_tokens, H, d)) != FA_OK)
-    return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   int4* tasks = scratch;
   int* count = reinterpret_cast<int*>(scratch + kNoAllocMaxTasks);
-  fa::fa_varlen_schedule_kernel<<<1, 1024, 0, s>>>(cu_seqlens, num_seqs, H, causal, (int)cap, tasks, count);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  p.o = static_cast<__nv_bfloat16*>(o);
-  p.lse = lse;
-  p.cu_seqlens = cu_seqlens;
-  p.tasks = tasks;
-  p.task_count = count;
-  p.H = H;
-  p.total_tokens = total_tokens;
-  p.num_tasks = (int)cap;
-  p.varlen = 1;
-  fill_common(p, scale);
-  const int grid = grid_for(p, dev, (int)cap);
-  return dispatch(dev, p, d, causal != 0, grid, s);
+  return varlen_launch(dev, q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, H, H, gshift, d, scale, causal,
+                       false, tasks, count, (int)cap, static_cast<cudaStream_t>(stream));
 }
 
 int fa_last_device_status(void* stream, unsigned long long* detail) {

@@ -1,19 +1,25 @@
 // fa_fwd.cuh -- the attention forward kernel for GB300 (sm_103a).
 //
 // One CTA of 512 threads works on tasks of 256 query rows of one (sequence,
-// head): two Q tiles of 128 rows that share every streamed K/V block. The four
-// warpgroups have fixed roles ("Flash Attention 4", section "Warp 角色与 Scope"):
+// K/V head): two Q tiles of 128 rows that share every streamed K/V block. With
+// grouped-query attention (G = H / H_kv query heads per K/V head, G a power of
+// two up to 128) the rows of a tile are packed: row r holds sequence position
+// tile_pos0 + r / G of query head kv * G + r % G, so one K/V block serves all
+// G heads ("Flash Attention 4", section "GQA 支持"); G = 1 is plain multi-head
+// attention. The four warpgroups have fixed roles ("Flash Attention 4", section
+// "Warp 角色与 Scope"):
 //
 //   WG0, WG1  softmax of Q tile 0 / Q tile 1 (thread r owns row r of its tile)
 //   WG2       correction (rescale of O in tensor memory) and the epilogue
-//             (O / row_sum -> bf16 -> global memory)
+//             (O / row_sum -> bf16 or fp16 -> global memory)
 //   WG3       warp 12: tcgen05 MMA issue; warp 13: TMA loads and task claims
 //             (work stealing by cluster launch control); warps 14-15 idle
 //
 // Per K/V block j (visited from the last block down to block 0, section
 // "Pipeline 时间线"):   S_t = Q_t K_j^T  (tcgen05, smem x smem -> TMEM fp32)
 //                      P_t = exp2(S_t * scale_log2 - ref_t * scale_log2)  (registers,
-//                            written back to TMEM as bf16 over the upper half of S_t)
+//                            written back to TMEM as bf16 / fp16 (the input type)
+//                            over the upper half of S_t)
 //                      O_t (+)= P_t V_j  (tcgen05, A from TMEM, B from smem)
 // with the delayed-rescale rule of section "算法结构": the reference ref_t of a
 // row moves to the new maximum only when that maximum exceeds it by more than
@@ -23,7 +29,7 @@
 //
 // Tensor memory (512 columns x 128 lanes x 32 bit, section "TMEM 布局与复用"):
 //   S_0 [0,128)   S_1 [128,256)   O_0 [256,256+D)   O_1 [384,384+D)
-//   P_t = bf16 pairs over columns [64,128) of S_t.
+//   P_t = 16-bit (bf16 / fp16) pairs over columns [64,128) of S_t.
 //
 // Shared memory: Q tiles (2), a ring of K/V stages (K and V blocks alternate
 // through the same ring), mbarriers, and a 2x128 float mailbox that carries
@@ -35,7 +41,7 @@
 // its tensor memory and exits.
 #pragma once
 
-#include <cuda_bf16.h>
+#include <cstdint>
 
 #include "ptx.cuh"
 
@@ -60,18 +66,22 @@ enum : uint32_t { kRoleMma = 1, kRoleLoad = 2, kRoleSoftmax0 = 3, kRoleSoftmax1 
 constexpr unsigned long long kStatusTimeout = 4;  // == FA_ERR_TIMEOUT
 
 struct FwdParams {
-  CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps of [tokens, H, d]: x = d, y = token, z = head
-  CUtensorMap tm_o;              // the same view of O, for the TMA store of full tiles
-  __nv_bfloat16* o;              // [tokens, H, d]
+  // 3-D maps of [tokens, heads, d]: x = d, y = head, z = token. Q and O: box
+  // 64 x G x 128/G (one packed 128-row tile); K and V: box 64 x 1 x 128.
+  CUtensorMap tm_q, tm_k, tm_v;
+  CUtensorMap tm_o;              // the view of O for the TMA store of full tiles
+  uint16_t* o;                   // [tokens, H, d] bf16 / fp16
   float* lse;                    // fixed length [B, H, N]; varlen [H, tokens]; may be null
   const int* cu_seqlens;         // varlen only
-  const int4* tasks;             // varlen only: {seq, head, m_block, cost}, longest first
+  const int4* tasks;             // varlen only: {seq, kv head, m_block, cost}, longest first
   const int* task_count;         // varlen only
-  int B, H, N;                   // fixed length: batch, heads, sequence length
+  int B, H, N;                   // fixed length: batch, query heads, sequence length
+  int Hkv;                       // K/V heads; H = Hkv << gshift
+  int gshift;                    // log2 of G, the query heads per K/V head (packed rows per position)
   int total_tokens;
   int num_tasks;                 // fixed length: exact; varlen: upper bound (grid sizing)
-  int num_m;                     // fixed length: 256-row blocks per (b, h)
-  int lpt_group;                 // causal fixed length: (b, h) pairs per L2 section
+  int num_m;                     // fixed length: 256-row blocks of packed rows per (b, kv head)
+  int lpt_group;                 // causal fixed length: (b, kv head) pairs per L2 section
   int varlen;
   float scale_log2;              // scale * log2(e)
   float tau;                     // delayed-rescale threshold
@@ -121,7 +131,7 @@ struct Tracer {
 template <int D>
 struct Layout {
   static_assert(D == 64 || D == 128, "head dim");
-  static constexpr int kHalves = D / 64;                   // 128-byte (64 x bf16) column slabs
+  static constexpr int kHalves = D / 64;                   // 128-byte (64-element) column slabs
   static constexpr int kSlabBytes = kBlockM * 128;          // one slab: 128 rows x 128 bytes
   static constexpr int kTileBytes = kHalves * kSlabBytes;   // one Q, K or V tile
   static constexpr int kStages = D == 128 ? FA_KV_STAGES_D128 : 8;  // K/V ring depth
@@ -148,26 +158,33 @@ struct Layout {
 
 // ------------------------------------------------------------------ tasks
 struct Task {
-  int h, tok0, len, m;   // head, first token of the sequence, its length, 256-row block
-  int lse_base;          // lse index of row 0 of the sequence for this head
+  int kvh, tok0, len, m;   // K/V head, first token of the sequence, its length, 256-row block
+  int lse_base;            // lse index of position 0 of query head kvh * G
+  int lse_hstride;         // lse distance between consecutive query heads
 };
+
+// First sequence position of the packed rows from `row` on (row a multiple of G).
+__device__ __forceinline__ int packed_pos(const Task& t, int row, int gshift) {
+  return (t.m * kTaskRows + row) >> gshift;
+}
 
 __device__ __forceinline__ bool get_task(const FwdParams& p, bool causal, int idx, Task& t) {
   if (p.varlen) {
     if (idx >= *p.task_count) return false;
     const int4 e = p.tasks[idx];
     const int s0 = p.cu_seqlens[e.x], s1 = p.cu_seqlens[e.x + 1];
-    t.h = e.y; t.m = e.z; t.tok0 = s0; t.len = s1 - s0;
-    t.lse_base = t.h * p.total_tokens + s0;
+    t.kvh = e.y; t.m = e.z; t.tok0 = s0; t.len = s1 - s0;
+    t.lse_base = (t.kvh << p.gshift) * p.total_tokens + s0;
+    t.lse_hstride = p.total_tokens;
     return true;
   }
   if (idx >= p.num_tasks) return false;
   int bh, m;
   if (causal) {
     // Longest-processing-time order: heavy m-blocks first, inside sections of
-    // lpt_group (b, h) pairs so that a section's K/V stays resident in L2
+    // lpt_group (b, kv head) pairs so that a section's K/V stays resident in L2
     // ("Flash Attention 4", section "Tile 调度"; "FlashAttention-4（下）", section "6. LPT 调度").
-    const int bh_total = p.B * p.H;
+    const int bh_total = p.B * p.Hkv;
     const int per_group = p.lpt_group * p.num_m;
     const int g = idx / per_group;
     const int r = idx - g * per_group;
@@ -178,17 +195,18 @@ __device__ __forceinline__ bool get_task(const FwdParams& p, bool causal, int id
     bh = idx / p.num_m;
     m = idx - bh * p.num_m;
   }
-  const int b = bh / p.H;
-  t.h = bh - b * p.H; t.m = m; t.tok0 = b * p.N; t.len = p.N;
-  t.lse_base = bh * p.N;
+  const int b = bh / p.Hkv;
+  t.kvh = bh - b * p.Hkv; t.m = m; t.tok0 = b * p.N; t.len = p.N;
+  t.lse_base = (b * p.H + (t.kvh << p.gshift)) * p.N;
+  t.lse_hstride = p.N;
   return true;
 }
 
 // Number of K/V blocks a task visits: keys [0, n*128) (causal stops at the last
 // key the bottom row of the task may see; "Flash Attention 4", section "Causal Mask").
-__device__ __forceinline__ int task_blocks(const Task& t, bool causal) {
+__device__ __forceinline__ int task_blocks(const Task& t, bool causal, int gshift) {
   int kmax = t.len;
-  if (causal) kmax = min(t.m * kTaskRows + kTaskRows, t.len);
+  if (causal) kmax = min(packed_pos(t, kTaskRows - 1, gshift) + 1, t.len);
   return (kmax + kBlockN - 1) / kBlockN;
 }
 
@@ -201,8 +219,8 @@ constexpr int kTaskConsumerWarps = 13;
 
 // Causal tasks: the top K/V block lies entirely above Q tile 0's last row, so
 // tile 0 skips it (its scores there would all be masked). Returns 1 or 0.
-__device__ __forceinline__ int task_skip0(const Task& t, int nb, bool causal) {
-  return (causal && nb >= 2 && (nb - 1) * kBlockN > t.m * kTaskRows + kBlockM - 1) ? 1 : 0;
+__device__ __forceinline__ int task_skip0(const Task& t, int nb, bool causal, int gshift) {
+  return (causal && nb >= 2 && (nb - 1) * kBlockN > packed_pos(t, kBlockM - 1, gshift)) ? 1 : 0;
 }
 
 // ------------------------------------------------------------------ bounded waits
@@ -257,10 +275,11 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
   asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
-__device__ __forceinline__ uint32_t pack_bf16x2_u64(uint64_t v) {
+template <bool F16>
+__device__ __forceinline__ uint32_t pack_16x2_u64(uint64_t v) {
   float lo, hi;
   unpack2(v, lo, hi);
-  return pack_bf16x2(lo, hi);
+  return pack_16x2<F16>(lo, hi);
 }
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float m;
@@ -311,35 +330,35 @@ __device__ __forceinline__ uint64_t exp2_poly2(uint64_t x2) {
 
 // ------------------------------------------------------------------ MMA issue helpers
 // S = Q K^T : M = 128 rows, N = 128 keys, K = D (16 per instruction). Both
-// operands K-major with 128-byte swizzle; a K step of 16 bf16 is a 32-byte
+// operands K-major with 128-byte swizzle; a K step of 16 elements is a 32-byte
 // advance inside a 128-byte row; D = 128 spans two 64-column slabs.
 // qdesc / kdesc: descriptors of the tiles' first byte; the per-step offsets are
 // added to the 16-byte start-address field (shared-memory addresses stay below
 // 256 KiB, so the 14-bit field never carries).
-template <int D>
+template <int D, bool F16>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t qdesc, uint64_t kdesc) {
-  constexpr uint32_t idesc = idesc_bf16_f32(128, kBlockN, false);
+  constexpr uint32_t idesc = idesc_f32acc(128, kBlockN, false, F16);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = ((kk / 4) * Layout<D>::kSlabBytes + (kk % 4) * 32) >> 4;
     mma_ss(d_tmem, qdesc + off, kdesc + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
-// O (+)= P V : M = 128 rows, N = D, K = 128 keys. P (bf16 pairs) from TMEM,
+// O (+)= P V : M = 128 rows, N = D, K = 128 keys. P (16-bit pairs) from TMEM,
 // 8 columns per 16 keys. V is [keys, d] in smem = MN-major for the B operand:
 // 64-wide d slabs LBO = 16 KiB apart, 8-key groups SBO = 1 KiB apart; a K step
 // of 16 keys is a 2 KiB advance.
 // vdesc: MN-major descriptor of the V tile's first byte (LBO = one 64-column slab).
-template <int D, int K0, int K1>
+template <int D, int K0, int K1, bool F16>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t vdesc, bool accumulate) {
-  constexpr uint32_t idesc = idesc_bf16_f32(128, D, true);
+  constexpr uint32_t idesc = idesc_f32acc(128, D, true, F16);
 #pragma unroll
   for (int kk = K0 / 16; kk < K1 / 16; ++kk)
     mma_ts(d_tmem, p_tmem + kk * 8, vdesc + ((kk * 2048) >> 4), idesc, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int D, bool CAUSAL, bool EMU>
+template <int D, bool CAUSAL, bool EMU, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -434,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       int it = 0;
       auto load_tile = [&](const CUtensorMap* m, uint32_t dst, int tok, int h, uint32_t b) {
 #pragma unroll
-        for (int c = 0; c < L::kHalves; ++c) tma_load_3d(dst + c * L::kSlabBytes, m, c * 64, tok, h, b);
+        for (int c = 0; c < L::kHalves; ++c) tma_load_3d(dst + c * L::kSlabBytes, m, c * 64, h, tok, b);
       };
       auto load_kv = [&](const CUtensorMap* m, int tok, int h, int blk) -> bool {
         if (!w.wait(bar(L::bKVEmpty + stage), phase ^ 1, L::bKVEmpty + stage, blk)) return false;
@@ -503,17 +522,18 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         __syncwarp();
         if (idx < 0) break;
         get_task(p, CAUSAL, idx, tk);
-        const int nb = task_blocks(tk, CAUSAL);
-        const int row0 = tk.tok0 + tk.m * kTaskRows;
+        const int nb = task_blocks(tk, CAUSAL, p.gshift);
         // load order: Q_0, K_{nb-1}, Q_1, V_{nb-1}, K_{nb-2}, V_{nb-2}, ..., K_0, V_0
+        // (Q tile t: positions from packed_pos(t * 128) of query heads kvh*G .. kvh*G+G-1)
 #pragma unroll 1
         for (int e = 0; ok && e < 2 * nb + 2; ++e) {
           if (e == 0 || e == 2) {
-            ok = load_q(e >> 1, row0 + (e >> 1) * kBlockM, tk.h, nb - 1);
+            const int t = e >> 1;
+            ok = load_q(t, tk.tok0 + packed_pos(tk, t * kBlockM, p.gshift), tk.kvh << p.gshift, nb - 1);
           } else {
             const int kvi = e == 1 ? 0 : e - 2;          // even: K, odd: V
             const int j = nb - 1 - (kvi >> 1);
-            ok = load_kv((kvi & 1) ? &p.tm_v : &p.tm_k, tk.tok0 + j * kBlockN, tk.h, j);
+            ok = load_kv((kvi & 1) ? &p.tm_v : &p.tm_k, tk.tok0 + j * kBlockN, tk.kvh, j);
           }
         }
       }
@@ -554,8 +574,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         const int idx = take_task(w, k);
         if (idx < 0) break;
         get_task(p, CAUSAL, idx, tk);
-        const int nb = task_blocks(tk, CAUSAL);
-        const int skip0 = task_skip0(tk, nb, CAUSAL);   // tile 0 starts one block lower
+        const int nb = task_blocks(tk, CAUSAL, p.gshift);
+        const int skip0 = task_skip0(tk, nb, CAUSAL, p.gshift);   // tile 0 starts one block lower
         const uint32_t qpar = it & 1;
         // prologue: S_0 and S_1 for the last block (S_0 only if tile 0 sees it)
         uint32_t ks = stage;
@@ -568,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           tr.rec(kEvIssueBegin, 0);
           if (leader) {
             if (t == 1 || !skip0) {
-              issue_qk<D>(t ? S1 : S0, t ? Q1 : Q0, Kd + ks * kStageStep);
+              issue_qk<D, F16>(t ? S1 : S0, t ? Q1 : Q0, Kd + ks * kStageStep);
               mma_commit(bar(L::bSFull + t));
             }
             if (t == 1) mma_commit(bar(L::bKVEmpty + ks));
@@ -597,14 +617,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
               tr.rec(kEvPO0 + 4 * t, j);
               tc_fence_after();
               tr.rec(kEvIssueBegin, 0);
-              if (leader) issue_pv<D, 0, kSplitP>(Ot, Pt, Vd + vs * kStageStep, i > first_i);
+              if (leader) issue_pv<D, 0, kSplitP, F16>(Ot, Pt, Vd + vs * kStageStep, i > first_i);
               tr.rec(kEvPV0a + 4 * t, j);
               if (!w.wait(bar(L::bP2 + t), (p2_par >> t) & 1, L::bP2 + t, j)) { ok = false; break; }
               p2_par ^= 1u << t;
               tr.rec(kEvP20 + 4 * t, j);
               tc_fence_after();
               tr.rec(kEvIssueBegin, 0);
-              if (leader) issue_pv<D, kSplitP, kBlockN>(Ot, Pt, Vd + vs * kStageStep, true);
+              if (leader) issue_pv<D, kSplitP, kBlockN, F16>(Ot, Pt, Vd + vs * kStageStep, true);
               tr.rec(kEvPV0b + 4 * t, j);
             }
             if (t == 1 && leader) mma_commit(bar(L::bKVEmpty + vs));   // V_j read by both tiles
@@ -618,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
               }
               tr.rec(kEvIssueBegin, 0);
               if (leader) {
-                issue_qk<D>(St, Qt, Kd + ks * kStageStep);
+                issue_qk<D, F16>(St, Qt, Kd + ks * kStageStep);
                 mma_commit(bar(L::bSFull + t));
                 if (t == 1) mma_commit(bar(L::bKVEmpty + ks));           // K_{j-1} read by both tiles
                 if (j == 1) mma_commit(bar(L::bQEmpty + t));             // last use of Q_t in this task
@@ -656,11 +676,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       const int idx = take_task(w, k);
       if (idx < 0) break;
       get_task(p, CAUSAL, idx, tk);
-      const int nb_all = task_blocks(tk, CAUSAL);
-      const int nb = nb_all - (t == 0 ? task_skip0(tk, nb_all, CAUSAL) : 0);   // this tile's blocks
-      const int row = tk.m * kTaskRows + t * kBlockM + r;       // row within the sequence
-      const int tile_row0 = tk.m * kTaskRows + t * kBlockM;
-      const int row_limit = CAUSAL ? min(row + 1, tk.len) : tk.len;  // keys [0, row_limit) visible
+      const int nb_all = task_blocks(tk, CAUSAL, p.gshift);
+      const int nb = nb_all - (t == 0 ? task_skip0(tk, nb_all, CAUSAL, p.gshift) : 0);   // this tile's blocks
+      const int tile_pos0 = packed_pos(tk, t * kBlockM, p.gshift);  // sequence position of row 0
+      const int pos = tile_pos0 + (r >> p.gshift);                  // this row's sequence position
+      const int row_limit = CAUSAL ? min(pos + 1, tk.len) : tk.len;  // keys [0, row_limit) visible
       float row_max = -INFINITY, row_sum = 0.f;
       for (int i = 0; i < nb; ++i) {
         const int j = nb - 1 - i;
@@ -669,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         tr.rec(kEvSFull, j);
         tc_fence_after();
         const int k0 = j * kBlockN;
-        const bool need_mask = (k0 + kBlockN > tk.len) || (CAUSAL && k0 + kBlockN - 1 > tile_row0);
+        const bool need_mask = (k0 + kBlockN > tk.len) || (CAUSAL && k0 + kBlockN - 1 > tile_pos0);
         const int lim = need_mask ? row_limit - k0 : kBlockN;   // columns [lim, 128) are masked
         // S in two halves: the second half's TMEM load overlaps the first half's max
         float s[kBlockN];
@@ -746,7 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         const float ref_safe = ref == -INFINITY ? 0.f : ref;
         const uint64_t scale2 = pack2(sl2, sl2);
         const uint64_t bias2 = pack2(-ref_safe * sl2, -ref_safe * sl2);
-        // P = exp2(S * sl2 - ref * sl2) -> bf16 pairs; with EMU the first emu_groups
+        // P = exp2(S * sl2 - ref * sl2) -> 16-bit pairs; with EMU the first emu_groups
         // 16-column groups use the FMA polynomial (blocks without masked columns only)
         const int emu = (EMU && !need_mask) ? p.emu_groups : 0;
         uint64_t sum2a = 0, sum2b = 0;
@@ -761,7 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                 const int c = g * 16 + e;
                 const uint64_t pp = exp2_poly2(fma2(pack2(s[c], s[c + 1]), scale2, bias2));
                 if (e & 2) sum2b = add2(sum2b, pp); else sum2a = add2(sum2a, pp);
-                pk[c >> 1] = pack_bf16x2_u64(pp);
+                pk[c >> 1] = pack_16x2_u64<F16>(pp);
               }
             } else {
 #pragma unroll
@@ -771,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                 unpack2(fma2(pack2(s[c], s[c + 1]), scale2, bias2), x0, x1);
                 const uint64_t pp = pack2(ex2_approx(x0), ex2_approx(x1));
                 if (e & 2) sum2b = add2(sum2b, pp); else sum2a = add2(sum2a, pp);
-                pk[c >> 1] = pack_bf16x2_u64(pp);
+                pk[c >> 1] = pack_16x2_u64<F16>(pp);
               }
             }
           }
@@ -793,11 +813,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       mail[t * kBlockM + r] = row_sum;
       mbar_arrive(bar(L::bCorrFull + t));
       tr.rec(kEvStats, -1);
-      if (p.lse != nullptr && row < tk.len && tk.tok0 + row < p.total_tokens) {
+      if (p.lse != nullptr && pos < tk.len && tk.tok0 + pos < p.total_tokens) {
         const float ref_safe = row_max == -INFINITY ? 0.f : row_max;
         const float lse = row_sum > 0.f ? (lg2_approx(row_sum) + ref_safe * sl2) * 0.69314718055994531f
                                         : -INFINITY;
-        p.lse[tk.lse_base + row] = lse;
+        p.lse[tk.lse_base + (r & ((1 << p.gshift) - 1)) * tk.lse_hstride + pos] = lse;
       }
     }
   } else if (warp < 12) {
@@ -821,8 +841,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       const int idx = take_task(w, k);
       if (idx < 0) break;
       get_task(p, CAUSAL, idx, tk);
-      const int nb = task_blocks(tk, CAUSAL);
-      const int skip0 = task_skip0(tk, nb, CAUSAL);
+      const int nb = task_blocks(tk, CAUSAL, p.gshift);
+      const int skip0 = task_skip0(tk, nb, CAUSAL, p.gshift);
       tr.rec(kEvTask, nb);
       for (int i = 1; ok && i < nb; ++i) {
         const int j = nb - 1 - i;
@@ -854,7 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         }
       }
       if (!ok) break;
-      // epilogue: O_t / row_sum -> bf16 -> global
+      // epilogue: O_t / row_sum -> bf16 / fp16 -> global
 #pragma unroll 1
       for (int t = 0; t < 2; ++t) {
         if (!w.wait(bar(L::bCorrFull + t), (cf_par >> t) & 1, L::bCorrFull + t, -1)) { ok = false; break; }
@@ -866,10 +886,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         tr.rec(kEvEpiStart + t, -1);
         tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        const int tile_row0 = tk.m * kTaskRows + t * kBlockM;
-        const int row = tile_row0 + r;
+        const int tile_pos0 = packed_pos(tk, t * kBlockM, p.gshift);   // sequence position of row 0
+        const int tile_end = tile_pos0 + (kBlockM >> p.gshift);        // one past the tile's last position
         const uint32_t tO = tmem + lane_base + L::col_o(t);
-        const bool full_tile = tile_row0 + kBlockM <= tk.len && tk.tok0 + tile_row0 + kBlockM <= p.total_tokens;
+        const bool full_tile = tile_end <= tk.len && tk.tok0 + tile_end <= p.total_tokens;
         if (full_tile) {
           // Stage the tile in shared memory in the TMA's 128-byte-swizzled layout
           // (16-byte unit k of row r sits at unit k ^ (r % 8)), then one thread
@@ -885,7 +905,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             uint32_t pk[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-              pk[e] = pack_bf16x2(__uint_as_float(u[2 * e]) * inv, __uint_as_float(u[2 * e + 1]) * inv);
+              pk[e] = pack_16x2<F16>(__uint_as_float(u[2 * e]) * inv, __uint_as_float(u[2 * e + 1]) * inv);
             const uint32_t slab = row_base + (uint32_t)(c >> 2) * L::kSlabBytes;
             const uint32_t k0 = (uint32_t)(c & 3) * 2;
             st_shared_v4(slab + (((k0 + 0) ^ (r & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
@@ -898,7 +918,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             if (lane == 0) {
 #pragma unroll
               for (int c = 0; c < L::kHalves; ++c)
-                tma_store_3d(&p.tm_o, sOst + c * L::kSlabBytes, c * 64, tk.tok0 + tile_row0, tk.h);
+                tma_store_3d(&p.tm_o, sOst + c * L::kSlabBytes, c * 64, tk.kvh << p.gshift, tk.tok0 + tile_pos0);
               bulk_commit();
               bulk_wait_read_all();
               mbar_arrive(bar(L::bOstFree));
@@ -908,8 +928,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           ++ost_n;
         } else {
           // ragged tile: per-row stores, nothing past the sequence or the tensor
-          const bool valid = row < tk.len && tk.tok0 + row < p.total_tokens;
-          __nv_bfloat16* orow = p.o + ((size_t)(tk.tok0 + row) * p.H + tk.h) * D;
+          const int pos = tile_pos0 + (r >> p.gshift);
+          const int head = (tk.kvh << p.gshift) + (r & ((1 << p.gshift) - 1));
+          const bool valid = pos < tk.len && tk.tok0 + pos < p.total_tokens;
+          uint16_t* orow = p.o + ((size_t)(tk.tok0 + pos) * p.H + head) * D;
 #pragma unroll 1
           for (int c = 0; c < D / 16; ++c) {
             uint32_t u[16];
@@ -918,7 +940,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             uint32_t pk[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-              pk[e] = pack_bf16x2(__uint_as_float(u[2 * e]) * inv, __uint_as_float(u[2 * e + 1]) * inv);
+              pk[e] = pack_16x2<F16>(__uint_as_float(u[2 * e]) * inv, __uint_as_float(u[2 * e + 1]) * inv);
             if (valid) {
               uint4* dst = reinterpret_cast<uint4*>(orow + c * 16);
               dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);

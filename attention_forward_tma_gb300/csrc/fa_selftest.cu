@@ -16,7 +16,7 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-int tile_map(CUtensorMap* m, const void* base, int rows, int d) {
+int tile_map(CUtensorMap* m, const void* base, int rows, int d, bool f16) {
   void* fn = nullptr;
   cudaDriverEntryPointQueryResult q;
   if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
@@ -27,7 +27,8 @@ int tile_map(CUtensorMap* m, const void* base, int rows, int d) {
   const cuuint32_t box[3] = {64, 128, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = reinterpret_cast<EncodeTiledFn>(fn)(
-      m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+      m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+      strides, box, estr,
       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
@@ -37,7 +38,7 @@ struct TileMaps {
   CUtensorMap q, k, v;
 };
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(128, 1) mma_tile_kernel(const __grid_constant__ TileMaps maps,
                                                            const uint32_t* __restrict__ p_pairs,
                                                            float* __restrict__ s_out, float* __restrict__ o_out,
@@ -84,7 +85,7 @@ __global__ void __launch_bounds__(128, 1) mma_tile_kernel(const __grid_constant_
     if (leader) {
       if (ok) {
         tc_fence_after();
-        issue_qk<D>(tmem + L::col_s(0), smem_desc_sw128(sQ, 16, 1024), smem_desc_sw128(sK, 16, 1024));
+        issue_qk<D, F16>(tmem + L::col_s(0), smem_desc_sw128(sQ, 16, 1024), smem_desc_sw128(sK, 16, 1024));
       }
       mma_commit(bMma);
     }
@@ -109,8 +110,8 @@ __global__ void __launch_bounds__(128, 1) mma_tile_kernel(const __grid_constant_
   tc_fence_after();
   if (warp == 0) {
     if (elect_one()) {
-      if (ok) issue_pv<D, 0, kBlockN>(tmem + L::col_o(0), tmem + L::col_s(0) + 64,
-                                      smem_desc_sw128(sV, L::kSlabBytes, 1024), false);
+      if (ok) issue_pv<D, 0, kBlockN, F16>(tmem + L::col_o(0), tmem + L::col_s(0) + 64,
+                                           smem_desc_sw128(sV, L::kSlabBytes, 1024), false);
       mma_commit(bMma);
     }
     __syncwarp();
@@ -169,6 +170,13 @@ int read_and_clear_status() {
   return (int)(word & 0xff);
 }
 
+template <int D, bool F16>
+void launch_mma_tile(const TileMaps& maps, const void* p, float* s_out, float* o_out, cudaStream_t s) {
+  const int smem = 3 * fa::Layout<D>::kTileBytes + 128 + 1024;
+  cudaFuncSetAttribute(mma_tile_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  mma_tile_kernel<D, F16><<<1, 128, smem, s>>>(maps, static_cast<const uint32_t*>(p), s_out, o_out, 2000000000ull);
+}
+
 bool is_sm103() {
   int dev = 0, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
@@ -182,26 +190,25 @@ bool is_sm103() {
 extern "C" {
 
 int fa_selftest_mma_tile(const void* q, const void* k, const void* v, const void* p, float* s_out, float* o_out,
-                         int d, void* stream) {
+                         int d, int dtype, void* stream) {
   if (!q || !k || !v || !p || !s_out || !o_out) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (!is_sm103()) return FA_ERR_UNSUPPORTED;
+  const bool f16 = dtype == FA_DTYPE_FP16;
   TileMaps maps;
   std::memset(&maps, 0, sizeof maps);
   int st;
-  if ((st = tile_map(&maps.q, q, 128, d)) != FA_OK || (st = tile_map(&maps.k, k, 128, d)) != FA_OK ||
-      (st = tile_map(&maps.v, v, 128, d)) != FA_OK)
+  if ((st = tile_map(&maps.q, q, 128, d, f16)) != FA_OK || (st = tile_map(&maps.k, k, 128, d, f16)) != FA_OK ||
+      (st = tile_map(&maps.v, v, 128, d, f16)) != FA_OK)
     return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const unsigned long long timeout = 2000000000ull;
   if (d == 128) {
-    const int smem = 3 * fa::Layout<128>::kTileBytes + 128 + 1024;
-    cudaFuncSetAttribute(mma_tile_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    mma_tile_kernel<128><<<1, 128, smem, s>>>(maps, static_cast<const uint32_t*>(p), s_out, o_out, timeout);
+    if (f16) launch_mma_tile<128, true>(maps, p, s_out, o_out, s);
+    else launch_mma_tile<128, false>(maps, p, s_out, o_out, s);
   } else {
-    const int smem = 3 * fa::Layout<64>::kTileBytes + 128 + 1024;
-    cudaFuncSetAttribute(mma_tile_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    mma_tile_kernel<64><<<1, 128, smem, s>>>(maps, static_cast<const uint32_t*>(p), s_out, o_out, timeout);
+    if (f16) launch_mma_tile<64, true>(maps, p, s_out, o_out, s);
+    else launch_mma_tile<64, false>(maps, p, s_out, o_out, s);
   }
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;

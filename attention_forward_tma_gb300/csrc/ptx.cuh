@@ -230,6 +230,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// The same descriptor with A and B in fp16 (format code 0) instead of bf16 (1);
+// kind::f16 takes both operands in one type.
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool b_mn_major, bool f16) {
+  return f16 ? (idesc_bf16_f32(M, N, b_mn_major) & ~((1u << 7) | (1u << 10))) : idesc_bf16_f32(M, N, b_mn_major);
+}
 
 // ---------------------------------------------------------------- scalar helpers
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -247,6 +252,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Two fp32 values -> a pair of 16-bit values (bf16 or fp16), round to nearest even.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack_16x2(float lo, float hi) {
+  return F16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
 }
 template <uint32_t N>
 __device__ __forceinline__ void setmaxnreg_inc() {

@@ -217,8 +217,8 @@ def run_oracle_rows(w, x, rows, threads):
     import oracle
     if w.varlen:
         return oracle.attention_rows_varlen(x["q"], x["k"], x["v"], x["cu_seqlens"], rows, w.scale, w.causal,
-                                            threads=threads)
-    return oracle.attention_rows(x["q"], x["k"], x["v"], rows, w.scale, w.causal, threads=threads)
+                                            threads=threads, dtype=w.dtype)
+    return oracle.attention_rows(x["q"], x["k"], x["v"], rows, w.scale, w.causal, threads=threads, dtype=w.dtype)
 
 
 def cpu_baseline(w, x, target_s: float = 10.0):
@@ -263,7 +263,8 @@ def run_reference(a, dist):
         run_oracle_rows(w, x, samples[i][0], threads)
     dt = time.perf_counter() - t0
     value = flops / dt / 1e12
-    cfg = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal}
+    cfg = {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.Hkv, "N": w.N, "d": w.d, "causal": w.causal,
+           "inputs": w.dtype}
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "impl": "reference", "n_gpus": a.gpus,
             "steps": a.steps, "warmup": a.warmup, "ms_per_step": dt / a.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
@@ -285,8 +286,10 @@ def run_ours(a, dist):
     x = fa_inputs.make_workload(w)
     flops = workload_flops(w, x)
 
+    tdt = torch.float16 if w.dtype == "f16" else torch.bfloat16
+
     def to_dev(bits):
-        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(tdt).to(dev)
 
     q, k, v = to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"])
     o = torch.empty_like(q)
@@ -364,7 +367,7 @@ def run_ours(a, dist):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_s = dist.max(e0.elapsed_time(e1) / 1e3)
-    h2d = 3 * q.numel() * 2 + (0 if not w.varlen else 0)
+    h2d = (q.numel() + k.numel() + v.numel()) * 2
     d2h = o.numel() * 2 + lse.numel() * 4
 
     if dist.rank != 0:
@@ -376,16 +379,16 @@ def run_ours(a, dist):
     theoretical = props.multi_processor_count * FLOP_PER_CLK_PER_SM * max_mhz * 1e6 / 1e12
     achieved = flops / avg_launch_s / 1e12
     traffic = profiled_traffic(w.name)
-    cfg = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+    cfg = {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.Hkv, "N": w.N, "d": w.d, "causal": w.causal,
            "scale": w.scale, "seed": w.seed, "l2": "inputs larger than L2 (Q+K+V+O = %.0f MiB), no flush"
-           % ((4 * q.numel() * 2) / 2 ** 20),
+           % ((2 * q.numel() + k.numel() + v.numel()) * 2 / 2 ** 20),
            "flops_per_step": flops}
     if w.varlen:
         cfg["lengths"] = [int(L) for L in x["lengths"]]
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": dist.world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": region_s / a.steps * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "config": cfg,
         "pct_of_measured_peak": 100.0 * value / dist.world / peak,
         "pct_of_theoretical_peak": 100.0 * value / dist.world / theoretical,
         "theoretical_peak_tflops": theoretical,

@@ -23,8 +23,8 @@
  * Conventions for every entry point below:
  *  - All tensor pointers are DEVICE pointers owned by the caller; the library
  *    never frees them and keeps no reference after the call returns.
- *  - bf16 tensors are row-major with the head dimension d innermost and must be
- *    16-byte aligned (TMA). d must be 64 or 128.
+ *  - bf16 / fp16 tensors are row-major with the head dimension d innermost and
+ *    must be 16-byte aligned (TMA). d must be 64 or 128.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Work is
  *    enqueued asynchronously; argument errors are reported synchronously by the
  *    return value and enqueue nothing.
@@ -50,6 +50,9 @@ typedef enum {
   FA_ERR_CAPACITY = 6      /* problem larger than the fixed scratch of fa_fwd_varlen_noalloc */
 } fa_status;
 
+/* Element type of q, k, v and o (all four share it). */
+typedef enum { FA_DTYPE_BF16 = 0, FA_DTYPE_FP16 = 1 } fa_dtype;
+
 /*
  * Fixed-length attention forward.
  *   q, k, v : bf16 [B, N, H, d]      (device, read only)
@@ -63,6 +66,26 @@ typedef enum {
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int N, int d, float scale, int causal, void* stream);
+
+/*
+ * Grouped-query attention ("Flash Attention 4", section "GQA 支持"), and the
+ * entry point for fp16 tensors.
+ *   q, o    : [B, N, H, d]      k, v : [B, N, H_kv, d]    (dtype elements, device)
+ *   lse     : fp32 [B, H, N] or NULL
+ *   H_kv >= 1 must divide H (else FA_ERR_INVALID_ARG), and G = H / H_kv must
+ *   divide 128, i.e. be a power of two up to 128 (else FA_ERR_UNSUPPORTED).
+ *   Query head h attends with K/V head h / G; H_kv = H is multi-head attention.
+ *   dtype   : FA_DTYPE_BF16 or FA_DTYPE_FP16; the weights P enter the second
+ *             matrix product in that type, and o is written in it (round to
+ *             nearest even).
+ * Other arguments, errors and the mask as for fa_fwd;
+ * fa_fwd(...) computes the same as fa_fwd_gqa(..., H_kv = H, ..., FA_DTYPE_BF16).
+ * The kernel packs the G query heads of a group into the 128 rows of each Q
+ * tile (128 / G positions x G heads), so every K/V block it loads serves the
+ * whole group.
+ */
+int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+               int B, int H, int H_kv, int N, int d, float scale, int causal, int dtype, void* stream);
 
 /*
  * Variable-length (packed) attention forward: sequence s owns the rows
@@ -85,6 +108,19 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
 int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                   const int* cu_seqlens, int num_seqs, int total_tokens, int max_seqlen,
                   int H, int d, float scale, int causal, void* stream);
+
+/*
+ * Variable-length grouped-query attention, bf16 or fp16:
+ *   q, o : [total_tokens, H, d]      k, v : [total_tokens, H_kv, d]
+ *   lse  : fp32 [H, total_tokens] or NULL
+ * H_kv, G and dtype as for fa_fwd_gqa; everything else as for fa_fwd_varlen
+ * (its temporary tile list holds H_kv * (ceil(total_tokens * G / 256) + num_seqs)
+ * entries of 16 bytes). fa_fwd_varlen(...) computes the same as
+ * fa_fwd_varlen_gqa(..., H_kv = H, ..., FA_DTYPE_BF16).
+ */
+int fa_fwd_varlen_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                      const int* cu_seqlens, int num_seqs, int total_tokens, int max_seqlen,
+                      int H, int H_kv, int d, float scale, int causal, int dtype, void* stream);
 
 /*
  * fa_fwd_varlen_noalloc: the same computation, arguments and results as
@@ -127,7 +163,9 @@ int fa_last_device_status(void* stream, unsigned long long* detail);
 
 /*
  * Process-wide tuning knobs (not thread-safe; meant for tests and benchmarks).
- *   FA_OPT_TAU             : rescale threshold tau in base-2 exponent units (default 8)
+ *   FA_OPT_TAU             : rescale threshold tau in base-2 exponent units (default 8);
+ *                            fp16 calls use min(tau, 15) so the weights P <= 2^tau
+ *                            stay finite in fp16
  *   FA_OPT_WAIT_TIMEOUT_NS : device wait limit in nanoseconds (default 2e9)
  *   FA_OPT_PERSISTENT      : task scheduling. 2 = one CTA per task in launch order, and
  *                            each running CTA takes over the tasks of CTAs not yet

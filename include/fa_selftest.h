@@ -18,12 +18,13 @@ extern "C" {
 /*
  * One tile through the kernel's own TMA maps, shared-memory descriptors and
  * tcgen05 instructions:
- *   s_out = Q K^T          (fp32 [128, 128])    q, k : bf16 [128, d]
- *   o_out = P V            (fp32 [128, d])      p : bf16 [128, 128], v : bf16 [128, d]
+ *   s_out = Q K^T          (fp32 [128, 128])    q, k : [128, d]
+ *   o_out = P V            (fp32 [128, d])      p : [128, 128], v : [128, d]
+ * q, k, v, p in the element type dtype (FA_DTYPE_BF16 or FA_DTYPE_FP16 of fa.h).
  * d in {64, 128}. Synchronizes the stream before returning.
  */
 int fa_selftest_mma_tile(const void* q, const void* k, const void* v, const void* p,
-                         float* s_out, float* o_out, int d, void* stream);
+                         float* s_out, float* o_out, int d, int dtype, void* stream);
 
 /* y[i] = 2^x[i] with the hardware ex2 unit (use_poly = 0), with the FMA
  * polynomial used for part of the softmax exponentials (use_poly = 1), or with
@@ -37,11 +38,14 @@ int fa_selftest_exp2(const float* x, float* y, int n, int use_poly, void* stream
  * (correct) outcome, FA_OK would mean the wait did not time out. */
 int fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream);
 
-/* The varlen longest-first tile schedule that fa_fwd_varlen computes, written
- * to caller buffers: tasks = int32 [capacity, 4] of {sequence, head, m_block,
- * cost in K/V blocks}, sorted by non-increasing cost; *count = number written.
+/* The varlen longest-first tile schedule that fa_fwd_varlen_gqa computes,
+ * written to caller buffers: tasks = int32 [capacity, 4] of {sequence, K/V
+ * head, m_block, cost in K/V blocks}, sorted by non-increasing cost; *count =
+ * number written. group = G, the query heads per K/V head (1 for fa_fwd_varlen;
+ * a power of two up to 128): a sequence of length L has L * G packed rows, cut
+ * into m_blocks of 256 rows, and row r of an m_block is position r / G.
  * cu_seqlens: device int32 [num_seqs + 1]. Asynchronous. */
-int fa_varlen_schedule(const int* cu_seqlens, int num_seqs, int H, int causal, int capacity,
+int fa_varlen_schedule(const int* cu_seqlens, int num_seqs, int H_kv, int group, int causal, int capacity,
                        void* tasks, int* count, void* stream);
 
 /*

@@ -87,12 +87,55 @@ def test_varlen_rejects_unsupported_head_dim():
     assert varlen(d=80) == fa.FA_ERR_UNSUPPORTED
 
 
+def gqa(**kw):
+    args = dict(q=16, k=16, v=16, o=16, lse=NULL, B=1, H=8, Hkv=2, N=128, d=128, scale=0.125, causal=0, dtype=0,
+                stream=NULL)
+    args.update(kw)
+    return fa.library().fa_fwd_gqa(args["q"], args["k"], args["v"], args["o"], args["lse"], args["B"], args["H"],
+                                   args["Hkv"], args["N"], args["d"], args["scale"], args["causal"], args["dtype"],
+                                   args["stream"])
+
+
+def varlen_gqa(**kw):
+    args = dict(q=16, k=16, v=16, o=16, lse=NULL, cu=16, S=2, T=256, maxL=200, H=8, Hkv=2, d=64, scale=0.125,
+                causal=1, dtype=1, stream=NULL)
+    args.update(kw)
+    return fa.library().fa_fwd_varlen_gqa(args["q"], args["k"], args["v"], args["o"], args["lse"], args["cu"],
+                                          args["S"], args["T"], args["maxL"], args["H"], args["Hkv"], args["d"],
+                                          args["scale"], args["causal"], args["dtype"], args["stream"])
+
+
+@pytest.mark.parametrize("kw", [dict(Hkv=0), dict(Hkv=-2), dict(H=8, Hkv=3), dict(H=2, Hkv=4), dict(dtype=2),
+                                dict(dtype=-1), dict(q=NULL), dict(k=8), dict(B=0), dict(N=0), dict(scale=0.0),
+                                dict(causal=3)])
+def test_gqa_rejects_invalid_arguments(kw):
+    assert gqa(**kw) == fa.FA_ERR_INVALID_ARG
+    if not set(kw) & {"B", "N"}:   # the varlen call has no B, N
+        assert varlen_gqa(**kw) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("H,Hkv", [(6, 2), (12, 1), (256, 1), (144, 3)])
+def test_gqa_rejects_group_sizes_that_do_not_divide_the_tile(H, Hkv):
+    # G = H / H_kv must be a power of two up to 128
+    assert gqa(H=H, Hkv=Hkv) == fa.FA_ERR_UNSUPPORTED
+    assert varlen_gqa(H=H, Hkv=Hkv) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_gqa_rejects_unsupported_head_dim():
+    assert gqa(d=96) == fa.FA_ERR_UNSUPPORTED
+    assert varlen_gqa(d=256) == fa.FA_ERR_UNSUPPORTED
+
+
 def test_valid_arguments_without_gpu_report_no_device():
     torch = pytest.importorskip("torch")
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert fwd() == fa.FA_ERR_NO_DEVICE
     assert varlen() == fa.FA_ERR_NO_DEVICE
+    for H, Hkv in ((8, 2), (128, 1), (4, 4)):
+        for dtype in (0, 1):
+            assert gqa(H=H, Hkv=Hkv, dtype=dtype) == fa.FA_ERR_NO_DEVICE
+            assert varlen_gqa(H=H, Hkv=Hkv, dtype=dtype) == fa.FA_ERR_NO_DEVICE
 
 
 @pytest.mark.parametrize("opt,val,ok", [(1, 8.0, True), (1, 0.0, True), (1, 1e30, True), (1, -1.0, False),
