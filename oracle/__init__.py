@@ -10,6 +10,8 @@ from them. Inputs come from ``fa_inputs`` (random numbers only).
   and its sources). Inputs are bf16 or fp16 bit patterns (``dtype``); K and V
   may have fewer heads than Q (grouped-query attention: query head h reads
   K/V head h // (H // H_kv)).
+* ``lse_combine`` merges partial results over disjoint key sets through their
+  LSE (``lse_combine.py``).
 * ``online_softmax`` is a separate, slow NumPy model of the blocked update with
   delayed rescaling, used to explain GPU differences and to check that the
   result does not depend on the threshold.
@@ -189,4 +191,5 @@ def attention_rows_varlen(q, k, v, cu_seqlens, rows, scale: float, causal: bool,
     return o, lse
 
 
+from .lse_combine import lse_combine  # noqa: E402,F401
 from .online_softmax import online_softmax_rows  # noqa: E402,F401

@@ -360,3 +360,54 @@ def test_gqa_and_dtype_arguments_are_checked():
         oracle.attention(q, k, k, 0.5, False)          # 6 query heads over 4 K/V heads
     with pytest.raises(ValueError):
         oracle.attention(q, q, q, 0.5, False, dtype="f32")
+
+
+# --------------------------------------------------------------------------- merging partial results
+def test_lse_combine_reproduces_the_two_round_example():
+    """The two rounds of "FlashAttention：一次前向计算" (figs. 5-10) taken as two
+    separate parts: round 1 = keys {0,1} (numerator fig. 6, denominators 3/2, max 1),
+    round 2 alone = keys {2,3} (weights fig. 7 against max 2, which is also each
+    row's own max over those keys; numerator fig. 8). Normalising each part and
+    merging through LSE must give the printed final output (fig. 10) and
+    L = ln 8, ln 9."""
+    g = fixtures.load("p3_two_round_example.txt")
+    l1 = as_float([g["l1"]])[0]
+    m1, m2 = as_float([g["m1"]])[0], as_float([g["m2"]])[0]
+    l2_alone = as_float(g["P2"]).sum(axis=1)                  # 5/4, 3/2 (printed after fig. 7)
+    o_parts = np.stack([as_float(g["O1"]) / l1[:, None], as_float(g["PV2"]) / l2_alone[:, None]])
+    lse_parts = np.stack([LN2 * m1 + np.log(l1), LN2 * m2 + np.log(l2_alone)])
+    o, lse = oracle.lse_combine(o_parts, lse_parts)
+    np.testing.assert_allclose(o, as_float(g["O"]), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, [math.log(float(x)) for x in g["LSE_ln"]], rtol=0, atol=1e-14)
+    # the oracle on each round's keys alone gives the same parts
+    q, k, v = (bits(as_float(g[n])) for n in ("Q", "K", "V"))
+    for part, (a, b) in enumerate(((0, 2), (2, 4))):
+        op, lp = oracle.attention(one_head(q), one_head(k[a:b]), one_head(v[a:b]), scale=LN2, causal=False)
+        np.testing.assert_allclose(op[0, :, 0], o_parts[part], rtol=0, atol=1e-14)
+        np.testing.assert_allclose(lp[0, 0], lse_parts[part], rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("n_parts", [1, 2, 5])
+def test_lse_combine_of_key_shards_equals_attention_over_all_keys(n_parts):
+    B, N, Nkv, H, d = 1, 40, 203, 2, 32
+    rng = np.random.default_rng(70 + n_parts)
+    q, k, v = (fa_inputs.f32_to_bf16_bits(rng.standard_normal(s).astype(np.float32))
+               for s in ((B, N, H, d), (B, Nkv, H, d), (B, Nkv, H, d)))
+    o_all, l_all = oracle.attention(q, k, v, 0.2, False)
+    cuts = np.linspace(0, Nkv, n_parts + 1).astype(int)
+    parts = [oracle.attention(q, k[:, a:b], v[:, a:b], 0.2, False) for a, b in zip(cuts, cuts[1:])]
+    o_parts = np.stack([p[0][0].transpose(1, 0, 2).reshape(H * N, d) for p in parts])   # rows (h, i)
+    lse_parts = np.stack([p[1][0].reshape(H * N) for p in parts])
+    o, lse = oracle.lse_combine(o_parts, lse_parts)
+    np.testing.assert_allclose(o, o_all[0].transpose(1, 0, 2).reshape(H * N, d), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, l_all[0].reshape(H * N), rtol=0, atol=1e-13)
+
+
+def test_lse_combine_skips_parts_without_keys():
+    o_parts = np.array([[[1.0, 2.0], [np.nan, np.inf]], [[3.0, -1.0], [np.nan, 5.0]]])   # [P=2, R=2, d=2]
+    lse_parts = np.array([[0.5, -np.inf], [-np.inf, -np.inf]])
+    o, lse = oracle.lse_combine(o_parts, lse_parts)
+    np.testing.assert_array_equal(o, [[1.0, 2.0], [0.0, 0.0]])     # row 0: part 0 only; row 1: nothing
+    np.testing.assert_array_equal(lse, [0.5, -np.inf])
+    with pytest.raises(ValueError):
+        oracle.lse_combine(o_parts, np.array([[np.nan, 0.0], [0.0, 0.0]]))
