@@ -16,7 +16,7 @@ import threading
 
 from . import _build
 
-__all__ = ["fa_fwd", "fa_fwd_varlen", "FaError", "set_option", "last_device_status", "library",
+__all__ = ["fa_fwd", "fa_fwd_varlen", "lse_combine", "FaError", "set_option", "last_device_status", "library",
            "FA_DTYPE_BF16", "FA_DTYPE_FP16",
            "selftest_mma_tile", "selftest_exp2", "selftest_wait_timeout", "varlen_schedule",
            "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
@@ -30,8 +30,12 @@ _vp, _ci, _cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 _SIGNATURES = {
     "fa_fwd": [_vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _cf, _ci, _vp],
     "fa_fwd_gqa": [_vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _ci, _vp],
+    "fa_fwd_kv": [_vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _ci, _ci, _vp],
     "fa_fwd_varlen": [_vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _vp],
     "fa_fwd_varlen_gqa": [_vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _ci, _vp],
+    "fa_fwd_varlen_kv": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _ci,
+                         _ci, _vp],
+    "fa_lse_combine": [_vp, _vp, _ci, _ci, _ci, _ci, _ci, _vp, _vp, _ci, _vp],
     "fa_fwd_varlen_noalloc": [_vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _vp],
     "fa_error_string": [_ci],
     "fa_last_device_status": [_vp, ctypes.POINTER(ctypes.c_ulonglong)],
@@ -40,7 +44,7 @@ _SIGNATURES = {
     "fa_selftest_mma_tile": [_vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _vp],
     "fa_selftest_exp2": [_vp, _vp, _ci, _ci, _vp],
     "fa_selftest_wait_timeout": [ctypes.c_ulonglong, _vp],
-    "fa_varlen_schedule": [_vp, _ci, _ci, _ci, _ci, _ci, _vp, _vp, _vp],
+    "fa_varlen_schedule": [_vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, _vp, _vp, _vp],
     "fa_trace_configure": [_vp, _ci],
     "fa_trace_layout": [ctypes.POINTER(_ci), ctypes.POINTER(_ci)],
 }
@@ -119,22 +123,25 @@ def _dtype_code(q):
 
 
 def fa_fwd(q, k, v, *, scale: float | None = None, causal: bool = False, out=None, lse=None,
-           return_lse: bool = True, stream=None):
-    """Attention forward: q [B, N, H, d], k and v [B, N, H_kv, d], all bf16 or all fp16.
+           return_lse: bool = True, num_splits: int = 1, stream=None):
+    """Attention forward: q [B, N_q, H, d], k and v [B, N_kv, H_kv, d], all bf16 or all fp16.
     Returns (o, lse) or o; o has q's shape and type.
 
     H_kv < H is grouped-query attention (query head h uses K/V head h // (H // H_kv));
-    H // H_kv must be a power of two up to 128. lse is fp32 [B, H, N] (natural log
-    of the scaled logits' sum of exponentials). scale defaults to 1/sqrt(d)."""
+    H // H_kv must be a power of two up to 128. N_kv may differ from N_q; the causal
+    mask is bottom-right aligned (query i sees keys j <= i + N_kv - N_q). lse is fp32
+    [B, H, N_q] (natural log of the scaled logits' sum of exponentials). scale
+    defaults to 1/sqrt(d). num_splits > 1 cuts the keys into ranges computed in
+    parallel and merged through their LSE (0: the library decides)."""
     torch = _torch()
     code = _dtype_code(q)
     _need(q, "q", q.dtype, 4)
     B, N, H, d = q.shape
-    Hkv = k.shape[2] if isinstance(k, torch.Tensor) and k.dim() == 4 else H
+    Nk, Hkv = (k.shape[1], k.shape[2]) if isinstance(k, torch.Tensor) and k.dim() == 4 else (N, H)
     for name, t in (("k", k), ("v", v)):
         _need(t, name, q.dtype, 4)
-        if tuple(t.shape) != (B, N, Hkv, d):
-            raise ValueError(f"{name} must have shape {(B, N, Hkv, d)}")
+        if tuple(t.shape) != (B, Nk, Hkv, d):
+            raise ValueError(f"{name} must have shape {(B, Nk, Hkv, d)}")
     if out is None:
         out = torch.empty_like(q)
     else:
@@ -148,27 +155,38 @@ def fa_fwd(q, k, v, *, scale: float | None = None, causal: bool = False, out=Non
         if tuple(lse.shape) != (B, H, N):
             raise ValueError("lse must have shape (B, H, N)")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    st = library().fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                              lse.data_ptr() if lse is not None else None, B, H, Hkv, N, d, scale,
-                              int(bool(causal)), code, _stream_handle(stream, q.device))
+    st = library().fa_fwd_kv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                             lse.data_ptr() if lse is not None else None, B, H, Hkv, N, Nk, d, scale,
+                             int(bool(causal)), code, int(num_splits), _stream_handle(stream, q.device))
     _check(st, "fa_fwd")
     return (out, lse) if lse is not None else out
 
 
 def fa_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, *, scale: float | None = None, causal: bool = False,
-                  out=None, lse=None, return_lse: bool = True, stream=None):
-    """Packed variable-length attention forward: q [T, H, d], k and v [T, H_kv, d] (bf16 or fp16);
-    cu_seqlens int32 [S+1] on the device. Returns (o, lse) or o; lse is fp32 [H, T]."""
+                  out=None, lse=None, return_lse: bool = True, cu_seqlens_k=None, max_seqlen_k: int | None = None,
+                  num_splits: int = 1, stream=None):
+    """Packed variable-length attention forward: q [T, H, d], k and v [T_kv, H_kv, d] (bf16 or fp16);
+    cu_seqlens int32 [S+1] on the device (query rows; also the key rows unless
+    cu_seqlens_k is given). Returns (o, lse) or o; lse is fp32 [H, T]."""
     torch = _torch()
     code = _dtype_code(q)
     _need(q, "q", q.dtype, 3)
     T, H, d = q.shape
-    Hkv = k.shape[1] if isinstance(k, torch.Tensor) and k.dim() == 3 else H
+    Tk, Hkv = (k.shape[0], k.shape[1]) if isinstance(k, torch.Tensor) and k.dim() == 3 else (T, H)
     for name, t in (("k", k), ("v", v)):
         _need(t, name, q.dtype, 3)
-        if tuple(t.shape) != (T, Hkv, d):
-            raise ValueError(f"{name} must have shape {(T, Hkv, d)}")
+        if tuple(t.shape) != (Tk, Hkv, d):
+            raise ValueError(f"{name} must have shape {(Tk, Hkv, d)}")
     _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    if cu_seqlens_k is None:
+        if Tk != T:
+            raise ValueError("k and v must have q's rows unless cu_seqlens_k is given")
+        cu_seqlens_k = cu_seqlens
+    else:
+        _need(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+        if cu_seqlens_k.numel() != cu_seqlens.numel():
+            raise ValueError("cu_seqlens_k must have as many entries as cu_seqlens")
+    max_seqlen_k = int(max_seqlen) if max_seqlen_k is None else int(max_seqlen_k)
     if out is None:
         out = torch.empty_like(q)
     else:
@@ -178,11 +196,37 @@ def fa_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, *, scale: float | None =
     elif lse is not None:
         _need(lse, "lse", torch.float32, 2)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    st = library().fa_fwd_varlen_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                                     lse.data_ptr() if lse is not None else None, cu_seqlens.data_ptr(),
-                                     cu_seqlens.numel() - 1, T, int(max_seqlen), H, Hkv, d, scale,
-                                     int(bool(causal)), code, _stream_handle(stream, q.device))
+    st = library().fa_fwd_varlen_kv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                    lse.data_ptr() if lse is not None else None, cu_seqlens.data_ptr(),
+                                    cu_seqlens_k.data_ptr(), cu_seqlens.numel() - 1, T, Tk, int(max_seqlen),
+                                    max_seqlen_k, H, Hkv, d, scale, int(bool(causal)), code, int(num_splits),
+                                    _stream_handle(stream, q.device))
     _check(st, "fa_fwd_varlen")
+    return (out, lse) if lse is not None else out
+
+
+def lse_combine(o_parts, lse_parts, *, out=None, lse=None, return_lse: bool = True, dtype=None, stream=None):
+    """Merge results over disjoint key sets: o_parts fp32 [P, B, N, H, d], lse_parts fp32 [P, B, H, N]
+    (-inf: the part saw no key). Returns (o [B, N, H, d] in bf16 (default) or fp16, lse fp32 [B, H, N])."""
+    torch = _torch()
+    _need(o_parts, "o_parts", torch.float32, 5)
+    _need(lse_parts, "lse_parts", torch.float32, 4)
+    P, B, N, H, d = o_parts.shape
+    if tuple(lse_parts.shape) != (P, B, H, N):
+        raise ValueError(f"lse_parts must have shape {(P, B, H, N)}")
+    if out is None:
+        out = torch.empty((B, N, H, d), dtype=dtype or torch.bfloat16, device=o_parts.device)
+    _need(out, "out", (torch.bfloat16, torch.float16), 4)
+    if tuple(out.shape) != (B, N, H, d):
+        raise ValueError("out has the wrong shape")
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=o_parts.device)
+    elif lse is not None:
+        _need(lse, "lse", torch.float32, 3)
+    code = FA_DTYPE_FP16 if out.dtype == torch.float16 else FA_DTYPE_BF16
+    _check(library().fa_lse_combine(o_parts.data_ptr(), lse_parts.data_ptr(), P, B, N, H, d, out.data_ptr(),
+                                    lse.data_ptr() if lse is not None else None, code,
+                                    _stream_handle(stream, o_parts.device)), "fa_lse_combine")
     return (out, lse) if lse is not None else out
 
 
@@ -226,15 +270,17 @@ def selftest_wait_timeout(timeout_ns: int, stream=None) -> int:
     return library().fa_selftest_wait_timeout(int(timeout_ns), _stream_handle(stream, torch.device("cuda")))
 
 
-def varlen_schedule(cu_seqlens, H: int, causal: bool, capacity: int, stream=None, group: int = 1):
-    """The longest-first varlen tile list: (tasks int32 [count, 4] of (seq, kv head, m_block, cost), count).
-    H is the number of K/V heads; group the query heads per K/V head."""
+def varlen_schedule(cu_seqlens, H: int, causal: bool, capacity: int, stream=None, group: int = 1,
+                    cu_seqlens_k=None, splits: int = 1):
+    """The longest-first varlen tile list: (tasks int32 [count, 4] of (seq, kv head | range << 16,
+    m_block, cost), count). H is the number of K/V heads; group the query heads per K/V head."""
     torch = _torch()
     _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    cu_seqlens_k = cu_seqlens if cu_seqlens_k is None else cu_seqlens_k
     tasks = torch.full((max(capacity, 1), 4), -1, dtype=torch.int32, device=cu_seqlens.device)
     count = torch.zeros(1, dtype=torch.int32, device=cu_seqlens.device)
-    _check(library().fa_varlen_schedule(cu_seqlens.data_ptr(), cu_seqlens.numel() - 1, H, int(group),
-                                        int(bool(causal)),
+    _check(library().fa_varlen_schedule(cu_seqlens.data_ptr(), cu_seqlens_k.data_ptr(), cu_seqlens.numel() - 1, H,
+                                        int(group), int(bool(causal)), int(splits),
                                         capacity, tasks.data_ptr(), count.data_ptr(),
                                         _stream_handle(stream, cu_seqlens.device)), "fa_varlen_schedule")
     n = int(count.item())

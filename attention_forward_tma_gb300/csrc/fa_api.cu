@@ -105,18 +105,65 @@ int make_map(CUtensorMap* m, const void* base, long long tokens, int heads, int 
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
-// The four maps of one call: Q and O with H heads in boxes of G, K and V with H_kv heads.
-int make_maps(fa::FwdParams& p, const void* q, const void* k, const void* v, void* o, long long tokens, int H,
-              int Hkv, int d, bool f16) {
+// The four maps of one call: Q and O ([tokens, H, d]) with H heads in boxes of G,
+// K and V ([tokens_k, H_kv, d]) with H_kv heads.
+int make_maps(fa::FwdParams& p, const void* q, const void* k, const void* v, void* o, long long tokens,
+              long long tokens_k, int H, int Hkv, int d, bool f16) {
   const int G = H / Hkv;
   int st;
   if ((st = make_map(&p.tm_q, q, tokens, H, d, G, f16)) != FA_OK ||
-      (st = make_map(&p.tm_k, k, tokens, Hkv, d, 1, f16)) != FA_OK ||
-      (st = make_map(&p.tm_v, v, tokens, Hkv, d, 1, f16)) != FA_OK ||
+      (st = make_map(&p.tm_k, k, tokens_k, Hkv, d, 1, f16)) != FA_OK ||
+      (st = make_map(&p.tm_v, v, tokens_k, Hkv, d, 1, f16)) != FA_OK ||
       (st = make_map(&p.tm_o, o, tokens, H, d, G, f16)) != FA_OK)
     return st;
   return FA_OK;
 }
+
+// Key ranges per task. requested > 0: that many (at most one per 128-key block
+// and kMaxSplits). requested = 0: split only when the unsplit tasks cannot fill
+// the SMs and the keys are long enough, aiming at about two tasks per SM with
+// at least four K/V blocks per range.
+constexpr int kMaxSplits = 128;
+int choose_splits(int requested, long long base_tasks, int key_blocks, int sm_count) {
+  const int most = key_blocks < 1 ? 1 : (key_blocks < kMaxSplits ? key_blocks : kMaxSplits);
+  if (requested > 0) return requested < most ? requested : most;
+  if (base_tasks >= sm_count || key_blocks < 8) return 1;
+  long long want = (2LL * sm_count + base_tasks - 1) / base_tasks;
+  const int by_len = key_blocks / 4;
+  if (want > by_len) want = by_len;
+  if (want > 64) want = 64;
+  return want < 1 ? 1 : (int)want;
+}
+
+// Stream-ordered temporary buffer: `head_bytes` for the caller (the varlen tile
+// list), then for splits > 0 the partial outputs o_part [splits][rows][d] fp32
+// and lse_part [splits][rows] fp32.
+struct Partials {
+  void* base = nullptr;
+  float* o_part = nullptr;
+  float* lse_part = nullptr;
+  int alloc(int splits, long long rows, int d, size_t head_bytes, cudaStream_t s) {
+    const size_t o_bytes = splits > 0 ? (size_t)splits * (size_t)rows * d * sizeof(float) : 0;
+    const size_t l_bytes = splits > 0 ? ((size_t)splits * (size_t)rows * sizeof(float) + 255) / 256 * 256 : 0;
+    if (head_bytes + o_bytes + l_bytes == 0) return FA_OK;
+    if (cudaMallocAsync(&base, head_bytes + o_bytes + l_bytes, s) != cudaSuccess) {
+      cudaGetLastError();
+      base = nullptr;
+      return FA_ERR_CUDA;
+    }
+    if (splits > 0) {
+      o_part = reinterpret_cast<float*>(static_cast<char*>(base) + head_bytes);
+      lse_part = reinterpret_cast<float*>(static_cast<char*>(base) + head_bytes + o_bytes);
+    }
+    return FA_OK;
+  }
+  int release(cudaStream_t s) {
+    if (base == nullptr) return FA_OK;
+    const bool ok = cudaFreeAsync(base, s) == cudaSuccess;
+    base = nullptr;
+    return ok ? FA_OK : FA_ERR_CUDA;
+  }
+};
 
 // H_kv must divide H, and the group size G = H / H_kv must divide the 128 rows of
 // a Q tile (a power of two up to 128). Sets gshift = log2(G).
@@ -199,28 +246,32 @@ int grid_for(const fa::FwdParams& p, const DevInfo* dev, int n_tasks) {
 namespace fa {
 constexpr int kSchedBuckets = 4096;
 
-// One CTA: enumerate the (sequence, 256-row block) work tiles, bucket them by
-// their number of K/V blocks, and write them longest first, each followed by
-// all Hkv K/V heads ("FlashAttention-4（下）" (argus lesson 7), section "6. LPT 调度":
-// sort work tiles by their cost, write a virtual -> actual map). Rows are packed
-// (sequence position, query head of the group): a sequence of length L has
-// L << gshift rows, and row r of a block sits at position r >> gshift.
-__global__ void __launch_bounds__(1024) fa_varlen_schedule_kernel(const int* cu, int num_seqs, int Hkv, int gshift,
-                                                                  int causal, int capacity, int4* tasks, int* count) {
+// One CTA: enumerate the (sequence, 256-row block, key range) work tiles, bucket
+// them by their number of K/V blocks, and write them longest first, each
+// followed by all Hkv K/V heads ("FlashAttention-4（下）" (argus lesson 7),
+// section "6. LPT 调度": sort work tiles by their cost, write a virtual -> actual
+// map). Rows are packed (sequence position, query head of the group): a
+// sequence of Lq query rows has Lq << gshift packed rows, and row r of a block
+// sits at position r >> gshift. Tiles without keys (cost 0) are listed too: they
+// write the rows' empty result.
+__global__ void __launch_bounds__(1024) fa_varlen_schedule_kernel(const int* cu_q, const int* cu_k, int num_seqs,
+                                                                  int Hkv, int gshift, int causal, int splits,
+                                                                  int capacity, int4* tasks, int* count) {
   __shared__ int hist[kSchedBuckets];
-  __shared__ int total_pairs;
+  __shared__ int total_tiles;
   for (int i = threadIdx.x; i < kSchedBuckets; i += blockDim.x) hist[i] = 0;
-  if (threadIdx.x == 0) total_pairs = 0;
+  if (threadIdx.x == 0) total_tiles = 0;
   __syncthreads();
-  auto cost_of = [&](int L, int m) {
-    const int kmax = causal ? min(((m * kTaskRows + kTaskRows - 1) >> gshift) + 1, L) : L;
-    return min((kmax + kBlockN - 1) / kBlockN, kSchedBuckets - 1);
+  auto cost_of = [&](int m, int Lq, int Lk, int sp) {
+    const KRange r = key_range(m, Lq, Lk, gshift, causal != 0, splits, sp);
+    return min(r.hi - r.lo, kSchedBuckets - 1);
   };
   for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
-    const int L = max(cu[s + 1] - cu[s], 0);
-    const int nm = ((L << gshift) + kTaskRows - 1) / kTaskRows;
-    for (int m = 0; m < nm; ++m) atomicAdd(&hist[cost_of(L, m)], 1);
-    atomicAdd(&total_pairs, nm);
+    const int Lq = max(cu_q[s + 1] - cu_q[s], 0), Lk = max(cu_k[s + 1] - cu_k[s], 0);
+    const int nm = ((Lq << gshift) + kTaskRows - 1) / kTaskRows;
+    for (int m = 0; m < nm; ++m)
+      for (int sp = 0; sp < splits; ++sp) atomicAdd(&hist[cost_of(m, Lq, Lk, sp)], 1);
+    atomicAdd(&total_tiles, nm * splits);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -232,24 +283,97 @@ __global__ void __launch_bounds__(1024) fa_varlen_schedule_kernel(const int* cu,
       hist[c] = run;
       run += n;
     }
-    const long long n_tasks = (long long)total_pairs * Hkv;
+    const long long n_tasks = (long long)total_tiles * Hkv;
     *count = (int)(n_tasks < capacity ? n_tasks : capacity);
   }
   __syncthreads();
   for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
-    const int L = max(cu[s + 1] - cu[s], 0);
-    const int nm = ((L << gshift) + kTaskRows - 1) / kTaskRows;
+    const int Lq = max(cu_q[s + 1] - cu_q[s], 0), Lk = max(cu_k[s + 1] - cu_k[s], 0);
+    const int nm = ((Lq << gshift) + kTaskRows - 1) / kTaskRows;
     for (int m = 0; m < nm; ++m) {
-      const int c = cost_of(L, m);
-      const int slot = atomicAdd(&hist[c], 1);
-      for (int h = 0; h < Hkv; ++h) {
-        const long long ti = (long long)slot * Hkv + h;
-        if (ti < capacity) tasks[ti] = make_int4(s, h, m, c);
+      for (int sp = 0; sp < splits; ++sp) {
+        const int c = cost_of(m, Lq, Lk, sp);
+        const int slot = atomicAdd(&hist[c], 1);
+        for (int h = 0; h < Hkv; ++h) {
+          const long long ti = (long long)slot * Hkv + h;
+          if (ti < capacity) tasks[ti] = make_int4(s, h | (sp << 16), m, c);
+        }
       }
     }
   }
 }
+
+// Merge of partial results over disjoint key ranges, one warp per (row, head):
+//   LSE = ln sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s
+// parts with LSE_s = -inf are skipped (their O_s is not read); a row without
+// any key gets O = 0, LSE = -inf. ("FlashAttention：一次前向计算", the two-round
+// example: partial results over key blocks are brought to one reference and
+// divided once by the total denominator; "Flash Attention 4", section
+// "重缩放与结果写回": the LSE of each part.)
+// o_part [parts][rows][H][D] fp32 (normalised per part); lse_part [parts][...]:
+// the LSE of (row, head) sits at ((row / nl) * H + head) * nl + row % nl.
+template <int D, bool F16>
+__global__ void __launch_bounds__(256) fa_combine_kernel(const float* __restrict__ o_part,
+                                                         const float* __restrict__ lse_part, int parts,
+                                                         long long o_stride, long long lse_stride, int rows, int H,
+                                                         int nl, uint16_t* __restrict__ o, float* __restrict__ lse) {
+  constexpr int E = D / 32;   // floats per lane
+  const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (w >= (long long)rows * H) return;
+  const int lane = threadIdx.x & 31;
+  const int row = (int)(w / H), h = (int)(w % H);
+  const long long li = ((long long)(row / nl) * H + h) * nl + row % nl;
+  float m = -INFINITY;
+  for (int s = lane; s < parts; s += 32) m = fmaxf(m, lse_part[s * lse_stride + li]);
+#pragma unroll
+  for (int x = 16; x > 0; x >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, x));
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float sum = 0.f;
+  if (m != -INFINITY) {
+    for (int s = 0; s < parts; ++s) {
+      const float l = lse_part[s * lse_stride + li];
+      if (l == -INFINITY) continue;
+      const float wgt = ex2_approx((l - m) * 1.4426950408889634f);
+      sum += wgt;
+      const float* src = o_part + s * o_stride + w * D + lane * E;
+      if constexpr (E == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(src);
+        acc[0] += wgt * x.x; acc[1] += wgt * x.y; acc[2] += wgt * x.z; acc[3] += wgt * x.w;
+      } else {
+        const float2 x = *reinterpret_cast<const float2*>(src);
+        acc[0] += wgt * x.x; acc[1] += wgt * x.y;
+      }
+    }
+  }
+  const float inv = sum > 0.f ? 1.f / sum : 0.f;
+  uint32_t* dst = reinterpret_cast<uint32_t*>(o + w * D + lane * E);
+#pragma unroll
+  for (int e = 0; e < E; e += 2) dst[e / 2] = pack_16x2<F16>(acc[e] * inv, acc[e + 1] * inv);
+  if (lse != nullptr && lane == 0)
+    lse[li] = m == -INFINITY ? -INFINITY : m + lg2_approx(sum) * 0.69314718055994531f;
+}
 }  // namespace fa
+
+namespace {
+int launch_combine(const float* o_part, const float* lse_part, int parts, long long o_stride, long long lse_stride,
+                   int rows, int H, int nl, int d, bool f16, void* o, float* lse, cudaStream_t s) {
+  const long long warps = (long long)rows * H;
+  const long long blocks = (warps + 7) / 8;
+  if (blocks > INT_MAX) return FA_ERR_INVALID_ARG;
+  uint16_t* out = static_cast<uint16_t*>(o);
+  const int g = (int)blocks;
+  if (d == 128) {
+    if (f16) fa::fa_combine_kernel<128, true><<<g, 256, 0, s>>>(o_part, lse_part, parts, o_stride, lse_stride, rows, H, nl, out, lse);
+    else fa::fa_combine_kernel<128, false><<<g, 256, 0, s>>>(o_part, lse_part, parts, o_stride, lse_stride, rows, H, nl, out, lse);
+  } else {
+    if (f16) fa::fa_combine_kernel<64, true><<<g, 256, 0, s>>>(o_part, lse_part, parts, o_stride, lse_stride, rows, H, nl, out, lse);
+    else fa::fa_combine_kernel<64, false><<<g, 256, 0, s>>>(o_part, lse_part, parts, o_stride, lse_stride, rows, H, nl, out, lse);
+  }
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+}  // namespace
 
 // ------------------------------------------------------------------ allocation-free scratch
 namespace {
@@ -320,12 +444,12 @@ int fa_set_option(int option, double value) {
   }
 }
 
-int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
-               int d, float scale, int causal, int dtype, void* stream) {
+int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N_q,
+              int N_kv, int d, float scale, int causal, int dtype, int num_splits, void* stream) {
   if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || (lse && !aligned(lse, 4)))
     return FA_ERR_INVALID_ARG;
-  if (B <= 0 || H <= 0 || H_kv <= 0 || N <= 0) return FA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || H_kv <= 0 || N_q <= 0 || N_kv <= 0 || num_splits < 0) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_INVALID_ARG;
@@ -333,27 +457,30 @@ int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
   int st = check_heads(H, H_kv, &gshift);
   if (st != FA_OK) return st;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  const long long tokens = (long long)B * N;
-  if (tokens * H > INT_MAX) return FA_ERR_INVALID_ARG;  // 32-bit row and LSE indexing
+  const long long tokens = (long long)B * N_q, tokens_k = (long long)B * N_kv;
+  if (tokens * H > INT_MAX || tokens_k * H_kv > INT_MAX) return FA_ERR_INVALID_ARG;  // 32-bit row indexing
   DevInfo* dev = nullptr;
   if ((st = device_info(&dev)) != FA_OK) return st;
   const bool f16 = dtype == FA_DTYPE_FP16;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   fa::FwdParams p;
   std::memset(&p, 0, sizeof p);
-  if ((st = make_maps(p, q, k, v, o, tokens, H, H_kv, d, f16)) != FA_OK) return st;
+  if ((st = make_maps(p, q, k, v, o, tokens, tokens_k, H, H_kv, d, f16)) != FA_OK) return st;
   p.o = static_cast<uint16_t*>(o);
   p.lse = lse;
-  p.B = B; p.H = H; p.N = N;
+  p.B = B; p.H = H; p.N = N_q; p.Nk = N_kv;
   p.Hkv = H_kv;
   p.gshift = gshift;
   p.total_tokens = (int)tokens;
-  // tasks of 256 packed rows; a (b, kv head) has N * G rows
-  p.num_m = (int)((((long long)N << gshift) + fa::kTaskRows - 1) / fa::kTaskRows);
-  const long long ntask = (long long)B * H_kv * p.num_m;
+  // tasks of 256 packed rows; a (b, kv head) has N_q * G rows
+  p.num_m = (int)((((long long)N_q << gshift) + fa::kTaskRows - 1) / fa::kTaskRows);
+  const long long base_tasks = (long long)B * H_kv * p.num_m;
+  p.splits = choose_splits(num_splits, base_tasks, (N_kv + fa::kBlockN - 1) / fa::kBlockN, dev->sm_count);
+  const long long ntask = base_tasks * p.splits;
   if (ntask > INT_MAX) return FA_ERR_INVALID_ARG;
   p.num_tasks = (int)ntask;
-  const long long kv_bytes = 4LL * N * d;                       // K + V of one (b, kv head)
+  const long long kv_bytes = 4LL * N_kv * d;                    // K + V of one (b, kv head)
   long long group = (dev->l2_bytes / 2) / (kv_bytes > 0 ? kv_bytes : 1);
   if (group < 1) group = 1;
   if (group > (long long)B * H_kv) group = (long long)B * H_kv;
@@ -361,7 +488,25 @@ int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
   p.varlen = 0;
   fill_common(p, scale, f16);
   const int grid = grid_for(p, dev, p.num_tasks);
-  return dispatch(dev, p, d, causal != 0, f16, grid, static_cast<cudaStream_t>(stream));
+  if (p.splits == 1) return dispatch(dev, p, d, causal != 0, f16, grid, s);
+
+  // split keys: partial results in a temporary buffer, then the merge
+  Partials ws;
+  if ((st = ws.alloc(p.splits, tokens * H, d, 0, s)) != FA_OK) return st;
+  p.o_part = ws.o_part;
+  p.lse_part = ws.lse_part;
+  p.lse_split_stride = tokens * H;
+  st = dispatch(dev, p, d, causal != 0, f16, grid, s);
+  if (st == FA_OK)
+    st = launch_combine(ws.o_part, ws.lse_part, p.splits, tokens * H * d, tokens * H, (int)tokens, H, N_q, d, f16,
+                        o, lse, s);
+  const int fst = ws.release(s);
+  return st != FA_OK ? st : fst;
+}
+
+int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
+               int d, float scale, int causal, int dtype, void* stream) {
+  return fa_fwd_kv(q, k, v, o, lse, B, H, H_kv, N, N, d, scale, causal, dtype, 1, stream);
 }
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
@@ -373,81 +518,105 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 
 namespace {
 // Argument checks shared by the varlen entry points; *cap = the task-list
-// capacity: H_kv * (ceil(T * G / 256) + num_seqs) tiles of 256 packed rows.
-int varlen_check(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
-                 int num_seqs, int total_tokens, int max_seqlen, int H, int H_kv, int d, float scale, int causal,
-                 int dtype, int* gshift, long long* cap) {
-  if (!q || !k || !v || !o || !cu_seqlens) return FA_ERR_INVALID_ARG;
+// capacity: H_kv * (ceil(T * G / 256) + num_seqs) tiles of 256 packed rows, per key range.
+int varlen_check(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_q, const int* cu_k,
+                 int num_seqs, int total_q, int total_k, int max_q, int max_k, int H, int H_kv, int d, float scale,
+                 int causal, int dtype, int num_splits, int* gshift, long long* base) {
+  if (!q || !k || !v || !o || !cu_q || !cu_k) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || (lse && !aligned(lse, 4)) ||
-      !aligned(cu_seqlens, 4))
+      !aligned(cu_q, 4) || !aligned(cu_k, 4))
     return FA_ERR_INVALID_ARG;
-  if (num_seqs <= 0 || total_tokens <= 0 || max_seqlen <= 0 || H <= 0 || H_kv <= 0) return FA_ERR_INVALID_ARG;
+  if (num_seqs <= 0 || total_q <= 0 || total_k <= 0 || max_q <= 0 || max_k < 0 || H <= 0 || H_kv <= 0 ||
+      num_splits < 0)
+    return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_INVALID_ARG;
   int st = check_heads(H, H_kv, gshift);
   if (st != FA_OK) return st;
+  if (H_kv > 0xffff) return FA_ERR_UNSUPPORTED;   // the task list keeps the K/V head in 16 bits
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if ((long long)total_tokens * H > INT_MAX) return FA_ERR_INVALID_ARG;
-  *cap = (long long)H_kv *
-         ((((long long)total_tokens << *gshift) + fa::kTaskRows - 1) / fa::kTaskRows + num_seqs);
+  if ((long long)total_q * H > INT_MAX || (long long)total_k * H_kv > INT_MAX) return FA_ERR_INVALID_ARG;
+  *base = (long long)H_kv * ((((long long)total_q << *gshift) + fa::kTaskRows - 1) / fa::kTaskRows + num_seqs);
   return FA_OK;
 }
 
-// Maps, schedule kernel and attention kernel of a varlen call whose task list
-// lives in tasks[0, cap) with its count at *count.
-int varlen_launch(DevInfo* dev, const void* q, const void* k, const void* v, void* o, float* lse,
-                  const int* cu_seqlens, int num_seqs, int total_tokens, int H, int H_kv, int gshift, int d,
-                  float scale, int causal, bool f16, int4* tasks, int* count, int cap, cudaStream_t s) {
+// Maps, schedule kernel, attention kernel (and with splits > 1 the merge) of a
+// varlen call whose task list lives in tasks[0, cap) with its count at *count.
+int varlen_launch(DevInfo* dev, const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_q,
+                  const int* cu_k, int num_seqs, int total_q, int total_k, int H, int H_kv, int gshift, int d,
+                  float scale, int causal, bool f16, int splits, const Partials* parts, int4* tasks, int* count,
+                  int cap, cudaStream_t s) {
   fa::FwdParams p;
   std::memset(&p, 0, sizeof p);
-  int st = make_maps(p, q, k, v, o, total_tokens, H, H_kv, d, f16);
+  int st = make_maps(p, q, k, v, o, total_q, total_k, H, H_kv, d, f16);
   if (st != FA_OK) return st;
-  fa::fa_varlen_schedule_kernel<<<1, 1024, 0, s>>>(cu_seqlens, num_seqs, H_kv, gshift, causal, cap, tasks, count);
+  fa::fa_varlen_schedule_kernel<<<1, 1024, 0, s>>>(cu_q, cu_k, num_seqs, H_kv, gshift, causal, splits, cap, tasks,
+                                                   count);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   p.o = static_cast<uint16_t*>(o);
   p.lse = lse;
-  p.cu_seqlens = cu_seqlens;
+  p.cu_seqlens = cu_q;
+  p.cu_seqlens_k = cu_k;
   p.tasks = tasks;
   p.task_count = count;
   p.H = H;
   p.Hkv = H_kv;
   p.gshift = gshift;
-  p.total_tokens = total_tokens;
+  p.total_tokens = total_q;
   p.num_tasks = cap;
   p.varlen = 1;
+  p.splits = splits;
+  if (splits > 1) {
+    p.o_part = parts->o_part;
+    p.lse_part = parts->lse_part;
+    p.lse_split_stride = (long long)total_q * H;
+  }
   fill_common(p, scale, f16);
   const int grid = grid_for(p, dev, cap);
-  return dispatch(dev, p, d, causal != 0, f16, grid, s);
+  st = dispatch(dev, p, d, causal != 0, f16, grid, s);
+  if (st != FA_OK || splits == 1) return st;
+  return launch_combine(parts->o_part, parts->lse_part, splits, (long long)total_q * H * d, (long long)total_q * H,
+                        total_q, H, total_q, d, f16, o, lse, s);
 }
 }  // namespace
 
 extern "C" {
 
+int fa_fwd_varlen_kv(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                     const int* cu_seqlens_kv, int num_seqs, int total_q, int total_kv, int max_seqlen_q,
+                     int max_seqlen_kv, int H, int H_kv, int d, float scale, int causal, int dtype, int num_splits,
+                     void* stream) {
+  int gshift = 0;
+  long long base = 0;
+  int st = varlen_check(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv, max_seqlen_q,
+                        max_seqlen_kv, H, H_kv, d, scale, causal, dtype, num_splits, &gshift, &base);
+  if (st != FA_OK) return st;
+  DevInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != FA_OK) return st;
+  const int splits = choose_splits(num_splits, base, (max_seqlen_kv + fa::kBlockN - 1) / fa::kBlockN,
+                                   dev->sm_count);
+  const long long cap = base * splits;
+  if (cap > INT_MAX) return FA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool f16 = dtype == FA_DTYPE_FP16;
+  // one temporary buffer: the tile list, its count, and with splits the partial results
+  Partials ws;
+  const size_t list_bytes = ((size_t)cap * sizeof(int4) + 16 + 255) / 256 * 256;
+  if ((st = ws.alloc(splits > 1 ? splits : 0, (long long)total_q * H, d, list_bytes, s)) != FA_OK) return st;
+  int4* tasks = static_cast<int4*>(ws.base);
+  int* count = reinterpret_cast<int*>(static_cast<char*>(ws.base) + (size_t)cap * sizeof(int4));
+  st = varlen_launch(dev, q, k, v, o, lse, cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv, H, H_kv, gshift,
+                     d, scale, causal, f16, splits, &ws, tasks, count, (int)cap, s);
+  const int fst = ws.release(s);
+  return st != FA_OK ? st : fst;
+}
+
 int fa_fwd_varlen_gqa(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
                       int num_seqs, int total_tokens, int max_seqlen, int H, int H_kv, int d, float scale,
                       int causal, int dtype, void* stream) {
-  int gshift = 0;
-  long long cap = 0;
-  int st = varlen_check(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, max_seqlen, H, H_kv, d, scale, causal,
-                        dtype, &gshift, &cap);
-  if (st != FA_OK) return st;
-  if (cap > INT_MAX) return FA_ERR_INVALID_ARG;
-  DevInfo* dev = nullptr;
-  if ((st = device_info(&dev)) != FA_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  void* ws = nullptr;
-  const size_t ws_bytes = (size_t)cap * sizeof(int4) + 16;
-  if (cudaMallocAsync(&ws, ws_bytes, s) != cudaSuccess) {
-    cudaGetLastError();
-    return FA_ERR_CUDA;
-  }
-  int4* tasks = static_cast<int4*>(ws);
-  int* count = reinterpret_cast<int*>(static_cast<char*>(ws) + (size_t)cap * sizeof(int4));
-  st = varlen_launch(dev, q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, H, H_kv, gshift, d, scale, causal,
-                     dtype == FA_DTYPE_FP16, tasks, count, (int)cap, s);
-  if (cudaFreeAsync(ws, s) != cudaSuccess && st == FA_OK) st = FA_ERR_CUDA;
-  return st;
+  return fa_fwd_varlen_kv(q, k, v, o, lse, cu_seqlens, cu_seqlens, num_seqs, total_tokens, total_tokens, max_seqlen,
+                          max_seqlen, H, H_kv, d, scale, causal, dtype, 1, stream);
 }
 
 int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
@@ -455,6 +624,23 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
                   void* stream) {
   return fa_fwd_varlen_gqa(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, max_seqlen, H, H, d, scale, causal,
                            FA_DTYPE_BF16, stream);
+}
+
+int fa_lse_combine(const float* o_parts, const float* lse_parts, int num_parts, int B, int N, int H, int d, void* o,
+                   float* lse, int dtype, void* stream) {
+  if (!o_parts || !lse_parts || !o) return FA_ERR_INVALID_ARG;
+  if (!aligned(o_parts, 16) || !aligned(lse_parts, 4) || !aligned(o, 16) || (lse && !aligned(lse, 4)))
+    return FA_ERR_INVALID_ARG;
+  if (num_parts <= 0 || B <= 0 || N <= 0 || H <= 0) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long rows = (long long)B * N;
+  if (rows > INT_MAX || rows * H > INT_MAX) return FA_ERR_INVALID_ARG;
+  DevInfo* dev = nullptr;
+  int st = device_info(&dev);
+  if (st != FA_OK) return st;
+  return launch_combine(o_parts, lse_parts, num_parts, rows * H * d, rows * H, (int)rows, H, N, d,
+                        dtype == FA_DTYPE_FP16, o, lse, static_cast<cudaStream_t>(stream));
 }
 
 int fa_trace_configure(void* buf, int ctas) {
@@ -477,11 +663,13 @@ int fa_trace_layout(int* roles, int* slots_per_role) {
   return FA_OK;
 }
 
-int fa_varlen_schedule(const int* cu_seqlens, int num_seqs, int H_kv, int group, int causal, int capacity,
-                       void* tasks, int* count, void* stream) {
-  if (!cu_seqlens || !tasks || !count || num_seqs <= 0 || H_kv <= 0 || capacity < 0 || (causal != 0 && causal != 1))
+int fa_varlen_schedule(const int* cu_seqlens_q, const int* cu_seqlens_kv, int num_seqs, int H_kv, int group,
+                       int causal, int splits, int capacity, void* tasks, int* count, void* stream) {
+  if (!cu_seqlens_q || !cu_seqlens_kv || !tasks || !count || num_seqs <= 0 || H_kv <= 0 || H_kv > 0xffff ||
+      capacity < 0 || splits <= 0 || splits > kMaxSplits || (causal != 0 && causal != 1))
     return FA_ERR_INVALID_ARG;
-  if (!aligned(tasks, 16) || !aligned(count, 4) || !aligned(cu_seqlens, 4)) return FA_ERR_INVALID_ARG;
+  if (!aligned(tasks, 16) || !aligned(count, 4) || !aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_kv, 4))
+    return FA_ERR_INVALID_ARG;
   int gshift = 0;
   if (group <= 0) return FA_ERR_INVALID_ARG;
   int st = check_heads(H_kv * group, H_kv, &gshift);
@@ -489,7 +677,7 @@ int fa_varlen_schedule(const int* cu_seqlens, int num_seqs, int H_kv, int group,
   DevInfo* dev = nullptr;
   if ((st = device_info(&dev)) != FA_OK) return st;
   fa::fa_varlen_schedule_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(
-      cu_seqlens, num_seqs, H_kv, gshift, causal, capacity, static_cast<int4*>(tasks), count);
+      cu_seqlens_q, cu_seqlens_kv, num_seqs, H_kv, gshift, causal, splits, capacity, static_cast<int4*>(tasks), count);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -498,8 +686,8 @@ int fa_fwd_varlen_noalloc(const void* q, const void* k, const void* v, void* o, 
                           void* stream) {
   int gshift = 0;
   long long cap = 0;
-  int st = varlen_check(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, max_seqlen, H, H, d, scale, causal,
-                        FA_DTYPE_BF16, &gshift, &cap);
+  int st = varlen_check(q, k, v, o, lse, cu_seqlens, cu_seqlens, num_seqs, total_tokens, total_tokens, max_seqlen,
+                        max_seqlen, H, H, d, scale, causal, FA_DTYPE_BF16, 1, &gshift, &cap);
   if (st != FA_OK) return st;
   if (cap > kNoAllocMaxTasks) return FA_ERR_CAPACITY;
   DevInfo* dev = nullptr;
@@ -508,8 +696,9 @@ int fa_fwd_varlen_noalloc(const void* q, const void* k, const void* v, void* o, 
   if ((st = noalloc_scratch(&scratch)) != FA_OK) return st;
   int4* tasks = scratch;
   int* count = reinterpret_cast<int*>(scratch + kNoAllocMaxTasks);
-  return varlen_launch(dev, q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, H, H, gshift, d, scale, causal,
-                       false, tasks, count, (int)cap, static_cast<cudaStream_t>(stream));
+  return varlen_launch(dev, q, k, v, o, lse, cu_seqlens, cu_seqlens, num_seqs, total_tokens, total_tokens, H, H,
+                       gshift, d, scale, causal, false, 1, nullptr, tasks, count, (int)cap,
+                       static_cast<cudaStream_t>(stream));
 }
 
 int fa_last_device_status(void* stream, unsigned long long* detail) {

@@ -70,15 +70,24 @@ struct FwdParams {
   // 64 x G x 128/G (one packed 128-row tile); K and V: box 64 x 1 x 128.
   CUtensorMap tm_q, tm_k, tm_v;
   CUtensorMap tm_o;              // the view of O for the TMA store of full tiles
-  uint16_t* o;                   // [tokens, H, d] bf16 / fp16
-  float* lse;                    // fixed length [B, H, N]; varlen [H, tokens]; may be null
-  const int* cu_seqlens;         // varlen only
-  const int4* tasks;             // varlen only: {seq, kv head, m_block, cost}, longest first
+  uint16_t* o;                   // [tokens, H, d] bf16 / fp16 (splits == 1)
+  float* lse;                    // fixed length [B, H, N]; varlen [H, tokens]; may be null (splits == 1)
+  // splits > 1: the keys of every task are cut into `splits` ranges of whole
+  // blocks, computed as separate tasks; each writes its normalised fp32 O and its
+  // LSE (-inf: no key in the range) here, and a merge kernel combines them.
+  float* o_part;                 // [splits, tokens, H, d]
+  float* lse_part;               // [splits, LSE layout]
+  long long lse_split_stride;    // elements between the splits of lse_part
+  int splits;
+  const int* cu_seqlens;         // varlen only: query rows of each sequence
+  const int* cu_seqlens_k;       // varlen only: key rows of each sequence
+  const int4* tasks;             // varlen only: {seq, kv head | split << 16, m_block, cost}, longest first
   const int* task_count;         // varlen only
-  int B, H, N;                   // fixed length: batch, query heads, sequence length
+  int B, H, N;                   // fixed length: batch, query heads, query rows per sequence
+  int Nk;                        // fixed length: key rows per sequence
   int Hkv;                       // K/V heads; H = Hkv << gshift
   int gshift;                    // log2 of G, the query heads per K/V head (packed rows per position)
-  int total_tokens;
+  int total_tokens;              // rows of Q and O
   int num_tasks;                 // fixed length: exact; varlen: upper bound (grid sizing)
   int num_m;                     // fixed length: 256-row blocks of packed rows per (b, kv head)
   int lpt_group;                 // causal fixed length: (b, kv head) pairs per L2 section
@@ -158,7 +167,9 @@ struct Layout {
 
 // ------------------------------------------------------------------ tasks
 struct Task {
-  int kvh, tok0, len, m;   // K/V head, first token of the sequence, its length, 256-row block
+  int kvh, tok0, len, m;   // K/V head, first query row of the sequence, its length, 256-row block
+  int tok0k, lenk;         // first key row of the sequence, its number of keys
+  int split;               // key range (splits > 1)
   int lse_base;            // lse index of position 0 of query head kvh * G
   int lse_hstride;         // lse distance between consecutive query heads
 };
@@ -173,12 +184,16 @@ __device__ __forceinline__ bool get_task(const FwdParams& p, bool causal, int id
     if (idx >= *p.task_count) return false;
     const int4 e = p.tasks[idx];
     const int s0 = p.cu_seqlens[e.x], s1 = p.cu_seqlens[e.x + 1];
-    t.kvh = e.y; t.m = e.z; t.tok0 = s0; t.len = s1 - s0;
+    const int k0 = p.cu_seqlens_k[e.x], k1 = p.cu_seqlens_k[e.x + 1];
+    t.kvh = e.y & 0xffff; t.split = e.y >> 16; t.m = e.z; t.tok0 = s0; t.len = s1 - s0;
+    t.tok0k = k0; t.lenk = k1 - k0;
     t.lse_base = (t.kvh << p.gshift) * p.total_tokens + s0;
     t.lse_hstride = p.total_tokens;
     return true;
   }
   if (idx >= p.num_tasks) return false;
+  t.split = idx % p.splits;   // the key ranges of one (b, kv head, m) are consecutive tasks
+  idx /= p.splits;
   int bh, m;
   if (causal) {
     // Longest-processing-time order: heavy m-blocks first, inside sections of
@@ -197,17 +212,36 @@ __device__ __forceinline__ bool get_task(const FwdParams& p, bool causal, int id
   }
   const int b = bh / p.Hkv;
   t.kvh = bh - b * p.Hkv; t.m = m; t.tok0 = b * p.N; t.len = p.N;
+  t.tok0k = b * p.Nk; t.lenk = p.Nk;
   t.lse_base = (b * p.H + (t.kvh << p.gshift)) * p.N;
   t.lse_hstride = p.N;
   return true;
 }
 
-// Number of K/V blocks a task visits: keys [0, n*128) (causal stops at the last
-// key the bottom row of the task may see; "Flash Attention 4", section "Causal Mask").
-__device__ __forceinline__ int task_blocks(const Task& t, bool causal, int gshift) {
-  int kmax = t.len;
-  if (causal) kmax = min(packed_pos(t, kTaskRows - 1, gshift) + 1, t.len);
-  return (kmax + kBlockN - 1) / kBlockN;
+// Causal offset: query position i sees keys j <= i + off, with off = N_kv - N_q
+// (bottom-right alignment, "Flash Attention 4", section "Causal Mask").
+__device__ __forceinline__ int task_off(const Task& t) { return t.lenk - t.len; }
+
+// K/V blocks [lo, hi) a task visits, from hi - 1 down to lo. Causal work stops
+// at the last key the bottom row of the task may see; with splits > 1 the
+// sequence's blocks are cut into `splits` ranges of ceil(blocks / splits) and
+// the task keeps its range's share. hi <= lo: the task sees no key.
+struct KRange {
+  int lo, hi;
+};
+// The same for the 256-row block m of a sequence with lenq query and lenk key rows.
+__device__ __forceinline__ KRange key_range(int m, int lenq, int lenk, int gshift, bool causal, int splits,
+                                            int split) {
+  int kmax = lenk;
+  if (causal) kmax = min(((m * kTaskRows + kTaskRows - 1) >> gshift) + (lenk - lenq) + 1, lenk);
+  const int nb = kmax > 0 ? (kmax + kBlockN - 1) / kBlockN : 0;
+  if (splits == 1) return {0, nb};
+  const int per = ((lenk + kBlockN - 1) / kBlockN + splits - 1) / splits;
+  const int lo = split * per;
+  return {lo, max(lo, min(lo + per, nb))};
+}
+__device__ __forceinline__ KRange task_range(const FwdParams& p, const Task& t, bool causal) {
+  return key_range(t.m, t.len, t.lenk, p.gshift, causal, p.splits, t.split);
 }
 
 // ------------------------------------------------------------------ task ring
@@ -219,8 +253,9 @@ constexpr int kTaskConsumerWarps = 13;
 
 // Causal tasks: the top K/V block lies entirely above Q tile 0's last row, so
 // tile 0 skips it (its scores there would all be masked). Returns 1 or 0.
-__device__ __forceinline__ int task_skip0(const Task& t, int nb, bool causal, int gshift) {
-  return (causal && nb >= 2 && (nb - 1) * kBlockN > packed_pos(t, kBlockM - 1, gshift)) ? 1 : 0;
+__device__ __forceinline__ int task_skip0(const Task& t, KRange r, bool causal, int gshift) {
+  return (causal && r.hi - r.lo >= 2 && (r.hi - 1) * kBlockN > packed_pos(t, kBlockM - 1, gshift) + task_off(t))
+             ? 1 : 0;
 }
 
 // ------------------------------------------------------------------ bounded waits
@@ -511,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       };
       int idx = (int)blockIdx.x;
       Task tk;
-      for (int k = 0; ok; ++k, ++it) {
+      for (int k = 0; ok; ++k) {
         if (k > 0 || idx >= limit) idx = claim_next(idx);
         const int slot = k & 1;
         if (!w.wait(bar(L::bTaskEmpty + slot), ((k >> 1) & 1) ^ 1, L::bTaskEmpty + slot, -1)) { ok = false; break; }
@@ -522,20 +557,23 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         __syncwarp();
         if (idx < 0) break;
         get_task(p, CAUSAL, idx, tk);
-        const int nb = task_blocks(tk, CAUSAL, p.gshift);
-        // load order: Q_0, K_{nb-1}, Q_1, V_{nb-1}, K_{nb-2}, V_{nb-2}, ..., K_0, V_0
+        const KRange kr = task_range(p, tk, CAUSAL);
+        if (kr.hi <= kr.lo) continue;   // no key to attend to: nothing to load
+        const int nb = kr.hi - kr.lo;
+        // load order: Q_0, K_{hi-1}, Q_1, V_{hi-1}, K_{hi-2}, V_{hi-2}, ..., K_lo, V_lo
         // (Q tile t: positions from packed_pos(t * 128) of query heads kvh*G .. kvh*G+G-1)
 #pragma unroll 1
         for (int e = 0; ok && e < 2 * nb + 2; ++e) {
           if (e == 0 || e == 2) {
             const int t = e >> 1;
-            ok = load_q(t, tk.tok0 + packed_pos(tk, t * kBlockM, p.gshift), tk.kvh << p.gshift, nb - 1);
+            ok = load_q(t, tk.tok0 + packed_pos(tk, t * kBlockM, p.gshift), tk.kvh << p.gshift, kr.hi - 1);
           } else {
             const int kvi = e == 1 ? 0 : e - 2;          // even: K, odd: V
-            const int j = nb - 1 - (kvi >> 1);
-            ok = load_kv((kvi & 1) ? &p.tm_v : &p.tm_k, tk.tok0 + j * kBlockN, tk.kvh, j);
+            const int j = kr.hi - 1 - (kvi >> 1);
+            ok = load_kv((kvi & 1) ? &p.tm_v : &p.tm_k, tk.tok0k + j * kBlockN, tk.kvh, j);
           }
         }
+        ++it;
       }
       if (!ok) {
         // drain: every armed full barrier completes once its bytes have landed
@@ -570,16 +608,18 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       const uint64_t Vd = smem_desc_sw128(sKV, L::kSlabBytes, 1024);   // V tile of stage 0 (MN-major)
       constexpr uint32_t kStageStep = L::kTileBytes >> 4;
       Task tk;
-      for (int k = 0; ok; ++k, ++it) {
+      for (int k = 0; ok; ++k) {
         const int idx = take_task(w, k);
         if (idx < 0) break;
         get_task(p, CAUSAL, idx, tk);
-        const int nb = task_blocks(tk, CAUSAL, p.gshift);
-        const int skip0 = task_skip0(tk, nb, CAUSAL, p.gshift);   // tile 0 starts one block lower
+        const KRange kr = task_range(p, tk, CAUSAL);
+        if (kr.hi <= kr.lo) continue;   // no key: no MMA (the epilogue writes the empty rows)
+        const int nb = kr.hi - kr.lo;
+        const int skip0 = task_skip0(tk, kr, CAUSAL, p.gshift);   // tile 0 starts one block lower
         const uint32_t qpar = it & 1;
-        // prologue: S_0 and S_1 for the last block (S_0 only if tile 0 sees it)
+        // prologue: S_0 and S_1 for the top block (S_0 only if tile 0 sees it)
         uint32_t ks = stage;
-        if (!w.wait(bar(L::bKVFull + ks), phase, L::bKVFull + ks, nb - 1)) { ok = false; break; }
+        if (!w.wait(bar(L::bKVFull + ks), phase, L::bKVFull + ks, kr.hi - 1)) { ok = false; break; }
         if (++stage == L::kStages) { stage = 0; phase ^= 1; }
 #pragma unroll 1
         for (int t = 0; t < 2; ++t) {
@@ -595,11 +635,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             if (nb == 1) mma_commit(bar(L::bQEmpty + t));   // Q_t's last use: the next task's Q may load
           }
           __syncwarp();
-          tr.rec(kEvS0 + t, nb - 1);
+          tr.rec(kEvS0 + t, kr.hi - 1);
         }
         if (!ok) break;
         for (int i = 0; i < nb; ++i) {
-          const int j = nb - 1 - i;
+          const int j = kr.hi - 1 - i;
           const bool last = (i == nb - 1);
           const uint32_t vs = stage;
           if (!w.wait(bar(L::bKVFull + vs), phase, L::bKVFull + vs, j)) { ok = false; break; }
@@ -641,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                 issue_qk<D, F16>(St, Qt, Kd + ks * kStageStep);
                 mma_commit(bar(L::bSFull + t));
                 if (t == 1) mma_commit(bar(L::bKVEmpty + ks));           // K_{j-1} read by both tiles
-                if (j == 1) mma_commit(bar(L::bQEmpty + t));             // last use of Q_t in this task
+                if (j - 1 == kr.lo) mma_commit(bar(L::bQEmpty + t));     // last use of Q_t in this task
               }
               tr.rec(kEvS0 + t, j - 1);
             } else if (leader) {
@@ -651,6 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           }
           if (!ok) break;
         }
+        ++it;
       }
       // all issued MMAs must finish before the tensor memory is released
       if (leader) mma_commit(bar(L::bDrain));
@@ -676,20 +717,34 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       const int idx = take_task(w, k);
       if (idx < 0) break;
       get_task(p, CAUSAL, idx, tk);
-      const int nb_all = task_blocks(tk, CAUSAL, p.gshift);
-      const int nb = nb_all - (t == 0 ? task_skip0(tk, nb_all, CAUSAL, p.gshift) : 0);   // this tile's blocks
+      const KRange kr = task_range(p, tk, CAUSAL);
       const int tile_pos0 = packed_pos(tk, t * kBlockM, p.gshift);  // sequence position of row 0
       const int pos = tile_pos0 + (r >> p.gshift);                  // this row's sequence position
-      const int row_limit = CAUSAL ? min(pos + 1, tk.len) : tk.len;  // keys [0, row_limit) visible
+      const int off = task_off(tk);
+      // LSE of this row (split mode: of its key range) -> global memory
+      auto store_lse = [&](float v) {
+        if (pos < tk.len && tk.tok0 + pos < p.total_tokens) {
+          const int li = tk.lse_base + (r & ((1 << p.gshift) - 1)) * tk.lse_hstride + pos;
+          if (p.splits > 1) p.lse_part[tk.split * p.lse_split_stride + li] = v;
+          else if (p.lse != nullptr) p.lse[li] = v;
+        }
+      };
+      if (kr.hi <= kr.lo) {   // no key for any row of the task: LSE = -inf (O = 0 is written by WG2)
+        store_lse(-INFINITY);
+        continue;
+      }
+      const int hi = kr.hi - (t == 0 ? task_skip0(tk, kr, CAUSAL, p.gshift) : 0);   // this tile's top block + 1
+      const int nb = hi - kr.lo;
+      const int row_limit = CAUSAL ? min(pos + off + 1, tk.lenk) : tk.lenk;  // keys [0, row_limit) visible
       float row_max = -INFINITY, row_sum = 0.f;
       for (int i = 0; i < nb; ++i) {
-        const int j = nb - 1 - i;
+        const int j = hi - 1 - i;
         if (!w.wait(bar(L::bSFull + t), s_par, L::bSFull + t, j)) { ok = false; break; }
         s_par ^= 1;
         tr.rec(kEvSFull, j);
         tc_fence_after();
         const int k0 = j * kBlockN;
-        const bool need_mask = (k0 + kBlockN > tk.len) || (CAUSAL && k0 + kBlockN - 1 > tile_pos0);
+        const bool need_mask = (k0 + kBlockN > tk.lenk) || (CAUSAL && k0 + kBlockN - 1 > tile_pos0 + off);
         const int lim = need_mask ? row_limit - k0 : kBlockN;   // columns [lim, 128) are masked
         // S in two halves: the second half's TMEM load overlaps the first half's max
         float s[kBlockN];
@@ -813,11 +868,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       mail[t * kBlockM + r] = row_sum;
       mbar_arrive(bar(L::bCorrFull + t));
       tr.rec(kEvStats, -1);
-      if (p.lse != nullptr && pos < tk.len && tk.tok0 + pos < p.total_tokens) {
+      {
         const float ref_safe = row_max == -INFINITY ? 0.f : row_max;
-        const float lse = row_sum > 0.f ? (lg2_approx(row_sum) + ref_safe * sl2) * 0.69314718055994531f
-                                        : -INFINITY;
-        p.lse[tk.lse_base + (r & ((1 << p.gshift) - 1)) * tk.lse_hstride + pos] = lse;
+        store_lse(row_sum > 0.f ? (lg2_approx(row_sum) + ref_safe * sl2) * 0.69314718055994531f : -INFINITY);
       }
     }
   } else if (warp < 12) {
@@ -841,11 +894,30 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       const int idx = take_task(w, k);
       if (idx < 0) break;
       get_task(p, CAUSAL, idx, tk);
-      const int nb = task_blocks(tk, CAUSAL, p.gshift);
-      const int skip0 = task_skip0(tk, nb, CAUSAL, p.gshift);
+      const KRange kr = task_range(p, tk, CAUSAL);
+      if (kr.hi <= kr.lo) {
+        // no key for any row of the task: O = 0 (its LSE = -inf comes from the softmax warps)
+#pragma unroll 1
+        for (int t = 0; t < 2; ++t) {
+          const int pos = packed_pos(tk, t * kBlockM, p.gshift) + (r >> p.gshift);
+          const int head = (tk.kvh << p.gshift) + (r & ((1 << p.gshift) - 1));
+          if (pos < tk.len && tk.tok0 + pos < p.total_tokens) {
+            const size_t row = (size_t)(tk.tok0 + pos) * p.H + head;
+            uint4* dst = p.splits > 1
+                             ? reinterpret_cast<uint4*>(p.o_part + ((size_t)tk.split * p.total_tokens * p.H + row) * D)
+                             : reinterpret_cast<uint4*>(p.o + row * D);
+            const int n16 = p.splits > 1 ? D / 4 : D / 8;   // 16-byte units per row
+#pragma unroll 1
+            for (int c = 0; c < n16; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        continue;
+      }
+      const int nb = kr.hi - kr.lo;
+      const int skip0 = task_skip0(tk, kr, CAUSAL, p.gshift);
       tr.rec(kEvTask, nb);
       for (int i = 1; ok && i < nb; ++i) {
-        const int j = nb - 1 - i;
+        const int j = kr.hi - 1 - i;
 #pragma unroll 1
         for (int t = 0; t < 2; ++t) {
           if (t == 0 && i - skip0 < 1) continue;   // tile 0's first block needs no correction
@@ -889,7 +961,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         const int tile_pos0 = packed_pos(tk, t * kBlockM, p.gshift);   // sequence position of row 0
         const int tile_end = tile_pos0 + (kBlockM >> p.gshift);        // one past the tile's last position
         const uint32_t tO = tmem + lane_base + L::col_o(t);
-        const bool full_tile = tile_end <= tk.len && tk.tok0 + tile_end <= p.total_tokens;
+        const bool full_tile = p.splits == 1 && tile_end <= tk.len && tk.tok0 + tile_end <= p.total_tokens;
         if (full_tile) {
           // Stage the tile in shared memory in the TMA's 128-byte-swizzled layout
           // (16-byte unit k of row r sits at unit k ^ (r % 8)), then one thread
@@ -926,6 +998,25 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             __syncwarp();
           }
           ++ost_n;
+        } else if (p.splits > 1) {
+          // one key range of a split task: normalised fp32 rows, merged later
+          const int pos = tile_pos0 + (r >> p.gshift);
+          const int head = (tk.kvh << p.gshift) + (r & ((1 << p.gshift) - 1));
+          const bool valid = pos < tk.len && tk.tok0 + pos < p.total_tokens;
+          float* orow = p.o_part + ((size_t)tk.split * p.total_tokens * p.H + (size_t)(tk.tok0 + pos) * p.H + head) * D;
+#pragma unroll 1
+          for (int c = 0; c < D / 16; ++c) {
+            uint32_t u[16];
+            tmem_ld16(tO + c * 16, u);
+            tmem_wait_ld();
+            if (valid) {
+              float4* dst = reinterpret_cast<float4*>(orow + c * 16);
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                dst[e] = make_float4(__uint_as_float(u[4 * e]) * inv, __uint_as_float(u[4 * e + 1]) * inv,
+                                     __uint_as_float(u[4 * e + 2]) * inv, __uint_as_float(u[4 * e + 3]) * inv);
+            }
+          }
         } else {
           // ragged tile: per-row stores, nothing past the sequence or the tensor
           const int pos = tile_pos0 + (r >> p.gshift);

@@ -95,12 +95,15 @@ class Workload:
     scale: float = field(default=float("nan"))
     Hkv: int = 0                  # K/V heads (0: the same as H)
     dtype: str = "bf16"           # element type of Q, K, V and O: "bf16" or "f16"
+    Nk: int = 0                   # key rows per sequence (0: the same as N)
 
     def __post_init__(self):
         if math.isnan(self.scale):
             self.scale = 1.0 / math.sqrt(self.d)
         if self.Hkv == 0:
             self.Hkv = self.H
+        if self.Nk == 0:
+            self.Nk = self.N
 
     @property
     def varlen(self) -> bool:
@@ -130,6 +133,14 @@ WORKLOADS.update({
     "g3_gqa_varlen8_h32kv4d128_causal_f16": Workload("g3_gqa_varlen8_h32kv4d128_causal_f16", B=1, H=32, N=0,
                                                      d=128, causal=True, seed=20268, varlen_seqs=8,
                                                      varlen_lo=512, varlen_hi=8192, Hkv=4, dtype="f16"),
+})
+
+# Decoding against a long key/value cache: one new query row per sequence,
+# grouped heads; the rows are few, so the keys are split into ranges that are
+# merged through their LSE.
+WORKLOADS.update({
+    "d1_decode_b8h32kv8nq1nk32768d128": Workload("d1_decode_b8h32kv8nq1nk32768d128", B=8, H=32, N=1, d=128,
+                                                 causal=True, seed=20269, Hkv=8, Nk=32768),
 })
 
 
@@ -186,14 +197,22 @@ def make_workload(w: Workload):
         lengths, cu, q, k, v = make_varlen(w.varlen_seqs, w.varlen_lo, w.varlen_hi, w.H, w.d, w.seed,
                                            Hkv=w.Hkv, dtype=w.dtype)
         return {"q": q, "k": k, "v": v, "lengths": lengths, "cu_seqlens": cu}
-    q, k, v = make_qkv(w.B, w.N, w.H, w.d, w.seed, spiky=w.spiky, Hkv=w.Hkv, dtype=w.dtype)
+    q, k, v = make_qkv(w.B, w.N, w.H, w.d, w.seed, spiky=w.spiky, Nkv=w.Nk, Hkv=w.Hkv, dtype=w.dtype)
     return {"q": q, "k": k, "v": v}
 
 
-def attention_flops(B: int, H: int, N: int, d: int, causal: bool) -> float:
-    """Conventional forward FLOP count: 4*B*H*N^2*d, halved for causal."""
-    f = 4.0 * B * H * N * N * d
-    return f / 2 if causal else f
+def attention_flops(B: int, H: int, N: int, d: int, causal: bool, Nk: int | None = None) -> float:
+    """Conventional forward FLOP count: 4*B*H*N^2*d, halved for causal. With N_k keys
+    (N_k != N), 4*d per visible (query, key) pair; bottom-right causal: query i sees
+    min(i + N_k - N + 1, N_k) keys (at least 0)."""
+    if Nk is None or Nk == N:
+        f = 4.0 * B * H * N * N * d
+        return f / 2 if causal else f
+    if not causal:
+        return 4.0 * B * H * N * Nk * d
+    i = np.arange(N, dtype=np.float64)
+    pairs = np.clip(i + (Nk - N) + 1, 0, Nk).sum()
+    return 4.0 * B * H * d * float(pairs)
 
 
 def varlen_flops(lengths, H: int, d: int, causal: bool) -> float:

@@ -88,6 +88,31 @@ int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
                int B, int H, int H_kv, int N, int d, float scale, int causal, int dtype, void* stream);
 
 /*
+ * The general fixed-length entry point: N_q query rows and N_kv key rows per
+ * sequence, grouped heads, bf16 / fp16, and an optional split of the keys.
+ *   q, o : [B, N_q, H, d]      k, v : [B, N_kv, H_kv, d]     lse : fp32 [B, H, N_q] or NULL
+ *   N_q, N_kv >= 1. causal = 1: query i sees keys j <= i + N_kv - N_q (bottom-right
+ *   alignment, "Flash Attention 4", section "Causal Mask"); a row that sees no
+ *   key (possible when N_q > N_kv) gets O = 0 and LSE = -inf.
+ *   num_splits: the 128-key blocks of every sequence are cut into num_splits
+ *   ranges (ceil(blocks / num_splits) blocks each) that run as separate tasks,
+ *   each producing its normalised fp32 output and its LSE; a second kernel
+ *   merges them: LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s
+ *   ("FlashAttention：一次前向计算" (qingsen), the two-round example: partial
+ *   results over key blocks merged through a common reference). This fills the
+ *   GPU when B * H_kv * ceil(N_q * G / 256) is small and N_kv long (decoding).
+ *   1 = no split; 0 = chosen by the library (split only when the unsplit tasks
+ *   cannot fill the GPU); larger values are capped at the number of key blocks
+ *   and at 128. With more than one range, partial results live in a temporary
+ *   buffer of num_splits * B * N_q * H * (d + 1) * 4 bytes from the
+ *   stream-ordered allocator (cudaMallocAsync / cudaFreeAsync on `stream`).
+ * Other arguments and errors as for fa_fwd_gqa.
+ */
+int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse,
+              int B, int H, int H_kv, int N_q, int N_kv, int d, float scale, int causal, int dtype,
+              int num_splits, void* stream);
+
+/*
  * Variable-length (packed) attention forward: sequence s owns the rows
  * [cu_seqlens[s], cu_seqlens[s+1]) of q, k, v and o; each sequence attends only
  * to itself (self-attention, causal mask aligned per sequence).
@@ -121,6 +146,40 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
 int fa_fwd_varlen_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
                       const int* cu_seqlens, int num_seqs, int total_tokens, int max_seqlen,
                       int H, int H_kv, int d, float scale, int causal, int dtype, void* stream);
+
+/*
+ * The general variable-length entry point: sequence s owns query rows
+ * [cu_seqlens_q[s], cu_seqlens_q[s+1]) of q and o and key rows
+ * [cu_seqlens_kv[s], cu_seqlens_kv[s+1]) of k and v (the two may be the same
+ * array); its causal mask is bottom-right aligned on its own lengths, and a
+ * sequence without keys gives O = 0, LSE = -inf for its rows.
+ *   q, o : [total_q, H, d]     k, v : [total_kv, H_kv, d]     lse : fp32 [H, total_q] or NULL
+ *   total_q, total_kv, max_seqlen_q >= 1; max_seqlen_kv >= 0 (only used to
+ *   choose num_splits = 0); num_splits as for fa_fwd_kv (per sequence: its own
+ *   key blocks are cut into num_splits ranges).
+ * The temporary buffer holds the tile list (H_kv * (ceil(total_q * G / 256) +
+ * num_seqs) * num_splits entries of 16 bytes) and, with more than one range,
+ * the partial results (num_splits * total_q * H * (d + 1) * 4 bytes).
+ */
+int fa_fwd_varlen_kv(const void* q, const void* k, const void* v, void* o, float* lse,
+                     const int* cu_seqlens_q, const int* cu_seqlens_kv, int num_seqs, int total_q,
+                     int total_kv, int max_seqlen_q, int max_seqlen_kv, int H, int H_kv, int d, float scale,
+                     int causal, int dtype, int num_splits, void* stream);
+
+/*
+ * Merge of attention results computed over disjoint key sets (for example the
+ * key ranges of one sequence held by different GPUs), through their LSE:
+ *   LSE = ln sum_p exp(LSE_p),   O = sum_p exp(LSE_p - LSE) * O_p
+ *   o_parts   : fp32 [num_parts, B, N, H, d]  (device; each part's normalised output)
+ *   lse_parts : fp32 [num_parts, B, H, N]     (device; natural-log LSE, -inf = the part
+ *                                              saw no key for that row: its O is not read)
+ *   o         : [B, N, H, d] of dtype (bf16 / fp16), written
+ *   lse       : fp32 [B, H, N] or NULL
+ * A row whose parts are all -inf gets O = 0, LSE = -inf. Packed varlen rows
+ * use B = 1, N = total rows (LSE layout [H, total]). d in {64, 128}.
+ */
+int fa_lse_combine(const float* o_parts, const float* lse_parts, int num_parts, int B, int N, int H, int d,
+                   void* o, float* lse, int dtype, void* stream);
 
 /*
  * fa_fwd_varlen_noalloc: the same computation, arguments and results as

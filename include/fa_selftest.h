@@ -38,15 +38,16 @@ int fa_selftest_exp2(const float* x, float* y, int n, int use_poly, void* stream
  * (correct) outcome, FA_OK would mean the wait did not time out. */
 int fa_selftest_wait_timeout(unsigned long long timeout_ns, void* stream);
 
-/* The varlen longest-first tile schedule that fa_fwd_varlen_gqa computes,
+/* The varlen longest-first tile schedule that fa_fwd_varlen_kv computes,
  * written to caller buffers: tasks = int32 [capacity, 4] of {sequence, K/V
- * head, m_block, cost in K/V blocks}, sorted by non-increasing cost; *count =
- * number written. group = G, the query heads per K/V head (1 for fa_fwd_varlen;
- * a power of two up to 128): a sequence of length L has L * G packed rows, cut
- * into m_blocks of 256 rows, and row r of an m_block is position r / G.
- * cu_seqlens: device int32 [num_seqs + 1]. Asynchronous. */
-int fa_varlen_schedule(const int* cu_seqlens, int num_seqs, int H_kv, int group, int causal, int capacity,
-                       void* tasks, int* count, void* stream);
+ * head | key range << 16, m_block, cost in K/V blocks}, sorted by
+ * non-increasing cost; *count = number written. group = G, the query heads per
+ * K/V head (1 for fa_fwd_varlen; a power of two up to 128): a sequence of L_q
+ * query rows has L_q * G packed rows, cut into m_blocks of 256 rows, and row r
+ * of an m_block is position r / G. splits = key ranges per tile (1..128).
+ * cu_seqlens_q / cu_seqlens_kv: device int32 [num_seqs + 1]. Asynchronous. */
+int fa_varlen_schedule(const int* cu_seqlens_q, const int* cu_seqlens_kv, int num_seqs, int H_kv, int group,
+                       int causal, int splits, int capacity, void* tasks, int* count, void* stream);
 
 /*
  * Pipeline tracing. Only the tracing build of the library (compiled with

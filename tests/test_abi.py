@@ -126,6 +126,54 @@ def test_gqa_rejects_unsupported_head_dim():
     assert varlen_gqa(d=256) == fa.FA_ERR_UNSUPPORTED
 
 
+def fwd_kv(**kw):
+    args = dict(q=16, k=16, v=16, o=16, lse=NULL, B=1, H=8, Hkv=2, Nq=1, Nk=4096, d=128, scale=0.125, causal=1,
+                dtype=0, splits=0, stream=NULL)
+    args.update(kw)
+    return fa.library().fa_fwd_kv(*[args[n] for n in ("q", "k", "v", "o", "lse", "B", "H", "Hkv", "Nq", "Nk", "d",
+                                                      "scale", "causal", "dtype", "splits", "stream")])
+
+
+def varlen_kv(**kw):
+    args = dict(q=16, k=16, v=16, o=16, lse=NULL, cuq=16, cuk=32, S=2, Tq=2, Tk=9000, maxq=1, maxk=5000, H=8,
+                Hkv=2, d=128, scale=0.125, causal=1, dtype=0, splits=4, stream=NULL)
+    args.update(kw)
+    return fa.library().fa_fwd_varlen_kv(*[args[n] for n in ("q", "k", "v", "o", "lse", "cuq", "cuk", "S", "Tq",
+                                                             "Tk", "maxq", "maxk", "H", "Hkv", "d", "scale",
+                                                             "causal", "dtype", "splits", "stream")])
+
+
+def combine(**kw):
+    args = dict(o=16, l=16, P=3, B=1, N=10, H=4, d=128, out=16, lse=NULL, dtype=0, stream=NULL)
+    args.update(kw)
+    return fa.library().fa_lse_combine(*[args[n] for n in ("o", "l", "P", "B", "N", "H", "d", "out", "lse", "dtype",
+                                                           "stream")])
+
+
+@pytest.mark.parametrize("kw", [dict(Nq=0), dict(Nk=0), dict(splits=-1), dict(Hkv=3), dict(k=NULL), dict(o=8),
+                                dict(dtype=5), dict(causal=2), dict(B=1 << 16, Nk=1 << 16)])
+def test_fwd_kv_rejects_invalid_arguments(kw):
+    assert fwd_kv(**kw) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(cuk=NULL), dict(cuk=2), dict(Tk=0), dict(maxq=0), dict(maxk=-1),
+                                dict(splits=-2), dict(Hkv=16), dict(dtype=3)])
+def test_varlen_kv_rejects_invalid_arguments(kw):
+    assert varlen_kv(**kw) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(o=NULL), dict(l=NULL), dict(out=NULL), dict(o=4), dict(out=8), dict(P=0),
+                                dict(B=0), dict(N=0), dict(H=0), dict(dtype=2), dict(N=1 << 20, H=1 << 12)])
+def test_lse_combine_rejects_invalid_arguments(kw):
+    assert combine(**kw) == fa.FA_ERR_INVALID_ARG
+
+
+def test_new_entry_points_reject_unsupported_head_dim():
+    assert fwd_kv(d=32) == fa.FA_ERR_UNSUPPORTED
+    assert varlen_kv(d=96) == fa.FA_ERR_UNSUPPORTED
+    assert combine(d=256) == fa.FA_ERR_UNSUPPORTED
+
+
 def test_valid_arguments_without_gpu_report_no_device():
     torch = pytest.importorskip("torch")
     if torch.cuda.is_available():
@@ -136,6 +184,11 @@ def test_valid_arguments_without_gpu_report_no_device():
         for dtype in (0, 1):
             assert gqa(H=H, Hkv=Hkv, dtype=dtype) == fa.FA_ERR_NO_DEVICE
             assert varlen_gqa(H=H, Hkv=Hkv, dtype=dtype) == fa.FA_ERR_NO_DEVICE
+    for splits in (0, 1, 3, 1000):
+        assert fwd_kv(splits=splits) == fa.FA_ERR_NO_DEVICE
+        assert varlen_kv(splits=splits) == fa.FA_ERR_NO_DEVICE
+    assert fwd_kv(Nq=300, Nk=100) == fa.FA_ERR_NO_DEVICE       # rows without keys are allowed
+    assert combine() == fa.FA_ERR_NO_DEVICE
 
 
 @pytest.mark.parametrize("opt,val,ok", [(1, 8.0, True), (1, 0.0, True), (1, 1e30, True), (1, -1.0, False),
