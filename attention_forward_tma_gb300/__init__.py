@@ -16,7 +16,7 @@ import threading
 
 from . import _build
 
-__all__ = ["fa_fwd", "fa_fwd_varlen", "lse_combine", "FaError", "set_option", "last_device_status", "library",
+__all__ = ["fa_fwd", "fa_fwd_varlen", "lse_combine", "num_splits", "num_splits_varlen", "FaError", "set_option", "last_device_status", "library",
            "FA_DTYPE_BF16", "FA_DTYPE_FP16",
            "selftest_mma_tile", "selftest_exp2", "selftest_wait_timeout", "varlen_schedule",
            "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
@@ -36,6 +36,8 @@ _SIGNATURES = {
     "fa_fwd_varlen_kv": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _ci,
                          _ci, _vp],
     "fa_lse_combine": [_vp, _vp, _ci, _ci, _ci, _ci, _ci, _vp, _vp, _ci, _vp],
+    "fa_fwd_kv_splits": [_ci, _ci, _ci, _ci, _ci, _ci, ctypes.POINTER(_ci)],
+    "fa_fwd_varlen_kv_splits": [_ci, _ci, _ci, _ci, _ci, _ci, ctypes.POINTER(_ci)],
     "fa_fwd_varlen_noalloc": [_vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _vp],
     "fa_error_string": [_ci],
     "fa_last_device_status": [_vp, ctypes.POINTER(ctypes.c_ulonglong)],
@@ -228,6 +230,21 @@ def lse_combine(o_parts, lse_parts, *, out=None, lse=None, return_lse: bool = Tr
                                     lse.data_ptr() if lse is not None else None, code,
                                     _stream_handle(stream, o_parts.device)), "fa_lse_combine")
     return (out, lse) if lse is not None else out
+
+
+def num_splits(B: int, H: int, H_kv: int, N_q: int, N_kv: int, requested: int = 0) -> int:
+    """Key ranges fa_fwd would use for these sizes with num_splits=requested (0: the library's choice)."""
+    n = ctypes.c_int(0)
+    _check(library().fa_fwd_kv_splits(B, H, H_kv, N_q, N_kv, requested, ctypes.byref(n)), "fa_fwd_kv_splits")
+    return n.value
+
+
+def num_splits_varlen(num_seqs: int, total_q: int, max_seqlen_k: int, H: int, H_kv: int, requested: int = 0) -> int:
+    """Key ranges fa_fwd_varlen would use with num_splits=requested."""
+    n = ctypes.c_int(0)
+    _check(library().fa_fwd_varlen_kv_splits(num_seqs, total_q, max_seqlen_k, H, H_kv, requested, ctypes.byref(n)),
+           "fa_fwd_varlen_kv_splits")
+    return n.value
 
 
 def last_device_status(stream=None):

@@ -121,14 +121,16 @@ int make_maps(fa::FwdParams& p, const void* q, const void* k, const void* v, voi
 
 // Key ranges per task. requested > 0: that many (at most one per 128-key block
 // and kMaxSplits). requested = 0: split only when the unsplit tasks cannot fill
-// the SMs and the keys are long enough, aiming at about two tasks per SM with
-// at least four K/V blocks per range.
+// the SMs, into as many ranges as keep all tasks in one wave (tasks <= SMs), with
+// at least four K/V blocks per range. (Measured on GB300 for one query row
+// against 4K-128K keys: one full wave beat both fewer ranges and a second,
+// partial wave; e.g. 64 tasks x 2 ranges 235 us, x 5 ranges 279 us.)
 constexpr int kMaxSplits = 128;
 int choose_splits(int requested, long long base_tasks, int key_blocks, int sm_count) {
   const int most = key_blocks < 1 ? 1 : (key_blocks < kMaxSplits ? key_blocks : kMaxSplits);
   if (requested > 0) return requested < most ? requested : most;
   if (base_tasks >= sm_count || key_blocks < 8) return 1;
-  long long want = (2LL * sm_count + base_tasks - 1) / base_tasks;
+  long long want = sm_count / base_tasks;
   const int by_len = key_blocks / 4;
   if (want > by_len) want = by_len;
   if (want > 64) want = 64;
@@ -624,6 +626,34 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
                   void* stream) {
   return fa_fwd_varlen_gqa(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, max_seqlen, H, H, d, scale, causal,
                            FA_DTYPE_BF16, stream);
+}
+
+int fa_fwd_kv_splits(int B, int H, int H_kv, int N_q, int N_kv, int num_splits, int* splits) {
+  if (!splits || B <= 0 || H <= 0 || H_kv <= 0 || N_q <= 0 || N_kv <= 0 || num_splits < 0) return FA_ERR_INVALID_ARG;
+  int gshift = 0;
+  int st = check_heads(H, H_kv, &gshift);
+  if (st != FA_OK) return st;
+  DevInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != FA_OK) return st;
+  const long long num_m = (((long long)N_q << gshift) + fa::kTaskRows - 1) / fa::kTaskRows;
+  *splits = choose_splits(num_splits, (long long)B * H_kv * num_m, (N_kv + fa::kBlockN - 1) / fa::kBlockN,
+                          dev->sm_count);
+  return FA_OK;
+}
+
+int fa_fwd_varlen_kv_splits(int num_seqs, int total_q, int max_seqlen_kv, int H, int H_kv, int num_splits,
+                            int* splits) {
+  if (!splits || num_seqs <= 0 || total_q <= 0 || max_seqlen_kv < 0 || H <= 0 || H_kv <= 0 || num_splits < 0)
+    return FA_ERR_INVALID_ARG;
+  int gshift = 0;
+  int st = check_heads(H, H_kv, &gshift);
+  if (st != FA_OK) return st;
+  DevInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != FA_OK) return st;
+  const long long base =
+      (long long)H_kv * ((((long long)total_q << gshift) + fa::kTaskRows - 1) / fa::kTaskRows + num_seqs);
+  *splits = choose_splits(num_splits, base, (max_seqlen_kv + fa::kBlockN - 1) / fa::kBlockN, dev->sm_count);
+  return FA_OK;
 }
 
 int fa_lse_combine(const float* o_parts, const float* lse_parts, int num_parts, int B, int N, int H, int d, void* o,

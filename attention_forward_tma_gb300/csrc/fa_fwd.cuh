@@ -46,7 +46,7 @@
 #include "ptx.cuh"
 
 #ifndef FA_KV_STAGES_D128
-#define FA_KV_STAGES_D128 3
+#define FA_KV_STAGES_D128 4
 #endif
 
 namespace fa {
@@ -160,6 +160,7 @@ struct Layout {
   static constexpr int kClcOff = kMiscOff + 64;                 // 16-byte launch-control response
   static constexpr int kSmemBytes = kClcOff + 16;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;         // slack for 1024-byte alignment
+  static_assert(kSmemAlloc <= 227 * 1024, "shared memory per CTA");
   // tensor memory columns of S_t and O_t
   static __device__ __forceinline__ uint32_t col_s(int t) { return (uint32_t)t * 128u; }
   static __device__ __forceinline__ uint32_t col_o(int t) { return 256u + (uint32_t)t * 128u; }
@@ -216,6 +217,13 @@ __device__ __forceinline__ bool get_task(const FwdParams& p, bool causal, int id
   t.lse_base = (b * p.H + (t.kvh << p.gshift)) * p.N;
   t.lse_hstride = p.N;
   return true;
+}
+
+// Q tile 1 of the task holds no query row of the sequence (its packed rows
+// start at or past the end): the task runs Q tile 0 only. Decoding (a few query
+// rows per sequence) and the ragged last block of a sequence are such tasks.
+__device__ __forceinline__ bool task_one_tile(const Task& t, int gshift) {
+  return packed_pos(t, kBlockM, gshift) >= t.len;
 }
 
 // Causal offset: query position i sees keys j <= i + off, with off = N_kv - N_q
@@ -484,8 +492,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       uint32_t stage = 0, phase = 0;
       // armed full barriers and the parity of their last arm, for the drain on abort
       uint32_t q_armed = 0, q_par = 0, kv_armed = 0, kv_par = 0;
+      uint32_t q_uses = 0;   // bit t: parity of the number of loads into Q slot t so far
       bool ok = true;
-      int it = 0;
       auto load_tile = [&](const CUtensorMap* m, uint32_t dst, int tok, int h, uint32_t b) {
 #pragma unroll
         for (int c = 0; c < L::kHalves; ++c) tma_load_3d(dst + c * L::kSlabBytes, m, c * 64, h, tok, b);
@@ -504,7 +512,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         return true;
       };
       auto load_q = [&](int t, int tok, int h, int blk) -> bool {
-        if (!w.wait(bar(L::bQEmpty + t), (it & 1) ^ 1, L::bQEmpty + t, blk)) return false;
+        const uint32_t use = (q_uses >> t) & 1u;
+        if (!w.wait(bar(L::bQEmpty + t), use ^ 1u, L::bQEmpty + t, blk)) return false;
         if (leader) {
           mbar_arrive_expect_tx(bar(L::bQFull + t), L::kTileBytes);
           load_tile(&p.tm_q, sQ + t * L::kTileBytes, tok, h, bar(L::bQFull + t));
@@ -512,7 +521,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         __syncwarp();
         tr.rec(t == 0 ? kEvQ0 : kEvQ1, blk);
         q_armed |= 1u << t;
-        q_par = (q_par & ~(1u << t)) | ((uint32_t)(it & 1) << t);
+        q_par = (q_par & ~(1u << t)) | (use << t);
+        q_uses ^= 1u << t;
         return true;
       };
       // The producer also claims this CTA's tasks and publishes them to the other
@@ -560,12 +570,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         const KRange kr = task_range(p, tk, CAUSAL);
         if (kr.hi <= kr.lo) continue;   // no key to attend to: nothing to load
         const int nb = kr.hi - kr.lo;
+        const bool one = task_one_tile(tk, p.gshift);
         // load order: Q_0, K_{hi-1}, Q_1, V_{hi-1}, K_{hi-2}, V_{hi-2}, ..., K_lo, V_lo
-        // (Q tile t: positions from packed_pos(t * 128) of query heads kvh*G .. kvh*G+G-1)
+        // (Q tile t: positions from packed_pos(t * 128) of query heads kvh*G .. kvh*G+G-1;
+        // no Q_1 when tile 1 has no row)
 #pragma unroll 1
         for (int e = 0; ok && e < 2 * nb + 2; ++e) {
           if (e == 0 || e == 2) {
             const int t = e >> 1;
+            if (t == 1 && one) continue;
             ok = load_q(t, tk.tok0 + packed_pos(tk, t * kBlockM, p.gshift), tk.kvh << p.gshift, kr.hi - 1);
           } else {
             const int kvi = e == 1 ? 0 : e - 2;          // even: K, odd: V
@@ -573,7 +586,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             ok = load_kv((kvi & 1) ? &p.tm_v : &p.tm_k, tk.tok0k + j * kBlockN, tk.kvh, j);
           }
         }
-        ++it;
       }
       if (!ok) {
         // drain: every armed full barrier completes once its bytes have landed
@@ -598,8 +610,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       const bool leader = elect_one();
       uint32_t stage = 0, phase = 0;
       uint32_t po_par = 0, p2_par = 0;  // bit t: parity of the next wait on p_o[t] / p2[t]
+      uint32_t qf_par = 0;              // bit t: parity of the next wait on q_full[t]
       bool ok = true;
-      int it = 0;
       const uint32_t S0 = tmem + L::col_s(0), S1 = tmem + L::col_s(1);
       const uint32_t O0 = tmem + L::col_o(0), O1 = tmem + L::col_o(1);
       const uint32_t P0 = S0 + 64, P1 = S1 + 64;
@@ -616,14 +628,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         if (kr.hi <= kr.lo) continue;   // no key: no MMA (the epilogue writes the empty rows)
         const int nb = kr.hi - kr.lo;
         const int skip0 = task_skip0(tk, kr, CAUSAL, p.gshift);   // tile 0 starts one block lower
-        const uint32_t qpar = it & 1;
+        const int t_last = task_one_tile(tk, p.gshift) ? 0 : 1;   // the tiles of this task: 0 .. t_last
         // prologue: S_0 and S_1 for the top block (S_0 only if tile 0 sees it)
         uint32_t ks = stage;
         if (!w.wait(bar(L::bKVFull + ks), phase, L::bKVFull + ks, kr.hi - 1)) { ok = false; break; }
         if (++stage == L::kStages) { stage = 0; phase ^= 1; }
 #pragma unroll 1
-        for (int t = 0; t < 2; ++t) {
-          if (!w.wait(bar(L::bQFull + t), qpar, L::bQFull + t, nb - 1)) { ok = false; break; }
+        for (int t = 0; t <= t_last; ++t) {
+          if (!w.wait(bar(L::bQFull + t), (qf_par >> t) & 1, L::bQFull + t, nb - 1)) { ok = false; break; }
+          qf_par ^= 1u << t;
           tc_fence_after();
           tr.rec(kEvIssueBegin, 0);
           if (leader) {
@@ -631,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
               issue_qk<D, F16>(t ? S1 : S0, t ? Q1 : Q0, Kd + ks * kStageStep);
               mma_commit(bar(L::bSFull + t));
             }
-            if (t == 1) mma_commit(bar(L::bKVEmpty + ks));
+            if (t == t_last) mma_commit(bar(L::bKVEmpty + ks));
             if (nb == 1) mma_commit(bar(L::bQEmpty + t));   // Q_t's last use: the next task's Q may load
           }
           __syncwarp();
@@ -647,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           if (++stage == L::kStages) { stage = 0; phase ^= 1; }
           // per Q tile t: O_t (+)= P_t V_j in two halves, then S_t for block j-1
 #pragma unroll 1
-          for (int t = 0; t < 2; ++t) {
+          for (int t = 0; t <= t_last; ++t) {
             const uint32_t Ot = t ? O1 : O0, Pt = t ? P1 : P0, St = t ? S1 : S0;
             const uint64_t Qt = t ? Q1 : Q0;
             const int first_i = t == 0 ? skip0 : 0;   // this tile's first block
@@ -667,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
               if (leader) issue_pv<D, kSplitP, kBlockN, F16>(Ot, Pt, Vd + vs * kStageStep, true);
               tr.rec(kEvPV0b + 4 * t, j);
             }
-            if (t == 1 && leader) mma_commit(bar(L::bKVEmpty + vs));   // V_j read by both tiles
+            if (t == t_last && leader) mma_commit(bar(L::bKVEmpty + vs));   // V_j read by the task's tiles
             if (!last) {
               if (t == 0) {
                 ks = stage;
@@ -680,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
               if (leader) {
                 issue_qk<D, F16>(St, Qt, Kd + ks * kStageStep);
                 mma_commit(bar(L::bSFull + t));
-                if (t == 1) mma_commit(bar(L::bKVEmpty + ks));           // K_{j-1} read by both tiles
+                if (t == t_last) mma_commit(bar(L::bKVEmpty + ks));      // K_{j-1} read by the task's tiles
                 if (j - 1 == kr.lo) mma_commit(bar(L::bQEmpty + t));     // last use of Q_t in this task
               }
               tr.rec(kEvS0 + t, j - 1);
@@ -691,7 +704,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           }
           if (!ok) break;
         }
-        ++it;
       }
       // all issued MMAs must finish before the tensor memory is released
       if (leader) mma_commit(bar(L::bDrain));
@@ -733,6 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         store_lse(-INFINITY);
         continue;
       }
+      if (t == 1 && task_one_tile(tk, p.gshift)) continue;   // this tile has no row of the sequence
       const int hi = kr.hi - (t == 0 ? task_skip0(tk, kr, CAUSAL, p.gshift) : 0);   // this tile's top block + 1
       const int nb = hi - kr.lo;
       const int row_limit = CAUSAL ? min(pos + off + 1, tk.lenk) : tk.lenk;  // keys [0, row_limit) visible
@@ -915,11 +928,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       }
       const int nb = kr.hi - kr.lo;
       const int skip0 = task_skip0(tk, kr, CAUSAL, p.gshift);
+      const int t_last = task_one_tile(tk, p.gshift) ? 0 : 1;   // the tiles of this task: 0 .. t_last
       tr.rec(kEvTask, nb);
       for (int i = 1; ok && i < nb; ++i) {
         const int j = kr.hi - 1 - i;
 #pragma unroll 1
-        for (int t = 0; t < 2; ++t) {
+        for (int t = 0; t <= t_last; ++t) {
           if (t == 0 && i - skip0 < 1) continue;   // tile 0's first block needs no correction
           if (!w.wait(bar(L::bCorrFull + t), (cf_par >> t) & 1, L::bCorrFull + t, j)) { ok = false; break; }
           cf_par ^= 1u << t;
@@ -948,7 +962,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       if (!ok) break;
       // epilogue: O_t / row_sum -> bf16 / fp16 -> global
 #pragma unroll 1
-      for (int t = 0; t < 2; ++t) {
+      for (int t = 0; t <= t_last; ++t) {
         if (!w.wait(bar(L::bCorrFull + t), (cf_par >> t) & 1, L::bCorrFull + t, -1)) { ok = false; break; }
         cf_par ^= 1u << t;
         const float l = mail[t * kBlockM + r];

@@ -187,7 +187,17 @@ class ClockSampler:
 def workload_flops(w, x=None):
     if w.varlen:
         return fa_inputs.varlen_flops(x["lengths"], w.H, w.d, w.causal)
-    return fa_inputs.attention_flops(w.B, w.H, w.N, w.d, w.causal)
+    return fa_inputs.attention_flops(w.B, w.H, w.N, w.d, w.causal, Nk=w.Nk)
+
+
+def workload_bytes(w, x=None):
+    """Compulsory HBM bytes of one step: read Q, K, V once, write O and LSE once."""
+    if w.varlen:
+        T = int(x["cu_seqlens"][-1])
+        rows_q, rows_k = T, T
+    else:
+        rows_q, rows_k = w.B * w.N, w.B * w.Nk
+    return 2.0 * w.d * (2 * rows_q * w.H + 2 * rows_k * w.Hkv) + 4.0 * rows_q * w.H
 
 
 def oracle_sample(w, x, budget_rows: int, seed: int):
@@ -208,7 +218,7 @@ def oracle_sample(w, x, budget_rows: int, seed: int):
         h = rng.integers(0, w.H, budget_rows)
         i = rng.integers(0, w.N, budget_rows)
         rows = np.stack([b, h, i], 1).astype(np.int64)
-        nkeys = np.minimum(i + 1, w.N) if w.causal else np.full(budget_rows, w.N)
+        nkeys = np.clip(i + (w.Nk - w.N) + 1, 0, w.Nk) if w.causal else np.full(budget_rows, w.Nk)
     flops = float((4.0 * w.d * nkeys).sum())
     return rows, flops
 
@@ -299,14 +309,17 @@ def run_ours(a, dist):
         lse = torch.empty((w.H, q.shape[0]), dtype=torch.float32, device=dev)
 
         def step(s=None):
-            fa.fa_fwd_varlen(q, k, v, cu, maxL, scale=w.scale, causal=w.causal, out=o, lse=lse, stream=s)
-        launches_per_step = 2
+            fa.fa_fwd_varlen(q, k, v, cu, maxL, scale=w.scale, causal=w.causal, out=o, lse=lse,
+                             num_splits=w.splits, stream=s)
+        splits = fa.num_splits_varlen(len(x["lengths"]), q.shape[0], maxL, w.H, w.Hkv, w.splits)
+        launches_per_step = 2 + (1 if splits > 1 else 0)   # schedule, attention (, merge)
     else:
         lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
 
         def step(s=None):
-            fa.fa_fwd(q, k, v, scale=w.scale, causal=w.causal, out=o, lse=lse, stream=s)
-        launches_per_step = 1
+            fa.fa_fwd(q, k, v, scale=w.scale, causal=w.causal, out=o, lse=lse, num_splits=w.splits, stream=s)
+        splits = fa.num_splits(w.B, w.H, w.Hkv, w.N, w.Nk, w.splits)
+        launches_per_step = 1 + (1 if splits > 1 else 0)   # attention (, merge)
 
     stream = torch.cuda.current_stream(dev)
     for _ in range(a.warmup):
@@ -316,6 +329,13 @@ def run_ours(a, dist):
     if st != fa.FA_OK:
         raise RuntimeError(f"device status {st} ({word:#x}) after warm-up")
 
+    # Inputs that fit in L2 would be served from L2 on repeated steps: then a
+    # 256 MiB buffer is written between steps (outside the per-step events) and
+    # the value comes from the per-step events alone.
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+    in_bytes = (2 * q.numel() + k.numel() + v.numel()) * 2
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if in_bytes <= l2_bytes else None
+
     # timed region: K steps, per-launch CUDA events on the launching stream
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
     dist.barrier()
@@ -323,6 +343,8 @@ def run_ours(a, dist):
     with ClockSampler(dist.local) as clocks:
         t0 = time.perf_counter()
         for i in range(a.steps):
+            if flush is not None:
+                flush.fill_(i & 0xff)
             ev[i][0].record(stream)
             step(stream)
             ev[i][1].record(stream)
@@ -333,7 +355,7 @@ def run_ours(a, dist):
     if st != fa.FA_OK:
         raise RuntimeError(f"device status {st} ({word:#x}) in the timed region")
     per_launch_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
-    region_ms = ev[0][0].elapsed_time(ev[-1][1])
+    region_ms = ev[0][0].elapsed_time(ev[-1][1]) if flush is None else sum(per_launch_ms)
     region_s = dist.max(region_ms / 1e3)
     value = dist.world * flops * a.steps / region_s / 1e12
     avg_launch_s = sum(per_launch_ms) / len(per_launch_ms) / 1e3
@@ -350,9 +372,10 @@ def run_ours(a, dist):
         dk.copy_(hk, non_blocking=True)
         dv.copy_(hv, non_blocking=True)
         if w.varlen:
-            fa.fa_fwd_varlen(dq, dk, dv, cu, maxL, scale=w.scale, causal=w.causal, out=o, lse=lse)
+            fa.fa_fwd_varlen(dq, dk, dv, cu, maxL, scale=w.scale, causal=w.causal, out=o, lse=lse,
+                             num_splits=w.splits)
         else:
-            fa.fa_fwd(dq, dk, dv, scale=w.scale, causal=w.causal, out=o, lse=lse)
+            fa.fa_fwd(dq, dk, dv, scale=w.scale, causal=w.causal, out=o, lse=lse, num_splits=w.splits)
         ho.copy_(o, non_blocking=True)
         hl.copy_(lse, non_blocking=True)
 
@@ -377,12 +400,31 @@ def run_ours(a, dist):
     clk = clocks.summary()
     max_mhz = clk["sm_max_mhz"] or 2070.0
     theoretical = props.multi_processor_count * FLOP_PER_CLK_PER_SM * max_mhz * 1e6 / 1e12
-    achieved = flops / avg_launch_s / 1e12
     traffic = profiled_traffic(w.name)
+    # the bound follows the arithmetic intensity: below the ridge of the measured
+    # peaks (FLOP per byte) the step is an HBM stream, above it a contraction
+    nbytes = workload_bytes(w, x)
+    if flops / nbytes < peak * 1e12 / (hbm * 1e9):
+        roof = {"bound": "hbm", "achieved": nbytes / avg_launch_s / 1e9, "peak": hbm, "unit": "GB/s",
+                "frac": nbytes / avg_launch_s / 1e9 / hbm, "traffic": traffic,
+                "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                "bytes_per_step": nbytes}
+    else:
+        achieved = flops / avg_launch_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": traffic,
+                "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)" if peak_src == "measured"
+                else "fallback 1.9 PFLOP/s bf16 burst"}
+    roof.update({"kernel": "fa_fwd_kernel" + (" + fa_combine_kernel" if splits > 1 else ""),
+                 "avg_launch_ms": avg_launch_s * 1e3, "min_launch_ms": min(per_launch_ms), "wall_s": wall})
     cfg = {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.Hkv, "N": w.N, "d": w.d, "causal": w.causal,
-           "scale": w.scale, "seed": w.seed, "l2": "inputs larger than L2 (Q+K+V+O = %.0f MiB), no flush"
-           % ((2 * q.numel() + k.numel() + v.numel()) * 2 / 2 ** 20),
-           "flops_per_step": flops}
+           "scale": w.scale, "seed": w.seed,
+           "l2": ("inputs larger than L2 (Q+K+V+O = %.0f MiB), no flush" % (in_bytes / 2 ** 20)) if flush is None
+           else ("inputs smaller than L2 (Q+K+V+O = %.1f MiB): 256 MiB written between steps, value from the "
+                 "per-step events" % (in_bytes / 2 ** 20)),
+           "flops_per_step": flops, "key_splits": splits}
+    if w.Nk != w.N:
+        cfg["N_kv"] = w.Nk
     if w.varlen:
         cfg["lengths"] = [int(L) for L in x["lengths"]]
     line = {
@@ -392,12 +434,7 @@ def run_ours(a, dist):
         "pct_of_measured_peak": 100.0 * value / dist.world / peak,
         "pct_of_theoretical_peak": 100.0 * value / dist.world / theoretical,
         "theoretical_peak_tflops": theoretical,
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)" if peak_src == "measured"
-                     else "fallback 1.9 PFLOP/s bf16 burst",
-                     "kernel": "fa_fwd_kernel", "avg_launch_ms": avg_launch_s * 1e3,
-                     "min_launch_ms": min(per_launch_ms), "wall_s": wall},
+        "roofline": roof,
         "e2e": {"value": dist.world * flops * n_e2e / e2e_s / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e},
         "gpu_launches": launches_per_step * a.steps,

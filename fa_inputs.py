@@ -96,6 +96,7 @@ class Workload:
     Hkv: int = 0                  # K/V heads (0: the same as H)
     dtype: str = "bf16"           # element type of Q, K, V and O: "bf16" or "f16"
     Nk: int = 0                   # key rows per sequence (0: the same as N)
+    splits: int = 1               # key ranges per task passed to the library (0: its choice)
 
     def __post_init__(self):
         if math.isnan(self.scale):
@@ -140,7 +141,7 @@ WORKLOADS.update({
 # merged through their LSE.
 WORKLOADS.update({
     "d1_decode_b8h32kv8nq1nk32768d128": Workload("d1_decode_b8h32kv8nq1nk32768d128", B=8, H=32, N=1, d=128,
-                                                 causal=True, seed=20269, Hkv=8, Nk=32768),
+                                                 causal=True, seed=20269, Hkv=8, Nk=32768, splits=0),
 })
 
 

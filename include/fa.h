@@ -167,6 +167,15 @@ int fa_fwd_varlen_kv(const void* q, const void* k, const void* v, void* o, float
                      int causal, int dtype, int num_splits, void* stream);
 
 /*
+ * The number of key ranges fa_fwd_kv / fa_fwd_varlen_kv would use for these
+ * sizes on the current device, given the same num_splits argument (0 = the
+ * library's choice). With *splits > 1 a call launches the merge kernel too.
+ */
+int fa_fwd_kv_splits(int B, int H, int H_kv, int N_q, int N_kv, int num_splits, int* splits);
+int fa_fwd_varlen_kv_splits(int num_seqs, int total_q, int max_seqlen_kv, int H, int H_kv, int num_splits,
+                            int* splits);
+
+/*
  * Merge of attention results computed over disjoint key sets (for example the
  * key ranges of one sequence held by different GPUs), through their LSE:
  *   LSE = ln sum_p exp(LSE_p),   O = sum_p exp(LSE_p - LSE) * O_p
