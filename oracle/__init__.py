@@ -12,6 +12,8 @@ from them. Inputs come from ``fa_inputs`` (random numbers only).
   K/V head h // (H // H_kv)).
 * ``lse_combine`` merges partial results over disjoint key sets through their
   LSE (``lse_combine.py``).
+* ``attention_backward`` gives the fp64 gradients dQ, dK, dV of the forward for
+  an upstream dO (``attn_backward.py``).
 * ``online_softmax`` is a separate, slow NumPy model of the blocked update with
   delayed rescaling, used to explain GPU differences and to check that the
   result does not depend on the threshold.
@@ -191,5 +193,6 @@ def attention_rows_varlen(q, k, v, cu_seqlens, rows, scale: float, causal: bool,
     return o, lse
 
 
+from .attn_backward import attention_backward, attention_forward  # noqa: E402,F401
 from .lse_combine import lse_combine  # noqa: E402,F401
 from .online_softmax import online_softmax_rows  # noqa: E402,F401
