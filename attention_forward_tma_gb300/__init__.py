@@ -16,7 +16,7 @@ import threading
 
 from . import _build
 
-__all__ = ["fa_fwd", "fa_fwd_varlen", "lse_combine", "num_splits", "num_splits_varlen", "FaError", "set_option", "last_device_status", "library",
+__all__ = ["fa_fwd", "fa_fwd_varlen", "fa_bwd", "lse_combine", "num_splits", "num_splits_varlen", "FaError", "set_option", "last_device_status", "library",
            "FA_DTYPE_BF16", "FA_DTYPE_FP16",
            "selftest_mma_tile", "selftest_exp2", "selftest_wait_timeout", "varlen_schedule",
            "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
@@ -36,6 +36,7 @@ _SIGNATURES = {
     "fa_fwd_varlen_kv": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _ci,
                          _ci, _vp],
     "fa_lse_combine": [_vp, _vp, _ci, _ci, _ci, _ci, _ci, _vp, _vp, _ci, _vp],
+    "fa_bwd": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _ci, _vp],
     "fa_fwd_kv_splits": [_ci, _ci, _ci, _ci, _ci, _ci, ctypes.POINTER(_ci)],
     "fa_fwd_varlen_kv_splits": [_ci, _ci, _ci, _ci, _ci, _ci, ctypes.POINTER(_ci)],
     "fa_fwd_varlen_noalloc": [_vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _vp],
@@ -205,6 +206,39 @@ def fa_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, *, scale: float | None =
                                     _stream_handle(stream, q.device))
     _check(st, "fa_fwd_varlen")
     return (out, lse) if lse is not None else out
+
+
+def fa_bwd(q, k, v, o, dout, lse, *, scale: float | None = None, causal: bool = False, dq=None, dk=None, dv=None,
+           stream=None):
+    """Backward of fa_fwd: q, o, dout [B, N_q, H, d]; k, v [B, N_kv, H_kv, d] (bf16 or fp16);
+    lse fp32 [B, H, N_q] as returned by fa_fwd for the same inputs. Returns (dq, dk, dv)."""
+    torch = _torch()
+    code = _dtype_code(q)
+    _need(q, "q", q.dtype, 4)
+    B, N, H, d = q.shape
+    if not (isinstance(k, torch.Tensor) and k.dim() == 4):
+        raise TypeError("k must be a 4-dimensional torch.Tensor")
+    Nk, Hkv = k.shape[1], k.shape[2]
+    for name, t, shape in (("k", k, (B, Nk, Hkv, d)), ("v", v, (B, Nk, Hkv, d)), ("o", o, (B, N, H, d)),
+                           ("dout", dout, (B, N, H, d))):
+        _need(t, name, q.dtype, 4)
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} must have shape {shape}")
+    _need(lse, "lse", torch.float32, 3)
+    if tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse must have shape (B, H, N_q)")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t, ref in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        _need(t, name, q.dtype, 4)
+        if t.shape != ref.shape:
+            raise ValueError(f"{name} has the wrong shape")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    _check(library().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                            dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Hkv, N, Nk, d, scale,
+                            int(bool(causal)), code, _stream_handle(stream, q.device)), "fa_bwd")
+    return dq, dk, dv
 
 
 def lse_combine(o_parts, lse_parts, *, out=None, lse=None, return_lse: bool = True, dtype=None, stream=None):

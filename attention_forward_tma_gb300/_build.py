@@ -1,6 +1,6 @@
 """In-tree build of libfa_gb300.so with nvcc for sm_103a (no CMake, no setuptools).
 
-The two translation units are compiled in parallel, then linked into a shared
+The translation units are compiled in parallel, then linked into a shared
 library next to this file. ``build()`` is a no-op when the library is newer than
 every source and header.
 """
@@ -21,7 +21,7 @@ LIB_TRACE = os.path.join(PKG, "libfa_gb300_trace.so")   # -DFA_TRACE: clock stam
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          f"-I{INCLUDE}", f"-I{CSRC}"]
-UNITS = ["fa_api.cu", "fa_selftest.cu"]
+UNITS = ["fa_api.cu", "fa_bwd_api.cu", "fa_selftest.cu"]
 
 
 def nvcc() -> str:

@@ -12,9 +12,13 @@
 
 #include "fa.h"
 #include "fa_fwd.cuh"
+#include "fa_host.cuh"
 #include "fa_selftest.h"
 
 namespace {
+using fa_host::aligned;
+using fa_host::check_heads;
+using fa_host::make_map;
 
 // ------------------------------------------------------------------ options
 struct Options {
@@ -28,25 +32,6 @@ Options g_opt;
 // tracing builds: where fa_fwd / fa_fwd_varlen write their clock stamps
 unsigned long long* g_trace_buf = nullptr;
 int g_trace_ctas = 0;
-
-// ------------------------------------------------------------------ driver entry point
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
 
 // ------------------------------------------------------------------ per-device facts
 struct DevInfo {
@@ -85,24 +70,6 @@ int device_info(DevInfo** out) {
   }
   *out = &d;
   return d.supported ? FA_OK : FA_ERR_UNSUPPORTED;
-}
-
-// 3-D map over a [tokens, heads, d] tensor of 16-bit elements: x = d (contiguous),
-// y = head, z = token. Box = 64 x box_heads x (128 / box_heads): one 128-byte
-// slab of a 128-row tile whose row r is token r / box_heads, head r % box_heads
-// (box_heads = G packs the query heads of one K/V group; K and V use 1).
-// 128-byte swizzle; rows outside the tensor read as 0.
-int make_map(CUtensorMap* m, const void* base, long long tokens, int heads, int d, int box_heads, bool f16) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return FA_ERR_CUDA;
-  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)tokens};
-  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
-  const cuuint32_t box[3] = {64, (cuuint32_t)box_heads, (cuuint32_t)(fa::kBlockM / box_heads)};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
 // The four maps of one call: Q and O ([tokens, H, d]) with H heads in boxes of G,
@@ -167,19 +134,6 @@ struct Partials {
   }
 };
 
-// H_kv must divide H, and the group size G = H / H_kv must divide the 128 rows of
-// a Q tile (a power of two up to 128). Sets gshift = log2(G).
-int check_heads(int H, int Hkv, int* gshift) {
-  if (H <= 0 || Hkv <= 0 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
-  const int G = H / Hkv;
-  if (G > fa::kBlockM || (G & (G - 1)) != 0) return FA_ERR_UNSUPPORTED;
-  int sh = 0;
-  while ((1 << sh) < G) ++sh;
-  *gshift = sh;
-  return FA_OK;
-}
-
-bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 template <int D, bool C, bool E, bool F>
 int launch_fwd(DevInfo* dev, const fa::FwdParams& p, int grid, cudaStream_t stream) {
@@ -733,15 +687,16 @@ int fa_fwd_varlen_noalloc(const void* q, const void* k, const void* v, void* o, 
 
 int fa_last_device_status(void* stream, unsigned long long* detail) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
-  unsigned long long word = 0;
+  unsigned long long word = 0, bwd_word = 0;
   if (cudaMemcpyFromSymbol(&word, fa::g_fa_status, sizeof word) != cudaSuccess) return FA_ERR_CUDA;
-  if (detail) *detail = word;
   if (word != 0) {
     const unsigned long long zero = 0;
     if (cudaMemcpyToSymbol(fa::g_fa_status, &zero, sizeof zero) != cudaSuccess) return FA_ERR_CUDA;
-    return (int)(word & 0xff);
   }
-  return FA_OK;
+  if (fa_host::bwd_take_status(&bwd_word) != FA_OK) return FA_ERR_CUDA;
+  if (word == 0) word = bwd_word;
+  if (detail) *detail = word;
+  return word != 0 ? (int)(word & 0xff) : FA_OK;
 }
 
 }  // extern "C"

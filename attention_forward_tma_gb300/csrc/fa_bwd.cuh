@@ -1,0 +1,537 @@
+// fa_bwd.cuh -- the attention backward pass for GB300 (sm_103a).
+//
+// Gradients of O = softmax(s * Q K^T) V for an upstream dO ("FlashAttention-4（下）"
+// (argus lesson 7), section 1: recompute S and P, then the products for dV, dP,
+// dK and dQ with the elementwise softmax gradient between them):
+//
+//   P  = exp2(S * s * log2 e - LSE * log2 e)    (S = Q K^T recomputed, LSE from the forward)
+//   dV += P^T dO          dP = dO V^T          dS = s * P * (dP - D),  D = rowsum(dO * O)
+//   dK += dS^T Q          dQ += dS K
+//
+// One CTA of 384 threads owns one block of 128 keys of one (sequence, K/V head)
+// and walks over the 128-row Q tiles that can see it, accumulating dK and dV in
+// tensor memory (section 2 of the same page: TMEM accumulators let several
+// products be in flight). S and P are computed transposed (S^T = K Q^T, keys on
+// the TMEM lanes), so P^T is already the A operand of the dV product, as the page
+// describes. dQ of each (Q tile, key block) pair is added to an fp32 buffer with
+// vector atomics (section 4: the dQ sum over key blocks is a global atomic
+// accumulation). With grouped heads the Q tiles hold the packed (position, query
+// head) rows of the forward, so every query head of the group contributes to the
+// CTA's dK and dV without atomics.
+//
+// Roles: WG0 (warps 0-3, one thread per key row) computes P and dS; WG1 (warps
+// 4-7, one thread per Q-tile row) drains dQ from TMEM into the atomics and at the
+// end writes dV; warp 8 issues the TMA loads, warp 9 the tcgen05 MMAs. WG0 writes
+// dK at the end.
+//
+// Tensor memory (512 columns): dV [0, d), dK [128, 128+d), S^T [256, 384) with P^T
+// as 16-bit pairs over its upper 64 columns, dP^T [384, 512) -- reused for dQ once
+// dS is in shared memory. Shared memory: K, V, two stages of (Q, dO) and the dS
+// tile (128 keys x 128 rows, 128-byte swizzle): the same bytes are the K-major A
+// operand of dK (M = keys) and the MN-major A operand of dQ (M = rows).
+//
+// Every wait is bounded as in the forward kernel.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "fa_fwd.cuh"
+
+namespace fa {
+
+constexpr int kBwdThreads = 384;
+
+struct BwdParams {
+  CUtensorMap tm_q, tm_do;   // [tokens_q, H, d]: box 64 x G x 128/G (one packed 128-row tile)
+  CUtensorMap tm_k, tm_v;    // [tokens_k, H_kv, d]: box 64 x 1 x 128
+  const float* lse2;         // [B, H_kv, mpad], packed rows: forward LSE * log2(e)
+  const float* dsum;         // [B, H_kv, mpad], packed rows: D = rowsum(dO * O)
+  float* dq_acc;             // fp32 [tokens_q, H, d]; zero on entry
+  uint16_t* dk;              // [tokens_k, H_kv, d]
+  uint16_t* dv;              // [tokens_k, H_kv, d]
+  int B, H, Hkv, gshift, Nq, Nk;
+  int nkb;                   // 128-key blocks per sequence
+  int mpad;                  // packed rows per (b, K/V head), rounded up to 128
+  int num_tasks;
+  float scale, scale_log2;
+  unsigned long long timeout_ns;
+};
+
+template <int D>
+struct BwdLayout {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kHalves = D / 64;
+  static constexpr int kSlab = 128 * 128;            // 128 rows x 128 bytes
+  static constexpr int kTile = kHalves * kSlab;       // 128 rows x D, 16-bit
+  static constexpr int kK = 0, kV = kTile, kQ = 2 * kTile, kDO = 4 * kTile, kDS = 6 * kTile;
+  static constexpr int kBar = kDS + 2 * kSlab;        // dS: 128 keys x 128 rows
+  enum : int {
+    bKV = 0, bQFull = 1, bQEmpty = 3, bSFull = 5, bPReady = 6, bdPFull = 7, bdPEmpty = 8, bdSReady = 9,
+    bdSEmpty = 10, bdQFull = 11, bFinal = 12, bDrain = 13, kNumBars = 14
+  };
+  static constexpr int kMisc = kBar + 128;
+  static constexpr int kBytes = kMisc + 64;
+  static constexpr int kAlloc = kBytes + 1024;        // slack for 1024-byte alignment
+  static_assert(kNumBars * 8 <= 128, "barriers");
+  static_assert(kAlloc <= 227 * 1024, "shared memory per CTA");
+  static constexpr uint32_t cDV = 0, cDK = 128, cS = 256, cDP = 384;
+};
+
+// Byte offset of K step kk (16 elements) in a K-major, 128-byte-swizzled operand
+// made of 64-element slabs of 128 rows.
+template <int SLAB>
+__device__ __forceinline__ uint32_t kmajor_step(int kk) {
+  return (uint32_t)((kk / 4) * SLAB + (kk % 4) * 32);
+}
+
+__device__ __forceinline__ float half_bits_to_f32(uint16_t x, bool f16) {
+  return f16 ? __half2float(__ushort_as_half(x)) : __uint_as_float((uint32_t)x << 16);
+}
+
+// ------------------------------------------------------------------ preprocessing
+// One warp per (b, position, query head): D = rowsum(dO * O) in fp32, and the
+// forward's LSE in base 2; both written at the row's packed index
+// (b, kv head, position * G + head % G).
+template <int D, bool F16>
+__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint16_t* __restrict__ o,
+                                                         const uint16_t* __restrict__ dout,
+                                                         const float* __restrict__ lse, float* __restrict__ lse2,
+                                                         float* __restrict__ dsum, int B, int H, int gshift, int Nq,
+                                                         int mpad) {
+  constexpr int E = D / 32;
+  const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (w >= (long long)B * Nq * H) return;
+  const int lane = threadIdx.x & 31;
+  const int h = (int)(w % H);
+  const long long bp = w / H;
+  const int b = (int)(bp / Nq), pos = (int)(bp % Nq);
+  const uint16_t* orow = o + w * D + lane * E;
+  const uint16_t* grow = dout + w * D + lane * E;
+  float acc = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc = fmaf(half_bits_to_f32(orow[e], F16), half_bits_to_f32(grow[e], F16), acc);
+#pragma unroll
+  for (int x = 16; x > 0; x >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, x);
+  if (lane == 0) {
+    const int Hkv = H >> gshift;
+    const size_t idx = ((size_t)b * Hkv + (h >> gshift)) * mpad + ((size_t)pos << gshift) + (h & ((1 << gshift) - 1));
+    dsum[idx] = acc;
+    lse2[idx] = lse[((size_t)b * H + h) * Nq + pos] * 1.4426950408889634f;
+  }
+}
+
+// dQ (16-bit) from the fp32 accumulator, 4 elements per thread.
+template <bool F16>
+__global__ void __launch_bounds__(256) fa_bwd_post_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq,
+                                                          long long n4) {
+  const long long i = (long long)blockIdx.x * 256 + threadIdx.x;
+  if (i >= n4) return;
+  const float4 x = acc[i];
+  dq[i] = make_uint2(pack_16x2<F16>(x.x, x.y), pack_16x2<F16>(x.z, x.w));
+}
+
+// ------------------------------------------------------------------ the main kernel
+template <int D, bool CAUSAL, bool F16>
+__global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_constant__ BwdParams p) {
+  using L = BwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sQ = sbase + L::kQ, sDO = sbase + L::kDO,
+                 sDS = sbase + L::kDS;
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * (uint32_t)i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  volatile int* never_abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 8);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // task: key block j of (b, kv head); heavy blocks (small j under the causal mask) first
+  const int bh_total = p.B * p.Hkv;
+  const int j = (int)blockIdx.x / bh_total;
+  const int bh = (int)blockIdx.x - j * bh_total;
+  const int b = bh / p.Hkv, kvh = bh - b * p.Hkv;
+  const int off = p.Nk - p.Nq;                         // bottom-right causal offset
+  const int ntiles = ((p.Nq << p.gshift) + 127) / 128;
+  int i0 = 0;
+  if (CAUSAL) {
+    const long long pmin = (long long)j * 128 - off;   // the first position that sees key j*128
+    if (pmin > 0) i0 = (int)min((long long)ntiles, (pmin << p.gshift) / 128);
+  }
+  const int n = ntiles - i0;                           // Q tiles of this task
+  const int tok_q = b * p.Nq, tok_k = b * p.Nk;
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    *never_abort = 0;
+    for (int i = 0; i < L::kNumBars; ++i) mbar_init(bar(i), 1);
+    mbar_init(bar(L::bPReady), 128);
+    mbar_init(bar(L::bdPEmpty), 128);
+    mbar_init(bar(L::bdSReady), 128);
+    fence_mbar_init();
+  }
+  if (warp == 8 && lane == 0) {
+    prefetch_tmap(&p.tm_q);
+    prefetch_tmap(&p.tm_do);
+    prefetch_tmap(&p.tm_k);
+    prefetch_tmap(&p.tm_v);
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // register split 240 / 136 / 128 per thread for WG0 / WG1 / WG2 (sum = 3 x 168,
+  // the launch allocation)
+  if (warp >= 8) {
+    setmaxnreg_dec<128>();
+    if (warp == 8) {
+      // ============================================================ TMA producer
+      Waiter w{abort_flag, p.timeout_ns, kRoleLoad};
+      const bool leader = elect_one();
+      uint32_t q_armed = 0;   // bit s: stage s has an armed load whose completion may still be pending
+      bool kv_armed = false;
+      uint32_t q_par = 0;     // bit s: parity of the last arm of stage s
+      bool ok = true;
+      if (n > 0) {
+        if (leader) {
+          mbar_arrive_expect_tx(bar(L::bKV), 2 * L::kTile);
+#pragma unroll
+          for (int c = 0; c < L::kHalves; ++c) {
+            tma_load_3d(sK + c * L::kSlab, &p.tm_k, c * 64, kvh, tok_k + j * 128, bar(L::bKV));
+            tma_load_3d(sV + c * L::kSlab, &p.tm_v, c * 64, kvh, tok_k + j * 128, bar(L::bKV));
+          }
+        }
+        __syncwarp();
+        kv_armed = true;
+#pragma unroll 1
+        for (int k = 0; k < n; ++k) {
+          const int s = k & 1;
+          const uint32_t use = (uint32_t)(k >> 1) & 1u;
+          if (!w.wait(bar(L::bQEmpty + s), use ^ 1u, L::bQEmpty + s, k)) { ok = false; break; }
+          const int i = i0 + k;
+          const int tok = tok_q + ((i * 128) >> p.gshift);
+          if (leader) {
+            mbar_arrive_expect_tx(bar(L::bQFull + s), 2 * L::kTile);
+#pragma unroll
+            for (int c = 0; c < L::kHalves; ++c) {
+              tma_load_3d(sQ + s * L::kTile + c * L::kSlab, &p.tm_q, c * 64, kvh << p.gshift, tok, bar(L::bQFull + s));
+              tma_load_3d(sDO + s * L::kTile + c * L::kSlab, &p.tm_do, c * 64, kvh << p.gshift, tok,
+                          bar(L::bQFull + s));
+            }
+          }
+          __syncwarp();
+          q_armed |= 1u << s;
+          q_par = (q_par & ~(1u << s)) | (use << s);
+        }
+      }
+      if (!ok) {
+        Waiter d{never_abort, p.timeout_ns, kRoleDrain};
+        if (kv_armed) d.wait(bar(L::bKV), 0, L::bKV, -1);
+#pragma unroll 1
+        for (int s = 0; s < 2; ++s)
+          if (q_armed & (1u << s)) d.wait(bar(L::bQFull + s), (q_par >> s) & 1, L::bQFull + s, -1);
+      }
+    } else if (warp == 9) {
+      // ============================================================ MMA issuer
+      Waiter w{abort_flag, p.timeout_ns, kRoleMma};
+      const bool leader = elect_one();
+      constexpr uint32_t idS = idesc_f32acc2(128, 128, false, false, F16);   // S^T, dP^T: both K-major
+      constexpr uint32_t idV = idesc_f32acc2(128, D, false, true, F16);      // dV: A = P^T (TMEM), B = dO MN-major
+      constexpr uint32_t idK = idesc_f32acc2(128, D, false, true, F16);      // dK: A = dS^T K-major, B = Q MN-major
+      constexpr uint32_t idQ = idesc_f32acc2(128, D, true, true, F16);       // dQ: A = dS MN-major, B = K MN-major
+      const uint64_t Kk = smem_desc_sw128(sK, 16, 1024), Vk = smem_desc_sw128(sV, 16, 1024);
+      const uint64_t Kmn = smem_desc_sw128(sK, L::kSlab, 1024);
+      const uint64_t dSk = smem_desc_sw128(sDS, 16, 1024), dSmn = smem_desc_sw128(sDS, L::kSlab, 1024);
+      const uint32_t tS = tmem + L::cS, tP = tmem + L::cS + 64, tdP = tmem + L::cDP;
+      const uint32_t tdV = tmem + L::cDV, tdK = tmem + L::cDK;
+      auto qk = [&](int s) { return smem_desc_sw128(sQ + s * L::kTile, 16, 1024); };
+      auto qmn = [&](int s) { return smem_desc_sw128(sQ + s * L::kTile, L::kSlab, 1024); };
+      auto dok = [&](int s) { return smem_desc_sw128(sDO + s * L::kTile, 16, 1024); };
+      auto domn = [&](int s) { return smem_desc_sw128(sDO + s * L::kTile, L::kSlab, 1024); };
+      // S^T = K Q_s^T (M = keys, N = rows, K = d)
+      auto issue_s = [&](int s) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = kmajor_step<L::kSlab>(kk) >> 4;
+          mma_ss(tS, Kk + o, qk(s) + o, idS, kk > 0 ? 1u : 0u);
+        }
+      };
+      // dP^T = V dO_s^T
+      auto issue_dp = [&](int s) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = kmajor_step<L::kSlab>(kk) >> 4;
+          mma_ss(tdP, Vk + o, dok(s) + o, idS, kk > 0 ? 1u : 0u);
+        }
+      };
+      bool ok = true;
+      if (n > 0) {
+        ok = w.wait(bar(L::bKV), 0, L::bKV, -1);
+        if (ok) ok = w.wait(bar(L::bQFull + 0), 0, L::bQFull, 0);
+        if (ok) {
+          tc_fence_after();
+          if (leader) {
+            issue_s(0);
+            mma_commit(bar(L::bSFull));
+            issue_dp(0);
+            mma_commit(bar(L::bdPFull));
+          }
+          __syncwarp();
+        }
+#pragma unroll 1
+        for (int k = 0; ok && k < n; ++k) {
+          const int s = k & 1;
+          // dV += P^T dO (K = 128 rows: P^T from TMEM, 8 columns of 16-bit pairs per step)
+          if (!w.wait(bar(L::bPReady), k & 1, L::bPReady, k)) { ok = false; break; }
+          tc_fence_after();
+          if (leader) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts(tdV, tP + kk * 8, domn(s) + ((kk * 2048) >> 4), idV, (k > 0 || kk > 0) ? 1u : 0u);
+          }
+          __syncwarp();
+          // the next tile's S^T: its columns are free once this dV (issued before it) has read P^T
+          if (k + 1 < n) {
+            const int s1 = (k + 1) & 1;
+            if (!w.wait(bar(L::bQFull + s1), ((k + 1) >> 1) & 1, L::bQFull + s1, k + 1)) { ok = false; break; }
+            tc_fence_after();
+            if (leader) {
+              issue_s(s1);
+              mma_commit(bar(L::bSFull));
+            }
+            __syncwarp();
+          }
+          // dK += dS^T Q and dQ = dS K, once dS is in shared memory
+          if (!w.wait(bar(L::bdSReady), k & 1, L::bdSReady, k)) { ok = false; break; }
+          tc_fence_after();
+          if (leader) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss(tdK, dSk + (kmajor_step<L::kSlab>(kk) >> 4), qmn(s) + ((kk * 2048) >> 4), idK,
+                     (k > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss(tdP, dSmn + ((kk * 2048) >> 4), Kmn + ((kk * 2048) >> 4), idQ, kk > 0 ? 1u : 0u);
+            mma_commit(bar(L::bdQFull));
+            mma_commit(bar(L::bdSEmpty));
+            mma_commit(bar(L::bQEmpty + s));
+          }
+          __syncwarp();
+          // the next tile's dP^T, once WG1 has taken dQ out of those columns
+          if (k + 1 < n) {
+            const int s1 = (k + 1) & 1;
+            if (!w.wait(bar(L::bdPEmpty), (k + 1) & 1, L::bdPEmpty, k + 1)) { ok = false; break; }
+            tc_fence_after();
+            if (leader) {
+              issue_dp(s1);
+              mma_commit(bar(L::bdPFull));
+            }
+            __syncwarp();
+          }
+        }
+        if (ok && leader) mma_commit(bar(L::bFinal));
+        __syncwarp();
+      }
+      // every issued MMA must finish before the tensor memory is released
+      if (leader) mma_commit(bar(L::bDrain));
+      __syncwarp();
+      Waiter d{never_abort, p.timeout_ns, kRoleDrain};
+      d.wait(bar(L::bDrain), 0, L::bDrain, -1);
+    }
+  } else if (warp < 4) {
+    // ================================================================ WG0: P and dS (one key per thread)
+    setmaxnreg_inc<240>();
+    const int kr = tid;                                   // key row == TMEM lane
+    const int kabs = j * 128 + kr;
+    const bool key_ok = kabs < p.Nk;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t tS = tmem + lane_base + L::cS, tdP = tmem + lane_base + L::cDP;
+    Waiter w{abort_flag, p.timeout_ns, kRoleSoftmax0};
+    const float sl2 = p.scale_log2, sc = p.scale;
+    const size_t pk_base = ((size_t)b * p.Hkv + kvh) * p.mpad;
+    bool ok = true;
+#pragma unroll 1
+    for (int k = 0; k < n; ++k) {
+      const int i = i0 + k;
+      const float4* L2 = reinterpret_cast<const float4*>(p.lse2 + pk_base + (size_t)i * 128);
+      const float4* DS = reinterpret_cast<const float4*>(p.dsum + pk_base + (size_t)i * 128);
+      // rows [qlo, qhi) of this tile see this key: causal needs position >= kabs - off,
+      // and rows past the sequence's packed end are padding
+      const int qlo = CAUSAL ? (int)max(-1LL, min(129LL, ((long long)kabs - off) * (1LL << p.gshift) - (long long)i * 128))
+                             : 0;
+      const int qhi = key_ok ? min(128, (p.Nq << p.gshift) - i * 128) : 0;
+      if (!w.wait(bar(L::bSFull), k & 1, L::bSFull, k)) { ok = false; break; }
+      tc_fence_after();
+      float P[128];
+      {
+        uint32_t u[128];
+        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+        tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&u[64]));
+        tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&u[96]));
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 128; c += 4) {
+          const float4 l = L2[c / 4];
+          const float lv[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int q = c + e;
+            const float x = fmaf(__uint_as_float(u[q]), sl2, -lv[e]);
+            P[q] = (q >= qlo && q < qhi) ? ex2_approx(x) : 0.f;
+          }
+        }
+      }
+      // P^T as 16-bit pairs over the upper half of the S^T columns: the A operand of dV
+      {
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) pk[c] = pack_16x2<F16>(P[2 * c], P[2 * c + 1]);
+        tmem_st32(tS + 64, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(tS + 96, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      mbar_arrive(bar(L::bPReady));
+      // dS = s * P * (dP - D) -> 16-bit -> the shared dS tile (row = key, 128-byte swizzle)
+      if (k > 0 && !w.wait(bar(L::bdSEmpty), (k - 1) & 1, L::bdSEmpty, k)) { ok = false; break; }
+      if (!w.wait(bar(L::bdPFull), k & 1, L::bdPFull, k)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t u[32];
+        tmem_ld32(tdP + ch * 32, u);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          const float4 dd = DS[(ch * 32 + c) / 4];
+          const float dv[4] = {dd.x, dd.y, dd.z, dd.w};
+          float g[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) g[e] = P[ch * 32 + c + e] * (__uint_as_float(u[c + e]) - dv[e]) * sc;
+          pk[c / 2] = pack_16x2<F16>(g[0], g[1]);
+          pk[c / 2 + 1] = pack_16x2<F16>(g[2], g[3]);
+        }
+        // 32 rows = four 16-byte units of row kr in slab ch / 2
+        const uint32_t row = sDS + (uint32_t)(ch >> 1) * L::kSlab + (uint32_t)kr * 128u;
+#pragma unroll
+        for (int uu = 0; uu < 4; ++uu) {
+          const uint32_t unit = (uint32_t)((ch & 1) * 4 + uu);
+          st_shared_v4(row + ((unit ^ (uint32_t)(kr & 7)) << 4), pk[4 * uu], pk[4 * uu + 1], pk[4 * uu + 2],
+                       pk[4 * uu + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(L::bdSReady));
+    }
+    // dK (scale already in dS) -> 16-bit -> global
+    if (ok) {
+      if (n > 0 && !w.wait(bar(L::bFinal), 0, L::bFinal, -1)) ok = false;
+    }
+    if (ok) {
+      tc_fence_after();
+      uint16_t* dst = p.dk + ((size_t)(tok_k + kabs) * p.Hkv + kvh) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t u[32];
+        if (n > 0) {
+          tmem_ld32(tmem + lane_base + L::cDK + c * 32, u);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) u[e] = 0u;
+        }
+        if (key_ok) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            d4[e] = make_uint4(pack_16x2<F16>(__uint_as_float(u[8 * e]), __uint_as_float(u[8 * e + 1])),
+                               pack_16x2<F16>(__uint_as_float(u[8 * e + 2]), __uint_as_float(u[8 * e + 3])),
+                               pack_16x2<F16>(__uint_as_float(u[8 * e + 4]), __uint_as_float(u[8 * e + 5])),
+                               pack_16x2<F16>(__uint_as_float(u[8 * e + 6]), __uint_as_float(u[8 * e + 7])));
+        }
+      }
+    }
+  } else {
+    // ================================================================ WG1: dQ atomics, then dV
+    setmaxnreg_dec<136>();
+    const int r = tid - 128;                              // Q-tile row (dQ) / key row (dV) == TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    Waiter w{abort_flag, p.timeout_ns, kRoleCorr};
+    mbar_arrive(bar(L::bdPEmpty));                        // the dP columns start free
+    bool ok = true;
+#pragma unroll 1
+    for (int k = 0; k < n; ++k) {
+      const int i = i0 + k;
+      const int prow = i * 128 + r;                       // packed row
+      const int pos = prow >> p.gshift;
+      const int head = (kvh << p.gshift) + (r & ((1 << p.gshift) - 1));
+      const bool valid = pos < p.Nq;
+      float* dst = p.dq_acc + ((size_t)(tok_q + pos) * p.H + head) * D;
+      if (!w.wait(bar(L::bdQFull), k & 1, L::bdQFull, k)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll 1
+      for (int half = 0; half < D / 64; ++half) {
+        uint32_t u[64];
+        tmem_ld32(tmem + lane_base + L::cDP + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        tmem_ld32(tmem + lane_base + L::cDP + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+        tmem_wait_ld();
+        if (half == D / 64 - 1) {                         // all of dQ is in registers: free the columns
+          tc_fence_before();
+          mbar_arrive(bar(L::bdPEmpty));
+        }
+        if (valid) {
+          float4* d4 = reinterpret_cast<float4*>(dst + half * 64);
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            atomicAdd(d4 + e, make_float4(__uint_as_float(u[4 * e]), __uint_as_float(u[4 * e + 1]),
+                                          __uint_as_float(u[4 * e + 2]), __uint_as_float(u[4 * e + 3])));
+        }
+      }
+    }
+    // dV -> 16-bit -> global
+    if (ok && n > 0 && !w.wait(bar(L::bFinal), 0, L::bFinal, -1)) ok = false;
+    if (ok) {
+      tc_fence_after();
+      const int kabs = j * 128 + r;
+      uint16_t* dst = p.dv + ((size_t)(tok_k + kabs) * p.Hkv + kvh) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t u[32];
+        if (n > 0) {
+          tmem_ld32(tmem + lane_base + L::cDV + c * 32, u);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) u[e] = 0u;
+        }
+        if (kabs < p.Nk) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            d4[e] = make_uint4(pack_16x2<F16>(__uint_as_float(u[8 * e]), __uint_as_float(u[8 * e + 1])),
+                               pack_16x2<F16>(__uint_as_float(u[8 * e + 2]), __uint_as_float(u[8 * e + 3])),
+                               pack_16x2<F16>(__uint_as_float(u[8 * e + 4]), __uint_as_float(u[8 * e + 5])),
+                               pack_16x2<F16>(__uint_as_float(u[8 * e + 6]), __uint_as_float(u[8 * e + 7])));
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace fa

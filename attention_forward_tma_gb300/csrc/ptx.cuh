@@ -235,6 +235,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
 __host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool b_mn_major, bool f16) {
   return f16 ? (idesc_bf16_f32(M, N, b_mn_major) & ~((1u << 7) | (1u << 10))) : idesc_bf16_f32(M, N, b_mn_major);
 }
+// With the major-ness of A chosen too (A major bit 15: 1 = MN-major, the M
+// dimension contiguous in shared memory).
+__host__ __device__ constexpr uint32_t idesc_f32acc2(int M, int N, bool a_mn_major, bool b_mn_major, bool f16) {
+  return idesc_f32acc(M, N, b_mn_major, f16) | ((a_mn_major ? 1u : 0u) << 15);
+}
 
 // ---------------------------------------------------------------- scalar helpers
 __device__ __forceinline__ float ex2_approx(float x) {

@@ -218,6 +218,26 @@ int fa_fwd_varlen_noalloc(const void* q, const void* k, const void* v, void* o, 
                           const int* cu_seqlens, int num_seqs, int total_tokens, int max_seqlen,
                           int H, int d, float scale, int causal, void* stream);
 
+/*
+ * Backward pass of fa_fwd_kv without key splits: gradients of
+ * O = softmax(scale * Q K^T) V for an upstream gradient dO ("FlashAttention-4（下）"
+ * (argus lesson 7), section 1: S and P are recomputed from Q, K and the forward's
+ * LSE; dV = P^T dO, dP = dO V^T, dS = P * (dP - rowsum(dO * O)), dQ = scale * dS K,
+ * dK = scale * dS^T Q; with grouped heads dK and dV of a K/V head sum over its G
+ * query heads).
+ *   q, o, dout, dq : [B, N_q, H, d]      k, v, dk, dv : [B, N_kv, H_kv, d]
+ *                    (dtype elements, device; dq, dk, dv written)
+ *   lse            : fp32 [B, H, N_q], the LSE that fa_fwd* wrote for these q, k, v
+ *   other arguments as for fa_fwd_kv (bottom-right causal mask).
+ * dQ is accumulated over key blocks in fp32 with atomic additions, so its last
+ * bits may differ from run to run; dK and dV are deterministic. A temporary buffer
+ * of B*N_q*H*d*4 + 2*B*H_kv*ceil(N_q*G/128)*128*4 bytes comes from the
+ * stream-ordered allocator (cudaMallocAsync / cudaFreeAsync on `stream`).
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+           void* dq, void* dk, void* dv, int B, int H, int H_kv, int N_q, int N_kv, int d, float scale,
+           int causal, int dtype, void* stream);
+
 /* Text for a status code (static storage; never NULL). */
 const char* fa_error_string(int status);
 

@@ -1,0 +1,114 @@
+"""GPU parity for the backward pass (fa_bwd) against the fp64 oracle gradients.
+
+The forward runs on the GPU first (it supplies O and the LSE the backward
+reuses); the oracle differentiates the exact definition from the same 16-bit
+inputs. Tolerance: the gradients pass through three 16-bit roundings (P for dV,
+dS for dQ and dK, and the outputs), each a relative 2^-9 (bf16) of terms of the
+size of the gradient; the bound is max |grad - oracle| <= 2e-2 * max(1, max |oracle|)
+per tensor, the forward's O tolerance scaled by the gradient's magnitude.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import attention_forward_tma_gb300 as fa
+import fa_inputs
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    fa.library()
+    yield torch
+
+
+def tdtype(dtype):
+    import torch
+    return torch.float16 if dtype == "f16" else torch.bfloat16
+
+
+def dev(bits, dtype="bf16"):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(tdtype(dtype)).cuda()
+
+
+def host(t):
+    import torch
+    dtype = "f16" if t.dtype == torch.float16 else "bf16"
+    return fa_inputs.bits_to_f32(t.view(torch.int16).cpu().numpy().view(np.uint16), dtype).astype(np.float64)
+
+
+def run_bwd(q, k, v, do, causal, dtype="bf16", scale=None):
+    qd, kd, vd, dod = dev(q, dtype), dev(k, dtype), dev(v, dtype), dev(do, dtype)
+    o, lse = fa.fa_fwd(qd, kd, vd, causal=causal, scale=scale)
+    dq, dk, dv = fa.fa_bwd(qd, kd, vd, o, dod, lse, causal=causal, scale=scale)
+    st, word = fa.last_device_status()
+    assert st == fa.FA_OK, hex(word)
+    return host(dq), host(dk), host(dv)
+
+
+def check(got, ref, what):
+    errs = []
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        assert np.isfinite(g).all(), f"{what}: non-finite {name}"
+        bound = TOL * max(1.0, np.abs(r).max())
+        err = np.abs(g - r).max()
+        errs.append(f"{name} {err:.2e}/{bound:.2e}")
+        assert err <= bound, f"{what}: max |{name} - oracle| = {err} > {bound}"
+    print(what, " ".join(errs))
+
+
+SHAPES = [  # (B, H, H_kv, N_q, N_kv, d)
+    (1, 1, 1, 128, 128, 128),
+    (1, 2, 2, 300, 300, 128),
+    (2, 4, 1, 129, 129, 64),      # multi-query, ragged
+    (1, 8, 2, 200, 333, 128),     # G = 4, N_q < N_kv
+    (1, 4, 4, 100, 257, 64),
+    (1, 32, 1, 40, 40, 64),       # G = 32
+    (1, 2, 2, 257, 100, 128),     # N_q > N_kv: causal rows without keys
+    (1, 1, 1, 640, 640, 128),     # several key blocks and Q tiles
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "B%dH%dKV%dNq%dNk%dd%d" % s)
+def test_backward_elementwise(shape, causal):
+    B, H, Hkv, Nq, Nk, d = shape
+    q, k, v = fa_inputs.make_qkv(B, Nq, H, d, seed=4000 + Nq + Nk + H, Nkv=Nk, Hkv=Hkv)
+    do = fa_inputs.make_qkv(B, Nq, H, d, seed=5000 + Nq)[0]
+    got = run_bwd(q, k, v, do, causal)
+    ref = oracle.attention_backward(q, k, v, do, 1 / math.sqrt(d), causal)
+    check(got, ref, f"{shape} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_fp16(causal):
+    q, k, v = fa_inputs.make_qkv(1, 300, 8, 128, seed=4100, Hkv=2, dtype="f16")
+    do = fa_inputs.make_qkv(1, 300, 8, 128, seed=4101, dtype="f16")[0]
+    got = run_bwd(q, k, v, do, causal, "f16")
+    ref = oracle.attention_backward(q, k, v, do, 1 / math.sqrt(128), causal, dtype="f16")
+    check(got, ref, f"fp16 causal={causal}")
+
+
+def test_backward_spiky_scores():
+    q, k, v = fa_inputs.make_qkv(1, 400, 2, 128, seed=20264, spiky=True)
+    do = fa_inputs.make_qkv(1, 400, 2, 128, seed=4200)[0]
+    got = run_bwd(q, k, v, do, True)
+    ref = oracle.attention_backward(q, k, v, do, 1 / math.sqrt(128), True)
+    check(got, ref, "spiky")
+
+
+def test_backward_dk_dv_deterministic():
+    q, k, v = fa_inputs.make_qkv(1, 500, 4, 128, seed=4300, Hkv=2)
+    do = fa_inputs.make_qkv(1, 500, 4, 128, seed=4301)[0]
+    a = run_bwd(q, k, v, do, True)
+    b = run_bwd(q, k, v, do, True)
+    assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
+    assert np.abs(a[0] - b[0]).max() <= 2.0 ** -7 * max(1.0, np.abs(a[0]).max())
