@@ -13,22 +13,26 @@
 // tensor memory (section 2 of the same page: TMEM accumulators let several
 // products be in flight). S and P are computed transposed (S^T = K Q^T, keys on
 // the TMEM lanes), so P^T is already the A operand of the dV product, as the page
-// describes. dQ of each (Q tile, key block) pair is added to an fp32 buffer with
-// vector atomics (section 4: the dQ sum over key blocks is a global atomic
-// accumulation). With grouped heads the Q tiles hold the packed (position, query
+// describes. dQ of each (Q tile, key block) pair is added to an fp32 buffer in
+// global memory (section 4: the dQ sum over key blocks is a global atomic
+// accumulation): staged in shared memory and sent as TMA reduce-adds, 16 KB per
+// operation, in place of per-thread atomics. With grouped heads the Q tiles hold the packed (position, query
 // head) rows of the forward, so every query head of the group contributes to the
 // CTA's dK and dV without atomics.
 //
 // Roles: WG0 (warps 0-3, one thread per key row) computes P and dS; WG1 (warps
-// 4-7, one thread per Q-tile row) drains dQ from TMEM into the atomics and at the
-// end writes dV; warp 8 issues the TMA loads, warp 9 the tcgen05 MMAs. WG0 writes
-// dK at the end.
+// 4-7, one thread per Q-tile row) moves dQ from TMEM into shared memory and
+// issues its reduce-adds, and at the end writes dV; warp 8 issues the TMA loads
+// (Q, dO and the tile's base-2 LSE and D), warp 9 the tcgen05 MMAs. WG0 writes dK
+// at the end.
 //
 // Tensor memory (512 columns): dV [0, d), dK [128, 128+d), S^T [256, 384) with P^T
 // as 16-bit pairs over its upper 64 columns, dP^T [384, 512) -- reused for dQ once
-// dS is in shared memory. Shared memory: K, V, two stages of (Q, dO) and the dS
-// tile (128 keys x 128 rows, 128-byte swizzle): the same bytes are the K-major A
-// operand of dK (M = keys) and the MN-major A operand of dQ (M = rows).
+// dS is in shared memory. Shared memory (226 KB of the 227 KB a CTA may have):
+// K, V, two stages of (Q, dO, LSE, D), and the dS tile (128 keys x 128 rows,
+// 128-byte swizzle): the same bytes are the K-major A operand of dK (M = keys)
+// and the MN-major A operand of dQ (M = rows). Once a step's products are done,
+// its Q and dO buffers hold the staged fp32 dQ tile for the reduce-adds.
 //
 // Every wait is bounded as in the forward kernel.
 #pragma once
@@ -44,6 +48,7 @@ constexpr int kBwdThreads = 384;
 struct BwdParams {
   CUtensorMap tm_q, tm_do;   // [tokens_q, H, d]: box 64 x G x 128/G (one packed 128-row tile)
   CUtensorMap tm_k, tm_v;    // [tokens_k, H_kv, d]: box 64 x 1 x 128
+  CUtensorMap tm_dq;         // fp32 dq_acc [tokens_q, H, d]: box 32 x G x 128/G, reduce-adds
   const float* lse2;         // [B, H_kv, mpad], packed rows: forward LSE * log2(e)
   const float* dsum;         // [B, H_kv, mpad], packed rows: D = rowsum(dO * O)
   float* dq_acc;             // fp32 [tokens_q, H, d]; zero on entry
@@ -64,14 +69,16 @@ struct BwdLayout {
   static constexpr int kSlab = 128 * 128;            // 128 rows x 128 bytes
   static constexpr int kTile = kHalves * kSlab;       // 128 rows x D, 16-bit
   static constexpr int kK = 0, kV = kTile, kQ = 2 * kTile, kDO = 4 * kTile, kDS = 6 * kTile;
-  static constexpr int kBar = kDS + 2 * kSlab;        // dS: 128 keys x 128 rows
+  static constexpr int kStats = kDS + 2 * kSlab;      // dS: 128 keys x 128 rows
+  static constexpr int kStatsBytes = 1024;            // per stage: 128 base-2 LSE, then 128 D (fp32)
+  static constexpr int kBar = kStats + 2 * kStatsBytes;
   enum : int {
     bKV = 0, bQFull = 1, bQEmpty = 3, bSFull = 5, bPReady = 6, bdPFull = 7, bdPEmpty = 8, bdSReady = 9,
-    bdSEmpty = 10, bdQFull = 11, bFinal = 12, bDrain = 13, kNumBars = 14
+    bdSEmpty = 10, bdQFull = 11, bFinal = 12, bDrain = 13, bdQStaged = 14, kNumBars = 15
   };
   static constexpr int kMisc = kBar + 128;
   static constexpr int kBytes = kMisc + 64;
-  static constexpr int kAlloc = kBytes + 1024;        // slack for 1024-byte alignment
+  static constexpr int kAlloc = kBytes;               // the dynamic shared memory is 1024-byte aligned
   static_assert(kNumBars * 8 <= 128, "barriers");
   static_assert(kAlloc <= 227 * 1024, "shared memory per CTA");
   static constexpr uint32_t cDV = 0, cDK = 128, cS = 256, cDP = 384;
@@ -134,9 +141,15 @@ __global__ void __launch_bounds__(256) fa_bwd_post_kernel(const float4* __restri
 template <int D, bool CAUSAL, bool F16>
 __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_constant__ BwdParams p) {
   using L = BwdLayout<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
   const uint32_t sbase = smem_u32(smem);
+  // the 128-byte-swizzled tiles need 1024-byte alignment and there is no room for
+  // padding: a misaligned window is reported, not used
+  if ((sbase & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicCAS(&g_fa_status, 0ull, kStatusUnsupported);
+    return;
+  }
   const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sQ = sbase + L::kQ, sDO = sbase + L::kDO,
                  sDS = sbase + L::kDS;
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * (uint32_t)i; };
@@ -168,6 +181,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
     mbar_init(bar(L::bPReady), 128);
     mbar_init(bar(L::bdPEmpty), 128);
     mbar_init(bar(L::bdSReady), 128);
+    mbar_init(bar(L::bdQStaged), 128);
     fence_mbar_init();
   }
   if (warp == 8 && lane == 0) {
@@ -176,6 +190,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
     prefetch_tmap(&p.tm_k);
     prefetch_tmap(&p.tm_v);
   }
+  if (warp == 4 && lane == 0) prefetch_tmap(&p.tm_dq);
   if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -216,13 +231,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
           const int i = i0 + k;
           const int tok = tok_q + ((i * 128) >> p.gshift);
           if (leader) {
-            mbar_arrive_expect_tx(bar(L::bQFull + s), 2 * L::kTile);
+            mbar_arrive_expect_tx(bar(L::bQFull + s), 2 * L::kTile + L::kStatsBytes);
 #pragma unroll
             for (int c = 0; c < L::kHalves; ++c) {
               tma_load_3d(sQ + s * L::kTile + c * L::kSlab, &p.tm_q, c * 64, kvh << p.gshift, tok, bar(L::bQFull + s));
               tma_load_3d(sDO + s * L::kTile + c * L::kSlab, &p.tm_do, c * 64, kvh << p.gshift, tok,
                           bar(L::bQFull + s));
             }
+            const size_t pk = ((size_t)b * p.Hkv + kvh) * p.mpad + (size_t)i * 128;
+            const uint32_t st = sbase + L::kStats + s * L::kStatsBytes;
+            bulk_load(st, p.lse2 + pk, 512, bar(L::bQFull + s));
+            bulk_load(st + 512, p.dsum + pk, 512, bar(L::bQFull + s));
           }
           __syncwarp();
           q_armed |= 1u << s;
@@ -317,9 +336,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
               mma_ss(tdP, dSmn + ((kk * 2048) >> 4), Kmn + ((kk * 2048) >> 4), idQ, kk > 0 ? 1u : 0u);
-            mma_commit(bar(L::bdQFull));
+            mma_commit(bar(L::bdQFull));   // also: this step's Q and dO are no longer read
             mma_commit(bar(L::bdSEmpty));
-            mma_commit(bar(L::bQEmpty + s));
           }
           __syncwarp();
           // the next tile's dP^T, once WG1 has taken dQ out of those columns
@@ -353,18 +371,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
     const uint32_t tS = tmem + lane_base + L::cS, tdP = tmem + lane_base + L::cDP;
     Waiter w{abort_flag, p.timeout_ns, kRoleSoftmax0};
     const float sl2 = p.scale_log2, sc = p.scale;
-    const size_t pk_base = ((size_t)b * p.Hkv + kvh) * p.mpad;
     bool ok = true;
 #pragma unroll 1
     for (int k = 0; k < n; ++k) {
       const int i = i0 + k;
-      const float4* L2 = reinterpret_cast<const float4*>(p.lse2 + pk_base + (size_t)i * 128);
-      const float4* DS = reinterpret_cast<const float4*>(p.dsum + pk_base + (size_t)i * 128);
+      // this tile's base-2 LSE and D, loaded with Q and dO (q_full of the stage, waited below)
+      const float4* L2 = reinterpret_cast<const float4*>(smem + L::kStats + (k & 1) * L::kStatsBytes);
+      const float4* DS = L2 + 32;
       // rows [qlo, qhi) of this tile see this key: causal needs position >= kabs - off,
       // and rows past the sequence's packed end are padding
       const int qlo = CAUSAL ? (int)max(-1LL, min(129LL, ((long long)kabs - off) * (1LL << p.gshift) - (long long)i * 128))
                              : 0;
       const int qhi = key_ok ? min(128, (p.Nq << p.gshift) - i * 128) : 0;
+      if (!w.wait(bar(L::bQFull + (k & 1)), (k >> 1) & 1, L::bQFull + (k & 1), k)) { ok = false; break; }
       if (!w.wait(bar(L::bSFull), k & 1, L::bSFull, k)) { ok = false; break; }
       tc_fence_after();
       float P[128];
@@ -460,7 +479,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
       }
     }
   } else {
-    // ================================================================ WG1: dQ atomics, then dV
+    // ================================================================ WG1: dQ reduce-adds, then dV
     setmaxnreg_dec<136>();
     const int r = tid - 128;                              // Q-tile row (dQ) / key row (dV) == TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -470,32 +489,51 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
 #pragma unroll 1
     for (int k = 0; k < n; ++k) {
       const int i = i0 + k;
-      const int prow = i * 128 + r;                       // packed row
-      const int pos = prow >> p.gshift;
-      const int head = (kvh << p.gshift) + (r & ((1 << p.gshift) - 1));
-      const bool valid = pos < p.Nq;
-      float* dst = p.dq_acc + ((size_t)(tok_q + pos) * p.H + head) * D;
+      const int s = k & 1;
+      const bool valid = ((i * 128 + r) >> p.gshift) < p.Nq;   // padding rows add zeros
       if (!w.wait(bar(L::bdQFull), k & 1, L::bdQFull, k)) { ok = false; break; }
       tc_fence_after();
+      // dQ in 32-column chunks -> fp32 rows in the freed Q_s / dO_s buffers, in the
+      // 128-byte-swizzled layout of the reduce map (16-byte unit u of row r at u ^ (r % 8))
 #pragma unroll 1
-      for (int half = 0; half < D / 64; ++half) {
-        uint32_t u[64];
-        tmem_ld32(tmem + lane_base + L::cDP + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-        tmem_ld32(tmem + lane_base + L::cDP + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tmem + lane_base + L::cDP + c * 32, u);
         tmem_wait_ld();
-        if (half == D / 64 - 1) {                         // all of dQ is in registers: free the columns
+        if (c == D / 32 - 1) {                            // all of dQ has left TMEM: free the columns
           tc_fence_before();
           mbar_arrive(bar(L::bdPEmpty));
         }
-        if (valid) {
-          float4* d4 = reinterpret_cast<float4*>(dst + half * 64);
+        const uint32_t chunk = c < L::kHalves ? sQ + s * L::kTile + c * L::kSlab
+                                              : sDO + s * L::kTile + (c - L::kHalves) * L::kSlab;
+        const uint32_t row = chunk + (uint32_t)r * 128u;
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            atomicAdd(d4 + e, make_float4(__uint_as_float(u[4 * e]), __uint_as_float(u[4 * e + 1]),
-                                          __uint_as_float(u[4 * e + 2]), __uint_as_float(u[4 * e + 3])));
+        for (int uu = 0; uu < 8; ++uu) {
+          const uint32_t a0 = valid ? u[4 * uu] : 0u, a1 = valid ? u[4 * uu + 1] : 0u;
+          const uint32_t a2 = valid ? u[4 * uu + 2] : 0u, a3 = valid ? u[4 * uu + 3] : 0u;
+          st_shared_v4(row + (((uint32_t)uu ^ (uint32_t)(r & 7)) << 4), a0, a1, a2, a3);
         }
       }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(L::bdQStaged));
+      if (warp == 4) {
+        if (!w.wait(bar(L::bdQStaged), k & 1, L::bdQStaged, k)) { ok = false; break; }
+        if (lane == 0) {
+          const int tok = tok_q + ((i * 128) >> p.gshift);
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            const uint32_t chunk = c < L::kHalves ? sQ + s * L::kTile + c * L::kSlab
+                                                  : sDO + s * L::kTile + (c - L::kHalves) * L::kSlab;
+            tma_reduce_add_3d(&p.tm_dq, chunk, c * 32, kvh << p.gshift, tok);
+          }
+          bulk_commit();
+          bulk_wait_read_all();                           // the staging may be overwritten now
+          mbar_arrive(bar(L::bQEmpty + s));               // Q_s and dO_s may be reloaded
+        }
+        __syncwarp();
+      }
     }
+    if (warp == 4 && lane == 0) bulk_wait_all();          // reduce-adds complete before dV / exit
     // dV -> 16-bit -> global
     if (ok && n > 0 && !w.wait(bar(L::bFinal), 0, L::bFinal, -1)) ok = false;
     if (ok) {

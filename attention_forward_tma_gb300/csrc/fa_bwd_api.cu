@@ -152,6 +152,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   if (cudaMemsetAsync(ws, 0, acc_bytes + 2 * vec_bytes, s) != cudaSuccess) st = FA_ERR_CUDA;
   if (st == FA_OK)
     st = pre_post_any(false, d, f16, o, dout, lse, lse2, dsum, nullptr, nullptr, B, H, gshift, N_q, (int)mpad, s);
+  if (st == FA_OK) st = fa_host::make_map_f32(&p.tm_dq, dq_acc, tokens, H, d, G);
   if (st == FA_OK) {
     p.lse2 = lse2;
     p.dsum = dsum;

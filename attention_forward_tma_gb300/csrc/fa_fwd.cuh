@@ -64,6 +64,7 @@ static __device__ unsigned long long g_fa_status;  // one copy per translation u
 enum : uint32_t { kRoleMma = 1, kRoleLoad = 2, kRoleSoftmax0 = 3, kRoleSoftmax1 = 4, kRoleCorr = 5,
                   kRoleDrain = 6 };
 constexpr unsigned long long kStatusTimeout = 4;  // == FA_ERR_TIMEOUT
+constexpr unsigned long long kStatusUnsupported = 2;  // == FA_ERR_UNSUPPORTED
 
 struct FwdParams {
   // 3-D maps of [tokens, heads, d]: x = d, y = head, z = token. Q and O: box

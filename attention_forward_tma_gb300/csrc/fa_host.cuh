@@ -51,6 +51,22 @@ inline int make_map(CUtensorMap* m, const void* base, long long tokens, int head
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// 3-D map over an fp32 [tokens, heads, d] tensor for tiled reduce-adds: box =
+// 32 x box_heads x (128 / box_heads) (one 128-byte column slab of a packed
+// 128-row tile), 128-byte swizzle.
+inline int make_map_f32(CUtensorMap* m, void* base, long long tokens, int heads, int d, int box_heads) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return FA_ERR_CUDA;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)tokens};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)heads * d * 4};
+  const cuuint32_t box[3] = {32, (cuuint32_t)box_heads, (cuuint32_t)(fa::kBlockM / box_heads)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 // H_kv must divide H, and the group size G = H / H_kv must divide the 128 rows of
 // a Q tile (a power of two up to 128). Sets gshift = log2(G).
 inline int check_heads(int H, int Hkv, int* gshift) {

@@ -38,6 +38,7 @@ sys.path.insert(0, ROOT)
 import fa_inputs  # noqa: E402
 
 METRIC = "attention fwd TFLOPS (bf16, d=128) and % of GB300 dense BF16 tensor peak"
+METRIC_BWD = "attention bwd TFLOPS (bf16, d=128) and % of GB300 dense BF16 tensor peak"
 DEFAULT_WORKLOAD = "c3_b4h16n4096d128_causal"
 FALLBACK_PEAK_TFLOPS = 1900.0
 FLOP_PER_CLK_PER_SM = 8192  # dense bf16 tcgen05 rate per SM per clock
@@ -52,7 +53,11 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"],
+                    help="bwd: time the backward pass (fixed-length workloads) instead of the forward")
     a = ap.parse_args()
+    if a.which == "bwd" and fa_inputs.WORKLOADS[a.workload].varlen:
+        ap.error("--pass bwd takes a fixed-length workload")
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
     return a
@@ -249,6 +254,21 @@ def cpu_baseline(w, x, target_s: float = 10.0):
                       f"{flops / 1e9:.1f} GFLOP by the 4*d*keys count), {dt:.1f} s"}
 
 
+def cpu_baseline_bwd(w, x):
+    """The backward oracle (fp64 NumPy, as it stands) on one (batch, K/V head group) of the workload."""
+    import oracle
+    Gq = w.H // w.Hkv
+    q, k, v = x["q"][:1, :, :Gq], x["k"][:1, :, :1], x["v"][:1, :, :1]
+    do = fa_inputs.make_qkv(1, w.N, Gq, w.d, w.seed + 1000, dtype=w.dtype)[0]
+    t0 = time.perf_counter()
+    oracle.attention_backward(q, k, v, do, w.scale, w.causal, dtype=w.dtype)
+    dt = time.perf_counter() - t0
+    flops = 2.5 * fa_inputs.attention_flops(1, Gq, w.N, w.d, w.causal, Nk=w.Nk)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count() or 1, "kind": "oracle",
+            "sample": f"backward of batch 0, K/V head 0 with its {Gq} query head(s) of {w.name} "
+                      f"(fp64 NumPy, full matrices per head), {dt:.1f} s"}
+
+
 # --------------------------------------------------------------------------- the reference arm
 def run_reference(a, dist):
     w = fa_inputs.WORKLOADS[a.workload]
@@ -303,7 +323,20 @@ def run_ours(a, dist):
 
     q, k, v = to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"])
     o = torch.empty_like(q)
-    if w.varlen:
+    bwd = a.which == "bwd"
+    if bwd:
+        # dO drawn like Q from its own seed; O and LSE from one untimed forward
+        dout = to_dev(fa_inputs.make_qkv(w.B, w.N, w.H, w.d, w.seed + 1000, dtype=w.dtype)[0])
+        lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+        fa.fa_fwd(q, k, v, scale=w.scale, causal=w.causal, out=o, lse=lse)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        flops = 2.5 * flops   # five products against the forward's two
+
+        def step(s=None):
+            fa.fa_bwd(q, k, v, o, dout, lse, scale=w.scale, causal=w.causal, dq=dq, dk=dk, dv=dv, stream=s)
+        splits = 1
+        launches_per_step = 3   # preprocessing, backward, dQ conversion
+    elif w.varlen:
         cu = torch.from_numpy(x["cu_seqlens"]).to(dev)
         maxL = int(x["lengths"].max())
         lse = torch.empty((w.H, q.shape[0]), dtype=torch.float32, device=dev)
@@ -361,23 +394,30 @@ def run_ours(a, dist):
     avg_launch_s = sum(per_launch_ms) / len(per_launch_ms) / 1e3
 
     # end to end through the public API with host buffers (pinned), copies inside the region
-    hq, hk, hv = (t.to("cpu").pin_memory() for t in (q, k, v))
-    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
     n_e2e = max(1, min(a.e2e_steps, a.steps))
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if bwd:
+        ins = [q, k, v, o, dout, lse]
+        outs = [dq, dk, dv]
+    else:
+        ins = [q, k, v]
+        outs = [o, lse]
+    h_in = [t.to("cpu").pin_memory() for t in ins]
+    d_in = [torch.empty_like(t) for t in ins]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    d_out = [torch.empty_like(t) for t in outs]
 
     def e2e_step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        if w.varlen:
-            fa.fa_fwd_varlen(dq, dk, dv, cu, maxL, scale=w.scale, causal=w.causal, out=o, lse=lse,
+        for d_, h_ in zip(d_in, h_in):
+            d_.copy_(h_, non_blocking=True)
+        if bwd:
+            fa.fa_bwd(*d_in, scale=w.scale, causal=w.causal, dq=d_out[0], dk=d_out[1], dv=d_out[2])
+        elif w.varlen:
+            fa.fa_fwd_varlen(*d_in, cu, maxL, scale=w.scale, causal=w.causal, out=d_out[0], lse=d_out[1],
                              num_splits=w.splits)
         else:
-            fa.fa_fwd(dq, dk, dv, scale=w.scale, causal=w.causal, out=o, lse=lse, num_splits=w.splits)
-        ho.copy_(o, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
+            fa.fa_fwd(*d_in, scale=w.scale, causal=w.causal, out=d_out[0], lse=d_out[1], num_splits=w.splits)
+        for h_, d_ in zip(h_out, d_out):
+            h_.copy_(d_, non_blocking=True)
 
     for _ in range(2):
         e2e_step()
@@ -390,8 +430,8 @@ def run_ours(a, dist):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_s = dist.max(e0.elapsed_time(e1) / 1e3)
-    h2d = (q.numel() + k.numel() + v.numel()) * 2
-    d2h = o.numel() * 2 + lse.numel() * 4
+    h2d = sum(t.numel() * t.element_size() for t in ins)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
 
     if dist.rank != 0:
         return
@@ -403,7 +443,7 @@ def run_ours(a, dist):
     traffic = profiled_traffic(w.name)
     # the bound follows the arithmetic intensity: below the ridge of the measured
     # peaks (FLOP per byte) the step is an HBM stream, above it a contraction
-    nbytes = workload_bytes(w, x)
+    nbytes = workload_bytes(w, x) * (2.0 if bwd else 1.0)   # bwd: Q, K, V, O, dO read; dQ, dK, dV written
     if flops / nbytes < peak * 1e12 / (hbm * 1e9):
         roof = {"bound": "hbm", "achieved": nbytes / avg_launch_s / 1e9, "peak": hbm, "unit": "GB/s",
                 "frac": nbytes / avg_launch_s / 1e9 / hbm, "traffic": traffic,
@@ -415,7 +455,8 @@ def run_ours(a, dist):
                 "traffic": traffic,
                 "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)" if peak_src == "measured"
                 else "fallback 1.9 PFLOP/s bf16 burst"}
-    roof.update({"kernel": "fa_fwd_kernel" + (" + fa_combine_kernel" if splits > 1 else ""),
+    roof.update({"kernel": ("fa_bwd_kernel (+ preprocessing, dQ conversion)" if bwd else
+                            "fa_fwd_kernel" + (" + fa_combine_kernel" if splits > 1 else "")),
                  "avg_launch_ms": avg_launch_s * 1e3, "min_launch_ms": min(per_launch_ms), "wall_s": wall})
     cfg = {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.Hkv, "N": w.N, "d": w.d, "causal": w.causal,
            "scale": w.scale, "seed": w.seed,
@@ -423,12 +464,14 @@ def run_ours(a, dist):
            else ("inputs smaller than L2 (Q+K+V+O = %.1f MiB): 256 MiB written between steps, value from the "
                  "per-step events" % (in_bytes / 2 ** 20)),
            "flops_per_step": flops, "key_splits": splits}
+    if bwd:
+        cfg["pass"] = "backward (FLOPs = 2.5 x the forward count)"
     if w.Nk != w.N:
         cfg["N_kv"] = w.Nk
     if w.varlen:
         cfg["lengths"] = [int(L) for L in x["lengths"]]
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": dist.world, "steps": a.steps,
+        "metric": METRIC_BWD if bwd else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": dist.world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": region_s / a.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "config": cfg,
         "pct_of_measured_peak": 100.0 * value / dist.world / peak,
@@ -441,7 +484,7 @@ def run_ours(a, dist):
         "clocks": clk,
     }
     if not a.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, x)
+        line["cpu_baseline"] = cpu_baseline_bwd(w, x) if bwd else cpu_baseline(w, x)
     print(json.dumps(line), flush=True)
 
 
