@@ -359,6 +359,13 @@ int noalloc_scratch(int4** out) {
 }
 }  // namespace
 
+namespace fa_host {
+void trace_target(unsigned long long** buf, int* ctas) {
+  *buf = g_trace_buf;
+  *ctas = g_trace_ctas;
+}
+}  // namespace fa_host
+
 // ------------------------------------------------------------------ C ABI
 extern "C" {
 

@@ -8,7 +8,7 @@
 //   dV += P^T dO          dP = dO V^T          dS = s * P * (dP - D),  D = rowsum(dO * O)
 //   dK += dS^T Q          dQ += dS K
 //
-// One CTA of 384 threads owns one block of 128 keys of one (sequence, K/V head)
+// One CTA of 512 threads owns one block of 128 keys of one (sequence, K/V head)
 // and walks over the 128-row Q tiles that can see it, accumulating dK and dV in
 // tensor memory (section 2 of the same page: TMEM accumulators let several
 // products be in flight). S and P are computed transposed (S^T = K Q^T, keys on
@@ -20,14 +20,16 @@
 // head) rows of the forward, so every query head of the group contributes to the
 // CTA's dK and dV without atomics.
 //
-// Roles: WG0 (warps 0-3, one thread per key row) computes P and dS; WG1 (warps
-// 4-7, one thread per Q-tile row) moves dQ from TMEM into shared memory and
-// issues its reduce-adds, and at the end writes dV; warp 8 issues the TMA loads
-// (Q, dO and the tile's base-2 LSE and D), warp 9 the tcgen05 MMAs. WG0 writes dK
-// at the end.
+// Roles: WG0 and WG1 (warps 0-7, one thread per key row) compute P and dS for
+// query columns 0-63 and 64-127 of the tile (the LSE is known, so the halves need
+// no exchange); WG2 (warps 8-11, one thread per Q-tile row) moves dQ from TMEM
+// into shared memory and issues its reduce-adds, and at the end writes dV; warp 12
+// issues the TMA loads (Q, dO and the tile's base-2 LSE and D), warp 13 the
+// tcgen05 MMAs. WG0 and WG1 write the two halves of dK at the end.
 //
 // Tensor memory (512 columns): dV [0, d), dK [128, 128+d), S^T [256, 384) with P^T
-// as 16-bit pairs over its upper 64 columns, dP^T [384, 512) -- reused for dQ once
+// as 16-bit pairs over the upper 32 columns of each 64-column half, dP^T [384, 512)
+// -- reused for dQ once
 // dS is in shared memory. Shared memory (226 KB of the 227 KB a CTA may have):
 // K, V, two stages of (Q, dO, LSE, D), and the dS tile (128 keys x 128 rows,
 // 128-byte swizzle): the same bytes are the K-major A operand of dK (M = keys)
@@ -43,7 +45,7 @@
 
 namespace fa {
 
-constexpr int kBwdThreads = 384;
+constexpr int kBwdThreads = 512;
 
 struct BwdParams {
   CUtensorMap tm_q, tm_do;   // [tokens_q, H, d]: box 64 x G x 128/G (one packed 128-row tile)
@@ -60,6 +62,8 @@ struct BwdParams {
   int num_tasks;
   float scale, scale_log2;
   unsigned long long timeout_ns;
+  unsigned long long* trace;     // tracing build only: clock stamps per CTA and role (else null)
+  int trace_ctas;
 };
 
 template <int D>
@@ -178,20 +182,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
     *abort_flag = 0;
     *never_abort = 0;
     for (int i = 0; i < L::kNumBars; ++i) mbar_init(bar(i), 1);
-    mbar_init(bar(L::bPReady), 128);
+    mbar_init(bar(L::bPReady), 256);
     mbar_init(bar(L::bdPEmpty), 128);
-    mbar_init(bar(L::bdSReady), 128);
+    mbar_init(bar(L::bdSReady), 256);
     mbar_init(bar(L::bdQStaged), 128);
     fence_mbar_init();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == 12 && lane == 0) {
     prefetch_tmap(&p.tm_q);
     prefetch_tmap(&p.tm_do);
     prefetch_tmap(&p.tm_k);
     prefetch_tmap(&p.tm_v);
   }
-  if (warp == 4 && lane == 0) prefetch_tmap(&p.tm_dq);
-  if (warp == 9) {
+  if (warp == 8 && lane == 0) prefetch_tmap(&p.tm_dq);
+  if (warp == 13) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -200,13 +204,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // register split 240 / 136 / 128 per thread for WG0 / WG1 / WG2 (sum = 3 x 168,
-  // the launch allocation)
-  if (warp >= 8) {
-    setmaxnreg_dec<128>();
-    if (warp == 8) {
+  // register split 136 / 136 / 120 / 120 per thread for WG0 / WG1 / WG2 / WG3 (sum =
+  // 4 x 128, the launch allocation)
+  if (warp >= 12) {
+    setmaxnreg_dec<120>();
+    if (warp == 12) {
       // ============================================================ TMA producer
       Waiter w{abort_flag, p.timeout_ns, kRoleLoad};
+      Tracer tr;
+      tr.init(p.trace, p.trace_ctas, 0, lane == 0);
       const bool leader = elect_one();
       uint32_t q_armed = 0;   // bit s: stage s has an armed load whose completion may still be pending
       bool kv_armed = false;
@@ -244,6 +250,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
             bulk_load(st + 512, p.dsum + pk, 512, bar(L::bQFull + s));
           }
           __syncwarp();
+          tr.rec(kEvBQLoad, k);
           q_armed |= 1u << s;
           q_par = (q_par & ~(1u << s)) | (use << s);
         }
@@ -255,9 +262,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
         for (int s = 0; s < 2; ++s)
           if (q_armed & (1u << s)) d.wait(bar(L::bQFull + s), (q_par >> s) & 1, L::bQFull + s, -1);
       }
-    } else if (warp == 9) {
+    } else if (warp == 13) {
       // ============================================================ MMA issuer
       Waiter w{abort_flag, p.timeout_ns, kRoleMma};
+      Tracer tr;
+      tr.init(p.trace, p.trace_ctas, 1, lane == 0);
       const bool leader = elect_one();
       constexpr uint32_t idS = idesc_f32acc2(128, 128, false, false, F16);   // S^T, dP^T: both K-major
       constexpr uint32_t idV = idesc_f32acc2(128, D, false, true, F16);      // dV: A = P^T (TMEM), B = dO MN-major
@@ -266,7 +275,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
       const uint64_t Kk = smem_desc_sw128(sK, 16, 1024), Vk = smem_desc_sw128(sV, 16, 1024);
       const uint64_t Kmn = smem_desc_sw128(sK, L::kSlab, 1024);
       const uint64_t dSk = smem_desc_sw128(sDS, 16, 1024), dSmn = smem_desc_sw128(sDS, L::kSlab, 1024);
-      const uint32_t tS = tmem + L::cS, tP = tmem + L::cS + 64, tdP = tmem + L::cDP;
+      const uint32_t tS = tmem + L::cS, tP = tmem + L::cS + 32, tdP = tmem + L::cDP;
       const uint32_t tdV = tmem + L::cDV, tdK = tmem + L::cDK;
       auto qk = [&](int s) { return smem_desc_sw128(sQ + s * L::kTile, 16, 1024); };
       auto qmn = [&](int s) { return smem_desc_sw128(sQ + s * L::kTile, L::kSlab, 1024); };
@@ -305,42 +314,63 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
 #pragma unroll 1
         for (int k = 0; ok && k < n; ++k) {
           const int s = k & 1;
-          // dV += P^T dO (K = 128 rows: P^T from TMEM, 8 columns of 16-bit pairs per step)
+          // dV += P^T dO (K = 128 rows: P^T from TMEM, 8 columns of 16-bit pairs per step;
+          // rows 0-63 in columns [32, 64) of S^T, rows 64-127 in [96, 128))
           if (!w.wait(bar(L::bPReady), k & 1, L::bPReady, k)) { ok = false; break; }
           tc_fence_after();
           if (leader) {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              mma_ts(tdV, tP + kk * 8, domn(s) + ((kk * 2048) >> 4), idV, (k > 0 || kk > 0) ? 1u : 0u);
-          }
-          __syncwarp();
-          // the next tile's S^T: its columns are free once this dV (issued before it) has read P^T
-          if (k + 1 < n) {
-            const int s1 = (k + 1) & 1;
-            if (!w.wait(bar(L::bQFull + s1), ((k + 1) >> 1) & 1, L::bQFull + s1, k + 1)) { ok = false; break; }
-            tc_fence_after();
-            if (leader) {
-              issue_s(s1);
-              mma_commit(bar(L::bSFull));
-            }
-            __syncwarp();
-          }
-          // dK += dS^T Q and dQ = dS K, once dS is in shared memory
-          if (!w.wait(bar(L::bdSReady), k & 1, L::bdSReady, k)) { ok = false; break; }
-          tc_fence_after();
-          if (leader) {
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ss(tdK, dSk + (kmajor_step<L::kSlab>(kk) >> 4), qmn(s) + ((kk * 2048) >> 4), idK,
+              mma_ts(tdV, tP + (kk >> 2) * 64 + (kk & 3) * 8, domn(s) + ((kk * 2048) >> 4), idV,
                      (k > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ss(tdP, dSmn + ((kk * 2048) >> 4), Kmn + ((kk * 2048) >> 4), idQ, kk > 0 ? 1u : 0u);
-            mma_commit(bar(L::bdQFull));   // also: this step's Q and dO are no longer read
-            mma_commit(bar(L::bdSEmpty));
           }
           __syncwarp();
-          // the next tile's dP^T, once WG1 has taken dQ out of those columns
+          tr.rec(kEvBdV, k);
+          // dK += dS^T Q and dQ = dS K (once dS is in shared memory) and the next tile's
+          // S^T (once its Q has landed; its columns are free, the dV above has read P^T):
+          // whichever input arrives first is issued first (non-blocking tests: a try_wait
+          // on the barrier that is not ready would hold the warp until that one completes)
+          {
+            const int s1 = (k + 1) & 1;
+            bool s_done = k + 1 >= n, dq_done = false;
+            uint32_t it = 0;
+            uint64_t t0 = 0;
+            while (!(s_done && dq_done)) {
+              if (!s_done && __all_sync(0xffffffffu, mbar_test_wait(bar(L::bQFull + s1), ((k + 1) >> 1) & 1))) {
+                tc_fence_after();
+                if (leader) {
+                  issue_s(s1);
+                  mma_commit(bar(L::bSFull));
+                }
+                __syncwarp();
+                tr.rec(kEvBS, k + 1);
+                s_done = true;
+                continue;
+              }
+              if (!dq_done && __all_sync(0xffffffffu, mbar_test_wait(bar(L::bdSReady), k & 1))) {
+                tc_fence_after();
+                if (leader) {
+                  // dQ first, so WG2 can start on it while dK runs
+#pragma unroll
+                  for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tdP, dSmn + ((kk * 2048) >> 4), Kmn + ((kk * 2048) >> 4), idQ, kk > 0 ? 1u : 0u);
+                  mma_commit(bar(L::bdQFull));
+#pragma unroll
+                  for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tdK, dSk + (kmajor_step<L::kSlab>(kk) >> 4), qmn(s) + ((kk * 2048) >> 4), idK,
+                           (k > 0 || kk > 0) ? 1u : 0u);
+                  mma_commit(bar(L::bdSEmpty));  // also: this step's Q and dO are no longer read
+                }
+                __syncwarp();
+                tr.rec(kEvBdKdQ, k);
+                dq_done = true;
+                continue;
+              }
+              if (!w.still_waiting(it, t0, dq_done ? L::bQFull + s1 : L::bdSReady, k)) { ok = false; break; }
+            }
+            if (!ok) break;
+          }
+          // the next tile's dP^T, once WG2 has taken dQ out of those columns
           if (k + 1 < n) {
             const int s1 = (k + 1) & 1;
             if (!w.wait(bar(L::bdPEmpty), (k + 1) & 1, L::bdPEmpty, k + 1)) { ok = false; break; }
@@ -350,6 +380,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
               mma_commit(bar(L::bdPFull));
             }
             __syncwarp();
+            tr.rec(kEvBdP, k + 1);
           }
         }
         if (ok && leader) mma_commit(bar(L::bFinal));
@@ -361,41 +392,45 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
       Waiter d{never_abort, p.timeout_ns, kRoleDrain};
       d.wait(bar(L::bDrain), 0, L::bDrain, -1);
     }
-  } else if (warp < 4) {
-    // ================================================================ WG0: P and dS (one key per thread)
-    setmaxnreg_inc<240>();
-    const int kr = tid;                                   // key row == TMEM lane
+  } else if (warp < 8) {
+    // ================================================================ WG0 / WG1: P and dS (one key per thread)
+    setmaxnreg_inc<136>();
+    const int hq = warp >> 2;                             // query columns [64 hq, 64 hq + 64) of the tile
+    const int cq = hq * 64;
+    const int kr = tid & 127;                             // key row == TMEM lane
     const int kabs = j * 128 + kr;
     const bool key_ok = kabs < p.Nk;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const uint32_t tS = tmem + lane_base + L::cS, tdP = tmem + lane_base + L::cDP;
-    Waiter w{abort_flag, p.timeout_ns, kRoleSoftmax0};
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + L::cS + cq, tdP = tmem + lane_base + L::cDP + cq;
+    Waiter w{abort_flag, p.timeout_ns, hq == 0 ? kRoleSoftmax0 : kRoleSoftmax1};
+    Tracer tr;
+    tr.init(p.trace, p.trace_ctas, 2 + hq, kr == 0);
     const float sl2 = p.scale_log2, sc = p.scale;
     bool ok = true;
 #pragma unroll 1
     for (int k = 0; k < n; ++k) {
       const int i = i0 + k;
       // this tile's base-2 LSE and D, loaded with Q and dO (q_full of the stage, waited below)
-      const float4* L2 = reinterpret_cast<const float4*>(smem + L::kStats + (k & 1) * L::kStatsBytes);
+      const float4* L2 = reinterpret_cast<const float4*>(smem + L::kStats + (k & 1) * L::kStatsBytes) + cq / 4;
       const float4* DS = L2 + 32;
       // rows [qlo, qhi) of this tile see this key: causal needs position >= kabs - off,
-      // and rows past the sequence's packed end are padding
+      // and rows past the sequence's packed end are padding (local to this half)
       const int qlo = CAUSAL ? (int)max(-1LL, min(129LL, ((long long)kabs - off) * (1LL << p.gshift) - (long long)i * 128))
-                             : 0;
-      const int qhi = key_ok ? min(128, (p.Nq << p.gshift) - i * 128) : 0;
+                                   - cq
+                             : -cq;
+      const int qhi = (key_ok ? min(128, (p.Nq << p.gshift) - i * 128) : 0) - cq;
       if (!w.wait(bar(L::bQFull + (k & 1)), (k >> 1) & 1, L::bQFull + (k & 1), k)) { ok = false; break; }
       if (!w.wait(bar(L::bSFull), k & 1, L::bSFull, k)) { ok = false; break; }
+      tr.rec(kEvBSFull, k);
       tc_fence_after();
-      float P[128];
+      float P[64];
       {
-        uint32_t u[128];
+        uint32_t u[64];
         tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
         tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
-        tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&u[64]));
-        tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&u[96]));
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 128; c += 4) {
+        for (int c = 0; c < 64; c += 4) {
           const float4 l = L2[c / 4];
           const float lv[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
@@ -406,27 +441,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
           }
         }
       }
-      // P^T as 16-bit pairs over the upper half of the S^T columns: the A operand of dV
+      // P^T as 16-bit pairs over the upper 32 columns of this half of S^T (all of the
+      // half was read above): the A operand of dV
       {
-        uint32_t pk[64];
+        uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 64; ++c) pk[c] = pack_16x2<F16>(P[2 * c], P[2 * c + 1]);
-        tmem_st32(tS + 64, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(tS + 96, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+        for (int c = 0; c < 32; ++c) pk[c] = pack_16x2<F16>(P[2 * c], P[2 * c + 1]);
+        tmem_st32(tS + 32, pk);
         tmem_wait_st();
       }
       tc_fence_before();
       mbar_arrive(bar(L::bPReady));
-      // dS = s * P * (dP - D) -> 16-bit -> the shared dS tile (row = key, 128-byte swizzle)
-      if (k > 0 && !w.wait(bar(L::bdSEmpty), (k - 1) & 1, L::bdSEmpty, k)) { ok = false; break; }
+      tr.rec(kEvBPReady, k);
+      // dS = s * P * (dP - D) -> 16-bit -> slab hq of the shared dS tile (row = key, 128-byte
+      // swizzle), stored once the previous step's dK has finished reading the tile
       if (!w.wait(bar(L::bdPFull), k & 1, L::bdPFull, k)) { ok = false; break; }
+      tr.rec(kEvBdPFull, k);
       tc_fence_after();
+      uint32_t pk[32];
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 0; ch < 2; ++ch) {
         uint32_t u[32];
         tmem_ld32(tdP + ch * 32, u);
         tmem_wait_ld();
-        uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 4) {
           const float4 dd = DS[(ch * 32 + c) / 4];
@@ -434,23 +471,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
           float g[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) g[e] = P[ch * 32 + c + e] * (__uint_as_float(u[c + e]) - dv[e]) * sc;
-          pk[c / 2] = pack_16x2<F16>(g[0], g[1]);
-          pk[c / 2 + 1] = pack_16x2<F16>(g[2], g[3]);
-        }
-        // 32 rows = four 16-byte units of row kr in slab ch / 2
-        const uint32_t row = sDS + (uint32_t)(ch >> 1) * L::kSlab + (uint32_t)kr * 128u;
-#pragma unroll
-        for (int uu = 0; uu < 4; ++uu) {
-          const uint32_t unit = (uint32_t)((ch & 1) * 4 + uu);
-          st_shared_v4(row + ((unit ^ (uint32_t)(kr & 7)) << 4), pk[4 * uu], pk[4 * uu + 1], pk[4 * uu + 2],
-                       pk[4 * uu + 3]);
+          pk[(ch * 32 + c) / 2] = pack_16x2<F16>(g[0], g[1]);
+          pk[(ch * 32 + c) / 2 + 1] = pack_16x2<F16>(g[2], g[3]);
         }
       }
+      if (k > 0 && !w.wait(bar(L::bdSEmpty), (k - 1) & 1, L::bdSEmpty, k)) { ok = false; break; }
+      const uint32_t row = sDS + (uint32_t)hq * L::kSlab + (uint32_t)kr * 128u;
+#pragma unroll
+      for (int uu = 0; uu < 8; ++uu)
+        st_shared_v4(row + (((uint32_t)uu ^ (uint32_t)(kr & 7)) << 4), pk[4 * uu], pk[4 * uu + 1], pk[4 * uu + 2],
+                     pk[4 * uu + 3]);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(L::bdSReady));
+      tr.rec(kEvBdSReady, k);
     }
-    // dK (scale already in dS) -> 16-bit -> global
+    // dK (scale already in dS) -> 16-bit -> global; this warpgroup writes columns
+    // [hq * D / 2, (hq + 1) * D / 2)
     if (ok) {
       if (n > 0 && !w.wait(bar(L::bFinal), 0, L::bFinal, -1)) ok = false;
     }
@@ -458,7 +495,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
       tc_fence_after();
       uint16_t* dst = p.dk + ((size_t)(tok_k + kabs) * p.Hkv + kvh) * D;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = hq * (D / 64); c < (hq + 1) * (D / 64); ++c) {
         uint32_t u[32];
         if (n > 0) {
           tmem_ld32(tmem + lane_base + L::cDK + c * 32, u);
@@ -478,12 +515,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
         }
       }
     }
-  } else {
-    // ================================================================ WG1: dQ reduce-adds, then dV
-    setmaxnreg_dec<136>();
-    const int r = tid - 128;                              // Q-tile row (dQ) / key row (dV) == TMEM lane
+  } else if (warp < 12) {
+    // ================================================================ WG2: dQ reduce-adds, then dV
+    setmaxnreg_dec<120>();
+    const int r = tid - 256;                              // Q-tile row (dQ) / key row (dV) == TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     Waiter w{abort_flag, p.timeout_ns, kRoleCorr};
+    Tracer tr;
+    tr.init(p.trace, p.trace_ctas, 4, r == 0);
     mbar_arrive(bar(L::bdPEmpty));                        // the dP columns start free
     bool ok = true;
 #pragma unroll 1
@@ -492,20 +531,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
       const int s = k & 1;
       const bool valid = ((i * 128 + r) >> p.gshift) < p.Nq;   // padding rows add zeros
       if (!w.wait(bar(L::bdQFull), k & 1, L::bdQFull, k)) { ok = false; break; }
+      tr.rec(kEvBdQFull, k);
       tc_fence_after();
-      // dQ in 32-column chunks -> fp32 rows in the freed Q_s / dO_s buffers, in the
-      // 128-byte-swizzled layout of the reduce map (16-byte unit u of row r at u ^ (r % 8))
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t u[32];
-        tmem_ld32(tmem + lane_base + L::cDP + c * 32, u);
-        tmem_wait_ld();
-        if (c == D / 32 - 1) {                            // all of dQ has left TMEM: free the columns
-          tc_fence_before();
-          mbar_arrive(bar(L::bdPEmpty));
-        }
-        const uint32_t chunk = c < L::kHalves ? sQ + s * L::kTile + c * L::kSlab
-                                              : sDO + s * L::kTile + (c - L::kHalves) * L::kSlab;
+      // dQ in 32-column chunks -> fp32 rows in the freed dO_s / Q_s buffers, in the
+      // 128-byte-swizzled layout of the reduce map (16-byte unit u of row r at u ^ (r % 8)).
+      // dO_s is free once dQ is done (dV and dP, the products that read it, came before);
+      // Q_s only once dK (issued after dQ) is done: round 0 stages the upper chunks in
+      // dO_s, round 1 loads the lower chunks, frees the TMEM columns, waits for dK and
+      // stages them in Q_s. Each round's reduce-adds leave once all 128 rows are staged.
+      const int tok = tok_q + ((i * 128) >> p.gshift);
+      auto stage_chunk = [&](const uint32_t (&u)[32], uint32_t chunk) {
         const uint32_t row = chunk + (uint32_t)r * 128u;
 #pragma unroll
         for (int uu = 0; uu < 8; ++uu) {
@@ -513,27 +548,58 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
           const uint32_t a2 = valid ? u[4 * uu + 2] : 0u, a3 = valid ? u[4 * uu + 3] : 0u;
           st_shared_v4(row + (((uint32_t)uu ^ (uint32_t)(r & 7)) << 4), a0, a1, a2, a3);
         }
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(bar(L::bdQStaged));
-      if (warp == 4) {
-        if (!w.wait(bar(L::bdQStaged), k & 1, L::bdQStaged, k)) { ok = false; break; }
-        if (lane == 0) {
-          const int tok = tok_q + ((i * 128) >> p.gshift);
+      };
+      auto round_done = [&](int rnd) -> bool {           // all rows of the round staged: send them
+        fence_proxy_async_smem();
+        mbar_arrive(bar(L::bdQStaged));
+        if (warp == 8) {
+          if (!w.wait(bar(L::bdQStaged), (uint32_t)(k * 2 + rnd) & 1u, L::bdQStaged, k)) return false;
+          if (lane == 0) {
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            const uint32_t chunk = c < L::kHalves ? sQ + s * L::kTile + c * L::kSlab
-                                                  : sDO + s * L::kTile + (c - L::kHalves) * L::kSlab;
-            tma_reduce_add_3d(&p.tm_dq, chunk, c * 32, kvh << p.gshift, tok);
+            for (int h = 0; h < L::kHalves; ++h) {
+              const int c = rnd == 0 ? L::kHalves + h : h;
+              const uint32_t chunk = (rnd == 0 ? sDO : sQ) + s * L::kTile + h * L::kSlab;
+              tma_reduce_add_3d(&p.tm_dq, chunk, c * 32, kvh << p.gshift, tok);
+            }
           }
+          __syncwarp();
+        }
+        return true;
+      };
+#pragma unroll 1
+      for (int h = 0; h < L::kHalves; ++h) {
+        uint32_t u[32];
+        tmem_ld32(tmem + lane_base + L::cDP + (L::kHalves + h) * 32, u);
+        tmem_wait_ld();
+        stage_chunk(u, sDO + s * L::kTile + h * L::kSlab);
+      }
+      {
+        uint32_t u[L::kHalves][32];
+#pragma unroll
+        for (int h = 0; h < L::kHalves; ++h) tmem_ld32(tmem + lane_base + L::cDP + h * 32, u[h]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar(L::bdPEmpty));                    // all of dQ has left TMEM: free the columns
+        tr.rec(kEvBdPEmpty, k);
+        if (!round_done(0)) { ok = false; break; }
+        if (!w.wait(bar(L::bdSEmpty), k & 1, L::bdSEmpty, k)) { ok = false; break; }   // dK has read Q_s
+#pragma unroll
+        for (int h = 0; h < L::kHalves; ++h) stage_chunk(u[h], sQ + s * L::kTile + h * L::kSlab);
+      }
+      if (!round_done(1)) { ok = false; break; }
+      if (!ok) break;
+      tr.rec(kEvBStaged, k);
+      if (warp == 8) {
+        if (lane == 0) {
           bulk_commit();
           bulk_wait_read_all();                           // the staging may be overwritten now
           mbar_arrive(bar(L::bQEmpty + s));               // Q_s and dO_s may be reloaded
+          tr.rec(kEvBReduced, k);
         }
         __syncwarp();
       }
     }
-    if (warp == 4 && lane == 0) bulk_wait_all();          // reduce-adds complete before dV / exit
+    if (warp == 8 && lane == 0) bulk_wait_all();          // reduce-adds complete before dV / exit
     // dV -> 16-bit -> global
     if (ok && n > 0 && !w.wait(bar(L::bFinal), 0, L::bFinal, -1)) ok = false;
     if (ok) {
@@ -566,7 +632,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

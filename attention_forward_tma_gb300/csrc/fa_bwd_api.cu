@@ -37,9 +37,9 @@ int launch(const fa::BwdParams& p, cudaStream_t s) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess ||
           cudaFuncGetAttributes(&a, kern) != cudaSuccess)
         r = FA_ERR_CUDA;
-      // the warpgroup register split (240/136/128) needs exactly 168 registers per
+      // the warpgroup register split (136/136/120/120) needs exactly 128 registers per
       // thread at launch
-      else if (a.numRegs != 168)
+      else if (a.numRegs != 128)
         r = FA_ERR_UNSUPPORTED;
       else
         r = 1;
@@ -166,6 +166,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.timeout_ns = 2000000000ull;
+    fa_host::trace_target(&p.trace, &p.trace_ctas);
     if (d == 128)
       st = f16 ? launch_c<128, true>(p, causal != 0, s) : launch_c<128, false>(p, causal != 0, s);
     else

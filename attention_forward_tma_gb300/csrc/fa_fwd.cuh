@@ -115,15 +115,21 @@ enum : uint32_t {
   kEvPV1a = 17, kEvP21 = 18, kEvPV1b = 19, kEvKVV = 20, kEvKVK = 21,
   kEvSFull = 30, kEvSMax = 31, kEvMail = 32, kEvHalf1 = 33, kEvHalf2 = 34, kEvStats = 35,
   kEvCorrFull = 40, kEvCorrDone = 42, kEvEpiStart = 44, kEvEpiEnd = 46, kEvTask = 48,
-  kEvIssueBegin = 50
+  kEvIssueBegin = 50,
+  // backward: producer, MMA issuer, P/dS warpgroups (roles 2, 3), dQ warpgroup (role 4)
+  kEvBQLoad = 60, kEvBdV = 61, kEvBS = 62, kEvBdKdQ = 63, kEvBdP = 64, kEvBSFull = 70, kEvBPReady = 71,
+  kEvBdPFull = 72, kEvBdSReady = 73, kEvBdQFull = 80, kEvBdPEmpty = 81, kEvBStaged = 82, kEvBReduced = 83
 };
 struct Tracer {
 #ifdef FA_TRACE
   unsigned long long* buf = nullptr;
   uint32_t n = 0;
+  __device__ __forceinline__ void init(unsigned long long* trace, int trace_ctas, int role, bool leader) {
+    if (leader && trace != nullptr && (int)blockIdx.x < trace_ctas)
+      buf = trace + ((size_t)blockIdx.x * kTraceRoles + role) * kTraceSlots;
+  }
   __device__ __forceinline__ void init(const FwdParams& p, int role, bool leader) {
-    if (leader && p.trace != nullptr && (int)blockIdx.x < p.trace_ctas)
-      buf = p.trace + ((size_t)blockIdx.x * kTraceRoles + role) * kTraceSlots;
+    init(p.trace, p.trace_ctas, role, leader);
   }
   __device__ __forceinline__ void rec(uint32_t code, int blk) {
     if (buf != nullptr && 2 * n + 2 < (uint32_t)kTraceSlots) {
@@ -133,6 +139,7 @@ struct Tracer {
     }
   }
 #else
+  __device__ __forceinline__ void init(unsigned long long*, int, int, bool) {}
   __device__ __forceinline__ void init(const FwdParams&, int, bool) {}
   __device__ __forceinline__ void rec(uint32_t, int) {}
 #endif
@@ -289,6 +296,21 @@ struct Waiter {
         }
       }
     }
+  }
+  // For loops that poll several barriers in turn: call once per round; returns
+  // false (after recording a timeout once the limit has passed) when the loop
+  // must give up. Warp-uniform like wait().
+  __device__ __forceinline__ bool still_waiting(uint32_t& it, uint64_t& t0, uint32_t bar_id, int block) {
+    if ((++it & 63) != 0) return true;
+    if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
+    const uint64_t now = __shfl_sync(0xffffffffu, globaltimer(), 0);
+    if (t0 == 0) {
+      t0 = now;
+    } else if (now - t0 > timeout_ns) {
+      give_up(bar_id, block);
+      return false;
+    }
+    return true;
   }
   // Cold path: raise the CTA's abort flag and record the first timeout.
   __device__ __noinline__ void give_up(uint32_t bar_id, int block) {

@@ -85,4 +85,7 @@ inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 // has its own copy of the status variable): returns it and clears it.
 int bwd_take_status(unsigned long long* word);
 
+// The clock-stamp buffer set by fa_trace_configure (tracing builds; else null, 0).
+void trace_target(unsigned long long** buf, int* ctas);
+
 }  // namespace fa_host

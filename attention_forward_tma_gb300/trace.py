@@ -1,13 +1,12 @@
 """Pipeline traces from the tracing build of the library (libfa_gb300_trace.so).
 
-python -m attention_forward_tma_gb300.trace [--workload NAME] [--ctas N] [--json FILE]
+python -m attention_forward_tma_gb300.trace [--workload NAME] [--ctas N] [--json FILE] [--pass fwd|bwd]
 
-Runs one attention forward of a synthetic workload with clock stamps at every
-hand-off of the pipeline (TMA issue, MMA issue, softmax phases, correction and
-epilogue) for the first N CTAs, then prints per-role cycle statistics: the
-softmax latency per K/V block, how long the MMA issuer waited for each tile's
-P, the MMA issue period per block pair, and the epilogue time.
-Stamps are SM clock cycles (clock64) of the CTA's own SM.
+Runs one attention forward (or backward) of a synthetic workload with clock
+stamps at every hand-off of the pipeline (TMA issue, MMA issue, softmax phases,
+correction and epilogue; for the backward: Q/dO loads, the five products, the
+P and dS phases and the dQ reduce) for the first N CTAs, then prints per-role
+cycle statistics. Stamps are SM clock cycles (clock64) of the CTA's own SM.
 """
 from __future__ import annotations
 
@@ -23,7 +22,8 @@ EVENTS = {1: "Q0", 2: "K", 3: "Q1", 4: "V", 10: "S0", 11: "S1", 12: "PO0", 13: "
           16: "PO1", 17: "PV1a", 18: "P2_1", 19: "PV1b", 20: "KVfull_V", 21: "KVfull_K", 30: "SFull", 31: "SMax",
           32: "Mail", 33: "Half1", 34: "Half2", 35: "Stats", 40: "CorrFull0", 41: "CorrFull1", 42: "CorrDone0",
           43: "CorrDone1", 44: "EpiStart0", 45: "EpiStart1", 46: "EpiEnd0", 47: "EpiEnd1", 48: "Task",
-          50: "IssueBegin"}
+          50: "IssueBegin", 60: "QLoad", 61: "dV", 62: "S", 63: "dKdQ", 64: "dP", 70: "SFull", 71: "PReady",
+          72: "dPFull", 73: "dSReady", 80: "dQFull", 81: "dPEmpty", 82: "Staged", 83: "Reduced"}
 ROLES = ["producer", "mma", "softmax0", "softmax1", "correction"]
 
 
@@ -102,6 +102,50 @@ def summarize(trace) -> dict:
     return res
 
 
+def _gaps(events, a, b):
+    """Per step (the event's block field): cycles from event a to event b of the same step."""
+    ta = {blk: clk for clk, name, blk in events if name == a}
+    return [clk - ta[blk] for clk, name, blk in events if name == b and blk in ta]
+
+
+def _period(events, a):
+    t = [clk for clk, name, _ in events if name == a]
+    return [y - x for x, y in zip(t, t[1:])]
+
+
+def summarize_bwd(trace) -> dict:
+    res = {}
+    for c, roles in trace.items():
+        m, s0, g = roles["mma"], roles["softmax0"], roles["correction"]
+        d = {"steps": len([1 for _, n_, _ in m if n_ == "dV"])}
+        d["step_period(dSReady)"] = _period(s0, "dSReady")
+        d["mma_dV_to_S(next)"] = _gaps_shift(m, "dV", "S", 1)
+        d["mma_dV_to_dKdQ"] = _gaps(m, "dV", "dKdQ")
+        d["mma_dKdQ_to_dP(next)"] = _gaps_shift(m, "dKdQ", "dP", 1)
+        d["wg0_SFull_to_PReady"] = _gaps(s0, "SFull", "PReady")
+        d["wg0_PReady_to_dPFull"] = _gaps(s0, "PReady", "dPFull")
+        d["wg0_dPFull_to_dSReady"] = _gaps(s0, "dPFull", "dSReady")
+        d["wg2_dQFull_to_dPEmpty"] = _gaps(g, "dQFull", "dPEmpty")
+        d["wg2_dQFull_to_Staged"] = _gaps(g, "dQFull", "Staged")
+        d["wg2_Staged_to_Reduced"] = _gaps(g, "Staged", "Reduced")
+        d["dSReady_to_dQFull"] = _cross(s0, "dSReady", g, "dQFull")
+        d["dPEmpty_to_dPFull(next)"] = _cross(g, "dPEmpty", s0, "dPFull", 1)
+        d["Reduced_to_QLoad(k+2)"] = _cross(g, "Reduced", roles["producer"], "QLoad", 2)
+        d["QLoad_to_SFull"] = _cross(roles["producer"], "QLoad", s0, "SFull")
+        res[c] = d
+    return res
+
+
+def _gaps_shift(events, a, b, shift):
+    ta = {blk: clk for clk, name, blk in events if name == a}
+    return [clk - ta[blk - shift] for clk, name, blk in events if name == b and blk - shift in ta]
+
+
+def _cross(ea, a, eb, b, shift=0):
+    ta = {blk: clk for clk, name, blk in ea if name == a}
+    return [clk - ta[blk - shift] for clk, name, blk in eb if name == b and blk - shift in ta]
+
+
 def _fmt(v):
     if isinstance(v, list):
         if not v:
@@ -115,6 +159,7 @@ def main():
     ap.add_argument("--workload", default="c4_b1h32n16384d128_causal_spiky")
     ap.add_argument("--ctas", type=int, default=2)
     ap.add_argument("--json", default=None)
+    ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"])
     a = ap.parse_args()
     sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
     import numpy as np
@@ -130,7 +175,12 @@ def main():
         return torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
 
     q, k, v = dev(x["q"]), dev(x["k"]), dev(x["v"])
-    if w.varlen:
+    if a.which == "bwd":
+        from . import fa_bwd
+        dout = dev(fa_inputs.make_qkv(w.B, w.N, w.H, w.d, w.seed + 1000, dtype=w.dtype)[0])
+        o, lse = fa_fwd(q, k, v, scale=w.scale, causal=w.causal)
+        run = lambda: fa_bwd(q, k, v, o, dout, lse, scale=w.scale, causal=w.causal)  # noqa: E731
+    elif w.varlen:
         cu = torch.from_numpy(x["cu_seqlens"]).cuda()
         run = lambda: fa_fwd_varlen(q, k, v, cu, int(x["lengths"].max()), scale=w.scale, causal=w.causal)  # noqa: E731
     else:
@@ -141,7 +191,7 @@ def main():
     if a.json:
         with open(a.json, "w") as f:
             json.dump({str(c): r for c, r in tr.items()}, f)
-    for c, d in summarize(tr).items():
+    for c, d in (summarize_bwd(tr) if a.which == "bwd" else summarize(tr)).items():
         print(f"CTA {c}")
         for key, val in d.items():
             print(f"  {key:28s} {_fmt(val)}")
