@@ -100,27 +100,35 @@ __device__ __forceinline__ float half_bits_to_f32(uint16_t x, bool f16) {
 }
 
 // ------------------------------------------------------------------ preprocessing
-// One warp per (b, position, query head): D = rowsum(dO * O) in fp32, and the
-// forward's LSE in base 2; both written at the row's packed index
-// (b, kv head, position * G + head % G).
+// One warp per (b, position, query head): D = rowsum(dO * O) in fp32 and the
+// forward's LSE in base 2, both written at the row's packed index (b, kv head,
+// position * G + head % G); the row of the fp32 dQ accumulator is zeroed on the way.
 template <int D, bool F16>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint16_t* __restrict__ o,
                                                          const uint16_t* __restrict__ dout,
                                                          const float* __restrict__ lse, float* __restrict__ lse2,
-                                                         float* __restrict__ dsum, int B, int H, int gshift, int Nq,
-                                                         int mpad) {
-  constexpr int E = D / 32;
+                                                         float* __restrict__ dsum, float* __restrict__ dq_acc, int B,
+                                                         int H, int gshift, int Nq, int mpad) {
+  constexpr int E = D / 32;   // elements per lane: 4 (d = 128) or 2 (d = 64)
   const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (w >= (long long)B * Nq * H) return;
   const int lane = threadIdx.x & 31;
   const int h = (int)(w % H);
   const long long bp = w / H;
   const int b = (int)(bp / Nq), pos = (int)(bp % Nq);
-  const uint16_t* orow = o + w * D + lane * E;
-  const uint16_t* grow = dout + w * D + lane * E;
+  uint16_t ov[E], gv[E];
+  if constexpr (E == 4) {
+    *reinterpret_cast<uint2*>(ov) = *reinterpret_cast<const uint2*>(o + w * D + lane * E);
+    *reinterpret_cast<uint2*>(gv) = *reinterpret_cast<const uint2*>(dout + w * D + lane * E);
+    *reinterpret_cast<float4*>(dq_acc + w * D + lane * E) = make_float4(0.f, 0.f, 0.f, 0.f);
+  } else {
+    *reinterpret_cast<uint32_t*>(ov) = *reinterpret_cast<const uint32_t*>(o + w * D + lane * E);
+    *reinterpret_cast<uint32_t*>(gv) = *reinterpret_cast<const uint32_t*>(dout + w * D + lane * E);
+    *reinterpret_cast<float2*>(dq_acc + w * D + lane * E) = make_float2(0.f, 0.f);
+  }
   float acc = 0.f;
 #pragma unroll
-  for (int e = 0; e < E; ++e) acc = fmaf(half_bits_to_f32(orow[e], F16), half_bits_to_f32(grow[e], F16), acc);
+  for (int e = 0; e < E; ++e) acc = fmaf(half_bits_to_f32(ov[e], F16), half_bits_to_f32(gv[e], F16), acc);
 #pragma unroll
   for (int x = 16; x > 0; x >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, x);
   if (lane == 0) {

@@ -57,11 +57,12 @@ int launch_c(const fa::BwdParams& p, bool causal, cudaStream_t s) {
 
 template <int D, bool F>
 int pre_post(bool post, const void* o, const void* dout, const float* lse, float* lse2, float* dsum,
-             const float* dq_acc, void* dq, int B, int H, int gshift, int Nq, int mpad, cudaStream_t s) {
+             float* dq_acc, void* dq, int B, int H, int gshift, int Nq, int mpad, cudaStream_t s) {
   if (!post) {
     const long long rows = (long long)B * Nq * H;
     fa::fa_bwd_pre_kernel<D, F><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
-        static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, lse2, dsum, B, H, gshift, Nq, mpad);
+        static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, lse2, dsum, dq_acc, B, H, gshift,
+        Nq, mpad);
   } else {
     const long long n4 = (long long)B * Nq * H * D / 4;
     fa::fa_bwd_post_kernel<F><<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(
@@ -71,7 +72,7 @@ int pre_post(bool post, const void* o, const void* dout, const float* lse, float
 }
 
 int pre_post_any(bool post, int d, bool f16, const void* o, const void* dout, const float* lse, float* lse2,
-                 float* dsum, const float* dq_acc, void* dq, int B, int H, int gshift, int Nq, int mpad,
+                 float* dsum, float* dq_acc, void* dq, int B, int H, int gshift, int Nq, int mpad,
                  cudaStream_t s) {
   if (d == 128)
     return f16 ? pre_post<128, true>(post, o, dout, lse, lse2, dsum, dq_acc, dq, B, H, gshift, Nq, mpad, s)
@@ -137,8 +138,9 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
       (st = make_map(&p.tm_v, v, tokens_k, H_kv, d, 1, f16)) != FA_OK)
     return st;
 
-  // temporary buffer: dQ accumulator (fp32 [tokens, H, d]), then packed base-2 LSE
-  // and D ([B, H_kv, mpad] each); zeroed so padding rows read 0
+  // temporary buffer: dQ accumulator (fp32 [tokens, H, d], zeroed by the
+  // preprocessing kernel), then packed base-2 LSE and D ([B, H_kv, mpad] each,
+  // zeroed here so padding rows read 0)
   const size_t acc_bytes = (size_t)tokens * H * d * sizeof(float);
   const size_t vec_bytes = ((size_t)B * H_kv * mpad * sizeof(float) + 255) / 256 * 256;
   void* ws = nullptr;
@@ -149,9 +151,9 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   float* dq_acc = static_cast<float*>(ws);
   float* lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes);
   float* dsum = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes + vec_bytes);
-  if (cudaMemsetAsync(ws, 0, acc_bytes + 2 * vec_bytes, s) != cudaSuccess) st = FA_ERR_CUDA;
+  if (cudaMemsetAsync(lse2, 0, 2 * vec_bytes, s) != cudaSuccess) st = FA_ERR_CUDA;
   if (st == FA_OK)
-    st = pre_post_any(false, d, f16, o, dout, lse, lse2, dsum, nullptr, nullptr, B, H, gshift, N_q, (int)mpad, s);
+    st = pre_post_any(false, d, f16, o, dout, lse, lse2, dsum, dq_acc, nullptr, B, H, gshift, N_q, (int)mpad, s);
   if (st == FA_OK) st = fa_host::make_map_f32(&p.tm_dq, dq_acc, tokens, H, d, G);
   if (st == FA_OK) {
     p.lse2 = lse2;

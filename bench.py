@@ -116,9 +116,9 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
+def profiled_traffic(workload: str, which: str = "fwd"):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
-    path = os.path.join(ROOT, "profiles", f"fa_fwd_{workload}_dram.txt")
+    path = os.path.join(ROOT, "profiles", f"fa_{which}_{workload}_dram.txt")
     try:
         kv = {}
         with open(path) as f:
@@ -440,7 +440,7 @@ def run_ours(a, dist):
     clk = clocks.summary()
     max_mhz = clk["sm_max_mhz"] or 2070.0
     theoretical = props.multi_processor_count * FLOP_PER_CLK_PER_SM * max_mhz * 1e6 / 1e12
-    traffic = profiled_traffic(w.name)
+    traffic = profiled_traffic(w.name, a.which)
     # the bound follows the arithmetic intensity: below the ridge of the measured
     # peaks (FLOP per byte) the step is an HBM stream, above it a contraction
     nbytes = workload_bytes(w, x) * (2.0 if bwd else 1.0)   # bwd: Q, K, V, O, dO read; dQ, dK, dV written
