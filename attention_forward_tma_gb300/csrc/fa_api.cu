@@ -26,6 +26,7 @@ struct Options {
   unsigned long long timeout_ns = 2000000000ull;
   int persistent = -1;   // -1: default (work stealing)
   int emu_groups = 0;
+  int bwd_deterministic = 0;
 };
 Options g_opt;
 
@@ -364,6 +365,8 @@ void trace_target(unsigned long long** buf, int* ctas) {
   *buf = g_trace_buf;
   *ctas = g_trace_ctas;
 }
+bool bwd_deterministic() { return g_opt.bwd_deterministic != 0; }
+unsigned long long wait_timeout_ns() { return g_opt.timeout_ns; }
 }  // namespace fa_host
 
 // ------------------------------------------------------------------ C ABI
@@ -401,6 +404,10 @@ int fa_set_option(int option, double value) {
     case FA_OPT_EXP2_EMULATION:
       if (!(value >= 0.0 && value <= 8.0) || value != std::floor(value)) return FA_ERR_INVALID_ARG;
       g_opt.emu_groups = (int)value;
+      return FA_OK;
+    case FA_OPT_BWD_DETERMINISTIC:
+      if (value != 0.0 && value != 1.0) return FA_ERR_INVALID_ARG;
+      g_opt.bwd_deterministic = (int)value;
       return FA_OK;
     default:
       return FA_ERR_INVALID_ARG;

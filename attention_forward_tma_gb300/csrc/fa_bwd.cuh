@@ -64,6 +64,11 @@ struct BwdParams {
   unsigned long long timeout_ns;
   unsigned long long* trace;     // tracing build only: clock stamps per CTA and role (else null)
   int trace_ctas;
+  // deterministic dQ: per (b, kv head, Q tile) the number of key blocks that have
+  // added their dQ so far (zero on entry); key block j adds only after blocks
+  // 0 .. j-1 did, so every dQ element is summed in one fixed order. Null: no order.
+  int* sem;
+  int ntiles;
 };
 
 template <int D>
@@ -557,18 +562,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
           st_shared_v4(row + (((uint32_t)uu ^ (uint32_t)(r & 7)) << 4), a0, a1, a2, a3);
         }
       };
-      auto round_done = [&](int rnd) -> bool {           // all rows of the round staged: send them
+      int* sem = p.sem != nullptr ? p.sem + ((size_t)b * p.Hkv + kvh) * p.ntiles + i : nullptr;
+      // All rows of the round staged: send them. Every warp waits for the round's phase,
+      // so that none arrives for the next round before this phase has completed (warp 8
+      // may be held below, waiting for its turn).
+      // Deterministic order: the key blocks add this tile's dQ one after another (key
+      // block j once blocks 0 .. j-1 have), so warp 8 sends both rounds together in
+      // round 1, after a bounded wait for its turn. The wait comes after this tile's
+      // bdSEmpty has been observed: while warp 8 waits, the MMA warp may complete the
+      // next tile's dK, and a parity wait on bdSEmpty two phases behind would never end.
+      auto send = [&](int rnd) {
+        if (lane == 0) {
+#pragma unroll
+          for (int h = 0; h < L::kHalves; ++h) {
+            const int c = rnd == 0 ? L::kHalves + h : h;
+            const uint32_t chunk = (rnd == 0 ? sDO : sQ) + s * L::kTile + h * L::kSlab;
+            tma_reduce_add_3d(&p.tm_dq, chunk, c * 32, kvh << p.gshift, tok);
+          }
+        }
+      };
+      auto round_done = [&](int rnd) -> bool {
         fence_proxy_async_smem();
         mbar_arrive(bar(L::bdQStaged));
+        if (!w.wait(bar(L::bdQStaged), (uint32_t)(k * 2 + rnd) & 1u, L::bdQStaged, k)) return false;
         if (warp == 8) {
-          if (!w.wait(bar(L::bdQStaged), (uint32_t)(k * 2 + rnd) & 1u, L::bdQStaged, k)) return false;
-          if (lane == 0) {
-#pragma unroll
-            for (int h = 0; h < L::kHalves; ++h) {
-              const int c = rnd == 0 ? L::kHalves + h : h;
-              const uint32_t chunk = (rnd == 0 ? sDO : sQ) + s * L::kTile + h * L::kSlab;
-              tma_reduce_add_3d(&p.tm_dq, chunk, c * 32, kvh << p.gshift, tok);
-            }
+          if (sem == nullptr) {
+            send(rnd);
+          } else if (rnd == 1) {
+            uint32_t it = 0;
+            uint64_t t0 = 0;
+            while (__shfl_sync(0xffffffffu, lane == 0 ? ld_acquire_gpu(sem) : 0, 0) != j)
+              if (!w.still_waiting(it, t0, L::kNumBars, k)) return false;
+            fence_proxy_async_global();
+            send(0);
+            send(1);
           }
           __syncwarp();
         }
@@ -600,7 +627,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
       if (warp == 8) {
         if (lane == 0) {
           bulk_commit();
-          bulk_wait_read_all();                           // the staging may be overwritten now
+          if (sem != nullptr) {
+            bulk_wait_all();                              // the additions are done: pass the turn on
+            fence_proxy_async_global();
+            st_release_gpu(sem, j + 1);
+          } else {
+            bulk_wait_read_all();                         // the staging may be overwritten now
+          }
           mbar_arrive(bar(L::bQEmpty + s));               // Q_s and dO_s may be reloaded
           tr.rec(kEvBReduced, k);
         }

@@ -143,15 +143,19 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   // zeroed here so padding rows read 0)
   const size_t acc_bytes = (size_t)tokens * H * d * sizeof(float);
   const size_t vec_bytes = ((size_t)B * H_kv * mpad * sizeof(float) + 255) / 256 * 256;
+  const bool det = fa_host::bwd_deterministic();
+  const int ntiles = (int)(mpad / 128);
+  const size_t sem_bytes = det ? ((size_t)B * H_kv * ntiles * sizeof(int) + 255) / 256 * 256 : 0;
   void* ws = nullptr;
-  if (cudaMallocAsync(&ws, acc_bytes + 2 * vec_bytes, s) != cudaSuccess) {
+  if (cudaMallocAsync(&ws, acc_bytes + 2 * vec_bytes + sem_bytes, s) != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_CUDA;
   }
   float* dq_acc = static_cast<float*>(ws);
   float* lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes);
   float* dsum = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes + vec_bytes);
-  if (cudaMemsetAsync(lse2, 0, 2 * vec_bytes, s) != cudaSuccess) st = FA_ERR_CUDA;
+  int* sem = det ? reinterpret_cast<int*>(static_cast<char*>(ws) + acc_bytes + 2 * vec_bytes) : nullptr;
+  if (cudaMemsetAsync(lse2, 0, 2 * vec_bytes + sem_bytes, s) != cudaSuccess) st = FA_ERR_CUDA;
   if (st == FA_OK)
     st = pre_post_any(false, d, f16, o, dout, lse, lse2, dsum, dq_acc, nullptr, B, H, gshift, N_q, (int)mpad, s);
   if (st == FA_OK) st = fa_host::make_map_f32(&p.tm_dq, dq_acc, tokens, H, d, G);
@@ -167,7 +171,9 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
     p.num_tasks = (int)(B * H_kv * nkb);
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
-    p.timeout_ns = 2000000000ull;
+    p.timeout_ns = fa_host::wait_timeout_ns();
+    p.sem = sem;
+    p.ntiles = ntiles;
     fa_host::trace_target(&p.trace, &p.trace_ctas);
     if (d == 128)
       st = f16 ? launch_c<128, true>(p, causal != 0, s) : launch_c<128, false>(p, causal != 0, s);

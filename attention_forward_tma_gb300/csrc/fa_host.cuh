@@ -87,5 +87,8 @@ int bwd_take_status(unsigned long long* word);
 
 // The clock-stamp buffer set by fa_trace_configure (tracing builds; else null, 0).
 void trace_target(unsigned long long** buf, int* ctas);
+// Process-wide options of fa_set_option read by the backward translation unit.
+bool bwd_deterministic();
+unsigned long long wait_timeout_ns();
 
 }  // namespace fa_host

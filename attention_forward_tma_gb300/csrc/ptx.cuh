@@ -269,6 +269,21 @@ __host__ __device__ constexpr uint32_t idesc_f32acc2(int M, int N, bool a_mn_maj
   return idesc_f32acc(M, N, b_mn_major, f16) | ((a_mn_major ? 1u : 0u) << 15);
 }
 
+// ---------------------------------------------------------------- global flags
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int x;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(x) : "l"(p) : "memory");
+  return x;
+}
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Orders this thread's generic-proxy accesses to global memory with its later
+// async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- scalar helpers
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;

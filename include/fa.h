@@ -229,10 +229,12 @@ int fa_fwd_varlen_noalloc(const void* q, const void* k, const void* v, void* o, 
  *                    (dtype elements, device; dq, dk, dv written)
  *   lse            : fp32 [B, H, N_q], the LSE that fa_fwd* wrote for these q, k, v
  *   other arguments as for fa_fwd_kv (bottom-right causal mask).
- * dQ is accumulated over key blocks in fp32 with atomic additions, so its last
- * bits may differ from run to run; dK and dV are deterministic. A temporary buffer
- * of B*N_q*H*d*4 + 2*B*H_kv*ceil(N_q*G/128)*128*4 bytes comes from the
- * stream-ordered allocator (cudaMallocAsync / cudaFreeAsync on `stream`).
+ * dQ is accumulated over key blocks in fp32 by reduce-adds in arrival order, so
+ * its last bits may differ from run to run unless FA_OPT_BWD_DETERMINISTIC is set;
+ * dK and dV are always deterministic. A temporary buffer of B*N_q*H*d*4 +
+ * 2*B*H_kv*ceil(N_q*G/128)*128*4 bytes (+ 4 bytes per 128-row Q tile in the
+ * deterministic mode) comes from the stream-ordered allocator (cudaMallocAsync /
+ * cudaFreeAsync on `stream`).
  */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
            void* dq, void* dk, void* dv, int B, int H, int H_kv, int N_q, int N_kv, int d, float scale,
@@ -263,9 +265,17 @@ int fa_last_device_status(void* stream, unsigned long long* detail);
  *   FA_OPT_EXP2_EMULATION  : number of 16-element groups per 128-wide row (0..8)
  *                            whose exp2 is evaluated with the FMA polynomial instead
  *                            of the hardware ex2 unit (default 0)
+ *   FA_OPT_BWD_DETERMINISTIC : 1 = fa_bwd adds the dQ contributions of the key blocks
+ *                            of every Q tile in one fixed order (key block 0 first),
+ *                            so dQ is bitwise reproducible ("FlashAttention-4（下）"
+ *                            section 5, deterministic mode: a semaphore per tile
+ *                            serialises the global accumulation); key blocks wait for
+ *                            their predecessors, which costs speed. 0 = arrival order
+ *                            (default).
  * Returns FA_OK or FA_ERR_INVALID_ARG.
  */
-enum { FA_OPT_TAU = 1, FA_OPT_WAIT_TIMEOUT_NS = 2, FA_OPT_PERSISTENT = 3, FA_OPT_EXP2_EMULATION = 4 };
+enum { FA_OPT_TAU = 1, FA_OPT_WAIT_TIMEOUT_NS = 2, FA_OPT_PERSISTENT = 3, FA_OPT_EXP2_EMULATION = 4,
+       FA_OPT_BWD_DETERMINISTIC = 5 };
 int fa_set_option(int option, double value);
 
 /* Library version, as major*10000 + minor*100 + patch. */

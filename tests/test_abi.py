@@ -195,6 +195,7 @@ def test_valid_arguments_without_gpu_report_no_device():
                                         (1, math.nan, False), (2, 1e9, True), (2, 10.0, False),
                                         (3, 1, True), (3, 0, True), (3, -1, True), (3, 2, True), (3, 3, False),
                                         (4, 0, True), (4, 8, True), (4, 9, False), (4, 2.5, False),
+                                        (5, 0, True), (5, 1, True), (5, 2, False), (5, 0.5, False),
                                         (99, 1, False)])
 def test_set_option_validation(opt, val, ok):
     lib = fa.library()
@@ -205,3 +206,4 @@ def test_set_option_validation(opt, val, ok):
     lib.fa_set_option(2, 2e9)
     lib.fa_set_option(3, -1)
     lib.fa_set_option(4, 0)
+    lib.fa_set_option(5, 0)

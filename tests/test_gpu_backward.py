@@ -112,3 +112,23 @@ def test_backward_dk_dv_deterministic():
     b = run_bwd(q, k, v, do, True)
     assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
     assert np.abs(a[0] - b[0]).max() <= 2.0 ** -7 * max(1.0, np.abs(a[0]).max())
+
+
+@pytest.mark.parametrize("shape", [(1, 4, 2, 500, 500, 128, True), (2, 8, 1, 300, 700, 64, False),
+                                   (1, 2, 2, 900, 900, 128, False)],
+                         ids=lambda s: "B%dH%dKV%dNq%dNk%dd%d_causal%d" % s)
+def test_backward_deterministic_mode(shape):
+    """With bwd_deterministic set, the key blocks add their dQ contributions in
+    key-block order: two runs give bitwise-equal dQ, and parity holds."""
+    B, H, Hkv, Nq, Nk, d, causal = shape
+    q, k, v = fa_inputs.make_qkv(B, Nq, H, d, seed=4400 + Nq, Nkv=Nk, Hkv=Hkv)
+    do = fa_inputs.make_qkv(B, Nq, H, d, seed=4401 + Nq)[0]
+    fa.set_option("bwd_deterministic", 1)
+    try:
+        a = run_bwd(q, k, v, do, causal)
+        b = run_bwd(q, k, v, do, causal)
+    finally:
+        fa.set_option("bwd_deterministic", 0)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    check(a, oracle.attention_backward(q, k, v, do, 1 / math.sqrt(d), causal), f"deterministic {shape}")
