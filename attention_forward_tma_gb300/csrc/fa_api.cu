@@ -27,6 +27,8 @@ struct Options {
   int persistent = -1;   // -1: default (work stealing)
   int emu_groups = 0;
   int bwd_deterministic = 0;
+  int stagger = 0;
+  int stats_tmem = 1;
 };
 Options g_opt;
 
@@ -189,6 +191,8 @@ void fill_common(fa::FwdParams& p, float scale, bool f16) {
   p.scale_log2 = scale * 1.4426950408889634f;
   p.tau = f16 && g_opt.tau > kTauMaxF16 ? kTauMaxF16 : g_opt.tau;
   p.emu_groups = g_opt.emu_groups;
+  p.stagger = g_opt.stagger;
+  p.stats_tmem = g_opt.stats_tmem;
   p.timeout_ns = g_opt.timeout_ns;
 }
 
@@ -408,6 +412,14 @@ int fa_set_option(int option, double value) {
     case FA_OPT_BWD_DETERMINISTIC:
       if (value != 0.0 && value != 1.0) return FA_ERR_INVALID_ARG;
       g_opt.bwd_deterministic = (int)value;
+      return FA_OK;
+    case FA_OPT_SOFTMAX_STAGGER:
+      if (value != 0.0 && value != 1.0) return FA_ERR_INVALID_ARG;
+      g_opt.stagger = (int)value;
+      return FA_OK;
+    case FA_OPT_STATS_TMEM:
+      if (value != 0.0 && value != 1.0) return FA_ERR_INVALID_ARG;
+      g_opt.stats_tmem = (int)value;
       return FA_OK;
     default:
       return FA_ERR_INVALID_ARG;

@@ -97,6 +97,8 @@ struct FwdParams {
   float tau;                     // delayed-rescale threshold
   int emu_groups;                // 16-column groups per row evaluated with the polynomial exp2
   int sched;                     // 0: one task per CTA; 1: static stride; 2: work stealing (launch control)
+  int stagger;                   // 1: WG0 and WG1 take turns at their exponential phases
+  int stats_tmem;                // 1: acc_scale goes to WG2 through tensor memory (column 0 of S_t)
   unsigned long long timeout_ns;
   unsigned long long* trace;     // tracing build only: clock stamps per CTA and role (else null)
   int trace_ctas;
@@ -161,8 +163,9 @@ struct Layout {
   static constexpr int bSFull = 4 + 2 * kStages, bPO = bSFull + 2, bP2 = bPO + 2, bCorrFull = bP2 + 2,
                        bCorrEmpty = bCorrFull + 2, bOFinal = bCorrEmpty + 2, bDrain = bOFinal + 2,
                        bTaskFull = bDrain + 1, bTaskEmpty = bTaskFull + 2, bClc = bTaskEmpty + 2,
-                       bOstReady = bClc + 1, bOstFree = bOstReady + 1;
-  static constexpr int kNumBars = bOstFree + 1;
+                       bOstReady = bClc + 1, bOstFree = bOstReady + 1, bTurn = bOstFree + 1,
+                       bStats = bTurn + 2;
+  static constexpr int kNumBars = bStats + 2;
   static constexpr int kMailOff = kBarOff + ((kNumBars * 8 + 127) / 128) * 128;
   static constexpr int kMiscOff = kMailOff + 2 * kBlockM * 4;  // tmem slot, abort flags, task ring
   static constexpr int kClcOff = kMiscOff + 64;                 // 16-byte launch-control response
@@ -459,6 +462,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       mbar_init(bar(L::bCorrFull + i), kBlockM);
       mbar_init(bar(L::bCorrEmpty + i), kBlockM);
       mbar_init(bar(L::bOFinal + i), 1);
+      mbar_init(bar(L::bTurn + i), kBlockM);        // the other softmax warpgroup's exponentials done
+      mbar_init(bar(L::bStats + i), kBlockM);       // final row_sum in the mailbox (stats_tmem mode)
     }
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::bKVFull + s), 1);
@@ -746,6 +751,17 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     tr.init(p, 2 + t, r == 0);
     const float sl2 = p.scale_log2;
     uint32_t s_par = 0, ce_par = 0;
+    uint32_t turns = 0;   // exponential phases taken in turn so far (stagger mode)
+    // Stagger mode ("Flash Attention 4", section "论文与当前 TIRx 实现的差异": the two
+    // softmax warpgroups' exponential phases do not overlap): the warpgroups pass a
+    // turn back and forth through bTurn, WG0 first. In a task of both tiles each takes
+    // nb turns (WG0's first turn is an empty pass when tile 0 skips the top block),
+    // so the turn is back at WG0 when the task ends.
+    auto take_turn = [&](int j) -> bool {
+      const uint32_t par = t == 0 ? (turns & 1u) ^ 1u : turns & 1u;
+      ++turns;
+      return w.wait(bar(L::bTurn + t), par, L::bTurn + t, j);
+    };
     bool ok = true;
     Task tk;
     for (int k = 0; ok; ++k) {
@@ -771,6 +787,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       if (t == 1 && task_one_tile(tk, p.gshift)) continue;   // this tile has no row of the sequence
       const int hi = kr.hi - (t == 0 ? task_skip0(tk, kr, CAUSAL, p.gshift) : 0);   // this tile's top block + 1
       const int nb = hi - kr.lo;
+      const bool stagger = p.stagger != 0 && !task_one_tile(tk, p.gshift);
+      if (stagger && hi < kr.hi) {   // tile 0 skips the top block: hand the first turn to WG1
+        if (!take_turn(kr.hi - 1)) { ok = false; break; }
+        mbar_arrive(bar(L::bTurn + 1));
+      }
       const int row_limit = CAUSAL ? min(pos + off + 1, tk.lenk) : tk.lenk;  // keys [0, row_limit) visible
       float row_max = -INFINITY, row_sum = 0.f;
       for (int i = 0; i < nb; ++i) {
@@ -848,12 +869,22 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         row_max = ref;
         // hand acc_scale to WG2 now, so the O rescale runs while P is computed
         if (i > 0) {
-          if (!w.wait(bar(L::bCorrEmpty + t), ce_par ^ 1, L::bCorrEmpty + t, j)) { ok = false; break; }
-          ce_par ^= 1;
-          mail[t * kBlockM + r] = acc;
+          if (p.stats_tmem) {
+            // through column 0 of S_t (all of S is in registers): the next write to S_t
+            // is the QK^T of block j-1, issued only after the PV that waits for WG2's
+            // rescale, so the slot needs no empty barrier
+            tmem_st1(tS, __float_as_uint(acc));
+            tmem_wait_st();
+            tc_fence_before();
+          } else {
+            if (!w.wait(bar(L::bCorrEmpty + t), ce_par ^ 1, L::bCorrEmpty + t, j)) { ok = false; break; }
+            ce_par ^= 1;
+            mail[t * kBlockM + r] = acc;
+          }
           mbar_arrive(bar(L::bCorrFull + t));
           tr.rec(kEvMail, j);
         }
+        if (stagger && !take_turn(j)) { ok = false; break; }
         const float ref_safe = ref == -INFINITY ? 0.f : ref;
         const uint64_t scale2 = pack2(sl2, sl2);
         const uint64_t bias2 = pack2(-ref_safe * sl2, -ref_safe * sl2);
@@ -893,6 +924,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           mbar_arrive(bar(h == 0 ? L::bPO + t : L::bP2 + t));
           tr.rec(h == 0 ? kEvHalf1 : kEvHalf2, j);
         }
+        if (stagger) mbar_arrive(bar(L::bTurn + (t ^ 1)));   // the other warpgroup's turn
         float sa, sb;
         unpack2(add2(sum2a, sum2b), sa, sb);
         row_sum = row_sum * acc + (sa + sb);
@@ -902,7 +934,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       if (!w.wait(bar(L::bCorrEmpty + t), ce_par ^ 1, L::bCorrEmpty + t, -1)) { ok = false; break; }
       ce_par ^= 1;
       mail[t * kBlockM + r] = row_sum;
-      mbar_arrive(bar(L::bCorrFull + t));
+      // with acc_scale in tensor memory the per-block hand-offs have no empty barrier,
+      // so the final one takes a barrier of its own: on corr_full it could complete a
+      // second phase before WG2 has waited for the last block's
+      mbar_arrive(bar(p.stats_tmem ? L::bStats + t : L::bCorrFull + t));
       tr.rec(kEvStats, -1);
       {
         const float ref_safe = row_max == -INFINITY ? 0.f : row_max;
@@ -918,6 +953,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     Tracer tr;
     tr.init(p, 4, r == 0);
     uint32_t cf_par = 0, of_par = 0;  // bit t: parity of the next wait on corr_full[t] / o_final[t]
+    uint32_t fs_par = 0;              // bit t: parity of the next wait on stats[t] (stats_tmem mode)
     uint32_t ost_n = 0;               // uses of the O staging tile so far
     bool ok = true;
     Task tk;
@@ -961,8 +997,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           if (!w.wait(bar(L::bCorrFull + t), (cf_par >> t) & 1, L::bCorrFull + t, j)) { ok = false; break; }
           cf_par ^= 1u << t;
           tr.rec(kEvCorrFull + t, j);
-          const float a = mail[t * kBlockM + r];
-          mbar_arrive(bar(L::bCorrEmpty + t));
+          float a;
+          if (p.stats_tmem) {
+            tc_fence_after();
+            a = __uint_as_float(tmem_ld1(tmem + lane_base + L::col_s(t)));
+            tmem_wait_ld();
+          } else {
+            a = mail[t * kBlockM + r];
+            mbar_arrive(bar(L::bCorrEmpty + t));
+          }
           if (__any_sync(0xffffffffu, a < 1.f)) {
             tc_fence_after();
             const uint32_t tO = tmem + lane_base + L::col_o(t);
@@ -986,8 +1029,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       // epilogue: O_t / row_sum -> bf16 / fp16 -> global
 #pragma unroll 1
       for (int t = 0; t <= t_last; ++t) {
-        if (!w.wait(bar(L::bCorrFull + t), (cf_par >> t) & 1, L::bCorrFull + t, -1)) { ok = false; break; }
-        cf_par ^= 1u << t;
+        if (p.stats_tmem) {
+          if (!w.wait(bar(L::bStats + t), (fs_par >> t) & 1, L::bStats + t, -1)) { ok = false; break; }
+          fs_par ^= 1u << t;
+        } else {
+          if (!w.wait(bar(L::bCorrFull + t), (cf_par >> t) & 1, L::bCorrFull + t, -1)) { ok = false; break; }
+          cf_par ^= 1u << t;
+        }
         const float l = mail[t * kBlockM + r];
         mbar_arrive(bar(L::bCorrEmpty + t));
         if (!w.wait(bar(L::bOFinal + t), (of_par >> t) & 1, L::bOFinal + t, -1)) { ok = false; break; }

@@ -272,10 +272,23 @@ int fa_last_device_status(void* stream, unsigned long long* detail);
  *                            serialises the global accumulation); key blocks wait for
  *                            their predecessors, which costs speed. 0 = arrival order
  *                            (default).
+ *   FA_OPT_SOFTMAX_STAGGER : 1 = the two softmax warpgroups of the forward take turns at
+ *                            their exponential phases, so they never compete for the
+ *                            exp2 unit at once ("Flash Attention 4", section on the
+ *                            differences between the paper and the TIRx kernel: the
+ *                            paper's ordering of the two softmax warpgroups).
+ *                            0 = no ordering (default).
+ *   FA_OPT_STATS_TMEM      : 1 = the forward's per-block rescale factor acc_scale goes
+ *                            from the softmax warpgroup to the correction warpgroup
+ *                            through tensor memory (a free column of the score tile)
+ *                            instead of a shared-memory mailbox (same section: the
+ *                            paper passes the statistics through spare TMEM);
+ *                            default 1. 0 = shared memory.
+ * Both forward variants compute the same result as the default path.
  * Returns FA_OK or FA_ERR_INVALID_ARG.
  */
 enum { FA_OPT_TAU = 1, FA_OPT_WAIT_TIMEOUT_NS = 2, FA_OPT_PERSISTENT = 3, FA_OPT_EXP2_EMULATION = 4,
-       FA_OPT_BWD_DETERMINISTIC = 5 };
+       FA_OPT_BWD_DETERMINISTIC = 5, FA_OPT_SOFTMAX_STAGGER = 6, FA_OPT_STATS_TMEM = 7 };
 int fa_set_option(int option, double value);
 
 /* Library version, as major*10000 + minor*100 + patch. */

@@ -196,6 +196,8 @@ def test_valid_arguments_without_gpu_report_no_device():
                                         (3, 1, True), (3, 0, True), (3, -1, True), (3, 2, True), (3, 3, False),
                                         (4, 0, True), (4, 8, True), (4, 9, False), (4, 2.5, False),
                                         (5, 0, True), (5, 1, True), (5, 2, False), (5, 0.5, False),
+                                        (6, 0, True), (6, 1, True), (6, -1, False),
+                                        (7, 0, True), (7, 1, True), (7, 3, False),
                                         (99, 1, False)])
 def test_set_option_validation(opt, val, ok):
     lib = fa.library()
@@ -207,3 +209,5 @@ def test_set_option_validation(opt, val, ok):
     lib.fa_set_option(3, -1)
     lib.fa_set_option(4, 0)
     lib.fa_set_option(5, 0)
+    lib.fa_set_option(6, 0)
+    lib.fa_set_option(7, 1)
