@@ -16,7 +16,7 @@ import threading
 
 from . import _build
 
-__all__ = ["fa_fwd", "fa_fwd_varlen", "fa_bwd", "lse_combine", "num_splits", "num_splits_varlen", "FaError", "set_option", "last_device_status", "library",
+__all__ = ["fa_fwd", "fa_fwd_varlen", "fa_bwd", "fa_bwd_varlen", "lse_combine", "num_splits", "num_splits_varlen", "FaError", "set_option", "last_device_status", "library",
            "FA_DTYPE_BF16", "FA_DTYPE_FP16",
            "selftest_mma_tile", "selftest_exp2", "selftest_wait_timeout", "varlen_schedule",
            "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
@@ -38,6 +38,8 @@ _SIGNATURES = {
                          _ci, _vp],
     "fa_lse_combine": [_vp, _vp, _ci, _ci, _ci, _ci, _ci, _vp, _vp, _ci, _vp],
     "fa_bwd": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _ci, _vp],
+    "fa_bwd_varlen": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci,
+                      _cf, _ci, _ci, _vp],
     "fa_fwd_kv_splits": [_ci, _ci, _ci, _ci, _ci, _ci, ctypes.POINTER(_ci)],
     "fa_fwd_varlen_kv_splits": [_ci, _ci, _ci, _ci, _ci, _ci, ctypes.POINTER(_ci)],
     "fa_fwd_varlen_noalloc": [_vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _vp],
@@ -240,6 +242,53 @@ def fa_bwd(q, k, v, o, dout, lse, *, scale: float | None = None, causal: bool = 
     _check(library().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
                             dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Hkv, N, Nk, d, scale,
                             int(bool(causal)), code, _stream_handle(stream, q.device)), "fa_bwd")
+    return dq, dk, dv
+
+
+def fa_bwd_varlen(q, k, v, o, dout, lse, cu_seqlens, max_seqlen: int, *, cu_seqlens_k=None,
+                  max_seqlen_k: int | None = None, scale: float | None = None, causal: bool = False, dq=None,
+                  dk=None, dv=None, stream=None):
+    """Backward of fa_fwd_varlen: q, o, dout [T, H, d]; k, v [T_kv, H_kv, d] (bf16 or fp16);
+    lse fp32 [H, T] as returned by fa_fwd_varlen for the same inputs; cu_seqlens (and
+    cu_seqlens_k, default cu_seqlens) int32 [S+1] on the device. Returns (dq, dk, dv)."""
+    torch = _torch()
+    code = _dtype_code(q)
+    _need(q, "q", q.dtype, 3)
+    T, H, d = q.shape
+    if not (isinstance(k, torch.Tensor) and k.dim() == 3):
+        raise TypeError("k must be a 3-dimensional torch.Tensor")
+    Tk, Hkv = k.shape[0], k.shape[1]
+    for name, t, shape in (("k", k, (Tk, Hkv, d)), ("v", v, (Tk, Hkv, d)), ("o", o, (T, H, d)),
+                           ("dout", dout, (T, H, d))):
+        _need(t, name, q.dtype, 3)
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} must have shape {shape}")
+    _need(lse, "lse", torch.float32, 2)
+    if tuple(lse.shape) != (H, T):
+        raise ValueError("lse must have shape (H, T)")
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    if cu_seqlens_k is None:
+        if Tk != T:
+            raise ValueError("k and v must have q's rows unless cu_seqlens_k is given")
+        cu_seqlens_k = cu_seqlens
+    else:
+        _need(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+        if cu_seqlens_k.numel() != cu_seqlens.numel():
+            raise ValueError("cu_seqlens_k must have as many entries as cu_seqlens")
+    max_seqlen_k = int(max_seqlen) if max_seqlen_k is None else int(max_seqlen_k)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t, ref in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        _need(t, name, q.dtype, 3)
+        if t.shape != ref.shape:
+            raise ValueError(f"{name} has the wrong shape")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    _check(library().fa_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                                   lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), cu_seqlens.data_ptr(),
+                                   cu_seqlens_k.data_ptr(), cu_seqlens.numel() - 1, T, Tk, int(max_seqlen),
+                                   max_seqlen_k, H, Hkv, d, scale, int(bool(causal)), code,
+                                   _stream_handle(stream, q.device)), "fa_bwd_varlen")
     return dq, dk, dv
 
 

@@ -53,6 +53,11 @@ struct BwdParams {
   CUtensorMap tm_dq;         // fp32 dq_acc [tokens_q, H, d]: box 32 x G x 128/G, reduce-adds
   const float* lse2;         // [B, H_kv, mpad], packed rows: forward LSE * log2(e)
   const float* dsum;         // [B, H_kv, mpad], packed rows: D = rowsum(dO * O)
+  // variable length (both null for fixed length): B = number of sequences, sequence b
+  // has query rows [cu_q[b], cu_q[b+1]) and key rows [cu_k[b], cu_k[b+1]); Nq, Nk,
+  // mpad and nkb are then those of the longest sequence (grid and packed-row stride)
+  const int* cu_q;
+  const int* cu_k;
   float* dq_acc;             // fp32 [tokens_q, H, d]; zero on entry
   uint16_t* dk;              // [tokens_k, H_kv, d]
   uint16_t* dv;              // [tokens_k, H_kv, d]
@@ -105,22 +110,41 @@ __device__ __forceinline__ float half_bits_to_f32(uint16_t x, bool f16) {
 }
 
 // ------------------------------------------------------------------ preprocessing
-// One warp per (b, position, query head): D = rowsum(dO * O) in fp32 and the
-// forward's LSE in base 2, both written at the row's packed index (b, kv head,
-// position * G + head % G); the row of the fp32 dQ accumulator is zeroed on the way.
+// One warp per (query row, head) of the [tokens, H, d] tensors: D = rowsum(dO * O) in
+// fp32 and the forward's LSE in base 2, both written at the row's packed index
+// (sequence, kv head, position * G + head % G); the row of the fp32 dQ accumulator is
+// zeroed on the way. Fixed length: sequence b holds rows [b * Nq, (b + 1) * Nq) and the
+// LSE is [B, H, Nq]; variable length (cu_q not null): the sequence of a row is found by
+// bisection in cu_q[0 .. B] and the LSE is [H, tokens].
 template <int D, bool F16>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint16_t* __restrict__ o,
                                                          const uint16_t* __restrict__ dout,
                                                          const float* __restrict__ lse, float* __restrict__ lse2,
-                                                         float* __restrict__ dsum, float* __restrict__ dq_acc, int B,
+                                                         float* __restrict__ dsum, float* __restrict__ dq_acc,
+                                                         long long tokens, const int* __restrict__ cu_q, int B,
                                                          int H, int gshift, int Nq, int mpad) {
   constexpr int E = D / 32;   // elements per lane: 4 (d = 128) or 2 (d = 64)
   const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (w >= (long long)B * Nq * H) return;
+  if (w >= tokens * H) return;
   const int lane = threadIdx.x & 31;
   const int h = (int)(w % H);
   const long long bp = w / H;
-  const int b = (int)(bp / Nq), pos = (int)(bp % Nq);
+  int b, pos;
+  size_t li;
+  if (cu_q == nullptr) {
+    b = (int)(bp / Nq);
+    pos = (int)(bp % Nq);
+    li = ((size_t)b * H + h) * Nq + pos;
+  } else {
+    int lo = 0, hi = B;   // the last sequence starting at or before the row
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (cu_q[mid] <= bp) lo = mid; else hi = mid;
+    }
+    b = lo;
+    pos = (int)(bp - cu_q[lo]);
+    li = (size_t)h * tokens + bp;
+  }
   uint16_t ov[E], gv[E];
   if constexpr (E == 4) {
     *reinterpret_cast<uint2*>(ov) = *reinterpret_cast<const uint2*>(o + w * D + lane * E);
@@ -140,7 +164,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint16_t* __restr
     const int Hkv = H >> gshift;
     const size_t idx = ((size_t)b * Hkv + (h >> gshift)) * mpad + ((size_t)pos << gshift) + (h & ((1 << gshift) - 1));
     dsum[idx] = acc;
-    lse2[idx] = lse[((size_t)b * H + h) * Nq + pos] * 1.4426950408889634f;
+    lse2[idx] = lse[li] * 1.4426950408889634f;
   }
 }
 
@@ -181,15 +205,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
   const int j = (int)blockIdx.x / bh_total;
   const int bh = (int)blockIdx.x - j * bh_total;
   const int b = bh / p.Hkv, kvh = bh - b * p.Hkv;
-  const int off = p.Nk - p.Nq;                         // bottom-right causal offset
-  const int ntiles = ((p.Nq << p.gshift) + 127) / 128;
+  int Nq = p.Nq, Nk = p.Nk, tok_q = b * p.Nq, tok_k = b * p.Nk;   // this sequence
+  if (p.cu_q != nullptr) {
+    tok_q = p.cu_q[b];
+    Nq = p.cu_q[b + 1] - tok_q;
+    tok_k = p.cu_k[b];
+    Nk = p.cu_k[b + 1] - tok_k;
+    if (j * 128 >= Nk) return;                         // a shorter sequence: no such key block
+  }
+  const int off = Nk - Nq;                             // bottom-right causal offset
+  const int ntiles = ((Nq << p.gshift) + 127) / 128;
   int i0 = 0;
   if (CAUSAL) {
     const long long pmin = (long long)j * 128 - off;   // the first position that sees key j*128
     if (pmin > 0) i0 = (int)min((long long)ntiles, (pmin << p.gshift) / 128);
   }
   const int n = ntiles - i0;                           // Q tiles of this task
-  const int tok_q = b * p.Nq, tok_k = b * p.Nk;
 
   if (tid == 0) {
     *abort_flag = 0;
@@ -412,7 +443,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
     const int cq = hq * 64;
     const int kr = tid & 127;                             // key row == TMEM lane
     const int kabs = j * 128 + kr;
-    const bool key_ok = kabs < p.Nk;
+    const bool key_ok = kabs < Nk;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + L::cS + cq, tdP = tmem + lane_base + L::cDP + cq;
     Waiter w{abort_flag, p.timeout_ns, hq == 0 ? kRoleSoftmax0 : kRoleSoftmax1};
@@ -431,7 +462,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
       const int qlo = CAUSAL ? (int)max(-1LL, min(129LL, ((long long)kabs - off) * (1LL << p.gshift) - (long long)i * 128))
                                    - cq
                              : -cq;
-      const int qhi = (key_ok ? min(128, (p.Nq << p.gshift) - i * 128) : 0) - cq;
+      const int qhi = (key_ok ? min(128, (Nq << p.gshift) - i * 128) : 0) - cq;
       if (!w.wait(bar(L::bQFull + (k & 1)), (k >> 1) & 1, L::bQFull + (k & 1), k)) { ok = false; break; }
       if (!w.wait(bar(L::bSFull), k & 1, L::bSFull, k)) { ok = false; break; }
       tr.rec(kEvBSFull, k);
@@ -542,7 +573,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
     for (int k = 0; k < n; ++k) {
       const int i = i0 + k;
       const int s = k & 1;
-      const bool valid = ((i * 128 + r) >> p.gshift) < p.Nq;   // padding rows add zeros
+      const bool valid = ((i * 128 + r) >> p.gshift) < Nq;     // padding rows add zeros
       if (!w.wait(bar(L::bdQFull), k & 1, L::bdQFull, k)) { ok = false; break; }
       tr.rec(kEvBdQFull, k);
       tc_fence_after();
@@ -657,7 +688,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
 #pragma unroll
           for (int e = 0; e < 32; ++e) u[e] = 0u;
         }
-        if (kabs < p.Nk) {
+        if (kabs < Nk) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
           for (int e = 0; e < 4; ++e)

@@ -55,30 +55,116 @@ int launch_c(const fa::BwdParams& p, bool causal, cudaStream_t s) {
   return causal ? launch<D, true, F>(p, s) : launch<D, false, F>(p, s);
 }
 
+// Shape of one call: fixed length (cu_q == nullptr: B sequences of N_q / N_kv rows) or
+// variable length (B sequences given by cu_q / cu_k; N_q, N_kv the longest ones).
+struct Shape {
+  int B, H, H_kv, N_q, N_kv, d, gshift;
+  long long tokens_q, tokens_k;
+  const int* cu_q;
+  const int* cu_k;
+};
+
 template <int D, bool F>
 int pre_post(bool post, const void* o, const void* dout, const float* lse, float* lse2, float* dsum,
-             float* dq_acc, void* dq, int B, int H, int gshift, int Nq, int mpad, cudaStream_t s) {
+             float* dq_acc, void* dq, const Shape& sh, int mpad, cudaStream_t s) {
+  const long long rows = sh.tokens_q * sh.H;
+  if (rows == 0) return FA_OK;
   if (!post) {
-    const long long rows = (long long)B * Nq * H;
     fa::fa_bwd_pre_kernel<D, F><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
-        static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, lse2, dsum, dq_acc, B, H, gshift,
-        Nq, mpad);
+        static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, lse2, dsum, dq_acc, sh.tokens_q,
+        sh.cu_q, sh.B, sh.H, sh.gshift, sh.N_q, mpad);
   } else {
-    const long long n4 = (long long)B * Nq * H * D / 4;
+    const long long n4 = rows * D / 4;
     fa::fa_bwd_post_kernel<F><<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(
         reinterpret_cast<const float4*>(dq_acc), static_cast<uint2*>(dq), n4);
   }
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-int pre_post_any(bool post, int d, bool f16, const void* o, const void* dout, const float* lse, float* lse2,
-                 float* dsum, float* dq_acc, void* dq, int B, int H, int gshift, int Nq, int mpad,
-                 cudaStream_t s) {
-  if (d == 128)
-    return f16 ? pre_post<128, true>(post, o, dout, lse, lse2, dsum, dq_acc, dq, B, H, gshift, Nq, mpad, s)
-               : pre_post<128, false>(post, o, dout, lse, lse2, dsum, dq_acc, dq, B, H, gshift, Nq, mpad, s);
-  return f16 ? pre_post<64, true>(post, o, dout, lse, lse2, dsum, dq_acc, dq, B, H, gshift, Nq, mpad, s)
-             : pre_post<64, false>(post, o, dout, lse, lse2, dsum, dq_acc, dq, B, H, gshift, Nq, mpad, s);
+int pre_post_any(bool post, bool f16, const void* o, const void* dout, const float* lse, float* lse2, float* dsum,
+                 float* dq_acc, void* dq, const Shape& sh, int mpad, cudaStream_t s) {
+  if (sh.d == 128)
+    return f16 ? pre_post<128, true>(post, o, dout, lse, lse2, dsum, dq_acc, dq, sh, mpad, s)
+               : pre_post<128, false>(post, o, dout, lse, lse2, dsum, dq_acc, dq, sh, mpad, s);
+  return f16 ? pre_post<64, true>(post, o, dout, lse, lse2, dsum, dq_acc, dq, sh, mpad, s)
+             : pre_post<64, false>(post, o, dout, lse, lse2, dsum, dq_acc, dq, sh, mpad, s);
+}
+
+int device_check() {
+  int dev = 0, n = 0, major = 0, minor = 0;
+  if (cudaGetDeviceCount(&n) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return FA_ERR_NO_DEVICE;
+  }
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return major == 10 && minor == 3 ? FA_OK : FA_ERR_UNSUPPORTED;
+}
+
+// The three launches of one backward call (arguments already checked).
+int bwd_run(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+            void* dq, void* dk, void* dv, const Shape& sh, float scale, int causal, bool f16, cudaStream_t s) {
+  const int d = sh.d;
+  fa::BwdParams p;
+  std::memset(&p, 0, sizeof p);
+  const int G = sh.H / sh.H_kv;
+  int st;
+  if ((st = make_map(&p.tm_q, q, sh.tokens_q, sh.H, d, G, f16)) != FA_OK ||
+      (st = make_map(&p.tm_do, dout, sh.tokens_q, sh.H, d, G, f16)) != FA_OK ||
+      (st = make_map(&p.tm_k, k, sh.tokens_k, sh.H_kv, d, 1, f16)) != FA_OK ||
+      (st = make_map(&p.tm_v, v, sh.tokens_k, sh.H_kv, d, 1, f16)) != FA_OK)
+    return st;
+  const long long mpad = (((long long)sh.N_q << sh.gshift) + 127) / 128 * 128;
+  const long long nkb = (sh.N_kv + 127) / 128;
+
+  // temporary buffer: dQ accumulator (fp32 [tokens, H, d], zeroed by the
+  // preprocessing kernel), then packed base-2 LSE and D ([B, H_kv, mpad] each,
+  // zeroed here so padding rows read 0), then the deterministic mode's counters
+  const size_t acc_bytes = ((size_t)sh.tokens_q * sh.H * d * sizeof(float) + 255) / 256 * 256;
+  const size_t vec_bytes = ((size_t)sh.B * sh.H_kv * mpad * sizeof(float) + 255) / 256 * 256;
+  const bool det = fa_host::bwd_deterministic();
+  const int ntiles = (int)(mpad / 128);
+  const size_t sem_bytes = det ? ((size_t)sh.B * sh.H_kv * ntiles * sizeof(int) + 255) / 256 * 256 : 0;
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, acc_bytes + 2 * vec_bytes + sem_bytes, s) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  float* dq_acc = static_cast<float*>(ws);
+  float* lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes);
+  float* dsum = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes + vec_bytes);
+  int* sem = det ? reinterpret_cast<int*>(static_cast<char*>(ws) + acc_bytes + 2 * vec_bytes) : nullptr;
+  if (cudaMemsetAsync(lse2, 0, 2 * vec_bytes + sem_bytes, s) != cudaSuccess) st = FA_ERR_CUDA;
+  if (st == FA_OK) st = pre_post_any(false, f16, o, dout, lse, lse2, dsum, dq_acc, nullptr, sh, (int)mpad, s);
+  if (st == FA_OK && sh.tokens_q > 0) st = fa_host::make_map_f32(&p.tm_dq, dq_acc, sh.tokens_q, sh.H, d, G);
+  if (st == FA_OK && sh.tokens_q > 0 && sh.tokens_k > 0 && nkb > 0) {
+    p.lse2 = lse2;
+    p.dsum = dsum;
+    p.dq_acc = dq_acc;
+    p.dk = static_cast<uint16_t*>(dk);
+    p.dv = static_cast<uint16_t*>(dv);
+    p.cu_q = sh.cu_q;
+    p.cu_k = sh.cu_k;
+    p.B = sh.B; p.H = sh.H; p.Hkv = sh.H_kv; p.gshift = sh.gshift; p.Nq = sh.N_q; p.Nk = sh.N_kv;
+    p.nkb = (int)nkb;
+    p.mpad = (int)mpad;
+    p.num_tasks = (int)(sh.B * sh.H_kv * nkb);
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.timeout_ns = fa_host::wait_timeout_ns();
+    p.sem = sem;
+    p.ntiles = ntiles;
+    fa_host::trace_target(&p.trace, &p.trace_ctas);
+    if (d == 128)
+      st = f16 ? launch_c<128, true>(p, causal != 0, s) : launch_c<128, false>(p, causal != 0, s);
+    else
+      st = f16 ? launch_c<64, true>(p, causal != 0, s) : launch_c<64, false>(p, causal != 0, s);
+  }
+  if (st == FA_OK) st = pre_post_any(true, f16, nullptr, nullptr, nullptr, nullptr, nullptr, dq_acc, dq, sh, (int)mpad, s);
+  if (cudaFreeAsync(ws, s) != cudaSuccess && st == FA_OK) st = FA_ERR_CUDA;
+  return st;
 }
 }  // namespace
 
@@ -116,75 +202,42 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   const long long mpad = (((long long)N_q << gshift) + 127) / 128 * 128;
   const long long nkb = (N_kv + 127) / 128;
   if ((long long)B * H_kv * mpad > INT_MAX || (long long)B * H_kv * nkb > INT_MAX) return FA_ERR_INVALID_ARG;
-  int dev = 0, n = 0, major = 0, minor = 0;
-  if (cudaGetDeviceCount(&n) != cudaSuccess || n <= 0) {
-    cudaGetLastError();
-    return FA_ERR_NO_DEVICE;
-  }
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-    return FA_ERR_CUDA;
-  if (major != 10 || minor != 3) return FA_ERR_UNSUPPORTED;
-  const bool f16 = dtype == FA_DTYPE_FP16;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = device_check()) != FA_OK) return st;
+  const Shape sh{B, H, H_kv, N_q, N_kv, d, gshift, tokens, tokens_k, nullptr, nullptr};
+  return bwd_run(q, k, v, o, dout, lse, dq, dk, dv, sh, scale, causal, dtype == FA_DTYPE_FP16,
+                 static_cast<cudaStream_t>(stream));
+}
 
-  fa::BwdParams p;
-  std::memset(&p, 0, sizeof p);
-  const int G = H / H_kv;
-  if ((st = make_map(&p.tm_q, q, tokens, H, d, G, f16)) != FA_OK ||
-      (st = make_map(&p.tm_do, dout, tokens, H, d, G, f16)) != FA_OK ||
-      (st = make_map(&p.tm_k, k, tokens_k, H_kv, d, 1, f16)) != FA_OK ||
-      (st = make_map(&p.tm_v, v, tokens_k, H_kv, d, 1, f16)) != FA_OK)
-    return st;
-
-  // temporary buffer: dQ accumulator (fp32 [tokens, H, d], zeroed by the
-  // preprocessing kernel), then packed base-2 LSE and D ([B, H_kv, mpad] each,
-  // zeroed here so padding rows read 0)
-  const size_t acc_bytes = (size_t)tokens * H * d * sizeof(float);
-  const size_t vec_bytes = ((size_t)B * H_kv * mpad * sizeof(float) + 255) / 256 * 256;
-  const bool det = fa_host::bwd_deterministic();
-  const int ntiles = (int)(mpad / 128);
-  const size_t sem_bytes = det ? ((size_t)B * H_kv * ntiles * sizeof(int) + 255) / 256 * 256 : 0;
-  void* ws = nullptr;
-  if (cudaMallocAsync(&ws, acc_bytes + 2 * vec_bytes + sem_bytes, s) != cudaSuccess) {
-    cudaGetLastError();
-    return FA_ERR_CUDA;
-  }
-  float* dq_acc = static_cast<float*>(ws);
-  float* lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes);
-  float* dsum = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes + vec_bytes);
-  int* sem = det ? reinterpret_cast<int*>(static_cast<char*>(ws) + acc_bytes + 2 * vec_bytes) : nullptr;
-  if (cudaMemsetAsync(lse2, 0, 2 * vec_bytes + sem_bytes, s) != cudaSuccess) st = FA_ERR_CUDA;
-  if (st == FA_OK)
-    st = pre_post_any(false, d, f16, o, dout, lse, lse2, dsum, dq_acc, nullptr, B, H, gshift, N_q, (int)mpad, s);
-  if (st == FA_OK) st = fa_host::make_map_f32(&p.tm_dq, dq_acc, tokens, H, d, G);
-  if (st == FA_OK) {
-    p.lse2 = lse2;
-    p.dsum = dsum;
-    p.dq_acc = dq_acc;
-    p.dk = static_cast<uint16_t*>(dk);
-    p.dv = static_cast<uint16_t*>(dv);
-    p.B = B; p.H = H; p.Hkv = H_kv; p.gshift = gshift; p.Nq = N_q; p.Nk = N_kv;
-    p.nkb = (int)nkb;
-    p.mpad = (int)mpad;
-    p.num_tasks = (int)(B * H_kv * nkb);
-    p.scale = scale;
-    p.scale_log2 = scale * 1.4426950408889634f;
-    p.timeout_ns = fa_host::wait_timeout_ns();
-    p.sem = sem;
-    p.ntiles = ntiles;
-    fa_host::trace_target(&p.trace, &p.trace_ctas);
-    if (d == 128)
-      st = f16 ? launch_c<128, true>(p, causal != 0, s) : launch_c<128, false>(p, causal != 0, s);
-    else
-      st = f16 ? launch_c<64, true>(p, causal != 0, s) : launch_c<64, false>(p, causal != 0, s);
-  }
-  if (st == FA_OK)
-    st = pre_post_any(true, d, f16, nullptr, nullptr, nullptr, nullptr, nullptr, dq_acc, dq, B, H, gshift, N_q,
-                      (int)mpad, s);
-  if (cudaFreeAsync(ws, s) != cudaSuccess && st == FA_OK) st = FA_ERR_CUDA;
-  return st;
+int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                  void* dq, void* dk, void* dv, const int* cu_seqlens_q, const int* cu_seqlens_kv, int num_seqs,
+                  int total_q, int total_kv, int max_seqlen_q, int max_seqlen_kv, int H, int H_kv, int d,
+                  float scale, int causal, int dtype, void* stream) {
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !cu_seqlens_q || !cu_seqlens_kv)
+    return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) || !aligned(cu_seqlens_q, 4) ||
+      !aligned(cu_seqlens_kv, 4))
+    return FA_ERR_INVALID_ARG;
+  if (num_seqs <= 0 || total_q <= 0 || total_kv <= 0 || max_seqlen_q <= 0 || max_seqlen_kv <= 0 || H <= 0 ||
+      H_kv <= 0)
+    return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_INVALID_ARG;
+  int gshift = 0;
+  int st = check_heads(H, H_kv, &gshift);
+  if (st != FA_OK) return st;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if ((long long)total_q * H > INT_MAX || (long long)total_kv * H_kv > INT_MAX) return FA_ERR_INVALID_ARG;
+  const long long mpad = (((long long)max_seqlen_q << gshift) + 127) / 128 * 128;
+  const long long nkb = ((long long)max_seqlen_kv + 127) / 128;
+  if ((long long)num_seqs * H_kv * mpad > INT_MAX || (long long)num_seqs * H_kv * nkb > INT_MAX)
+    return FA_ERR_INVALID_ARG;
+  if ((st = device_check()) != FA_OK) return st;
+  const Shape sh{num_seqs, H, H_kv, max_seqlen_q, max_seqlen_kv, d, gshift, total_q, total_kv, cu_seqlens_q,
+                 cu_seqlens_kv};
+  return bwd_run(q, k, v, o, dout, lse, dq, dk, dv, sh, scale, causal, dtype == FA_DTYPE_FP16,
+                 static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -54,10 +54,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"],
-                    help="bwd: time the backward pass (fixed-length workloads) instead of the forward")
+                    help="bwd: time the backward pass instead of the forward")
     a = ap.parse_args()
-    if a.which == "bwd" and fa_inputs.WORKLOADS[a.workload].varlen:
-        ap.error("--pass bwd takes a fixed-length workload")
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
     return a
@@ -255,18 +253,24 @@ def cpu_baseline(w, x, target_s: float = 10.0):
 
 
 def cpu_baseline_bwd(w, x):
-    """The backward oracle (fp64 NumPy, as it stands) on one (batch, K/V head group) of the workload."""
+    """The backward oracle (fp64 NumPy, as it stands) on one (sequence, K/V head group) of the workload."""
     import oracle
     Gq = w.H // w.Hkv
-    q, k, v = x["q"][:1, :, :Gq], x["k"][:1, :, :1], x["v"][:1, :, :1]
-    do = fa_inputs.make_qkv(1, w.N, Gq, w.d, w.seed + 1000, dtype=w.dtype)[0]
+    if w.varlen:
+        a_, b_ = int(x["cu_seqlens"][0]), int(x["cu_seqlens"][1])
+        N, Nk = b_ - a_, b_ - a_
+        q, k, v = (x[n][None, a_:b_, :g] for n, g in (("q", Gq), ("k", 1), ("v", 1)))
+    else:
+        N, Nk = w.N, w.Nk
+        q, k, v = x["q"][:1, :, :Gq], x["k"][:1, :, :1], x["v"][:1, :, :1]
+    do = fa_inputs.make_qkv(1, N, Gq, w.d, w.seed + 1000, dtype=w.dtype)[0]
     t0 = time.perf_counter()
     oracle.attention_backward(q, k, v, do, w.scale, w.causal, dtype=w.dtype)
     dt = time.perf_counter() - t0
-    flops = 2.5 * fa_inputs.attention_flops(1, Gq, w.N, w.d, w.causal, Nk=w.Nk)
+    flops = 2.5 * fa_inputs.attention_flops(1, Gq, N, w.d, w.causal, Nk=Nk)
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count() or 1, "kind": "oracle",
-            "sample": f"backward of batch 0, K/V head 0 with its {Gq} query head(s) of {w.name} "
-                      f"(fp64 NumPy, full matrices per head), {dt:.1f} s"}
+            "sample": f"backward of {'sequence' if w.varlen else 'batch'} 0, K/V head 0 with its {Gq} query "
+                      f"head(s) of {w.name} (fp64 NumPy, full matrices per head), {dt:.1f} s"}
 
 
 # --------------------------------------------------------------------------- the reference arm
@@ -324,21 +328,31 @@ def run_ours(a, dist):
     q, k, v = to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"])
     o = torch.empty_like(q)
     bwd = a.which == "bwd"
+    if w.varlen:
+        cu = torch.from_numpy(x["cu_seqlens"]).to(dev)
+        maxL = int(x["lengths"].max())
     if bwd:
         # dO drawn like Q from its own seed; O and LSE from one untimed forward
-        dout = to_dev(fa_inputs.make_qkv(w.B, w.N, w.H, w.d, w.seed + 1000, dtype=w.dtype)[0])
-        lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
-        fa.fa_fwd(q, k, v, scale=w.scale, causal=w.causal, out=o, lse=lse)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         flops = 2.5 * flops   # five products against the forward's two
+        if w.varlen:
+            dout = to_dev(fa_inputs.make_qkv(1, q.shape[0], w.H, w.d, w.seed + 1000, dtype=w.dtype)[0][0])
+            lse = torch.empty((w.H, q.shape[0]), dtype=torch.float32, device=dev)
+            fa.fa_fwd_varlen(q, k, v, cu, maxL, scale=w.scale, causal=w.causal, out=o, lse=lse)
 
-        def step(s=None):
-            fa.fa_bwd(q, k, v, o, dout, lse, scale=w.scale, causal=w.causal, dq=dq, dk=dk, dv=dv, stream=s)
+            def step(s=None):
+                fa.fa_bwd_varlen(q, k, v, o, dout, lse, cu, maxL, scale=w.scale, causal=w.causal, dq=dq, dk=dk,
+                                 dv=dv, stream=s)
+        else:
+            dout = to_dev(fa_inputs.make_qkv(w.B, w.N, w.H, w.d, w.seed + 1000, dtype=w.dtype)[0])
+            lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+            fa.fa_fwd(q, k, v, scale=w.scale, causal=w.causal, out=o, lse=lse)
+
+            def step(s=None):
+                fa.fa_bwd(q, k, v, o, dout, lse, scale=w.scale, causal=w.causal, dq=dq, dk=dk, dv=dv, stream=s)
         splits = 1
         launches_per_step = 3   # preprocessing, backward, dQ conversion
     elif w.varlen:
-        cu = torch.from_numpy(x["cu_seqlens"]).to(dev)
-        maxL = int(x["lengths"].max())
         lse = torch.empty((w.H, q.shape[0]), dtype=torch.float32, device=dev)
 
         def step(s=None):
@@ -409,7 +423,10 @@ def run_ours(a, dist):
     def e2e_step():
         for d_, h_ in zip(d_in, h_in):
             d_.copy_(h_, non_blocking=True)
-        if bwd:
+        if bwd and w.varlen:
+            fa.fa_bwd_varlen(*d_in, cu, maxL, scale=w.scale, causal=w.causal, dq=d_out[0], dk=d_out[1],
+                             dv=d_out[2])
+        elif bwd:
             fa.fa_bwd(*d_in, scale=w.scale, causal=w.causal, dq=d_out[0], dk=d_out[1], dv=d_out[2])
         elif w.varlen:
             fa.fa_fwd_varlen(*d_in, cu, maxL, scale=w.scale, causal=w.causal, out=d_out[0], lse=d_out[1],

@@ -240,6 +240,30 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            void* dq, void* dk, void* dv, int B, int H, int H_kv, int N_q, int N_kv, int d, float scale,
            int causal, int dtype, void* stream);
 
+/*
+ * Backward pass of fa_fwd_varlen_kv without key splits (same gradients as fa_bwd,
+ * per sequence): sequence s has query rows [cu_seqlens_q[s], cu_seqlens_q[s+1]) and
+ * key rows [cu_seqlens_kv[s], cu_seqlens_kv[s+1]), with its own bottom-right causal
+ * diagonal; rows of one sequence never see another's keys.
+ *   q, o, dout, dq : [total_q, H, d]     k, v, dk, dv : [total_kv, H_kv, d]
+ *                    (dtype elements, device; dq, dk, dv written)
+ *   lse            : fp32 [H, total_q], the LSE that fa_fwd_varlen* wrote
+ *   cu_seqlens_q, cu_seqlens_kv : device int32 [num_seqs + 1], non-decreasing, starting
+ *                    at 0 and ending at total_q / total_kv (not checked on the host);
+ *                    empty sequences are allowed (a query row without keys gets dQ = 0,
+ *                    a key without queries dK = dV = 0)
+ *   max_seqlen_q, max_seqlen_kv : the longest sequence's lengths (upper bounds suffice;
+ *                    they size the grid and the packed-row buffers)
+ *   other arguments as for fa_bwd. Errors: as fa_bwd, plus FA_ERR_INVALID_ARG for null
+ *   or misaligned cu_seqlens, num_seqs, totals or maxima <= 0. The temporary buffer is
+ *   total_q*H*d*4 + 2*num_seqs*H_kv*ceil(max_seqlen_q*G/128)*128*4 bytes (+ the
+ *   deterministic mode's counters), from the stream-ordered allocator.
+ */
+int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                  void* dq, void* dk, void* dv, const int* cu_seqlens_q, const int* cu_seqlens_kv, int num_seqs,
+                  int total_q, int total_kv, int max_seqlen_q, int max_seqlen_kv, int H, int H_kv, int d,
+                  float scale, int causal, int dtype, void* stream);
+
 /* Text for a status code (static storage; never NULL). */
 const char* fa_error_string(int status);
 

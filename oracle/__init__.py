@@ -193,6 +193,6 @@ def attention_rows_varlen(q, k, v, cu_seqlens, rows, scale: float, causal: bool,
     return o, lse
 
 
-from .attn_backward import attention_backward, attention_forward  # noqa: E402,F401
+from .attn_backward import attention_backward, attention_backward_varlen, attention_forward  # noqa: E402,F401
 from .lse_combine import lse_combine  # noqa: E402,F401
 from .online_softmax import online_softmax_rows  # noqa: E402,F401

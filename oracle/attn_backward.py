@@ -98,3 +98,23 @@ def attention_backward(q, k, v, do, scale: float, causal: bool, dtype: str = "bf
             dq[b, :, h] = scale * dS @ K
             dk[b, :, h // G] += scale * dS.T @ Q
     return dq, dk, dv
+
+
+def attention_backward_varlen(q, k, v, do, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool,
+                              dtype: str = "bf16"):
+    """Packed variable-length gradients: q, do [T, H, d]; k, v [T_kv, H_kv, d]; sequence s
+    has query rows [cu_q[s], cu_q[s+1]) and key rows [cu_k[s], cu_k[s+1]), with its own
+    bottom-right causal diagonal. Each sequence is ``attention_backward`` of its own
+    slices (a sequence without keys: dQ = 0; without queries: dK = dV = 0)."""
+    q, k, v, do = (_widen(x, dtype) for x in (q, k, v, do))
+    cu_q = np.asarray(cu_seqlens_q, dtype=np.int64)
+    cu_k = np.asarray(cu_seqlens_k, dtype=np.int64)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for s in range(len(cu_q) - 1):
+        a, b = cu_q[s], cu_q[s + 1]
+        c, e = cu_k[s], cu_k[s + 1]
+        if b == a or e == c:
+            continue
+        g = attention_backward(q[None, a:b], k[None, c:e], v[None, c:e], do[None, a:b], scale, causal)
+        dq[a:b], dk[c:e], dv[c:e] = g[0][0], g[1][0], g[2][0]
+    return dq, dk, dv

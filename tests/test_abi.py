@@ -168,7 +168,43 @@ def test_lse_combine_rejects_invalid_arguments(kw):
     assert combine(**kw) == fa.FA_ERR_INVALID_ARG
 
 
+def bwd(**kw):
+    args = dict(q=16, k=16, v=16, o=16, do=16, lse=16, dq=16, dk=16, dv=16, B=2, H=8, Hkv=2, Nq=300, Nk=200,
+                d=128, scale=0.125, causal=1, dtype=0, stream=NULL)
+    args.update(kw)
+    return fa.library().fa_bwd(*[args[n] for n in ("q", "k", "v", "o", "do", "lse", "dq", "dk", "dv", "B", "H",
+                                                   "Hkv", "Nq", "Nk", "d", "scale", "causal", "dtype", "stream")])
+
+
+def bwd_varlen(**kw):
+    args = dict(q=16, k=16, v=16, o=16, do=16, lse=16, dq=16, dk=16, dv=16, cuq=16, cuk=32, S=3, Tq=700,
+                Tk=900, maxq=400, maxk=500, H=8, Hkv=2, d=128, scale=0.125, causal=1, dtype=0, stream=NULL)
+    args.update(kw)
+    return fa.library().fa_bwd_varlen(*[args[n] for n in ("q", "k", "v", "o", "do", "lse", "dq", "dk", "dv", "cuq",
+                                                          "cuk", "S", "Tq", "Tk", "maxq", "maxk", "H", "Hkv", "d",
+                                                          "scale", "causal", "dtype", "stream")])
+
+
+@pytest.mark.parametrize("kw", [dict(q=NULL), dict(do=NULL), dict(lse=NULL), dict(dq=NULL), dict(dk=NULL),
+                                dict(dv=NULL), dict(o=8), dict(dq=24), dict(lse=2), dict(B=0), dict(Nq=0),
+                                dict(Nk=-1), dict(H=6, Hkv=4), dict(scale=0.0), dict(scale=math.nan),
+                                dict(causal=3), dict(dtype=2), dict(B=1 << 16, Nq=1 << 16)])
+def test_bwd_rejects_invalid_arguments(kw):
+    assert bwd(**kw) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(cuq=NULL), dict(cuk=NULL), dict(cuk=2), dict(dv=NULL), dict(S=0),
+                                dict(Tq=0), dict(Tk=0), dict(maxq=0), dict(maxk=0), dict(H=6, Hkv=4),
+                                dict(dtype=7), dict(causal=-1), dict(scale=-2.0)])
+def test_bwd_varlen_rejects_invalid_arguments(kw):
+    assert bwd_varlen(**kw) == fa.FA_ERR_INVALID_ARG
+
+
 def test_new_entry_points_reject_unsupported_head_dim():
+    assert bwd(d=96) == fa.FA_ERR_UNSUPPORTED
+    assert bwd_varlen(d=256) == fa.FA_ERR_UNSUPPORTED
+    assert bwd(H=144, Hkv=3) == fa.FA_ERR_UNSUPPORTED        # a group of 48 rows does not divide the tile
+    assert bwd_varlen(H=144, Hkv=3) == fa.FA_ERR_UNSUPPORTED
     assert fwd_kv(d=32) == fa.FA_ERR_UNSUPPORTED
     assert varlen_kv(d=96) == fa.FA_ERR_UNSUPPORTED
     assert combine(d=256) == fa.FA_ERR_UNSUPPORTED
@@ -189,6 +225,10 @@ def test_valid_arguments_without_gpu_report_no_device():
         assert varlen_kv(splits=splits) == fa.FA_ERR_NO_DEVICE
     assert fwd_kv(Nq=300, Nk=100) == fa.FA_ERR_NO_DEVICE       # rows without keys are allowed
     assert combine() == fa.FA_ERR_NO_DEVICE
+    for dtype in (0, 1):
+        assert bwd(dtype=dtype) == fa.FA_ERR_NO_DEVICE
+        assert bwd_varlen(dtype=dtype) == fa.FA_ERR_NO_DEVICE
+    assert bwd(H=4, Hkv=4, d=64, causal=0) == fa.FA_ERR_NO_DEVICE
 
 
 @pytest.mark.parametrize("opt,val,ok", [(1, 8.0, True), (1, 0.0, True), (1, 1e30, True), (1, -1.0, False),

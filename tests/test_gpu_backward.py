@@ -132,3 +132,56 @@ def test_backward_deterministic_mode(shape):
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
     check(a, oracle.attention_backward(q, k, v, do, 1 / math.sqrt(d), causal), f"deterministic {shape}")
+
+
+# --------------------------------------------------------------------------- varlen
+def run_bwd_varlen(lq, lk, H, Hkv, d, causal, dtype="bf16", seed=0):
+    """Packed sequences (query lengths lq, key lengths lk) through fa_fwd_varlen and
+    fa_bwd_varlen; returns the inputs, cu arrays and host gradients."""
+    import torch
+    rng = np.random.default_rng(seed)
+    cu_q = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(lk)]).astype(np.int32)
+    T, Tk = int(cu_q[-1]), int(cu_k[-1])
+    f = lambda shape: fa_inputs.f32_to_bits(rng.standard_normal(shape).astype(np.float32), dtype)  # noqa: E731
+    q, k, v, do = f((T, H, d)), f((Tk, Hkv, d)), f((Tk, Hkv, d)), f((T, H, d))
+    cq, ck = torch.from_numpy(cu_q).cuda(), torch.from_numpy(cu_k).cuda()
+    qd, kd, vd, dod = dev(q, dtype), dev(k, dtype), dev(v, dtype), dev(do, dtype)
+    o, lse = fa.fa_fwd_varlen(qd, kd, vd, cq, max(lq), cu_seqlens_k=ck, max_seqlen_k=max(lk), causal=causal)
+    dq, dk, dv = fa.fa_bwd_varlen(qd, kd, vd, o, dod, lse, cq, max(lq), cu_seqlens_k=ck, max_seqlen_k=max(lk),
+                                  causal=causal)
+    st, word = fa.last_device_status()
+    assert st == fa.FA_OK, hex(word)
+    return (q, k, v, do, cu_q, cu_k), (host(dq), host(dk), host(dv))
+
+
+VARLEN = [  # (query lengths, key lengths, H, H_kv, d)
+    ([7, 0, 129, 300, 1, 520], None, 4, 2, 128),
+    ([200, 64, 333], [250, 64, 100], 8, 2, 128),     # N_q != N_kv per sequence (causal rows without keys)
+    ([130, 5, 260], [0, 40, 300], 2, 1, 64),          # a sequence without keys
+    ([40, 90], None, 32, 1, 64),                       # G = 32
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("case", VARLEN, ids=lambda c: f"q{c[0]}_k{c[1]}_H{c[2]}KV{c[3]}d{c[4]}")
+def test_backward_varlen_elementwise(case, causal):
+    lq, lk, H, Hkv, d = case
+    lk = lq if lk is None else lk
+    (q, k, v, do, cu_q, cu_k), got = run_bwd_varlen(lq, lk, H, Hkv, d, causal, seed=sum(lq) + H)
+    ref = oracle.attention_backward_varlen(q, k, v, do, cu_q, cu_k, 1 / math.sqrt(d), causal)
+    check(got, ref, f"varlen {lq}/{lk} causal={causal}")
+
+
+def test_backward_varlen_fp16_and_deterministic():
+    lq = [300, 17, 450]
+    fa.set_option("bwd_deterministic", 1)
+    try:
+        (q, k, v, do, cu_q, cu_k), a = run_bwd_varlen(lq, lq, 8, 2, 128, True, "f16", seed=9)
+        _, b = run_bwd_varlen(lq, lq, 8, 2, 128, True, "f16", seed=9)
+    finally:
+        fa.set_option("bwd_deterministic", 0)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    ref = oracle.attention_backward_varlen(q, k, v, do, cu_q, cu_k, 1 / math.sqrt(128), True, dtype="f16")
+    check(a, ref, "varlen fp16 deterministic")

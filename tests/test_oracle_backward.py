@@ -109,3 +109,58 @@ def test_rows_without_keys_have_no_gradient():
     dq2, dk2, dv2 = oracle.attention_backward(q[:, 4:], k, v, do[:, 4:], 0.5, True)
     np.testing.assert_allclose(dk, dk2, rtol=0, atol=1e-13)
     np.testing.assert_allclose(dv, dv2, rtol=0, atol=1e-13)
+
+
+def test_varlen_with_equal_lengths_is_the_batched_gradient():
+    B, H, Hkv, N, d = 3, 4, 2, 9, 8
+    q, do = rand((B * N, H, d), 50), rand((B * N, H, d), 51)
+    k, v = rand((B * N, Hkv, d), 52), rand((B * N, Hkv, d), 53)
+    cu = np.arange(B + 1) * N
+    for causal in (False, True):
+        got = oracle.attention_backward_varlen(q, k, v, do, cu, cu, 0.4, causal)
+        ref = oracle.attention_backward(q.reshape(B, N, H, d), k.reshape(B, N, Hkv, d), v.reshape(B, N, Hkv, d),
+                                        do.reshape(B, N, H, d), 0.4, causal)
+        for g, r in zip(got, ref):
+            np.testing.assert_allclose(g, r.reshape(g.shape), rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_matches_float64_autograd_with_a_block_diagonal_mask(causal):
+    """The packed sequences as one attention with a block-diagonal mask (bottom-right
+    causal inside each block), differentiated by PyTorch's float64 autograd."""
+    torch = pytest.importorskip("torch")
+    lq, lk = [3, 5, 2], [4, 5, 6]   # every query row sees at least one key
+    H, Hkv, d = 2, 1, 8
+    cu_q, cu_k = np.concatenate([[0], np.cumsum(lq)]), np.concatenate([[0], np.cumsum(lk)])
+    T, Tk = cu_q[-1], cu_k[-1]
+    q, do = rand((T, H, d), 60), rand((T, H, d), 61)
+    k, v = rand((Tk, Hkv, d), 62), rand((Tk, Hkv, d), 63)
+    dq, dk, dv = oracle.attention_backward_varlen(q, k, v, do, cu_q, cu_k, 0.3, causal)
+    mask = torch.zeros(T, Tk, dtype=torch.bool)
+    for s in range(len(lq)):
+        i = torch.arange(lq[s])[:, None]
+        j = torch.arange(lk[s])[None, :]
+        blk = (j <= i + (lk[s] - lq[s])) if causal else torch.ones(lq[s], lk[s], dtype=torch.bool)
+        mask[cu_q[s]:cu_q[s + 1], cu_k[s]:cu_k[s + 1]] = blk
+    t = lambda a: torch.from_numpy(a).permute(1, 0, 2)[None]  # noqa: E731  [1, H, T, d]
+    tq, tk, tv = (t(x).clone().requires_grad_() for x in (q, k, v))
+    out = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask, scale=0.3, enable_gqa=True)
+    out.backward(t(do))
+    for g, tg in ((dq, tq), (dk, tk), (dv, tv)):
+        np.testing.assert_allclose(g, tg.grad[0].permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+
+
+def test_varlen_empty_sequences_and_no_cross_talk():
+    lq, lk = [3, 0, 4, 2], [2, 3, 0, 5]
+    cu_q, cu_k = np.concatenate([[0], np.cumsum(lq)]), np.concatenate([[0], np.cumsum(lk)])
+    q, do = rand((9, 2, 4), 70), rand((9, 2, 4), 71)
+    k, v = rand((10, 2, 4), 72), rand((10, 2, 4), 73)
+    dq, dk, dv = oracle.attention_backward_varlen(q, k, v, do, cu_q, cu_k, 0.5, False)
+    assert (dq[3:7] == 0).all()              # sequence 2 has no keys
+    assert (dk[2:5] == 0).all() and (dv[2:5] == 0).all()   # sequence 1 has no queries
+    # changing the last sequence's inputs leaves the first sequence's gradients alone
+    q2, k2 = q.copy(), k.copy()
+    q2[7:] += 1.0
+    k2[5:] -= 2.0
+    dq2, dk2, dv2 = oracle.attention_backward_varlen(q2, k2, v, do, cu_q, cu_k, 0.5, False)
+    assert np.array_equal(dq[:3], dq2[:3]) and np.array_equal(dk[:2], dk2[:2]) and np.array_equal(dv[:2], dv2[:2])
