@@ -29,6 +29,7 @@ struct Options {
   int bwd_deterministic = 0;
   int stagger = 0;
   int stats_tmem = 1;
+  int bwd_section = 0;
 };
 Options g_opt;
 
@@ -370,6 +371,7 @@ void trace_target(unsigned long long** buf, int* ctas) {
   *ctas = g_trace_ctas;
 }
 bool bwd_deterministic() { return g_opt.bwd_deterministic != 0; }
+int bwd_section_override() { return g_opt.bwd_section; }
 unsigned long long wait_timeout_ns() { return g_opt.timeout_ns; }
 }  // namespace fa_host
 
@@ -420,6 +422,10 @@ int fa_set_option(int option, double value) {
     case FA_OPT_STATS_TMEM:
       if (value != 0.0 && value != 1.0) return FA_ERR_INVALID_ARG;
       g_opt.stats_tmem = (int)value;
+      return FA_OK;
+    case FA_OPT_BWD_SECTION:
+      if (!(value >= 0.0 && value <= 1e6) || value != std::floor(value)) return FA_ERR_INVALID_ARG;
+      g_opt.bwd_section = (int)value;
       return FA_OK;
     default:
       return FA_ERR_INVALID_ARG;

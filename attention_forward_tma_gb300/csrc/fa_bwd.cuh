@@ -63,6 +63,7 @@ struct BwdParams {
   uint16_t* dv;              // [tokens_k, H_kv, d]
   int B, H, Hkv, gshift, Nq, Nk;
   int nkb;                   // 128-key blocks per sequence
+  int section;               // (sequence, K/V head) pairs per L2 section of the grid order
   int mpad;                  // packed rows per (b, K/V head), rounded up to 128
   int num_tasks;
   float scale, scale_log2;
@@ -200,10 +201,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // task: key block j of (b, kv head); heavy blocks (small j under the causal mask) first
-  const int bh_total = p.B * p.Hkv;
-  const int j = (int)blockIdx.x / bh_total;
-  const int bh = (int)blockIdx.x - j * bh_total;
+  // task: key block j of a (sequence, kv head) pair. The grid runs in sections of
+  // p.section pairs, so that the CTAs in flight share Q, dO and the fp32 dQ
+  // accumulator rows in L2; inside a section key block j of every pair before block j+1 (heavy blocks,
+  // small j under the causal mask, first; and block j of a pair always after block j-1,
+  // which the deterministic mode's ordered dQ additions rely on)
+  const int pairs = p.B * p.Hkv;
+  const int per_sec = p.section * p.nkb;
+  const int sec = (int)blockIdx.x / per_sec, rem = (int)blockIdx.x - sec * per_sec;
+  const int in_sec = min(p.section, pairs - sec * p.section);   // the last section may be smaller
+  const int j = rem / in_sec;
+  const int bh = sec * p.section + (rem - j * in_sec);
   const int b = bh / p.Hkv, kvh = bh - b * p.Hkv;
   int Nq = p.Nq, Nk = p.Nk, tok_q = b * p.Nq, tok_k = b * p.Nk;   // this sequence
   if (p.cu_q != nullptr) {

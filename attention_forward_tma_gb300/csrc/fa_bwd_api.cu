@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstring>
@@ -149,6 +150,13 @@ int bwd_run(const void* q, const void* k, const void* v, const void* o, const vo
     p.cu_k = sh.cu_k;
     p.B = sh.B; p.H = sh.H; p.Hkv = sh.H_kv; p.gshift = sh.gshift; p.Nq = sh.N_q; p.Nk = sh.N_kv;
     p.nkb = (int)nkb;
+    // L2 sections of about 512 CTAs (3 to 4 waves of 152): measured on B4 H16 N4096,
+    // B1 H32 N16384 and grouped B4 H32/8 N4096 against sections of 64 to 4096 CTAs.
+    // The deterministic mode keeps one section: there the key blocks of a pair take
+    // turns at every Q tile, and running all of them at once makes them wait longest.
+    const int pairs = sh.B * sh.H_kv;
+    p.section = det ? pairs : std::min(pairs, std::max(1, (int)((512 + nkb / 2) / nkb)));
+    if (fa_host::bwd_section_override() > 0) p.section = std::min(pairs, fa_host::bwd_section_override());
     p.mpad = (int)mpad;
     p.num_tasks = (int)(sh.B * sh.H_kv * nkb);
     p.scale = scale;

@@ -89,6 +89,7 @@ int bwd_take_status(unsigned long long* word);
 void trace_target(unsigned long long** buf, int* ctas);
 // Process-wide options of fa_set_option read by the backward translation unit.
 bool bwd_deterministic();
+int bwd_section_override();   // > 0: pairs per L2 section of the backward grid (tests, tuning)
 unsigned long long wait_timeout_ns();
 
 }  // namespace fa_host

@@ -308,11 +308,15 @@ int fa_last_device_status(void* stream, unsigned long long* detail);
  *                            instead of a shared-memory mailbox (same section: the
  *                            paper passes the statistics through spare TMEM);
  *                            default 1. 0 = shared memory.
+ *   FA_OPT_BWD_SECTION     : (sequence, K/V head) pairs per L2 section of the backward's
+ *                            grid order (whole number; 0 = the library's choice, about
+ *                            512 CTAs per section)
  * Both forward variants compute the same result as the default path.
  * Returns FA_OK or FA_ERR_INVALID_ARG.
  */
 enum { FA_OPT_TAU = 1, FA_OPT_WAIT_TIMEOUT_NS = 2, FA_OPT_PERSISTENT = 3, FA_OPT_EXP2_EMULATION = 4,
-       FA_OPT_BWD_DETERMINISTIC = 5, FA_OPT_SOFTMAX_STAGGER = 6, FA_OPT_STATS_TMEM = 7 };
+       FA_OPT_BWD_DETERMINISTIC = 5, FA_OPT_SOFTMAX_STAGGER = 6, FA_OPT_STATS_TMEM = 7,
+       FA_OPT_BWD_SECTION = 8 };
 int fa_set_option(int option, double value);
 
 /* Library version, as major*10000 + minor*100 + patch. */
