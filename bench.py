@@ -104,13 +104,20 @@ def measured_peaks():
         return FALLBACK_PEAK_TFLOPS, 1700.0, 6800.0, "fallback"
 
 
-def kernel_source_hash() -> str:
+# The sources each pass's kernels are compiled from (a DRAM record stays valid while
+# these are unchanged).
+KERNEL_SOURCES = {
+    "fwd": ("fa_api.cu", "fa_fwd.cuh", "fa_host.cuh", "ptx.cuh"),
+    "bwd": ("fa_bwd_api.cu", "fa_bwd.cuh", "fa_fwd.cuh", "fa_host.cuh", "ptx.cuh"),
+}
+
+
+def kernel_source_hash(which: str = "fwd") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "attention_forward_tma_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in sorted(KERNEL_SOURCES[which]):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -124,7 +131,7 @@ def profiled_traffic(workload: str, which: str = "fwd"):
                 if ":" in line and not line.startswith("#"):
                     k, v = line.split(":", 1)
                     kv[k.strip()] = v.strip()
-        if kv.get("kernel_source_sha256_16") != kernel_source_hash():
+        if kv.get("kernel_source_sha256_16") != kernel_source_hash(which):
             return None
         return float(kv["dram_bytes_per_launch"])
     except Exception:
