@@ -372,6 +372,7 @@ void trace_target(unsigned long long** buf, int* ctas) {
 }
 bool bwd_deterministic() { return g_opt.bwd_deterministic != 0; }
 int bwd_section_override() { return g_opt.bwd_section; }
+int persistent_mode() { return g_opt.persistent; }
 unsigned long long wait_timeout_ns() { return g_opt.timeout_ns; }
 }  // namespace fa_host
 

@@ -25,7 +25,7 @@ std::mutex g_mu;
 int g_ready[kMaxDevices][2][2][2];
 
 template <int D, bool C, bool F>
-int launch(const fa::BwdParams& p, cudaStream_t s) {
+int launch(const fa::BwdParams& p, int grid, cudaStream_t s) {
   using L = fa::BwdLayout<D>;
   auto kern = fa::fa_bwd_kernel<D, C, F>;
   int dev = 0;
@@ -47,13 +47,13 @@ int launch(const fa::BwdParams& p, cudaStream_t s) {
     }
     if (r != 1) return r;
   }
-  kern<<<p.num_tasks, fa::kBwdThreads, L::kAlloc, s>>>(p);
+  kern<<<grid, fa::kBwdThreads, L::kAlloc, s>>>(p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 template <int D, bool F>
-int launch_c(const fa::BwdParams& p, bool causal, cudaStream_t s) {
-  return causal ? launch<D, true, F>(p, s) : launch<D, false, F>(p, s);
+int launch_c(const fa::BwdParams& p, int grid, bool causal, cudaStream_t s) {
+  return causal ? launch<D, true, F>(p, grid, s) : launch<D, false, F>(p, grid, s);
 }
 
 // Shape of one call: fixed length (cu_q == nullptr: B sequences of N_q / N_kv rows) or
@@ -127,7 +127,7 @@ int bwd_run(const void* q, const void* k, const void* v, const void* o, const vo
   const size_t vec_bytes = ((size_t)sh.B * sh.H_kv * mpad * sizeof(float) + 255) / 256 * 256;
   const bool det = fa_host::bwd_deterministic();
   const int ntiles = (int)(mpad / 128);
-  const size_t sem_bytes = det ? ((size_t)sh.B * sh.H_kv * ntiles * sizeof(int) + 255) / 256 * 256 : 0;
+  const size_t sem_bytes = (det ? ((size_t)sh.B * sh.H_kv * ntiles * sizeof(int) + 255) / 256 * 256 : 0) + 256;
   void* ws = nullptr;
   if (cudaMallocAsync(&ws, acc_bytes + 2 * vec_bytes + sem_bytes, s) != cudaSuccess) {
     cudaGetLastError();
@@ -137,6 +137,7 @@ int bwd_run(const void* q, const void* k, const void* v, const void* o, const vo
   float* lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes);
   float* dsum = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes + vec_bytes);
   int* sem = det ? reinterpret_cast<int*>(static_cast<char*>(ws) + acc_bytes + 2 * vec_bytes) : nullptr;
+  int* counter = reinterpret_cast<int*>(static_cast<char*>(ws) + acc_bytes + 2 * vec_bytes + sem_bytes - 256);
   if (cudaMemsetAsync(lse2, 0, 2 * vec_bytes + sem_bytes, s) != cudaSuccess) st = FA_ERR_CUDA;
   if (st == FA_OK) st = pre_post_any(false, f16, o, dout, lse, lse2, dsum, dq_acc, nullptr, sh, (int)mpad, s);
   if (st == FA_OK && sh.tokens_q > 0) st = fa_host::make_map_f32(&p.tm_dq, dq_acc, sh.tokens_q, sh.H, d, G);
@@ -164,11 +165,21 @@ int bwd_run(const void* q, const void* k, const void* v, const void* o, const vo
     p.timeout_ns = fa_host::wait_timeout_ns();
     p.sem = sem;
     p.ntiles = ntiles;
+    p.task_counter = counter;
     fa_host::trace_target(&p.trace, &p.trace_ctas);
-    if (d == 128)
-      st = f16 ? launch_c<128, true>(p, causal != 0, s) : launch_c<128, false>(p, causal != 0, s);
+    // persistent CTAs, one per SM, claiming tasks in order (FA_OPT_PERSISTENT = 0: one
+    // CTA per task)
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+      st = FA_ERR_CUDA;
+    const int grid = fa_host::persistent_mode() == 0 ? p.num_tasks : std::min(p.num_tasks, std::max(sms, 1));
+    if (st != FA_OK)
+      ;
+    else if (d == 128)
+      st = f16 ? launch_c<128, true>(p, grid, causal != 0, s) : launch_c<128, false>(p, grid, causal != 0, s);
     else
-      st = f16 ? launch_c<64, true>(p, causal != 0, s) : launch_c<64, false>(p, causal != 0, s);
+      st = f16 ? launch_c<64, true>(p, grid, causal != 0, s) : launch_c<64, false>(p, grid, causal != 0, s);
   }
   if (st == FA_OK) st = pre_post_any(true, f16, nullptr, nullptr, nullptr, nullptr, nullptr, dq_acc, dq, sh, (int)mpad, s);
   if (cudaFreeAsync(ws, s) != cudaSuccess && st == FA_OK) st = FA_ERR_CUDA;

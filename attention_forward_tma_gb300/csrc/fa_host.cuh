@@ -90,6 +90,7 @@ void trace_target(unsigned long long** buf, int* ctas);
 // Process-wide options of fa_set_option read by the backward translation unit.
 bool bwd_deterministic();
 int bwd_section_override();   // > 0: pairs per L2 section of the backward grid (tests, tuning)
+int persistent_mode();        // FA_OPT_PERSISTENT (-1 = the default)
 unsigned long long wait_timeout_ns();
 
 }  // namespace fa_host

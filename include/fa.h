@@ -232,9 +232,10 @@ int fa_fwd_varlen_noalloc(const void* q, const void* k, const void* v, void* o, 
  * dQ is accumulated over key blocks in fp32 by reduce-adds in arrival order, so
  * its last bits may differ from run to run unless FA_OPT_BWD_DETERMINISTIC is set;
  * dK and dV are always deterministic. A temporary buffer of B*N_q*H*d*4 +
- * 2*B*H_kv*ceil(N_q*G/128)*128*4 bytes (+ 4 bytes per 128-row Q tile in the
+ * 2*B*H_kv*ceil(N_q*G/128)*128*4 + 256 bytes (+ 4 bytes per 128-row Q tile in the
  * deterministic mode) comes from the stream-ordered allocator (cudaMallocAsync /
- * cudaFreeAsync on `stream`).
+ * cudaFreeAsync on `stream`). One CTA per SM walks the tasks (key block of a
+ * (batch, K/V head) pair) in order, claiming the next from a counter in that buffer.
  */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
            void* dq, void* dk, void* dv, int B, int H, int H_kv, int N_q, int N_kv, int d, float scale,
@@ -285,7 +286,9 @@ int fa_last_device_status(void* stream, unsigned long long* detail);
  *                            each running CTA takes over the tasks of CTAs not yet
  *                            launched (cluster launch control; the default);
  *                            1 = one CTA per SM with a static task stride;
- *                            0 = one CTA per task, no take-over; -1 = restore the default
+ *                            0 = one CTA per task, no take-over; -1 = restore the default.
+ *                            fa_bwd / fa_bwd_varlen: 0 = one CTA per task; any other
+ *                            value = one CTA per SM claiming tasks in order (default)
  *   FA_OPT_EXP2_EMULATION  : number of 16-element groups per 128-wide row (0..8)
  *                            whose exp2 is evaluated with the FMA polynomial instead
  *                            of the hardware ex2 unit (default 0)
