@@ -97,15 +97,29 @@ int make_maps(fa::FwdParams& p, const void* q, const void* k, const void* v, voi
 // against 4K-128K keys: one full wave beat both fewer ranges and a second,
 // partial wave; e.g. 64 tasks x 2 ranges 235 us, x 5 ranges 279 us.)
 constexpr int kMaxSplits = 128;
+// The library's choice when fewer tasks than SMs: the number of key ranges s (at most
+// 64, at least 4 key blocks per range) that minimises the estimated time
+//   ceil(base_tasks * s / sm_count) rounds x (ceil(key_blocks / s) + 2) blocks,
+// the 2 standing for a task's fixed cost (its Q load, pipeline fill and epilogue), so
+// that the key ranges fill the SMs evenly (64 tasks on 152 SMs: 7 ranges, 448 tasks in
+// three rounds, rather than 2 ranges leaving 24 SMs idle).
 int choose_splits(int requested, long long base_tasks, int key_blocks, int sm_count) {
   const int most = key_blocks < 1 ? 1 : (key_blocks < kMaxSplits ? key_blocks : kMaxSplits);
   if (requested > 0) return requested < most ? requested : most;
-  if (base_tasks >= sm_count || key_blocks < 8) return 1;
-  long long want = sm_count / base_tasks;
-  const int by_len = key_blocks / 4;
-  if (want > by_len) want = by_len;
-  if (want > 64) want = 64;
-  return want < 1 ? 1 : (int)want;
+  if (base_tasks >= sm_count || key_blocks < 8 || sm_count < 1) return 1;
+  int limit = key_blocks / 4;
+  if (limit > 64) limit = 64;
+  int best = 1;
+  long long best_cost = -1;
+  for (int sp = 1; sp <= limit; ++sp) {
+    const long long rounds = (base_tasks * sp + sm_count - 1) / sm_count;
+    const long long cost = rounds * ((key_blocks + sp - 1) / sp + 2);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = sp;
+    }
+  }
+  return best;
 }
 
 // Stream-ordered temporary buffer: `head_bytes` for the caller (the varlen tile
