@@ -185,3 +185,65 @@ def test_backward_varlen_fp16_and_deterministic():
         assert np.array_equal(x, y)
     ref = oracle.attention_backward_varlen(q, k, v, do, cu_q, cu_k, 1 / math.sqrt(128), True, dtype="f16")
     check(a, ref, "varlen fp16 deterministic")
+
+
+# --------------------------------------------------------------------------- full sizes
+def _full_inputs(name):
+    """A named workload's inputs and the upstream gradient bench.py draws for it."""
+    w = fa_inputs.WORKLOADS[name]
+    x = fa_inputs.make_workload(w)
+    if w.varlen:
+        T = x["q"].shape[0]
+        do = fa_inputs.make_qkv(1, T, w.H, w.d, w.seed + 1000, dtype=w.dtype)[0][0]
+    else:
+        do = fa_inputs.make_qkv(w.B, w.N, w.H, w.d, w.seed + 1000, dtype=w.dtype)[0]
+    return w, x, do
+
+
+@pytest.mark.parametrize("name,b,kvh", [("c3_b4h16n4096d128_causal", 2, 11),
+                                        ("g2_gqa_b4h32kv8n4096d128_causal", 3, 5)])
+def test_backward_full_size_one_head_group(name, b, kvh):
+    """The whole workload through the kernel in bench.py's launch configuration; the
+    gradients of one (batch, K/V head) group checked in full against the oracle on that
+    group alone (its dK, dV and its query heads' dQ depend on nothing else)."""
+    w, x, do = _full_inputs(name)
+    got = run_bwd(x["q"], x["k"], x["v"], do, w.causal, w.dtype, scale=w.scale)
+    G = w.H // w.Hkv
+    hs = slice(kvh * G, (kvh + 1) * G)
+    q, k, v = x["q"][b:b + 1, :, hs], x["k"][b:b + 1, :, kvh:kvh + 1], x["v"][b:b + 1, :, kvh:kvh + 1]
+    ref = oracle.attention_backward(q, k, v, do[b:b + 1, :, hs], w.scale, w.causal, dtype=w.dtype)
+    sel = (got[0][b:b + 1, :, hs], got[1][b:b + 1, :, kvh:kvh + 1], got[2][b:b + 1, :, kvh:kvh + 1])
+    check(sel, ref, f"{name} b={b} kv head={kvh}")
+    for g in got:   # every other gradient at least finite
+        assert np.isfinite(g).all()
+
+
+def test_backward_full_size_varlen_one_sequence():
+    import torch
+    w, x, do = _full_inputs("c5_varlen8_h16d128_causal")
+    cu = x["cu_seqlens"]
+    qd, kd, vd, dod = dev(x["q"]), dev(x["k"]), dev(x["v"]), dev(do)
+    cd = torch.from_numpy(cu).cuda()
+    maxL = int(x["lengths"].max())
+    o, lse = fa.fa_fwd_varlen(qd, kd, vd, cd, maxL, scale=w.scale, causal=True)
+    dq, dk, dv = fa.fa_bwd_varlen(qd, kd, vd, o, dod, lse, cd, maxL, scale=w.scale, causal=True)
+    st, word = fa.last_device_status()
+    assert st == fa.FA_OK, hex(word)
+    s = int(np.argmax(x["lengths"]))          # the longest sequence, one head
+    a, e, h = int(cu[s]), int(cu[s + 1]), 9
+    ref = oracle.attention_backward(x["q"][None, a:e, h:h + 1], x["k"][None, a:e, h:h + 1],
+                                    x["v"][None, a:e, h:h + 1], do[None, a:e, h:h + 1], w.scale, True)
+    got = tuple(host(t)[None, a:e, h:h + 1] for t in (dq, dk, dv))
+    check(got, ref, f"c5 sequence {s} (length {e - a}) head {h}")
+
+
+def test_backward_full_size_deterministic_bits():
+    w, x, do = _full_inputs("c3_b4h16n4096d128_causal")
+    fa.set_option("bwd_deterministic", 1)
+    try:
+        a = run_bwd(x["q"], x["k"], x["v"], do, True, scale=w.scale)
+        b = run_bwd(x["q"], x["k"], x["v"], do, True, scale=w.scale)
+    finally:
+        fa.set_option("bwd_deterministic", 0)
+    for g, h in zip(a, b):
+        assert np.array_equal(g, h)
