@@ -8,17 +8,18 @@
 //   dV += P^T dO          dP = dO V^T          dS = s * P * (dP - D),  D = rowsum(dO * O)
 //   dK += dS^T Q          dQ += dS K
 //
-// One CTA of 512 threads owns one block of 128 keys of one (sequence, K/V head)
-// and walks over the 128-row Q tiles that can see it, accumulating dK and dV in
-// tensor memory (section 2 of the same page: TMEM accumulators let several
-// products be in flight). S and P are computed transposed (S^T = K Q^T, keys on
+// A task is one block of 128 keys of one (sequence, K/V head): it walks over the
+// 128-row Q tiles that can see the block, accumulating dK and dV in tensor memory
+// (section 2 of the same page: TMEM accumulators let several products be in
+// flight). CTAs of 512 threads, one per SM, claim the tasks in order and run them
+// back to back (see the kernel). S and P are computed transposed (S^T = K Q^T, keys on
 // the TMEM lanes), so P^T is already the A operand of the dV product, as the page
 // describes. dQ of each (Q tile, key block) pair is added to an fp32 buffer in
 // global memory (section 4: the dQ sum over key blocks is a global atomic
 // accumulation): staged in shared memory and sent as TMA reduce-adds, 16 KB per
-// operation, in place of per-thread atomics. With grouped heads the Q tiles hold the packed (position, query
-// head) rows of the forward, so every query head of the group contributes to the
-// CTA's dK and dV without atomics.
+// operation, in place of per-thread atomics. With grouped heads the Q tiles hold
+// the packed (position, query head) rows of the forward, so every query head of the
+// group contributes to the task's dK and dV without atomics.
 //
 // Roles: WG0 and WG1 (warps 0-7, one thread per key row) compute P and dS for
 // query columns 0-63 and 64-127 of the tile (the LSE is known, so the halves need
@@ -29,8 +30,7 @@
 //
 // Tensor memory (512 columns): dV [0, d), dK [128, 128+d), S^T [256, 384) with P^T
 // as 16-bit pairs over the upper 32 columns of each 64-column half, dP^T [384, 512)
-// -- reused for dQ once
-// dS is in shared memory. Shared memory (226 KB of the 227 KB a CTA may have):
+// -- reused for dQ once dS is in shared memory. Shared memory (226 KB of the 227 KB a CTA may have):
 // K, V, two stages of (Q, dO, LSE, D), and the dS tile (128 keys x 128 rows,
 // 128-byte swizzle): the same bytes are the K-major A operand of dK (M = keys)
 // and the MN-major A operand of dQ (M = rows). Once a step's products are done,
