@@ -114,8 +114,8 @@ __device__ __forceinline__ float half_bits_to_f32(uint16_t x, bool f16) {
 }
 
 // ------------------------------------------------------------------ preprocessing
-// One warp per (query row, head) of the [tokens, H, d] tensors: D = rowsum(dO * O) in
-// fp32 and the forward's LSE in base 2, both written at the row's packed index
+// D / 8 lanes per (query row, head) of the [tokens, H, d] tensors (16-byte loads):
+// D = rowsum(dO * O) in fp32 and the forward's LSE in base 2, both written at the row's packed index
 // (sequence, kv head, position * G + head % G); the row of the fp32 dQ accumulator is
 // zeroed on the way. Fixed length: sequence b holds rows [b * Nq, (b + 1) * Nq) and the
 // LSE is [B, H, Nq]; variable length (cu_q not null): the sequence of a row is found by
@@ -127,44 +127,48 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint16_t* __restr
                                                          float* __restrict__ dsum, float* __restrict__ dq_acc,
                                                          long long tokens, const int* __restrict__ cu_q, int B,
                                                          int H, int gshift, int Nq, int mpad) {
-  constexpr int E = D / 32;   // elements per lane: 4 (d = 128) or 2 (d = 64)
-  const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (w >= tokens * H) return;
+  constexpr int kLanes = D / 8;                // lanes per row: 16-byte loads of 8 elements
+  constexpr int kRowsPerWarp = 32 / kLanes;
   const int lane = threadIdx.x & 31;
-  const int h = (int)(w % H);
-  const long long bp = w / H;
-  int b, pos;
-  size_t li;
-  if (cu_q == nullptr) {
-    b = (int)(bp / Nq);
-    pos = (int)(bp % Nq);
-    li = ((size_t)b * H + h) * Nq + pos;
-  } else {
-    int lo = 0, hi = B;   // the last sequence starting at or before the row
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (cu_q[mid] <= bp) lo = mid; else hi = mid;
-    }
-    b = lo;
-    pos = (int)(bp - cu_q[lo]);
-    li = (size_t)h * tokens + bp;
-  }
-  uint16_t ov[E], gv[E];
-  if constexpr (E == 4) {
-    *reinterpret_cast<uint2*>(ov) = *reinterpret_cast<const uint2*>(o + w * D + lane * E);
-    *reinterpret_cast<uint2*>(gv) = *reinterpret_cast<const uint2*>(dout + w * D + lane * E);
-    *reinterpret_cast<float4*>(dq_acc + w * D + lane * E) = make_float4(0.f, 0.f, 0.f, 0.f);
-  } else {
-    *reinterpret_cast<uint32_t*>(ov) = *reinterpret_cast<const uint32_t*>(o + w * D + lane * E);
-    *reinterpret_cast<uint32_t*>(gv) = *reinterpret_cast<const uint32_t*>(dout + w * D + lane * E);
-    *reinterpret_cast<float2*>(dq_acc + w * D + lane * E) = make_float2(0.f, 0.f);
-  }
+  const long long w = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * kRowsPerWarp + lane / kLanes;
+  const int part = lane % kLanes;
+  const bool valid = w < tokens * H;
   float acc = 0.f;
+  if (valid) {
+    const uint4 ov = *reinterpret_cast<const uint4*>(o + w * D + part * 8);
+    const uint4 gv = *reinterpret_cast<const uint4*>(dout + w * D + part * 8);
+    float4* z = reinterpret_cast<float4*>(dq_acc + w * D + part * 8);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
-  for (int e = 0; e < E; ++e) acc = fmaf(half_bits_to_f32(ov[e], F16), half_bits_to_f32(gv[e], F16), acc);
+    for (int e = 0; e < 4; ++e) {
+      acc = fmaf(half_bits_to_f32((uint16_t)(ow[e] & 0xffffu), F16), half_bits_to_f32((uint16_t)(gw[e] & 0xffffu), F16),
+                 acc);
+      acc = fmaf(half_bits_to_f32((uint16_t)(ow[e] >> 16), F16), half_bits_to_f32((uint16_t)(gw[e] >> 16), F16), acc);
+    }
+  }
 #pragma unroll
-  for (int x = 16; x > 0; x >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, x);
-  if (lane == 0) {
+  for (int x = kLanes / 2; x > 0; x >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, x);
+  if (valid && part == 0) {
+    const int h = (int)(w % H);
+    const long long bp = w / H;
+    int b, pos;
+    size_t li;
+    if (cu_q == nullptr) {
+      b = (int)(bp / Nq);
+      pos = (int)(bp % Nq);
+      li = ((size_t)b * H + h) * Nq + pos;
+    } else {
+      int lo = 0, hi = B;   // the last sequence starting at or before the row
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cu_q[mid] <= bp) lo = mid; else hi = mid;
+      }
+      b = lo;
+      pos = (int)(bp - cu_q[lo]);
+      li = (size_t)h * tokens + bp;
+    }
     const int Hkv = H >> gshift;
     const size_t idx = ((size_t)b * Hkv + (h >> gshift)) * mpad + ((size_t)pos << gshift) + (h & ((1 << gshift) - 1));
     dsum[idx] = acc;

@@ -71,7 +71,8 @@ int pre_post(bool post, const void* o, const void* dout, const float* lse, float
   const long long rows = sh.tokens_q * sh.H;
   if (rows == 0) return FA_OK;
   if (!post) {
-    fa::fa_bwd_pre_kernel<D, F><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
+    const long long rows_per_block = 8LL * (32 / (D / 8));
+    fa::fa_bwd_pre_kernel<D, F><<<(unsigned)((rows + rows_per_block - 1) / rows_per_block), 256, 0, s>>>(
         static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, lse2, dsum, dq_acc, sh.tokens_q,
         sh.cu_q, sh.B, sh.H, sh.gshift, sh.N_q, mpad);
   } else {
