@@ -2,6 +2,7 @@
 gloo backend (replicas only: the ranks share nothing but the barrier around the
 timed region and the maximum of their times)."""
 import os
+import re
 import socket
 import subprocess
 import sys
@@ -44,8 +45,10 @@ def test_two_ranks_over_gloo_barrier_and_max(tmp_path):
            "--master-addr", "127.0.0.1", "--master-port", str(free_port()), str(script)]
     out = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=240)
     assert out.returncode == 0, out.stderr[-2000:]
-    lines = [l for l in out.stdout.splitlines() if l.startswith("rank ")]
-    assert len(lines) == 2, out.stdout
-    for l in lines:
-        assert " max 20.0 " in l, l                  # the maximum over both ranks
-        assert float(l.split("waited ")[1]) >= 0.25 or l.startswith("rank 1"), l   # rank 0 waited at the barrier
+    # the two ranks print concurrently: their lines may interleave
+    found = re.findall(r"rank (\d) max ([0-9.]+) waited ([0-9.]+)", out.stdout)
+    assert sorted(r for r, _, _ in found) == ["0", "1"], out.stdout
+    for rank, mx, waited in found:
+        assert float(mx) == 20.0                      # the maximum over both ranks
+        if rank == "0":
+            assert float(waited) >= 0.25              # rank 0 waited at the barrier for rank 1
