@@ -247,3 +247,26 @@ def test_backward_full_size_deterministic_bits():
         fa.set_option("bwd_deterministic", 0)
     for g, h in zip(a, b):
         assert np.array_equal(g, h)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_scheduling_modes_agree(causal):
+    """Persistent CTAs claiming tasks against one CTA per task, and L2 sections of
+    different sizes: dK and dV (accumulated in tensor memory in a fixed order) are
+    bitwise equal; dQ (added across key blocks in arrival order) agrees within the
+    tolerance."""
+    q, k, v = fa_inputs.make_qkv(2, 700, 8, 128, seed=4500, Hkv=2)
+    do = fa_inputs.make_qkv(2, 700, 8, 128, seed=4501)[0]
+    runs = []
+    for persistent, section in ((-1, 0), (0, 0), (-1, 1), (-1, 3)):
+        fa.set_option("persistent", persistent)
+        fa.set_option("bwd_section", section)
+        try:
+            runs.append(run_bwd(q, k, v, do, causal))
+        finally:
+            fa.set_option("persistent", -1)
+            fa.set_option("bwd_section", 0)
+    ref = oracle.attention_backward(q, k, v, do, 1 / math.sqrt(128), causal)
+    for got in runs:
+        assert np.array_equal(got[1], runs[0][1]) and np.array_equal(got[2], runs[0][2])
+        check(got, ref, f"scheduling causal={causal}")
