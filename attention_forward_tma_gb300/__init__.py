@@ -40,7 +40,7 @@ _SIGNATURES = {
     "fa_bwd": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _ci, _vp],
     "fa_bwd_varlen": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci,
                       _cf, _ci, _ci, _vp],
-    "fa_fwd_kv_splits": [_ci, _ci, _ci, _ci, _ci, _ci, ctypes.POINTER(_ci)],
+    "fa_fwd_kv_splits": [_ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci, ctypes.POINTER(_ci)],
     "fa_fwd_varlen_kv_splits": [_ci, _ci, _ci, _ci, _ci, _ci, ctypes.POINTER(_ci)],
     "fa_fwd_varlen_noalloc": [_vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _vp],
     "fa_error_string": [_ci],
@@ -317,10 +317,13 @@ def lse_combine(o_parts, lse_parts, *, out=None, lse=None, return_lse: bool = Tr
     return (out, lse) if lse is not None else out
 
 
-def num_splits(B: int, H: int, H_kv: int, N_q: int, N_kv: int, requested: int = 0) -> int:
-    """Key ranges fa_fwd would use for these sizes with num_splits=requested (0: the library's choice)."""
+def num_splits(B: int, H: int, H_kv: int, N_q: int, N_kv: int, requested: int = 0, causal: bool = False,
+               d: int = 128) -> int:
+    """Key ranges fa_fwd would use for these sizes, head dimension and mask with num_splits=requested
+    (0: the library's choice)."""
     n = ctypes.c_int(0)
-    _check(library().fa_fwd_kv_splits(B, H, H_kv, N_q, N_kv, requested, ctypes.byref(n)), "fa_fwd_kv_splits")
+    _check(library().fa_fwd_kv_splits(B, H, H_kv, N_q, N_kv, d, int(bool(causal)), requested, ctypes.byref(n)),
+           "fa_fwd_kv_splits")
     return n.value
 
 

@@ -6,6 +6,12 @@
 
 #include <climits>
 #include <cmath>
+#include <functional>
+#include <algorithm>
+#include <queue>
+#include <vector>
+#include <array>
+#include <map>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -103,6 +109,77 @@ constexpr int kMaxSplits = 128;
 // the 2 standing for a task's fixed cost (its Q load, pipeline fill and epilogue), so
 // that the key ranges fill the SMs evenly (64 tasks on 152 SMs: 7 ranges, 448 tasks in
 // three rounds, rather than 2 ranges leaving 24 SMs idle).
+// Fixed length: the estimate runs the tasks through longest-first list scheduling on
+// sm_count SMs, with each task's own key range (a causal task sees only the blocks up
+// to its diagonal; the kernel cuts ranges of ceil(key_blocks / s) blocks, so a short
+// causal task's upper ranges are empty) at (blocks + 2) for a range with keys and 1
+// for an empty one (it writes zero partials), all in units of one K/V block step
+// (about 2 us). With s > 1 it adds the merge: its launch (2.5 units) and the fp32
+// partials written and read back, at HBM speed (about 13 MB per unit). Picks the s
+// with the shortest estimate; cached per shape (a decoding loop asks every step).
+int choose_splits_fixed(int requested, int B, int H, int H_kv, int num_m, int N_q, int N_kv, int d, int gshift,
+                        bool causal, int sm_count) {
+  const int key_blocks = (N_kv + fa::kBlockN - 1) / fa::kBlockN;
+  const int most = key_blocks < 1 ? 1 : (key_blocks < kMaxSplits ? key_blocks : kMaxSplits);
+  if (requested > 0) return requested < most ? requested : most;
+  const long long base = (long long)B * H_kv * num_m;
+  if (base >= sm_count || key_blocks < 2 || sm_count < 1) return 1;
+  static std::mutex mu;
+  static std::map<std::array<long long, 7>, int> cache;
+  const std::array<long long, 7> key{B, (long long)H * 65536 + H_kv, num_m, N_q, N_kv,
+                                     (long long)d * 64 + gshift * 2 + (causal ? 1 : 0), sm_count};
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  // each m's visible block count (the same for every (b, kv head))
+  std::vector<int> nb(num_m);
+  for (int m = 0; m < num_m; ++m) {
+    long long kmax = N_kv;
+    if (causal) {
+      const long long last = ((long long)m * fa::kTaskRows + fa::kTaskRows - 1) >> gshift;
+      kmax = std::min<long long>(last + (N_kv - N_q) + 1, N_kv);
+    }
+    nb[m] = kmax > 0 ? (int)((kmax + fa::kBlockN - 1) / fa::kBlockN) : 0;
+  }
+  const int limit = std::min(64, key_blocks);
+  int best = 1;
+  double best_time = -1.0;
+  std::vector<double> costs;
+  for (int sp = 1; sp <= limit; ++sp) {
+    const int per = (key_blocks + sp - 1) / sp;
+    costs.clear();
+    for (long long bh = 0; bh < (long long)B * H_kv; ++bh)
+      for (int m = 0; m < num_m; ++m)
+        for (int r = 0; r < sp; ++r) {
+          const int len = std::max(0, std::min(nb[m], (r + 1) * per) - r * per);
+          costs.push_back(len > 0 ? len + 2.0 : 1.0);
+        }
+    std::sort(costs.begin(), costs.end(), std::greater<double>());
+    std::priority_queue<double, std::vector<double>, std::greater<double>> load;
+    for (int i = 0; i < sm_count; ++i) load.push(0.0);
+    double makespan = 0.0;
+    for (double c : costs) {
+      const double t = load.top() + c;
+      load.pop();
+      load.push(t);
+      makespan = std::max(makespan, t);
+    }
+    if (sp > 1) {
+      const double partial_bytes = 2.0 * sp * (double)B * N_q * H * d * sizeof(float);
+      makespan += 2.5 + partial_bytes / 13e6;
+    }
+    if (best_time < 0 || makespan < best_time - 1e-9) {
+      best_time = makespan;
+      best = sp;
+    }
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  cache[key] = best;
+  return best;
+}
+
 int choose_splits(int requested, long long base_tasks, int key_blocks, int sm_count) {
   const int most = key_blocks < 1 ? 1 : (key_blocks < kMaxSplits ? key_blocks : kMaxSplits);
   if (requested > 0) return requested < most ? requested : most;
@@ -133,7 +210,7 @@ struct Partials {
     const size_t o_bytes = splits > 0 ? (size_t)splits * (size_t)rows * d * sizeof(float) : 0;
     const size_t l_bytes = splits > 0 ? ((size_t)splits * (size_t)rows * sizeof(float) + 255) / 256 * 256 : 0;
     if (head_bytes + o_bytes + l_bytes == 0) return FA_OK;
-    if (cudaMallocAsync(&base, head_bytes + o_bytes + l_bytes, s) != cudaSuccess) {
+    if (fa_host::alloc_async(&base, head_bytes + o_bytes + l_bytes, s) != cudaSuccess) {
       cudaGetLastError();
       base = nullptr;
       return FA_ERR_CUDA;
@@ -388,6 +465,41 @@ bool bwd_deterministic() { return g_opt.bwd_deterministic != 0; }
 int bwd_section_override() { return g_opt.bwd_section; }
 int persistent_mode() { return g_opt.persistent; }
 unsigned long long wait_timeout_ns() { return g_opt.timeout_ns; }
+
+// The library's stream-ordered memory pool on the current device: unlike the default
+// pool (release threshold 0, so its memory goes back to the system at every
+// synchronisation and the next call maps it again, ~100 us), it keeps what it has
+// allocated for the next call.
+cudaError_t alloc_async(void** ptr, size_t bytes, cudaStream_t s) {
+  static std::mutex mu;
+  static cudaMemPool_t pools[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaMemPool_t pool = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (pools[dev] == nullptr) {
+      cudaMemPoolProps props;
+      std::memset(&props, 0, sizeof props);
+      props.allocType = cudaMemAllocationTypePinned;
+      props.handleTypes = cudaMemHandleTypeNone;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      cudaMemPool_t created = nullptr;
+      if ((e = cudaMemPoolCreate(&created, &props)) != cudaSuccess) return e;
+      uint64_t keep = UINT64_MAX;
+      if ((e = cudaMemPoolSetAttribute(created, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess) {
+        cudaMemPoolDestroy(created);
+        return e;
+      }
+      pools[dev] = created;
+    }
+    pool = pools[dev];
+  }
+  return cudaMallocFromPoolAsync(ptr, bytes, pool, s);
+}
 }  // namespace fa_host
 
 // ------------------------------------------------------------------ C ABI
@@ -479,7 +591,8 @@ int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, 
   // tasks of 256 packed rows; a (b, kv head) has N_q * G rows
   p.num_m = (int)((((long long)N_q << gshift) + fa::kTaskRows - 1) / fa::kTaskRows);
   const long long base_tasks = (long long)B * H_kv * p.num_m;
-  p.splits = choose_splits(num_splits, base_tasks, (N_kv + fa::kBlockN - 1) / fa::kBlockN, dev->sm_count);
+  p.splits =
+      choose_splits_fixed(num_splits, B, H, H_kv, p.num_m, N_q, N_kv, d, gshift, causal != 0, dev->sm_count);
   const long long ntask = base_tasks * p.splits;
   if (ntask > INT_MAX) return FA_ERR_INVALID_ARG;
   p.num_tasks = (int)ntask;
@@ -629,16 +742,19 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
                            FA_DTYPE_BF16, stream);
 }
 
-int fa_fwd_kv_splits(int B, int H, int H_kv, int N_q, int N_kv, int num_splits, int* splits) {
+int fa_fwd_kv_splits(int B, int H, int H_kv, int N_q, int N_kv, int d, int causal, int num_splits, int* splits) {
   if (!splits || B <= 0 || H <= 0 || H_kv <= 0 || N_q <= 0 || N_kv <= 0 || num_splits < 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   int gshift = 0;
   int st = check_heads(H, H_kv, &gshift);
   if (st != FA_OK) return st;
   DevInfo* dev = nullptr;
   if ((st = device_info(&dev)) != FA_OK) return st;
   const long long num_m = (((long long)N_q << gshift) + fa::kTaskRows - 1) / fa::kTaskRows;
-  *splits = choose_splits(num_splits, (long long)B * H_kv * num_m, (N_kv + fa::kBlockN - 1) / fa::kBlockN,
-                          dev->sm_count);
+  if ((long long)B * H_kv * num_m > INT_MAX) return FA_ERR_INVALID_ARG;
+  *splits = choose_splits_fixed(num_splits, B, H, H_kv, (int)num_m, N_q, N_kv, d, gshift, causal != 0,
+                                dev->sm_count);
   return FA_OK;
 }
 

@@ -130,7 +130,7 @@ int bwd_run(const void* q, const void* k, const void* v, const void* o, const vo
   const int ntiles = (int)(mpad / 128);
   const size_t sem_bytes = (det ? ((size_t)sh.B * sh.H_kv * ntiles * sizeof(int) + 255) / 256 * 256 : 0) + 256;
   void* ws = nullptr;
-  if (cudaMallocAsync(&ws, acc_bytes + 2 * vec_bytes + sem_bytes, s) != cudaSuccess) {
+  if (fa_host::alloc_async(&ws, acc_bytes + 2 * vec_bytes + sem_bytes, s) != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_CUDA;
   }

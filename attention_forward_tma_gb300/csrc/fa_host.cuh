@@ -91,6 +91,9 @@ void trace_target(unsigned long long** buf, int* ctas);
 bool bwd_deterministic();
 int bwd_section_override();   // > 0: pairs per L2 section of the backward grid (tests, tuning)
 int persistent_mode();        // FA_OPT_PERSISTENT (-1 = the default)
+// Stream-ordered allocation from the library's own pool on the current device (memory
+// kept between calls); free with cudaFreeAsync.
+cudaError_t alloc_async(void** ptr, size_t bytes, cudaStream_t s);
 unsigned long long wait_timeout_ns();
 
 }  // namespace fa_host

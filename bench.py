@@ -380,7 +380,7 @@ def run_ours(a, dist):
 
         def step(s=None):
             fa.fa_fwd(q, k, v, scale=w.scale, causal=w.causal, out=o, lse=lse, num_splits=w.splits, stream=s)
-        splits = fa.num_splits(w.B, w.H, w.Hkv, w.N, w.Nk, w.splits)
+        splits = fa.num_splits(w.B, w.H, w.Hkv, w.N, w.Nk, w.splits, causal=w.causal, d=w.d)
         launches_per_step = 1 + (1 if splits > 1 else 0)   # attention (, merge)
 
     stream = torch.cuda.current_stream(dev)

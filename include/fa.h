@@ -105,7 +105,8 @@ int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
  *   cannot fill the GPU); larger values are capped at the number of key blocks
  *   and at 128. With more than one range, partial results live in a temporary
  *   buffer of num_splits * B * N_q * H * (d + 1) * 4 bytes from the
- *   stream-ordered allocator (cudaMallocAsync / cudaFreeAsync on `stream`).
+ *   library's stream-ordered memory pool (cudaMallocFromPoolAsync / cudaFreeAsync on
+ *   `stream`; the pool keeps its memory between calls).
  * Other arguments and errors as for fa_fwd_gqa.
  */
 int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -125,8 +126,9 @@ int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse,
  * Work tiles are ordered longest-first by a small schedule kernel launched on
  * the same stream ("FlashAttention-4（下）" (argus lesson 7), section "6. LPT 调度":
  * a pre-kernel sorts work tiles by their cost). Its tile list lives in a
- * temporary device buffer taken from the stream-ordered allocator
- * (cudaMallocAsync / cudaFreeAsync on `stream`).
+ * temporary device buffer taken from the library's stream-ordered memory pool
+ * (cudaMallocFromPoolAsync / cudaFreeAsync on `stream`; the pool keeps its memory
+ * between calls).
  * The contents of cu_seqlens are trusted (they are on the device): lengths
  * above max_seqlen or a total other than total_tokens are not detected.
  */
@@ -168,10 +170,13 @@ int fa_fwd_varlen_kv(const void* q, const void* k, const void* v, void* o, float
 
 /*
  * The number of key ranges fa_fwd_kv / fa_fwd_varlen_kv would use for these
- * sizes on the current device, given the same num_splits argument (0 = the
- * library's choice). With *splits > 1 a call launches the merge kernel too.
+ * sizes (and, fixed length, this head dimension and mask: causal 0 or 1) on the
+ * current device, given the same num_splits argument (0 = the library's choice:
+ * for fixed length the count whose longest-first schedule of the tasks' key ranges
+ * on the SMs, plus the merge of the partial results, is estimated shortest). With
+ * *splits > 1 a call launches the merge kernel too.
  */
-int fa_fwd_kv_splits(int B, int H, int H_kv, int N_q, int N_kv, int num_splits, int* splits);
+int fa_fwd_kv_splits(int B, int H, int H_kv, int N_q, int N_kv, int d, int causal, int num_splits, int* splits);
 int fa_fwd_varlen_kv_splits(int num_seqs, int total_q, int max_seqlen_kv, int H, int H_kv, int num_splits,
                             int* splits);
 
@@ -233,8 +238,8 @@ int fa_fwd_varlen_noalloc(const void* q, const void* k, const void* v, void* o, 
  * its last bits may differ from run to run unless FA_OPT_BWD_DETERMINISTIC is set;
  * dK and dV are always deterministic. A temporary buffer of B*N_q*H*d*4 +
  * 2*B*H_kv*ceil(N_q*G/128)*128*4 + 256 bytes (+ 4 bytes per 128-row Q tile in the
- * deterministic mode) comes from the stream-ordered allocator (cudaMallocAsync /
- * cudaFreeAsync on `stream`). One CTA per SM walks the tasks (key block of a
+ * deterministic mode) comes from the library's stream-ordered memory pool
+ * (cudaMallocFromPoolAsync / cudaFreeAsync on `stream`; memory kept between calls). One CTA per SM walks the tasks (key block of a
  * (batch, K/V head) pair) in order, claiming the next from a counter in that buffer.
  */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
@@ -258,7 +263,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
  *   other arguments as for fa_bwd. Errors: as fa_bwd, plus FA_ERR_INVALID_ARG for null
  *   or misaligned cu_seqlens, num_seqs, totals or maxima <= 0. The temporary buffer is
  *   total_q*H*d*4 + 2*num_seqs*H_kv*ceil(max_seqlen_q*G/128)*128*4 bytes (+ the
- *   deterministic mode's counters), from the stream-ordered allocator.
+ *   deterministic mode's counters), from the library's stream-ordered memory pool.
  */
 int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                   void* dq, void* dk, void* dv, const int* cu_seqlens_q, const int* cu_seqlens_kv, int num_seqs,

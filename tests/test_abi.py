@@ -200,6 +200,17 @@ def test_bwd_varlen_rejects_invalid_arguments(kw):
     assert bwd_varlen(**kw) == fa.FA_ERR_INVALID_ARG
 
 
+def test_split_queries_reject_invalid_arguments():
+    lib = fa.library()
+    n = ctypes.c_int(0)
+    assert lib.fa_fwd_kv_splits(1, 8, 2, 100, 100, 128, 2, 0, ctypes.byref(n)) == fa.FA_ERR_INVALID_ARG  # causal 2
+    assert lib.fa_fwd_kv_splits(1, 8, 2, 100, 100, 128, 1, -1, ctypes.byref(n)) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_fwd_kv_splits(1, 8, 2, 0, 100, 128, 1, 0, ctypes.byref(n)) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_fwd_kv_splits(1, 8, 2, 100, 100, 128, 1, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_fwd_kv_splits(1, 8, 2, 100, 100, 96, 1, 0, ctypes.byref(n)) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_fwd_varlen_kv_splits(0, 10, 100, 8, 2, 0, ctypes.byref(n)) == fa.FA_ERR_INVALID_ARG
+
+
 def test_new_entry_points_reject_unsupported_head_dim():
     assert bwd(d=96) == fa.FA_ERR_UNSUPPORTED
     assert bwd_varlen(d=256) == fa.FA_ERR_UNSUPPORTED
