@@ -17,6 +17,7 @@ import threading
 from . import _build
 
 __all__ = ["fa_fwd", "fa_fwd_varlen", "fa_bwd", "fa_bwd_varlen", "lse_combine", "num_splits", "num_splits_varlen", "FaError", "set_option", "last_device_status", "library",
+           "release_cached_memory",
            "FA_DTYPE_BF16", "FA_DTYPE_FP16",
            "selftest_mma_tile", "selftest_exp2", "selftest_wait_timeout", "varlen_schedule",
            "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
@@ -47,6 +48,7 @@ _SIGNATURES = {
     "fa_last_device_status": [_vp, ctypes.POINTER(ctypes.c_ulonglong)],
     "fa_set_option": [_ci, ctypes.c_double],
     "fa_version": [],
+    "fa_release_cached_memory": [],
     "fa_selftest_mma_tile": [_vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _vp],
     "fa_selftest_exp2": [_vp, _vp, _ci, _ci, _vp],
     "fa_selftest_wait_timeout": [ctypes.c_ulonglong, _vp],
@@ -341,6 +343,12 @@ def last_device_status(stream=None):
     word = ctypes.c_ulonglong(0)
     st = library().fa_last_device_status(_stream_handle(stream, torch.device("cuda")), ctypes.byref(word))
     return st, word.value
+
+
+def release_cached_memory() -> None:
+    """Return the library's cached temporary memory (split partials, varlen tile lists,
+    backward workspaces) to the system; call after synchronising the streams it ran on."""
+    _check(library().fa_release_cached_memory(), "release_cached_memory")
 
 
 def selftest_mma_tile(q, k, v, p, stream=None):

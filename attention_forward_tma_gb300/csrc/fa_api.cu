@@ -470,17 +470,18 @@ unsigned long long wait_timeout_ns() { return g_opt.timeout_ns; }
 // pool (release threshold 0, so its memory goes back to the system at every
 // synchronisation and the next call maps it again, ~100 us), it keeps what it has
 // allocated for the next call.
+std::mutex g_pool_mu;
+cudaMemPool_t g_pools[kMaxDevices] = {};
+
 cudaError_t alloc_async(void** ptr, size_t bytes, cudaStream_t s) {
-  static std::mutex mu;
-  static cudaMemPool_t pools[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   cudaMemPool_t pool = nullptr;
   {
-    std::lock_guard<std::mutex> lk(mu);
-    if (pools[dev] == nullptr) {
+    std::lock_guard<std::mutex> lk(g_pool_mu);
+    if (g_pools[dev] == nullptr) {
       cudaMemPoolProps props;
       std::memset(&props, 0, sizeof props);
       props.allocType = cudaMemAllocationTypePinned;
@@ -494,11 +495,21 @@ cudaError_t alloc_async(void** ptr, size_t bytes, cudaStream_t s) {
         cudaMemPoolDestroy(created);
         return e;
       }
-      pools[dev] = created;
+      g_pools[dev] = created;
     }
-    pool = pools[dev];
+    pool = g_pools[dev];
   }
   return cudaMallocFromPoolAsync(ptr, bytes, pool, s);
+}
+
+cudaError_t release_pools() {
+  std::lock_guard<std::mutex> lk(g_pool_mu);
+  for (cudaMemPool_t pool : g_pools)
+    if (pool != nullptr) {
+      const cudaError_t e = cudaMemPoolTrimTo(pool, 0);
+      if (e != cudaSuccess) return e;
+    }
+  return cudaSuccess;
 }
 }  // namespace fa_host
 
@@ -506,6 +517,14 @@ cudaError_t alloc_async(void** ptr, size_t bytes, cudaStream_t s) {
 extern "C" {
 
 int fa_version(void) { return 100; }
+
+int fa_release_cached_memory(void) {
+  if (fa_host::release_pools() != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
 
 const char* fa_error_string(int status) {
   switch (status) {

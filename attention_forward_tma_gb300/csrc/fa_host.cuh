@@ -94,6 +94,8 @@ int persistent_mode();        // FA_OPT_PERSISTENT (-1 = the default)
 // Stream-ordered allocation from the library's own pool on the current device (memory
 // kept between calls); free with cudaFreeAsync.
 cudaError_t alloc_async(void** ptr, size_t bytes, cudaStream_t s);
+// Trim the pools of alloc_async to what pending allocations still need.
+cudaError_t release_pools();
 unsigned long long wait_timeout_ns();
 
 }  // namespace fa_host

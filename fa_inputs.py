@@ -20,6 +20,11 @@ Recipe (the same bytes go to the GPU and to the oracle):
   draws are the same with the K/V shapes changed;
 * fp16 inputs: the same float32 draws rounded to IEEE binary16 (numpy's
   correctly rounded float32 -> float16 conversion, ties to even).
+* tiled tensors (the maximum-size tests, whose tensors of 2^31 elements are too large
+  to draw on the host): a table of ``TILE_ROWS`` (a prime) rows drawn as above from
+  one seed; row r of the tensor, r the flat index over its leading dimensions in
+  order, is table row (r * ``TILE_MULT``) mod ``TILE_ROWS``. The device copy is
+  built by gathering table rows on the GPU, and any row can be rebuilt on the host.
 """
 from __future__ import annotations
 
@@ -190,6 +195,38 @@ def _pack_varlen(rng, lengths, H, d, Hkv=None, dtype="bf16"):
     k = _normal(rng, (T, Hkv, d), dtype)
     v = _normal(rng, (T, Hkv, d), dtype)
     return lengths, cu, q, k, v
+
+
+TILE_ROWS = 4099      # a prime, so the multiplier below visits every table row
+TILE_MULT = 40503
+
+
+def make_row_table(d: int, seed: int, dtype: str = "bf16") -> np.ndarray:
+    """The table [TILE_ROWS, d] (16-bit bit patterns) that a tiled tensor's rows come from."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return _normal(rng, (TILE_ROWS, d), dtype)
+
+
+def tiled_row_ids(r) -> np.ndarray:
+    """Table row of each flat row index r of a tiled tensor."""
+    return (np.asarray(r, dtype=np.int64) * TILE_MULT) % TILE_ROWS
+
+
+def tiled_rows(table: np.ndarray, r) -> np.ndarray:
+    """Rows r of the tiled tensor built from table (host copy, 16-bit bit patterns)."""
+    return table[tiled_row_ids(r)]
+
+
+def tiled_tensor_cuda(table: np.ndarray, shape, dtype: str = "bf16"):
+    """The whole tiled tensor of the given shape (its last dimension the table's width),
+    gathered on the current CUDA device as a torch tensor of the 16-bit type."""
+    import torch
+    rows = math.prod(shape[:-1])
+    t = torch.from_numpy(np.ascontiguousarray(table).view(np.int16)).cuda()
+    ids = (torch.arange(rows, dtype=torch.int64, device=t.device) * TILE_MULT) % TILE_ROWS
+    out = t[ids].view(*shape)
+    del ids
+    return out.view(torch.float16 if dtype == "f16" else torch.bfloat16)
 
 
 def make_workload(w: Workload):

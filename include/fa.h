@@ -327,6 +327,19 @@ enum { FA_OPT_TAU = 1, FA_OPT_WAIT_TIMEOUT_NS = 2, FA_OPT_PERSISTENT = 3, FA_OPT
        FA_OPT_BWD_SECTION = 8 };
 int fa_set_option(int option, double value);
 
+/*
+ * Hand the library's cached temporary memory back to the system. The split
+ * partials, the varlen tile list and the backward's workspace come from a
+ * stream-ordered pool that keeps its memory between calls (so that a caller
+ * which synchronises every step does not map it again each time); after a very
+ * large call that can be gigabytes (the backward's fp32 dQ accumulator is
+ * 4 * B * N_q * H * d bytes). This releases, on every device the library has
+ * used, the pool memory not backing an allocation still pending on a stream:
+ * call it once the streams that ran the library's calls have been synchronised.
+ * Returns FA_OK (also when no pool exists yet), or FA_ERR_CUDA.
+ */
+int fa_release_cached_memory(void);
+
 /* Library version, as major*10000 + minor*100 + patch. */
 int fa_version(void);
 

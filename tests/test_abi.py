@@ -45,6 +45,13 @@ def test_error_strings_and_version():
     assert lib.fa_version() >= 100
 
 
+def test_release_cached_memory_without_a_pool():
+    """No call has allocated from the library's pool in this process: nothing to release,
+    and no CUDA call is made."""
+    assert fa.library().fa_release_cached_memory() == fa.FA_OK
+    fa.release_cached_memory()
+
+
 NULL = None
 
 
