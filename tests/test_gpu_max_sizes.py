@@ -147,3 +147,63 @@ def test_backward_multi_head_2e31_elements(cuda, tables):
         check_grad(host(dq[b, :W, h]), rq[0, :, 0], f"dQ head batch {b} head {h}")
     del q, k, v, do, dq, dk, dv
     torch.cuda.empty_cache()
+
+
+def test_varlen_forward_and_backward_beyond_2e31_elements(cuda, tables):
+    """Packed sequences of 131072, 1, 65535 and 300 positions with H = 128, H_kv = 1:
+    Q, O, dO and dQ of 3.2 * 10^9 elements (6 GiB each), the LSE [H, T] of 2.5 * 10^7
+    entries. Forward rows at both ends of every sequence; backward: dQ of the long
+    sequence's last 128 positions, and every gradient of the last sequence in memory."""
+    torch = cuda
+    lengths = [131072, 1, 65535, 300]
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    T, H, d = int(cu[-1]), 128, 128
+    cu_d = torch.from_numpy(cu).cuda()
+    q, do = (fa_inputs.tiled_tensor_cuda(tables[x], (T, H, d)) for x in ("q", "do"))
+    k, v = (fa_inputs.tiled_tensor_cuda(tables[x], (T, 1, d)) for x in ("k", "v"))
+    assert q.numel() > 2 ** 31
+    o, lse = fa.fa_fwd_varlen(q, k, v, cu_d, max(lengths), causal=True)
+    st, word = fa.last_device_status()
+    assert st == fa.FA_OK, hex(word)
+    scale = 1 / math.sqrt(d)
+    heads = np.array([0, 127])
+    hi = torch.from_numpy(heads).cuda()
+
+    def seq_rows(name, s, p0, p1, heads_of_row):
+        """rows [p0, p1) of sequence s, every head, as [1, p1 - p0, heads_of_row, d]"""
+        t = cu[s] + np.arange(p0, p1, dtype=np.int64)
+        r = t[:, None] * heads_of_row + np.arange(heads_of_row)[None, :]
+        return fa_inputs.tiled_rows(tables[name], r)[None]
+
+    for s, L in enumerate(lengths):
+        ks, vs = seq_rows("k", s, 0, L, 1), seq_rows("v", s, 0, L, 1)
+        for p in sorted({0, L - 1}):
+            qt = seq_rows("q", s, p, p + 1, H)
+            rows = np.stack([np.zeros_like(heads), heads, np.zeros_like(heads)], axis=1)
+            o_ref, l_ref = oracle.attention_rows(qt, ks[:, :p + 1], vs[:, :p + 1], rows, scale, True)
+            t = int(cu[s]) + p
+            check_rows(host(o[t, hi]), host(lse[hi, t]), o_ref, l_ref, f"sequence {s} position {p}")
+
+    dq, dk, dv = fa.fa_bwd_varlen(q, k, v, o, do, lse, cu_d, max(lengths), causal=True)
+    st, word = fa.last_device_status()
+    assert st == fa.FA_OK, hex(word)
+    del o, lse
+    # the long sequence: dQ of its last W positions, head by head (a query head's dQ
+    # needs only its own rows and the sequence's keys)
+    L, W = lengths[0], 128
+    ks, vs = seq_rows("k", 0, 0, L, 1), seq_rows("v", 0, 0, L, 1)
+    qt, dot = seq_rows("q", 0, L - W, L, H), seq_rows("do", 0, L - W, L, H)
+    for h in heads:
+        rq, _, _ = oracle.attention_backward(qt[:, :, h:h + 1], ks, vs, dot[:, :, h:h + 1], scale, True)
+        check_grad(host(dq[L - W:L, h]), rq[0, :, 0], f"dQ tail of sequence 0 head {h}")
+    # the last sequence: all heads, all gradients
+    s = len(lengths) - 1
+    a, e = int(cu[s]), int(cu[s + 1])
+    ref = oracle.attention_backward(seq_rows("q", s, 0, e - a, H), seq_rows("k", s, 0, e - a, 1),
+                                    seq_rows("v", s, 0, e - a, 1), seq_rows("do", s, 0, e - a, H), scale, True)
+    for name, got, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        check_grad(host(got[a:e]), r[0], f"{name} of sequence {s}")
+    del q, k, v, do, dq, dk, dv
+    torch.cuda.synchronize()
+    fa.release_cached_memory()
+    torch.cuda.empty_cache()
