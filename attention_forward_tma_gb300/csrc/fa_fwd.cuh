@@ -794,6 +794,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       }
       const int row_limit = CAUSAL ? min(pos + off + 1, tk.lenk) : tk.lenk;  // keys [0, row_limit) visible
       float row_max = -INFINITY, row_sum = 0.f;
+#ifdef FA_TRACE
+      uint32_t n_upd = 0, n_resc = 0;   // this row's later-block updates and O rescales
+#endif
       for (int i = 0; i < nb; ++i) {
         const int j = hi - 1 - i;
         if (!w.wait(bar(L::bSFull + t), s_par, L::bSFull + t, j)) { ok = false; break; }
@@ -865,6 +868,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             ref = cand;
             acc = ex2_approx(delta);
           }
+#ifdef FA_TRACE
+          ++n_upd;
+          n_resc += (row_max != -INFINITY && acc < 1.f) ? 1u : 0u;
+#endif
         }
         row_max = ref;
         // hand acc_scale to WG2 now, so the O rescale runs while P is computed
@@ -943,6 +950,17 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         const float ref_safe = row_max == -INFINITY ? 0.f : row_max;
         store_lse(row_sum > 0.f ? (lg2_approx(row_sum) + ref_safe * sl2) * 0.69314718055994531f : -INFINITY);
       }
+#ifdef FA_TRACE
+      // every CTA: row updates and rescales summed into the two words after the stamps
+      if (p.trace != nullptr) {
+        const uint32_t u = __reduce_add_sync(0xffffffffu, n_upd), rs = __reduce_add_sync(0xffffffffu, n_resc);
+        if (lane == 0 && u != 0) {
+          unsigned long long* tot = p.trace + (size_t)p.trace_ctas * kTraceRoles * kTraceSlots;
+          atomicAdd(tot, (unsigned long long)u);
+          atomicAdd(tot + 1, (unsigned long long)rs);
+        }
+      }
+#endif
     }
   } else if (warp < 12) {
     // ================================================================ correction + epilogue (WG2)

@@ -27,9 +27,14 @@ EVENTS = {1: "Q0", 2: "K", 3: "Q1", 4: "V", 10: "S0", 11: "S1", 12: "PO0", 13: "
 ROLES = ["producer", "mma", "softmax0", "softmax1", "correction"]
 
 
+last_rescales = (0, 0)   # forward of the last capture(): (row updates from later key blocks, rescales)
+
+
 def capture(run, ctas: int = 2):
     """Call run() (which launches fa_fwd / fa_fwd_varlen) with tracing on; return decoded events
-    as {cta: {role: [(clock, event, block), ...]}}."""
+    as {cta: {role: [(clock, event, block), ...]}}. For the forward, last_rescales then
+    holds the softmax rows' updates from a later key block over every CTA and how many of
+    them moved the row's reference (an O rescale under the delayed-rescale rule)."""
     import ctypes
 
     import numpy as np
@@ -39,7 +44,8 @@ def capture(run, ctas: int = 2):
     lib = library()
     roles, slots = ctypes.c_int(), ctypes.c_int()
     lib.fa_trace_layout(ctypes.byref(roles), ctypes.byref(slots))
-    buf = torch.zeros(ctas * roles.value * slots.value, dtype=torch.int64, device="cuda")
+    stamps = ctas * roles.value * slots.value
+    buf = torch.zeros(stamps + 2, dtype=torch.int64, device="cuda")   # + the forward's rescale counters
     st = lib.fa_trace_configure(buf.data_ptr(), ctas)
     if st != 0:
         raise RuntimeError(f"fa_trace_configure failed with status {st} (not a tracing build?)")
@@ -48,7 +54,10 @@ def capture(run, ctas: int = 2):
         torch.cuda.synchronize()
     finally:
         lib.fa_trace_configure(None, 0)
-    raw = buf.cpu().numpy().view(np.uint64).reshape(ctas, roles.value, slots.value)
+    words = buf.cpu().numpy().view(np.uint64)
+    global last_rescales
+    last_rescales = (int(words[stamps]), int(words[stamps + 1]))
+    raw = words[:stamps].reshape(ctas, roles.value, slots.value)
     out = {}
     for c in range(ctas):
         out[c] = {}
@@ -191,6 +200,10 @@ def main():
     if a.json:
         with open(a.json, "w") as f:
             json.dump({str(c): r for c, r in tr.items()}, f)
+    if a.which == "fwd":
+        upd, resc = last_rescales
+        print(f"row updates from a later key block: {upd}, of which rescaled O (tau = 8): {resc} "
+              f"({100.0 * resc / max(upd, 1):.3f} %)")
     for c, d in (summarize_bwd(tr) if a.which == "bwd" else summarize(tr)).items():
         print(f"CTA {c}")
         for key, val in d.items():

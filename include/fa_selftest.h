@@ -59,7 +59,10 @@ int fa_varlen_schedule(const int* cu_seqlens_q, const int* cu_seqlens_kv, int nu
  * off. Per role, word 0 is the number of events, then each event is two
  * words: the SM clock and (event code << 32 | K/V block index). Roles:
  * 0 TMA producer, 1 MMA issuer, 2 softmax of Q tile 0, 3 softmax of Q tile 1,
- * 4 correction/epilogue. The buffer must hold ctas * roles * slots words.
+ * 4 correction/epilogue. The forward also adds, over every CTA, the softmax rows'
+ * updates from a later key block (word ctas * roles * slots) and those of them that
+ * moved the row's reference and rescaled O (the word after it). The buffer must hold
+ * ctas * roles * slots + 2 words, zeroed by the caller.
  * fa_trace_layout reports roles and slots per role (works in both builds).
  */
 int fa_trace_configure(void* buf, int ctas);
