@@ -114,6 +114,28 @@ def test_split_and_unsplit_agree_closely():
     assert np.abs(a[1] - b[1]).max() <= 1e-4
 
 
+def test_release_cached_memory_between_calls():
+    """The split partials come from the library's pool, which keeps them between calls;
+    fa_release_cached_memory hands them back (device free memory grows by at least the
+    partials' size) and the next call allocates afresh with the same result."""
+    import torch
+    q, k, v = fa_inputs.make_qkv(1, 4096, 32, 128, seed=93, Nkv=8192, Hkv=8)
+    qd, kd, vd = dev(q), dev(k), dev(v)
+    splits = 8
+    partial_bytes = splits * 4096 * 32 * (128 + 1) * 4      # fp32 O and LSE per key range
+    a = fa.fa_fwd(qd, kd, vd, causal=True, num_splits=splits)
+    torch.cuda.synchronize()
+    free_kept = torch.cuda.mem_get_info()[0]
+    fa.release_cached_memory()
+    free_released = torch.cuda.mem_get_info()[0]
+    assert free_released - free_kept >= partial_bytes
+    b = fa.fa_fwd(qd, kd, vd, causal=True, num_splits=splits)
+    st, word = fa.last_device_status()
+    assert st == fa.FA_OK, hex(word)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    fa.release_cached_memory()
+
+
 def test_spiky_scores_with_splits():
     """Large score gaps across ranges: each range has its own reference, the merge rescales."""
     q, k, v = fa_inputs.make_qkv(1, 200, 4, 128, seed=20264, spiky=True, Nkv=3000)
