@@ -26,7 +26,7 @@ __all__ = ["fa_fwd", "fa_fwd_varlen", "fa_bwd", "fa_bwd_varlen", "lse_combine", 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_NO_DEVICE, FA_ERR_CAPACITY = range(7)
 FA_DTYPE_BF16, FA_DTYPE_FP16 = 0, 1
 _OPTIONS = {"tau": 1, "wait_timeout_ns": 2, "persistent": 3, "exp2_emulation": 4, "bwd_deterministic": 5,
-            "softmax_stagger": 6, "stats_tmem": 7, "bwd_section": 8}
+            "softmax_stagger": 6, "stats_tmem": 7, "bwd_section": 8, "solo_tiles": 9}
 
 _vp, _ci, _cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 _SIGNATURES = {
@@ -94,7 +94,8 @@ def _check(status: int, what: str):
 
 def set_option(name: str, value: float) -> None:
     """Process-wide knobs: tau, wait_timeout_ns, persistent (-1/0/1/2), exp2_emulation (0..8),
-    bwd_deterministic, softmax_stagger, stats_tmem (0/1), bwd_section (0 = automatic)."""
+    bwd_deterministic, softmax_stagger, stats_tmem (0/1), bwd_section (0 = automatic),
+    solo_tiles (-1 = automatic, 0, 1)."""
     _check(library().fa_set_option(_OPTIONS[name], float(value)), f"set_option({name})")
 
 

@@ -36,6 +36,7 @@ struct Options {
   int stagger = 0;
   int stats_tmem = 1;
   int bwd_section = 0;
+  int solo = -1;         // -1: the library's choice
 };
 Options g_opt;
 
@@ -49,8 +50,8 @@ struct DevInfo {
   bool supported = false;
   int sm_count = 0;
   long long l2_bytes = 0;
-  bool attr_done[2][2][2][2] = {};   // [d == 128][causal][emulation][fp16]
-  int attr_status[2][2][2][2] = {};
+  bool attr_done[2][2][2][2][2] = {};   // [d == 128][causal][emulation][fp16][solo]
+  int attr_status[2][2][2][2][2] = {};
 };
 constexpr int kMaxDevices = 64;
 DevInfo g_dev[kMaxDevices];
@@ -117,8 +118,8 @@ constexpr int kMaxSplits = 128;
 // (about 2 us). With s > 1 it adds the merge: its launch (2.5 units) and the fp32
 // partials written and read back, at HBM speed (about 13 MB per unit). Picks the s
 // with the shortest estimate; cached per shape (a decoding loop asks every step).
-int choose_splits_fixed(int requested, int B, int H, int H_kv, int num_m, int N_q, int N_kv, int d, int gshift,
-                        bool causal, int sm_count) {
+int choose_splits_fixed(int requested, int B, int H, int H_kv, int num_m, int task_rows, int N_q, int N_kv, int d,
+                        int gshift, bool causal, int sm_count) {
   const int key_blocks = (N_kv + fa::kBlockN - 1) / fa::kBlockN;
   const int most = key_blocks < 1 ? 1 : (key_blocks < kMaxSplits ? key_blocks : kMaxSplits);
   if (requested > 0) return requested < most ? requested : most;
@@ -126,7 +127,7 @@ int choose_splits_fixed(int requested, int B, int H, int H_kv, int num_m, int N_
   if (base >= sm_count || key_blocks < 2 || sm_count < 1) return 1;
   static std::mutex mu;
   static std::map<std::array<long long, 7>, int> cache;
-  const std::array<long long, 7> key{B, (long long)H * 65536 + H_kv, num_m, N_q, N_kv,
+  const std::array<long long, 7> key{B, (long long)H * 65536 + H_kv, (long long)num_m * 1024 + task_rows, N_q, N_kv,
                                      (long long)d * 64 + gshift * 2 + (causal ? 1 : 0), sm_count};
   {
     std::lock_guard<std::mutex> lk(mu);
@@ -138,7 +139,7 @@ int choose_splits_fixed(int requested, int B, int H, int H_kv, int num_m, int N_
   for (int m = 0; m < num_m; ++m) {
     long long kmax = N_kv;
     if (causal) {
-      const long long last = ((long long)m * fa::kTaskRows + fa::kTaskRows - 1) >> gshift;
+      const long long last = ((long long)m * task_rows + task_rows - 1) >> gshift;
       kmax = std::min<long long>(last + (N_kv - N_q) + 1, N_kv);
     }
     nb[m] = kmax > 0 ? (int)((kmax + fa::kBlockN - 1) / fa::kBlockN) : 0;
@@ -178,6 +179,20 @@ int choose_splits_fixed(int requested, int B, int H, int H_kv, int num_m, int N_
   std::lock_guard<std::mutex> lk(mu);
   cache[key] = best;
   return best;
+}
+
+// Packed rows per fixed-length task: 256 (two Q tiles sharing each K/V block), or 128
+// ("solo": one Q tile whose score tile alternates between S_0 and S_1, so that each
+// block's QK^T overlaps the previous block's softmax) when the 256-row tasks leave SMs
+// idle and the 128-row ones still fit in one wave (decoding, small batches).
+int task_rows_fixed(int B, int H_kv, int N_q, int gshift, int sm_count) {
+  if (g_opt.solo == 0 || g_opt.emu_groups > 0) return fa::kTaskRows;
+  if (g_opt.solo == 1) return fa::kBlockM;
+  const long long rows = (long long)N_q << gshift;
+  const long long pairs = (long long)B * H_kv;
+  const long long t256 = pairs * ((rows + fa::kTaskRows - 1) / fa::kTaskRows);
+  const long long t128 = pairs * ((rows + fa::kBlockM - 1) / fa::kBlockM);
+  return (t256 < sm_count && t128 <= sm_count) ? fa::kBlockM : fa::kTaskRows;
 }
 
 int choose_splits(int requested, long long base_tasks, int key_blocks, int sm_count) {
@@ -230,14 +245,14 @@ struct Partials {
 };
 
 
-template <int D, bool C, bool E, bool F>
+template <int D, bool C, bool E, bool F, bool S>
 int launch_fwd(DevInfo* dev, const fa::FwdParams& p, int grid, cudaStream_t stream) {
   using L = fa::Layout<D>;
-  auto kern = fa::fa_fwd_kernel<D, C, E, F>;
-  const int di = D == 128 ? 1 : 0, ci = C ? 1 : 0, ei = E ? 1 : 0, fi = F ? 1 : 0;
+  auto kern = fa::fa_fwd_kernel<D, C, E, F, S>;
+  const int di = D == 128 ? 1 : 0, ci = C ? 1 : 0, ei = E ? 1 : 0, fi = F ? 1 : 0, si = S ? 1 : 0;
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (!dev->attr_done[di][ci][ei][fi]) {
+    if (!dev->attr_done[di][ci][ei][fi][si]) {
       int st = FA_OK;
       cudaFuncAttributes fa_attr;
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc) != cudaSuccess ||
@@ -247,18 +262,22 @@ int launch_fwd(DevInfo* dev, const fa::FwdParams& p, int grid, cudaStream_t stre
       // per thread at launch
       else if (fa_attr.numRegs != 128)
         st = FA_ERR_UNSUPPORTED;
-      dev->attr_status[di][ci][ei][fi] = st;
-      dev->attr_done[di][ci][ei][fi] = true;
+      dev->attr_status[di][ci][ei][fi][si] = st;
+      dev->attr_done[di][ci][ei][fi][si] = true;
     }
-    if (dev->attr_status[di][ci][ei][fi] != FA_OK) return dev->attr_status[di][ci][ei][fi];
+    if (dev->attr_status[di][ci][ei][fi][si] != FA_OK) return dev->attr_status[di][ci][ei][fi][si];
   }
   kern<<<grid, fa::kThreads, L::kSmemAlloc, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+// Solo tasks (task_rows 128) have their own kernel, without the polynomial exp2
+// (task_rows_fixed keeps two-tile tasks when the emulation is on).
 template <int D, bool C, bool F>
 int dispatch_emu(DevInfo* dev, const fa::FwdParams& p, int grid, cudaStream_t s) {
-  return p.emu_groups > 0 ? launch_fwd<D, C, true, F>(dev, p, grid, s) : launch_fwd<D, C, false, F>(dev, p, grid, s);
+  if (p.task_rows == fa::kBlockM) return launch_fwd<D, C, false, F, true>(dev, p, grid, s);
+  return p.emu_groups > 0 ? launch_fwd<D, C, true, F, false>(dev, p, grid, s)
+                          : launch_fwd<D, C, false, F, false>(dev, p, grid, s);
 }
 
 template <bool F>
@@ -316,7 +335,7 @@ __global__ void __launch_bounds__(1024) fa_varlen_schedule_kernel(const int* cu_
   if (threadIdx.x == 0) total_tiles = 0;
   __syncthreads();
   auto cost_of = [&](int m, int Lq, int Lk, int sp) {
-    const KRange r = key_range(m, Lq, Lk, gshift, causal != 0, splits, sp);
+    const KRange r = key_range(m * kTaskRows, kTaskRows, Lq, Lk, gshift, causal != 0, splits, sp);
     return min(r.hi - r.lo, kSchedBuckets - 1);
   };
   for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
@@ -573,6 +592,10 @@ int fa_set_option(int option, double value) {
       if (!(value >= 0.0 && value <= 1e6) || value != std::floor(value)) return FA_ERR_INVALID_ARG;
       g_opt.bwd_section = (int)value;
       return FA_OK;
+    case FA_OPT_SOLO_TILES:
+      if (value != -1.0 && value != 0.0 && value != 1.0) return FA_ERR_INVALID_ARG;
+      g_opt.solo = (int)value;
+      return FA_OK;
     default:
       return FA_ERR_INVALID_ARG;
   }
@@ -607,11 +630,12 @@ int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.Hkv = H_kv;
   p.gshift = gshift;
   p.total_tokens = (int)tokens;
-  // tasks of 256 packed rows; a (b, kv head) has N_q * G rows
-  p.num_m = (int)((((long long)N_q << gshift) + fa::kTaskRows - 1) / fa::kTaskRows);
+  // tasks of task_rows packed rows; a (b, kv head) has N_q * G rows
+  p.task_rows = task_rows_fixed(B, H_kv, N_q, gshift, dev->sm_count);
+  p.num_m = (int)((((long long)N_q << gshift) + p.task_rows - 1) / p.task_rows);
   const long long base_tasks = (long long)B * H_kv * p.num_m;
-  p.splits =
-      choose_splits_fixed(num_splits, B, H, H_kv, p.num_m, N_q, N_kv, d, gshift, causal != 0, dev->sm_count);
+  p.splits = choose_splits_fixed(num_splits, B, H, H_kv, p.num_m, p.task_rows, N_q, N_kv, d, gshift, causal != 0,
+                                 dev->sm_count);
   const long long ntask = base_tasks * p.splits;
   if (ntask > INT_MAX) return FA_ERR_INVALID_ARG;
   p.num_tasks = (int)ntask;
@@ -701,6 +725,7 @@ int varlen_launch(DevInfo* dev, const void* q, const void* k, const void* v, voi
   p.total_tokens = total_q;
   p.num_tasks = cap;
   p.varlen = 1;
+  p.task_rows = fa::kTaskRows;
   p.splits = splits;
   if (splits > 1) {
     p.o_part = parts->o_part;
@@ -770,9 +795,10 @@ int fa_fwd_kv_splits(int B, int H, int H_kv, int N_q, int N_kv, int d, int causa
   if (st != FA_OK) return st;
   DevInfo* dev = nullptr;
   if ((st = device_info(&dev)) != FA_OK) return st;
-  const long long num_m = (((long long)N_q << gshift) + fa::kTaskRows - 1) / fa::kTaskRows;
+  const int task_rows = task_rows_fixed(B, H_kv, N_q, gshift, dev->sm_count);
+  const long long num_m = (((long long)N_q << gshift) + task_rows - 1) / task_rows;
   if ((long long)B * H_kv * num_m > INT_MAX) return FA_ERR_INVALID_ARG;
-  *splits = choose_splits_fixed(num_splits, B, H, H_kv, (int)num_m, N_q, N_kv, d, gshift, causal != 0,
+  *splits = choose_splits_fixed(num_splits, B, H, H_kv, (int)num_m, task_rows, N_q, N_kv, d, gshift, causal != 0,
                                 dev->sm_count);
   return FA_OK;
 }

@@ -90,7 +90,9 @@ struct FwdParams {
   int gshift;                    // log2 of G, the query heads per K/V head (packed rows per position)
   int total_tokens;              // rows of Q and O
   int num_tasks;                 // fixed length: exact; varlen: upper bound (grid sizing)
-  int num_m;                     // fixed length: 256-row blocks of packed rows per (b, kv head)
+  int num_m;                     // fixed length: task_rows-row blocks of packed rows per (b, kv head)
+  int task_rows;                 // packed rows per task: 256 (two Q tiles) or 128 (solo: one Q tile whose
+                                 // score tile alternates between S_0 and S_1; fixed length only)
   int lpt_group;                 // causal fixed length: (b, kv head) pairs per L2 section
   int varlen;
   float scale_log2;              // scale * log2(e)
@@ -164,8 +166,8 @@ struct Layout {
                        bCorrEmpty = bCorrFull + 2, bOFinal = bCorrEmpty + 2, bDrain = bOFinal + 2,
                        bTaskFull = bDrain + 1, bTaskEmpty = bTaskFull + 2, bClc = bTaskEmpty + 2,
                        bOstReady = bClc + 1, bOstFree = bOstReady + 1, bTurn = bOstFree + 1,
-                       bStats = bTurn + 2;
-  static constexpr int kNumBars = bStats + 2;
+                       bStats = bTurn + 2, bPVDone = bStats + 2;
+  static constexpr int kNumBars = bPVDone + 1;
   static constexpr int kMailOff = kBarOff + ((kNumBars * 8 + 127) / 128) * 128;
   static constexpr int kMiscOff = kMailOff + 2 * kBlockM * 4;  // tmem slot, abort flags, task ring
   static constexpr int kClcOff = kMiscOff + 64;                 // 16-byte launch-control response
@@ -179,7 +181,8 @@ struct Layout {
 
 // ------------------------------------------------------------------ tasks
 struct Task {
-  int kvh, tok0, len, m;   // K/V head, first query row of the sequence, its length, 256-row block
+  int kvh, tok0, len;      // K/V head, first query row of the sequence, its length
+  int row0, rows;          // the task's packed rows [row0, row0 + rows) of the sequence (rows 256 or 128)
   int tok0k, lenk;         // first key row of the sequence, its number of keys
   int split;               // key range (splits > 1)
   int lse_base;            // lse index of position 0 of query head kvh * G
@@ -188,16 +191,19 @@ struct Task {
 
 // First sequence position of the packed rows from `row` on (row a multiple of G).
 __device__ __forceinline__ int packed_pos(const Task& t, int row, int gshift) {
-  return (t.m * kTaskRows + row) >> gshift;
+  return (t.row0 + row) >> gshift;
 }
 
+// ROWS: packed rows per fixed-length task (256, or 128 in a solo kernel).
+template <int ROWS>
 __device__ __forceinline__ bool get_task(const FwdParams& p, bool causal, int idx, Task& t) {
   if (p.varlen) {
     if (idx >= *p.task_count) return false;
     const int4 e = p.tasks[idx];
     const int s0 = p.cu_seqlens[e.x], s1 = p.cu_seqlens[e.x + 1];
     const int k0 = p.cu_seqlens_k[e.x], k1 = p.cu_seqlens_k[e.x + 1];
-    t.kvh = e.y & 0xffff; t.split = e.y >> 16; t.m = e.z; t.tok0 = s0; t.len = s1 - s0;
+    t.kvh = e.y & 0xffff; t.split = e.y >> 16; t.row0 = e.z * kTaskRows; t.rows = kTaskRows;
+    t.tok0 = s0; t.len = s1 - s0;
     t.tok0k = k0; t.lenk = k1 - k0;
     t.lse_base = (t.kvh << p.gshift) * p.total_tokens + s0;
     t.lse_hstride = p.total_tokens;
@@ -223,7 +229,7 @@ __device__ __forceinline__ bool get_task(const FwdParams& p, bool causal, int id
     m = idx - bh * p.num_m;
   }
   const int b = bh / p.Hkv;
-  t.kvh = bh - b * p.Hkv; t.m = m; t.tok0 = b * p.N; t.len = p.N;
+  t.kvh = bh - b * p.Hkv; t.row0 = m * ROWS; t.rows = ROWS; t.tok0 = b * p.N; t.len = p.N;
   t.tok0k = b * p.Nk; t.lenk = p.Nk;
   t.lse_base = (b * p.H + (t.kvh << p.gshift)) * p.N;
   t.lse_hstride = p.N;
@@ -231,10 +237,11 @@ __device__ __forceinline__ bool get_task(const FwdParams& p, bool causal, int id
 }
 
 // Q tile 1 of the task holds no query row of the sequence (its packed rows
-// start at or past the end): the task runs Q tile 0 only. Decoding (a few query
-// rows per sequence) and the ragged last block of a sequence are such tasks.
+// start at or past the end), or the task is a solo one of 128 rows: the task runs
+// Q tile 0 only. Decoding (a few query rows per sequence) and the ragged last block
+// of a sequence are such tasks.
 __device__ __forceinline__ bool task_one_tile(const Task& t, int gshift) {
-  return packed_pos(t, kBlockM, gshift) >= t.len;
+  return t.rows == kBlockM || packed_pos(t, kBlockM, gshift) >= t.len;
 }
 
 // Causal offset: query position i sees keys j <= i + off, with off = N_kv - N_q
@@ -248,11 +255,11 @@ __device__ __forceinline__ int task_off(const Task& t) { return t.lenk - t.len; 
 struct KRange {
   int lo, hi;
 };
-// The same for the 256-row block m of a sequence with lenq query and lenk key rows.
-__device__ __forceinline__ KRange key_range(int m, int lenq, int lenk, int gshift, bool causal, int splits,
-                                            int split) {
+// The same for the packed rows [row0, row0 + rows) of a sequence with lenq query and lenk key rows.
+__device__ __forceinline__ KRange key_range(int row0, int rows, int lenq, int lenk, int gshift, bool causal,
+                                            int splits, int split) {
   int kmax = lenk;
-  if (causal) kmax = min(((m * kTaskRows + kTaskRows - 1) >> gshift) + (lenk - lenq) + 1, lenk);
+  if (causal) kmax = min(((row0 + rows - 1) >> gshift) + (lenk - lenq) + 1, lenk);
   const int nb = kmax > 0 ? (kmax + kBlockN - 1) / kBlockN : 0;
   if (splits == 1) return {0, nb};
   const int per = ((lenk + kBlockN - 1) / kBlockN + splits - 1) / splits;
@@ -260,7 +267,7 @@ __device__ __forceinline__ KRange key_range(int m, int lenq, int lenk, int gshif
   return {lo, max(lo, min(lo + per, nb))};
 }
 __device__ __forceinline__ KRange task_range(const FwdParams& p, const Task& t, bool causal) {
-  return key_range(t.m, t.len, t.lenk, p.gshift, causal, p.splits, t.split);
+  return key_range(t.row0, t.rows, t.len, t.lenk, p.gshift, causal, p.splits, t.split);
 }
 
 // ------------------------------------------------------------------ task ring
@@ -272,8 +279,10 @@ constexpr int kTaskConsumerWarps = 13;
 
 // Causal tasks: the top K/V block lies entirely above Q tile 0's last row, so
 // tile 0 skips it (its scores there would all be masked). Returns 1 or 0.
+// (A solo task's range already ends at its only tile's last visible key.)
 __device__ __forceinline__ int task_skip0(const Task& t, KRange r, bool causal, int gshift) {
-  return (causal && r.hi - r.lo >= 2 && (r.hi - 1) * kBlockN > packed_pos(t, kBlockM - 1, gshift) + task_off(t))
+  return (causal && t.rows != kBlockM && r.hi - r.lo >= 2 &&
+          (r.hi - 1) * kBlockN > packed_pos(t, kBlockM - 1, gshift) + task_off(t))
              ? 1 : 0;
 }
 
@@ -427,8 +436,11 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int D, bool CAUSAL, bool EMU, bool F16>
+// SOLO: fixed-length tasks of one 128-row Q tile whose score tile alternates between
+// S_0 and S_1 (the host launches it when p.task_rows == 128).
+template <int D, bool CAUSAL, bool EMU, bool F16, bool SOLO = false>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+  constexpr int kRows = SOLO ? kBlockM : kTaskRows;   // packed rows per fixed-length task
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -470,6 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       mbar_init(bar(L::bKVEmpty + s), 1);
     }
     mbar_init(bar(L::bDrain), 1);
+    mbar_init(bar(L::bPVDone), 1);   // solo tasks: one phase per key block, once its PV has completed
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(L::bTaskFull + i), 1);
       mbar_init(bar(L::bTaskEmpty + i), kTaskConsumerWarps);
@@ -594,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         }
         __syncwarp();
         if (idx < 0) break;
-        get_task(p, CAUSAL, idx, tk);
+        get_task<kRows>(p, CAUSAL, idx, tk);
         const KRange kr = task_range(p, tk, CAUSAL);
         if (kr.hi <= kr.lo) continue;   // no key to attend to: nothing to load
         const int nb = kr.hi - kr.lo;
@@ -651,10 +664,67 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       for (int k = 0; ok; ++k) {
         const int idx = take_task(w, k);
         if (idx < 0) break;
-        get_task(p, CAUSAL, idx, tk);
+        get_task<kRows>(p, CAUSAL, idx, tk);
         const KRange kr = task_range(p, tk, CAUSAL);
         if (kr.hi <= kr.lo) continue;   // no key: no MMA (the epilogue writes the empty rows)
         const int nb = kr.hi - kr.lo;
+        if constexpr (SOLO) {
+          // Solo task: one Q tile whose score tile alternates between S_0 (even blocks i)
+          // and S_1 (odd), so block i+2's QK^T, issued as soon as PV_i has read P_i out of
+          // the same columns, runs while the softmax works on block i+1. The task's K/V
+          // items in ring order are K_{hi-1}, V_{hi-1}, K_{hi-2}, ...: item 2i is block
+          // i's K, item 2i+1 its V; the K items are used two blocks ahead of the V items.
+          // Step i issues PV_i (i >= 0) and then QK_{i+2}.
+          const uint32_t c0 = phase * L::kStages + stage;   // ring position of the task's first item
+#pragma unroll 1
+          for (int i = -2; i < nb; ++i) {
+            if (i >= 0) {
+              const int b = i & 1, j = kr.hi - 1 - i;
+              const uint32_t c = (c0 + 2u * (uint32_t)i + 1u) % (2u * L::kStages);
+              const uint32_t vs = c % L::kStages;
+              if (!w.wait(bar(L::bKVFull + vs), c / L::kStages, L::bKVFull + vs, j)) { ok = false; break; }
+              if (!w.wait(bar(L::bPO + b), (po_par >> b) & 1, L::bPO + b, j)) { ok = false; break; }
+              po_par ^= 1u << b;
+              tc_fence_after();
+              if (leader) issue_pv<D, 0, kSplitP, F16>(O0, b ? P1 : P0, Vd + vs * kStageStep, i > 0);
+              if (!w.wait(bar(L::bP2 + b), (p2_par >> b) & 1, L::bP2 + b, j)) { ok = false; break; }
+              p2_par ^= 1u << b;
+              tc_fence_after();
+              if (leader) {
+                issue_pv<D, kSplitP, kBlockN, F16>(O0, b ? P1 : P0, Vd + vs * kStageStep, true);
+                mma_commit(bar(L::bKVEmpty + vs));
+                mma_commit(bar(L::bPVDone));                         // O holds blocks 0 .. i
+                if (i == nb - 1) mma_commit(bar(L::bOFinal + 0));
+              }
+              __syncwarp();
+              tr.rec(kEvPV0b, j);
+            }
+            const int n = i + 2;   // S_(n&1) = Q K_n^T
+            if (n < nb) {
+              const uint32_t c = (c0 + 2u * (uint32_t)n) % (2u * L::kStages);
+              const uint32_t ks_ = c % L::kStages;
+              if (!w.wait(bar(L::bKVFull + ks_), c / L::kStages, L::bKVFull + ks_, kr.hi - 1 - n)) { ok = false; break; }
+              if (n == 0) {
+                if (!w.wait(bar(L::bQFull + 0), qf_par & 1u, L::bQFull + 0, kr.hi - 1)) { ok = false; break; }
+                qf_par ^= 1u;
+              }
+              tc_fence_after();
+              if (leader) {
+                issue_qk<D, F16>((n & 1) ? S1 : S0, Q0, Kd + ks_ * kStageStep);
+                mma_commit(bar(L::bSFull + (n & 1)));
+                mma_commit(bar(L::bKVEmpty + ks_));
+                if (n == nb - 1) mma_commit(bar(L::bQEmpty + 0));   // Q_0's last use in this task
+              }
+              __syncwarp();
+              tr.rec(kEvS0 + (n & 1), kr.hi - 1 - n);
+            }
+          }
+          if (!ok) break;
+          const uint32_t c = (c0 + 2u * (uint32_t)nb) % (2u * L::kStages);   // past the task's items
+          stage = c % L::kStages;
+          phase = c / L::kStages;
+          continue;
+        }
         const int skip0 = task_skip0(tk, kr, CAUSAL, p.gshift);   // tile 0 starts one block lower
         const int t_last = task_one_tile(tk, p.gshift) ? 0 : 1;   // the tiles of this task: 0 .. t_last
         // prologue: S_0 and S_1 for the top block (S_0 only if tile 0 sees it)
@@ -744,13 +814,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     const int t = warp >> 2;                 // Q tile of this warpgroup
     const int r = tid & 127;                 // row within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_base + L::col_s(t);
-    const uint32_t tP = tS + 64;
+    const uint32_t tS_t = tmem + lane_base + L::col_s(t);   // this warpgroup's score tile (solo: per block)
     Waiter w{abort_flag, p.timeout_ns, t == 0 ? kRoleSoftmax0 : kRoleSoftmax1};
     Tracer tr;
     tr.init(p, 2 + t, r == 0);
     const float sl2 = p.scale_log2;
-    uint32_t s_par = 0, ce_par = 0;
+    uint32_t s_par = 0, ce_par = 0;   // parity of the next wait on s_full / corr_empty (solo: bit = tile)
     uint32_t turns = 0;   // exponential phases taken in turn so far (stagger mode)
     // Stagger mode ("Flash Attention 4", section "论文与当前 TIRx 实现的差异": the two
     // softmax warpgroups' exponential phases do not overlap): the warpgroups pass a
@@ -767,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     for (int k = 0; ok; ++k) {
       const int idx = take_task(w, k);
       if (idx < 0) break;
-      get_task(p, CAUSAL, idx, tk);
+      get_task<kRows>(p, CAUSAL, idx, tk);
       const KRange kr = task_range(p, tk, CAUSAL);
       const int tile_pos0 = packed_pos(tk, t * kBlockM, p.gshift);  // sequence position of row 0
       const int pos = tile_pos0 + (r >> p.gshift);                  // this row's sequence position
@@ -780,6 +849,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           else if (p.lse != nullptr) p.lse[li] = v;
         }
       };
+      constexpr bool solo = SOLO;   // one Q tile, run by WG0 over both score tiles
+      if (t == 1 && solo) continue;
       if (kr.hi <= kr.lo) {   // no key for any row of the task: LSE = -inf (O = 0 is written by WG2)
         store_lse(-INFINITY);
         continue;
@@ -799,8 +870,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
 #endif
       for (int i = 0; i < nb; ++i) {
         const int j = hi - 1 - i;
-        if (!w.wait(bar(L::bSFull + t), s_par, L::bSFull + t, j)) { ok = false; break; }
-        s_par ^= 1;
+        const int pb = solo ? (i & 1) : 0;   // parity bit of this block's barriers
+        const int b = solo ? pb : t;          // the score tile (and barrier set) of this block
+        const uint32_t tS = solo ? tmem + lane_base + L::col_s(b) : tS_t;
+        const uint32_t tP = tS + 64;
+        if (!w.wait(bar(L::bSFull + b), (s_par >> pb) & 1, L::bSFull + b, j)) { ok = false; break; }
+        s_par ^= 1u << pb;
         tr.rec(kEvSFull, j);
         tc_fence_after();
         const int k0 = j * kBlockN;
@@ -884,11 +959,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             tmem_wait_st();
             tc_fence_before();
           } else {
-            if (!w.wait(bar(L::bCorrEmpty + t), ce_par ^ 1, L::bCorrEmpty + t, j)) { ok = false; break; }
-            ce_par ^= 1;
-            mail[t * kBlockM + r] = acc;
+            if (!w.wait(bar(L::bCorrEmpty + b), ((ce_par >> pb) & 1) ^ 1, L::bCorrEmpty + b, j)) { ok = false; break; }
+            ce_par ^= 1u << pb;
+            mail[b * kBlockM + r] = acc;
           }
-          mbar_arrive(bar(L::bCorrFull + t));
+          mbar_arrive(bar(L::bCorrFull + b));
           tr.rec(kEvMail, j);
         }
         if (stagger && !take_turn(j)) { ok = false; break; }
@@ -928,7 +1003,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           tmem_st32(tP + h * 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[h * 32]));
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(bar(h == 0 ? L::bPO + t : L::bP2 + t));
+          mbar_arrive(bar(h == 0 ? L::bPO + b : L::bP2 + b));
           tr.rec(h == 0 ? kEvHalf1 : kEvHalf2, j);
         }
         if (stagger) mbar_arrive(bar(L::bTurn + (t ^ 1)));   // the other warpgroup's turn
@@ -938,8 +1013,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       }
       if (!ok) break;
       // final statistics to WG2 (row_sum), LSE straight to global memory
-      if (!w.wait(bar(L::bCorrEmpty + t), ce_par ^ 1, L::bCorrEmpty + t, -1)) { ok = false; break; }
-      ce_par ^= 1;
+      if (!w.wait(bar(L::bCorrEmpty + t), (ce_par & 1) ^ 1, L::bCorrEmpty + t, -1)) { ok = false; break; }
+      ce_par ^= 1u;
       mail[t * kBlockM + r] = row_sum;
       // with acc_scale in tensor memory the per-block hand-offs have no empty barrier,
       // so the final one takes a barrier of its own: on corr_full it could complete a
@@ -973,22 +1048,24 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     uint32_t cf_par = 0, of_par = 0;  // bit t: parity of the next wait on corr_full[t] / o_final[t]
     uint32_t fs_par = 0;              // bit t: parity of the next wait on stats[t] (stats_tmem mode)
     uint32_t ost_n = 0;               // uses of the O staging tile so far
+    uint32_t pv_done = 0;             // solo tasks: key blocks whose PV completion bPVDone has counted
     bool ok = true;
     Task tk;
     // O_0 and O_1 are free for the first task's first PV; later tasks get this
     // arrival right after the epilogue of the same tile (below), so the next
-    // task's PV can start while the other tile is still being written out.
+    // task's PV can start while the other tile is still being written out. Solo
+    // tasks use O_0 only, their first PV always through p_o[0].
     mbar_arrive(bar(L::bPO + 0));
-    mbar_arrive(bar(L::bPO + 1));
+    if (!SOLO) mbar_arrive(bar(L::bPO + 1));
     for (int k = 0; ok; ++k) {
       const int idx = take_task(w, k);
       if (idx < 0) break;
-      get_task(p, CAUSAL, idx, tk);
+      get_task<kRows>(p, CAUSAL, idx, tk);
       const KRange kr = task_range(p, tk, CAUSAL);
       if (kr.hi <= kr.lo) {
         // no key for any row of the task: O = 0 (its LSE = -inf comes from the softmax warps)
 #pragma unroll 1
-        for (int t = 0; t < 2; ++t) {
+        for (int t = 0; t < tk.rows / kBlockM; ++t) {
           const int pos = packed_pos(tk, t * kBlockM, p.gshift) + (r >> p.gshift);
           const int head = (tk.kvh << p.gshift) + (r & ((1 << p.gshift) - 1));
           if (pos < tk.len && tk.tok0 + pos < p.total_tokens) {
@@ -1006,25 +1083,33 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       const int nb = kr.hi - kr.lo;
       const int skip0 = task_skip0(tk, kr, CAUSAL, p.gshift);
       const int t_last = task_one_tile(tk, p.gshift) ? 0 : 1;   // the tiles of this task: 0 .. t_last
+      constexpr bool solo = SOLO;   // one Q tile; block i's statistics come with score tile i & 1
       tr.rec(kEvTask, nb);
       for (int i = 1; ok && i < nb; ++i) {
         const int j = kr.hi - 1 - i;
 #pragma unroll 1
         for (int t = 0; t <= t_last; ++t) {
           if (t == 0 && i - skip0 < 1) continue;   // tile 0's first block needs no correction
-          if (!w.wait(bar(L::bCorrFull + t), (cf_par >> t) & 1, L::bCorrFull + t, j)) { ok = false; break; }
-          cf_par ^= 1u << t;
+          const int b = solo ? (i & 1) : t;
+          if (!w.wait(bar(L::bCorrFull + b), (cf_par >> b) & 1, L::bCorrFull + b, j)) { ok = false; break; }
+          cf_par ^= 1u << b;
           tr.rec(kEvCorrFull + t, j);
           float a;
           if (p.stats_tmem) {
             tc_fence_after();
-            a = __uint_as_float(tmem_ld1(tmem + lane_base + L::col_s(t)));
+            a = __uint_as_float(tmem_ld1(tmem + lane_base + L::col_s(b)));
             tmem_wait_ld();
           } else {
-            a = mail[t * kBlockM + r];
-            mbar_arrive(bar(L::bCorrEmpty + t));
+            a = mail[b * kBlockM + r];
+            mbar_arrive(bar(L::bCorrEmpty + b));
           }
           if (__any_sync(0xffffffffu, a < 1.f)) {
+            // a solo task's score tile for this block was ready before the previous
+            // block's PV had finished: wait for that PV before touching O
+            if (solo && !w.wait(bar(L::bPVDone), (pv_done + (uint32_t)i - 1u) & 1u, L::bPVDone, j)) {
+              ok = false;
+              break;
+            }
             tc_fence_after();
             const uint32_t tO = tmem + lane_base + L::col_o(t);
 #pragma unroll 1
@@ -1039,11 +1124,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             tmem_wait_st();
           }
           tc_fence_before();
-          mbar_arrive(bar(L::bPO + t));
+          mbar_arrive(bar(L::bPO + b));
           tr.rec(kEvCorrDone + t, j);
         }
       }
       if (!ok) break;
+      if (solo) pv_done += (uint32_t)nb;
       // epilogue: O_t / row_sum -> bf16 / fp16 -> global
 #pragma unroll 1
       for (int t = 0; t <= t_last; ++t) {

@@ -319,12 +319,20 @@ int fa_last_device_status(void* stream, unsigned long long* detail);
  *   FA_OPT_BWD_SECTION     : (sequence, K/V head) pairs per L2 section of the backward's
  *                            grid order (whole number; 0 = the library's choice, about
  *                            512 CTAs per section)
- * Both forward variants compute the same result as the default path.
+ *   FA_OPT_SOLO_TILES      : fixed-length forward tasks of one 128-row Q tile whose score
+ *                            tile alternates between the two S buffers of tensor memory,
+ *                            so a block's QK^T overlaps the previous block's softmax
+ *                            (instead of two Q tiles sharing each K/V block). -1 = the
+ *                            library's choice (default: when the 256-row tasks leave SMs
+ *                            idle and the 128-row ones fit in one wave, e.g. decoding and
+ *                            small batches), 0 = never, 1 = always. Varlen calls always
+ *                            use two-tile tasks.
+ * The forward variants compute the same result as the default path.
  * Returns FA_OK or FA_ERR_INVALID_ARG.
  */
 enum { FA_OPT_TAU = 1, FA_OPT_WAIT_TIMEOUT_NS = 2, FA_OPT_PERSISTENT = 3, FA_OPT_EXP2_EMULATION = 4,
        FA_OPT_BWD_DETERMINISTIC = 5, FA_OPT_SOFTMAX_STAGGER = 6, FA_OPT_STATS_TMEM = 7,
-       FA_OPT_BWD_SECTION = 8 };
+       FA_OPT_BWD_SECTION = 8, FA_OPT_SOLO_TILES = 9 };
 int fa_set_option(int option, double value);
 
 /*

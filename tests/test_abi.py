@@ -257,6 +257,7 @@ def test_valid_arguments_without_gpu_report_no_device():
                                         (6, 0, True), (6, 1, True), (6, -1, False),
                                         (7, 0, True), (7, 1, True), (7, 3, False),
                                         (8, 0, True), (8, 12, True), (8, -1, False), (8, 1.5, False),
+                                        (9, -1, True), (9, 0, True), (9, 1, True), (9, 2, False), (9, 0.5, False),
                                         (99, 1, False)])
 def test_set_option_validation(opt, val, ok):
     lib = fa.library()
@@ -271,3 +272,4 @@ def test_set_option_validation(opt, val, ok):
     lib.fa_set_option(6, 0)
     lib.fa_set_option(7, 1)
     lib.fa_set_option(8, 0)
+    lib.fa_set_option(9, -1)

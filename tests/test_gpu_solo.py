@@ -1,0 +1,106 @@
+"""Solo tasks of the forward: one 128-row Q tile per task, its score tile alternating
+between the two S buffers of tensor memory so that a key block's QK^T overlaps the
+previous block's softmax (the library's choice when the two-tile tasks would leave SMs
+idle). Every row still visits the same key blocks in the same order with the same
+arithmetic, so solo and two-tile tasks must give the same bits; both must match the
+fp64 oracle (O <= 2e-2, LSE <= 1e-3 max-abs).
+
+The shapes cover an even and an odd number of key blocks per task, one block, grouped
+heads up to G = 128, N_q != N_kv (causal rows without keys), key splits, decoding, and
+spiky scores whose delayed rescale makes the correction warpgroup wait for the previous
+block's PV (the statistics through tensor memory and through shared memory).
+"""
+import math
+
+import numpy as np
+import pytest
+
+import attention_forward_tma_gb300 as fa
+import fa_inputs
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+TOL_O, TOL_LSE = 2e-2, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    fa.library()
+    yield torch
+    fa.set_option("solo_tiles", -1)
+    fa.set_option("stats_tmem", 1)
+
+
+def dev(bits):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def host(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return fa_inputs.bf16_bits_to_f32(t.view(torch.int16).cpu().numpy().view(np.uint16)).astype(np.float64)
+    return t.cpu().numpy().astype(np.float64)
+
+
+def run(q, k, v, causal, splits, solo, stats_tmem=1):
+    fa.set_option("solo_tiles", solo)
+    fa.set_option("stats_tmem", stats_tmem)
+    try:
+        o, lse = fa.fa_fwd(dev(q), dev(k), dev(v), causal=causal, num_splits=splits)
+        st, word = fa.last_device_status()
+    finally:
+        fa.set_option("solo_tiles", -1)
+        fa.set_option("stats_tmem", 1)
+    assert st == fa.FA_OK, hex(word)
+    return host(o), host(lse)
+
+
+def check(o, lse, o_ref, l_ref, what):
+    assert np.isfinite(o).all(), what
+    err_o = np.abs(o - o_ref).max()
+    assert err_o <= TOL_O, f"{what}: max |O - oracle| = {err_o}"
+    fin = np.isfinite(l_ref)
+    assert (np.isneginf(lse) == ~fin).all(), what
+    err_l = np.abs(lse[fin] - l_ref[fin]).max() if fin.any() else 0.0
+    assert err_l <= TOL_LSE, f"{what}: max |LSE - oracle| = {err_l}"
+
+
+SHAPES = [  # (B, H, H_kv, N_q, N_kv, d, splits)
+    (1, 2, 2, 1100, 1100, 128, 1),    # 9 key blocks: odd count
+    (2, 3, 3, 700, 700, 64, 1),       # 6 key blocks: even count
+    (1, 2, 2, 100, 100, 128, 1),      # one key block
+    (1, 8, 2, 300, 300, 128, 1),      # G = 4
+    (1, 128, 1, 40, 300, 64, 1),      # G = 128: one position per tile
+    (1, 4, 1, 200, 650, 128, 1),      # N_q < N_kv
+    (1, 2, 2, 650, 200, 128, 1),      # N_q > N_kv: causal rows without keys
+    (1, 4, 2, 500, 1500, 128, 3),     # key ranges merged through their LSE
+    (2, 32, 8, 1, 4096, 128, 0),      # decoding, the library's key ranges
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "B%dH%dKV%dNq%dNk%dd%ds%d" % s)
+def test_solo_matches_two_tile_tasks_and_oracle(shape, causal):
+    B, H, Hkv, Nq, Nk, d, splits = shape
+    q, k, v = fa_inputs.make_qkv(B, Nq, H, d, seed=8000 + Nq + Nk + H, Nkv=Nk, Hkv=Hkv)
+    solo = run(q, k, v, causal, splits, 1)
+    two = run(q, k, v, causal, splits, 0)
+    assert np.array_equal(solo[0], two[0]) and np.array_equal(solo[1], two[1]), "solo differs from two-tile tasks"
+    o_ref, l_ref = oracle.attention(q, k, v, 1 / math.sqrt(d), causal)
+    check(solo[0], solo[1], o_ref, l_ref, f"{shape} causal={causal}")
+
+
+@pytest.mark.parametrize("stats_tmem", [1, 0])
+def test_solo_rescales_wait_for_the_previous_pv(stats_tmem):
+    """Spiky scores: row references move by more than tau, so the correction warpgroup
+    rescales O, which in a solo task first waits for the previous block's PV."""
+    q, k, v = fa_inputs.make_qkv(1, 1500, 4, 128, seed=20264, spiky=True)
+    solo = run(q, k, v, True, 1, 1, stats_tmem)
+    two = run(q, k, v, True, 1, 0, stats_tmem)
+    assert np.array_equal(solo[0], two[0]) and np.array_equal(solo[1], two[1])
+    o_ref, l_ref = oracle.attention(q, k, v, 1 / math.sqrt(128), True)
+    check(solo[0], solo[1], o_ref, l_ref, f"spiky stats_tmem={stats_tmem}")
