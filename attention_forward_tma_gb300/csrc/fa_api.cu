@@ -97,27 +97,23 @@ int make_maps(fa::FwdParams& p, const void* q, const void* k, const void* v, voi
   return FA_OK;
 }
 
-// Key ranges per task. requested > 0: that many (at most one per 128-key block
-// and kMaxSplits). requested = 0: split only when the unsplit tasks cannot fill
-// the SMs, into as many ranges as keep all tasks in one wave (tasks <= SMs), with
-// at least four K/V blocks per range. (Measured on GB300 for one query row
-// against 4K-128K keys: one full wave beat both fewer ranges and a second,
-// partial wave; e.g. 64 tasks x 2 ranges 235 us, x 5 ranges 279 us.)
+// Key ranges per task. requested > 0: that many (at most one per 128-key block and
+// kMaxSplits). requested = 0: the library's choice below.
 constexpr int kMaxSplits = 128;
-// The library's choice when fewer tasks than SMs: the number of key ranges s (at most
-// 64, at least 4 key blocks per range) that minimises the estimated time
-//   ceil(base_tasks * s / sm_count) rounds x (ceil(key_blocks / s) + 2) blocks,
-// the 2 standing for a task's fixed cost (its Q load, pipeline fill and epilogue), so
-// that the key ranges fill the SMs evenly (64 tasks on 152 SMs: 7 ranges, 448 tasks in
-// three rounds, rather than 2 ranges leaving 24 SMs idle).
-// Fixed length: the estimate runs the tasks through longest-first list scheduling on
-// sm_count SMs, with each task's own key range (a causal task sees only the blocks up
-// to its diagonal; the kernel cuts ranges of ceil(key_blocks / s) blocks, so a short
-// causal task's upper ranges are empty) at (blocks + 2) for a range with keys and 1
-// for an empty one (it writes zero partials), all in units of one K/V block step
-// (about 2 us). With s > 1 it adds the merge: its launch (2.5 units) and the fp32
-// partials written and read back, at HBM speed (about 13 MB per unit). Picks the s
-// with the shortest estimate; cached per shape (a decoding loop asks every step).
+// Fixed length: split only when the unsplit tasks leave SMs idle. For each s up to 64
+// the estimate runs the tasks through longest-first list scheduling on sm_count SMs,
+// each task with its own key range (a causal task sees only the blocks up to its
+// diagonal; the kernel cuts ranges of ceil(key_blocks / s) blocks, so a short causal
+// task's upper ranges are empty) at (blocks * step + 2) for a range with keys and 1 for
+// an empty one (it writes zero partials), in units of one two-tile K/V block step
+// (about 2 us; a solo task's step, its QK^T overlapping the previous softmax, measures
+// about 0.6 of it). The time is at least the unique K and V bytes at HBM speed (about
+// 13 MB per unit). With s > 1 it adds the merge: its launch (2.5 units) and the fp32
+// partials written and read back. A larger s must be at least 2 % faster to be taken.
+// Decoding, 64 (sequence, K/V head) tasks over 256 key blocks on 152 SMs: two-tile
+// tasks take 7 ranges (three rounds of 448 tasks, rather than 2 ranges leaving 24 SMs
+// idle); solo tasks take 2 (one wave at the HBM floor: 164 against 168 us with 7).
+// Cached per shape (a decoding loop asks every step).
 int choose_splits_fixed(int requested, int B, int H, int H_kv, int num_m, int task_rows, int N_q, int N_kv, int d,
                         int gshift, bool causal, int sm_count) {
   const int key_blocks = (N_kv + fa::kBlockN - 1) / fa::kBlockN;
@@ -145,6 +141,8 @@ int choose_splits_fixed(int requested, int B, int H, int H_kv, int num_m, int ta
     nb[m] = kmax > 0 ? (int)((kmax + fa::kBlockN - 1) / fa::kBlockN) : 0;
   }
   const int limit = std::min(64, key_blocks);
+  const double step = task_rows == fa::kBlockM ? 0.6 : 1.0;            // units per K/V block
+  const double kv_floor = 4.0 * B * H_kv * (double)N_kv * d / 13e6;     // K and V once from HBM
   int best = 1;
   double best_time = -1.0;
   std::vector<double> costs;
@@ -155,7 +153,7 @@ int choose_splits_fixed(int requested, int B, int H, int H_kv, int num_m, int ta
       for (int m = 0; m < num_m; ++m)
         for (int r = 0; r < sp; ++r) {
           const int len = std::max(0, std::min(nb[m], (r + 1) * per) - r * per);
-          costs.push_back(len > 0 ? len + 2.0 : 1.0);
+          costs.push_back(len > 0 ? len * step + 2.0 : 1.0);
         }
     std::sort(costs.begin(), costs.end(), std::greater<double>());
     std::priority_queue<double, std::vector<double>, std::greater<double>> load;
@@ -167,11 +165,12 @@ int choose_splits_fixed(int requested, int B, int H, int H_kv, int num_m, int ta
       load.push(t);
       makespan = std::max(makespan, t);
     }
+    makespan = std::max(makespan, kv_floor);
     if (sp > 1) {
       const double partial_bytes = 2.0 * sp * (double)B * N_q * H * d * sizeof(float);
       makespan += 2.5 + partial_bytes / 13e6;
     }
-    if (best_time < 0 || makespan < best_time - 1e-9) {
+    if (best_time < 0 || makespan < 0.98 * best_time) {
       best_time = makespan;
       best = sp;
     }
