@@ -166,8 +166,8 @@ struct Layout {
                        bCorrEmpty = bCorrFull + 2, bOFinal = bCorrEmpty + 2, bDrain = bOFinal + 2,
                        bTaskFull = bDrain + 1, bTaskEmpty = bTaskFull + 2, bClc = bTaskEmpty + 2,
                        bOstReady = bClc + 1, bOstFree = bOstReady + 1, bTurn = bOstFree + 1,
-                       bStats = bTurn + 2, bPVDone = bStats + 2;
-  static constexpr int kNumBars = bPVDone + 1;
+                       bStats = bTurn + 2, bPVDone = bStats + 2, bXchg = bPVDone + 1, bRowSum = bXchg + 2;
+  static constexpr int kNumBars = bRowSum + 1;
   static constexpr int kMailOff = kBarOff + ((kNumBars * 8 + 127) / 128) * 128;
   static constexpr int kMiscOff = kMailOff + 2 * kBlockM * 4;  // tmem slot, abort flags, task ring
   static constexpr int kClcOff = kMiscOff + 64;                 // 16-byte launch-control response
@@ -483,6 +483,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     }
     mbar_init(bar(L::bDrain), 1);
     mbar_init(bar(L::bPVDone), 1);   // solo tasks: one phase per key block, once its PV has completed
+    for (int i = 0; i < 2; ++i) mbar_init(bar(L::bXchg + i), 2 * kBlockM);   // solo: partial maxima swapped
+    mbar_init(bar(L::bRowSum), kBlockM);   // solo: WG1's row sums handed to WG0
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(L::bTaskFull + i), 1);
       mbar_init(bar(L::bTaskEmpty + i), kTaskConsumerWarps);
@@ -686,12 +688,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
               if (!w.wait(bar(L::bPO + b), (po_par >> b) & 1, L::bPO + b, j)) { ok = false; break; }
               po_par ^= 1u << b;
               tc_fence_after();
-              if (leader) issue_pv<D, 0, kSplitP, F16>(O0, b ? P1 : P0, Vd + vs * kStageStep, i > 0);
+              // P of keys 0-63 in columns [0, 32) of the score tile, of keys 64-127 in [64, 96)
+              if (leader) issue_pv<D, 0, kSplitP, F16>(O0, b ? S1 : S0, Vd + vs * kStageStep, i > 0);
               if (!w.wait(bar(L::bP2 + b), (p2_par >> b) & 1, L::bP2 + b, j)) { ok = false; break; }
               p2_par ^= 1u << b;
               tc_fence_after();
               if (leader) {
-                issue_pv<D, kSplitP, kBlockN, F16>(O0, b ? P1 : P0, Vd + vs * kStageStep, true);
+                issue_pv<D, kSplitP, kBlockN, F16>(O0, (b ? S1 : S0) + 32, Vd + vs * kStageStep, true);
                 mma_commit(bar(L::bKVEmpty + vs));
                 mma_commit(bar(L::bPVDone));                         // O holds blocks 0 .. i
                 if (i == nb - 1) mma_commit(bar(L::bOFinal + 0));
@@ -821,6 +824,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     const float sl2 = p.scale_log2;
     uint32_t s_par = 0, ce_par = 0;   // parity of the next wait on s_full / corr_empty (solo: bit = tile)
     uint32_t turns = 0;   // exponential phases taken in turn so far (stagger mode)
+    uint32_t x_par = 0, rs_par = 0;   // solo: bit b: next wait on xchg[b]; bit 0: on row_sum
     // Stagger mode ("Flash Attention 4", section "论文与当前 TIRx 实现的差异": the two
     // softmax warpgroups' exponential phases do not overlap): the warpgroups pass a
     // turn back and forth through bTurn, WG0 first. In a task of both tiles each takes
@@ -849,8 +853,138 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           else if (p.lse != nullptr) p.lse[li] = v;
         }
       };
-      constexpr bool solo = SOLO;   // one Q tile, run by WG0 over both score tiles
-      if (t == 1 && solo) continue;
+      if constexpr (SOLO) {
+        // Solo task: both warpgroups work on the one Q tile, warpgroup t on key columns
+        // [64 t, 64 t + 64) of every block (half a softmax each). Per block they swap
+        // their partial row maxima through shared memory (slot b = i & 1 of the second
+        // Q buffer, unused by solo tasks) and take the same reference and acc_scale; each
+        // keeps the row sum of its own columns, and WG1 hands its sum to WG0 at the end.
+        // P of WG0's keys goes to columns [0, 32) of the score tile and WG1's to
+        // [64, 96) (columns each has itself read); WG0 passes acc_scale in column 32.
+        float* xm = reinterpret_cast<float*>(smem + L::kQOff + L::kTileBytes);   // [2 blocks][2 halves][128]
+        float* ysum = xm + 4 * kBlockM;                                          // [128] WG1's row sums
+        if (kr.hi <= kr.lo) {   // no key for any row of the task: LSE = -inf (O = 0 is written by WG2)
+          if (t == 0) store_lse(-INFINITY);
+          continue;
+        }
+        const int nb = kr.hi - kr.lo;
+        const int c0 = t * 64;   // this warpgroup's first key column of a block
+        const int tp0 = packed_pos(tk, 0, p.gshift);   // both warpgroups: the rows of Q tile 0
+        const int row_limit = CAUSAL ? min(tp0 + (r >> p.gshift) + off + 1, tk.lenk) : tk.lenk;  // keys [0, row_limit)
+        float row_max = -INFINITY, row_sum = 0.f;
+        for (int i = 0; i < nb; ++i) {
+          const int j = kr.hi - 1 - i, b = i & 1;
+          const uint32_t tS = tmem + lane_base + L::col_s(b);
+          if (!w.wait(bar(L::bSFull + b), (s_par >> b) & 1, L::bSFull + b, j)) { ok = false; break; }
+          s_par ^= 1u << b;
+          tr.rec(kEvSFull, j);
+          tc_fence_after();
+          const int k0 = j * kBlockN + c0;   // key of this warpgroup's first column
+          const bool need_mask = (k0 + 64 > tk.lenk) || (CAUSAL && k0 + 63 > tp0 + off);
+          const int lim = need_mask ? row_limit - k0 : 64;   // columns [lim, 64) are masked
+          float s[64];
+          uint32_t u[64];
+          tmem_ld32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+          tmem_ld32(tS + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+          tmem_wait_ld();
+          float mx0 = -INFINITY, mx1 = -INFINITY;
+          if (need_mask) {
+#pragma unroll
+            for (int c = 0; c < 64; c += 4) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) s[c + e] = (c + e < lim) ? __uint_as_float(u[c + e]) : -INFINITY;
+              mx0 = max3(mx0, s[c], s[c + 1]);
+              mx1 = max3(mx1, s[c + 2], s[c + 3]);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 64; c += 4) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) s[c + e] = __uint_as_float(u[c + e]);
+              mx0 = max3(mx0, s[c], s[c + 1]);
+              mx1 = max3(mx1, s[c + 2], s[c + 3]);
+            }
+          }
+          const float part = fmaxf(mx0, mx1);
+          xm[(b * 2 + t) * kBlockM + r] = part;
+          mbar_arrive(bar(L::bXchg + b));
+          if (!w.wait(bar(L::bXchg + b), (x_par >> b) & 1, L::bXchg + b, j)) { ok = false; break; }
+          x_par ^= 1u << b;
+          const float blk_max = fmaxf(part, xm[(b * 2 + (t ^ 1)) * kBlockM + r]);
+          tr.rec(kEvSMax, j);
+          // delayed-rescale rule, on the whole row's maximum (the same in both warpgroups)
+          float ref, acc;
+          if (i == 0) {
+            ref = blk_max;
+            acc = 1.f;
+          } else {
+            const float cand = fmaxf(row_max, blk_max);
+            const float cand_safe = cand == -INFINITY ? 0.f : cand;
+            const float delta = (row_max - cand_safe) * sl2;
+            if (delta >= -p.tau && row_max != -INFINITY) {
+              ref = row_max;
+              acc = 1.f;
+            } else {
+              ref = cand;
+              acc = ex2_approx(delta);
+            }
+          }
+          row_max = ref;
+          if (i > 0 && t == 0) {   // acc_scale to WG2 before the exponentials
+            if (p.stats_tmem) {
+              tmem_st1(tS + 32, __float_as_uint(acc));
+              tmem_wait_st();
+              tc_fence_before();
+            } else {
+              if (!w.wait(bar(L::bCorrEmpty + b), ((ce_par >> b) & 1) ^ 1, L::bCorrEmpty + b, j)) { ok = false; break; }
+              ce_par ^= 1u << b;
+              mail[b * kBlockM + r] = acc;
+            }
+            mbar_arrive(bar(L::bCorrFull + b));
+            tr.rec(kEvMail, j);
+          }
+          const float ref_safe = ref == -INFINITY ? 0.f : ref;
+          const uint64_t scale2 = pack2(sl2, sl2);
+          const uint64_t bias2 = pack2(-ref_safe * sl2, -ref_safe * sl2);
+          uint64_t sum2a = 0, sum2b = 0;
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            float x0, x1;
+            unpack2(fma2(pack2(s[c], s[c + 1]), scale2, bias2), x0, x1);
+            const uint64_t pp = pack2(ex2_approx(x0), ex2_approx(x1));
+            if (c & 2) sum2b = add2(sum2b, pp); else sum2a = add2(sum2a, pp);
+            pk[c >> 1] = pack_16x2_u64<F16>(pp);
+          }
+          tmem_st32(tS + (t == 0 ? 0 : 64), pk);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar(t == 0 ? L::bPO + b : L::bP2 + b));
+          tr.rec(t == 0 ? kEvHalf1 : kEvHalf2, j);
+          float sa, sb;
+          unpack2(add2(sum2a, sum2b), sa, sb);
+          row_sum = row_sum * acc + (sa + sb);
+        }
+        if (!ok) break;
+        if (t == 1) {   // this half's row sums to WG0
+          ysum[r] = row_sum;
+          mbar_arrive(bar(L::bRowSum));
+          continue;
+        }
+        if (!w.wait(bar(L::bRowSum), rs_par & 1, L::bRowSum, -1)) { ok = false; break; }
+        rs_par ^= 1u;
+        row_sum += ysum[r];
+        // final statistics to WG2 (row_sum), LSE straight to global memory
+        if (!w.wait(bar(L::bCorrEmpty + 0), (ce_par & 1) ^ 1, L::bCorrEmpty + 0, -1)) { ok = false; break; }
+        ce_par ^= 1u;
+        mail[r] = row_sum;
+        mbar_arrive(bar(p.stats_tmem ? L::bStats + 0 : L::bCorrFull + 0));
+        tr.rec(kEvStats, -1);
+        const float ref_safe = row_max == -INFINITY ? 0.f : row_max;
+        store_lse(row_sum > 0.f ? (lg2_approx(row_sum) + ref_safe * sl2) * 0.69314718055994531f : -INFINITY);
+        continue;
+      }
+      constexpr bool solo = SOLO;   // (two-tile kernels: false)
       if (kr.hi <= kr.lo) {   // no key for any row of the task: LSE = -inf (O = 0 is written by WG2)
         store_lse(-INFINITY);
         continue;
@@ -1097,7 +1231,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           float a;
           if (p.stats_tmem) {
             tc_fence_after();
-            a = __uint_as_float(tmem_ld1(tmem + lane_base + L::col_s(b)));
+            a = __uint_as_float(tmem_ld1(tmem + lane_base + L::col_s(b) + (solo ? 32u : 0u)));
             tmem_wait_ld();
           } else {
             a = mail[b * kBlockM + r];

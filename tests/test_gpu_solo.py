@@ -1,9 +1,10 @@
 """Solo tasks of the forward: one 128-row Q tile per task, its score tile alternating
 between the two S buffers of tensor memory so that a key block's QK^T overlaps the
-previous block's softmax (the library's choice when the two-tile tasks would leave SMs
-idle). Every row still visits the same key blocks in the same order with the same
-arithmetic, so solo and two-tile tasks must give the same bits; both must match the
-fp64 oracle (O <= 2e-2, LSE <= 1e-3 max-abs).
+previous block's softmax, and both softmax warpgroups sharing the tile (64 key columns
+each). Every row visits the same key blocks in the same order with the same reference
+and the same P, so O and the LSE differ from two-tile tasks only through the row sum's
+summation order (two partial sums): at most one 16-bit unit in the last place of O and
+1e-5 in the LSE. Both must match the fp64 oracle (O <= 2e-2, LSE <= 1e-3 max-abs).
 
 The shapes cover an even and an odd number of key blocks per task, one block, grouped
 heads up to G = 128, N_q != N_kv (causal rows without keys), key splits, decoding, and
@@ -59,6 +60,20 @@ def run(q, k, v, causal, splits, solo, stats_tmem=1):
     return host(o), host(lse)
 
 
+def same_up_to_row_sum_order(a, b, what):
+    """O within one bf16 unit in the last place (2^-7 relative) plus 1e-5 absolute (an
+    output merged from key ranges can cancel to near zero while the ranges' own rounding
+    is relative to their larger partial outputs), LSE within 1e-5."""
+    bad = np.abs(a[0] - b[0]) > 2.0 ** -7 * np.abs(b[0]) + 1e-5
+    if bad.any():
+        idx = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{what}: O differs at {int(bad.sum())} elements, first {idx}: "
+                             f"{a[0][idx]} against {b[0][idx]}")
+    fin = np.isfinite(b[1])
+    assert (np.isfinite(a[1]) == fin).all(), what
+    assert np.abs(a[1][fin] - b[1][fin]).max(initial=0.0) <= 1e-5, f"{what}: LSE differs"
+
+
 def check(o, lse, o_ref, l_ref, what):
     assert np.isfinite(o).all(), what
     err_o = np.abs(o - o_ref).max()
@@ -89,7 +104,7 @@ def test_solo_matches_two_tile_tasks_and_oracle(shape, causal):
     q, k, v = fa_inputs.make_qkv(B, Nq, H, d, seed=8000 + Nq + Nk + H, Nkv=Nk, Hkv=Hkv)
     solo = run(q, k, v, causal, splits, 1)
     two = run(q, k, v, causal, splits, 0)
-    assert np.array_equal(solo[0], two[0]) and np.array_equal(solo[1], two[1]), "solo differs from two-tile tasks"
+    same_up_to_row_sum_order(solo, two, f"{shape} causal={causal}")
     o_ref, l_ref = oracle.attention(q, k, v, 1 / math.sqrt(d), causal)
     check(solo[0], solo[1], o_ref, l_ref, f"{shape} causal={causal}")
 
@@ -101,6 +116,6 @@ def test_solo_rescales_wait_for_the_previous_pv(stats_tmem):
     q, k, v = fa_inputs.make_qkv(1, 1500, 4, 128, seed=20264, spiky=True)
     solo = run(q, k, v, True, 1, 1, stats_tmem)
     two = run(q, k, v, True, 1, 0, stats_tmem)
-    assert np.array_equal(solo[0], two[0]) and np.array_equal(solo[1], two[1])
+    same_up_to_row_sum_order(solo, two, f"spiky stats_tmem={stats_tmem}")
     o_ref, l_ref = oracle.attention(q, k, v, 1 / math.sqrt(128), True)
     check(solo[0], solo[1], o_ref, l_ref, f"spiky stats_tmem={stats_tmem}")
