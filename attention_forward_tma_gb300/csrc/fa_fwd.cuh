@@ -817,12 +817,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     const int t = warp >> 2;                 // Q tile of this warpgroup
     const int r = tid & 127;                 // row within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tS_t = tmem + lane_base + L::col_s(t);   // this warpgroup's score tile (solo: per block)
+    const uint32_t tS = tmem + lane_base + L::col_s(t);   // two-tile tasks: this warpgroup's score tile
+    const uint32_t tP = tS + 64;
     Waiter w{abort_flag, p.timeout_ns, t == 0 ? kRoleSoftmax0 : kRoleSoftmax1};
     Tracer tr;
     tr.init(p, 2 + t, r == 0);
     const float sl2 = p.scale_log2;
-    uint32_t s_par = 0, ce_par = 0;   // parity of the next wait on s_full / corr_empty (solo: bit = tile)
+    uint32_t s_par = 0, ce_par = 0;   // parity of the next wait on s_full / corr_empty (solo: bit b for [b])
     uint32_t turns = 0;   // exponential phases taken in turn so far (stagger mode)
     uint32_t x_par = 0, rs_par = 0;   // solo: bit b: next wait on xchg[b]; bit 0: on row_sum
     // Stagger mode ("Flash Attention 4", section "论文与当前 TIRx 实现的差异": the two
@@ -984,7 +985,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         store_lse(row_sum > 0.f ? (lg2_approx(row_sum) + ref_safe * sl2) * 0.69314718055994531f : -INFINITY);
         continue;
       }
-      constexpr bool solo = SOLO;   // (two-tile kernels: false)
+      // two-tile task: this warpgroup runs Q tile t alone
       if (kr.hi <= kr.lo) {   // no key for any row of the task: LSE = -inf (O = 0 is written by WG2)
         store_lse(-INFINITY);
         continue;
@@ -1004,12 +1005,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
 #endif
       for (int i = 0; i < nb; ++i) {
         const int j = hi - 1 - i;
-        const int pb = solo ? (i & 1) : 0;   // parity bit of this block's barriers
-        const int b = solo ? pb : t;          // the score tile (and barrier set) of this block
-        const uint32_t tS = solo ? tmem + lane_base + L::col_s(b) : tS_t;
-        const uint32_t tP = tS + 64;
-        if (!w.wait(bar(L::bSFull + b), (s_par >> pb) & 1, L::bSFull + b, j)) { ok = false; break; }
-        s_par ^= 1u << pb;
+        if (!w.wait(bar(L::bSFull + t), s_par & 1, L::bSFull + t, j)) { ok = false; break; }
+        s_par ^= 1u;
         tr.rec(kEvSFull, j);
         tc_fence_after();
         const int k0 = j * kBlockN;
@@ -1093,11 +1090,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             tmem_wait_st();
             tc_fence_before();
           } else {
-            if (!w.wait(bar(L::bCorrEmpty + b), ((ce_par >> pb) & 1) ^ 1, L::bCorrEmpty + b, j)) { ok = false; break; }
-            ce_par ^= 1u << pb;
-            mail[b * kBlockM + r] = acc;
+            if (!w.wait(bar(L::bCorrEmpty + t), (ce_par & 1) ^ 1, L::bCorrEmpty + t, j)) { ok = false; break; }
+            ce_par ^= 1u;
+            mail[t * kBlockM + r] = acc;
           }
-          mbar_arrive(bar(L::bCorrFull + b));
+          mbar_arrive(bar(L::bCorrFull + t));
           tr.rec(kEvMail, j);
         }
         if (stagger && !take_turn(j)) { ok = false; break; }
@@ -1137,7 +1134,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           tmem_st32(tP + h * 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[h * 32]));
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(bar(h == 0 ? L::bPO + b : L::bP2 + b));
+          mbar_arrive(bar(h == 0 ? L::bPO + t : L::bP2 + t));
           tr.rec(h == 0 ? kEvHalf1 : kEvHalf2, j);
         }
         if (stagger) mbar_arrive(bar(L::bTurn + (t ^ 1)));   // the other warpgroup's turn
