@@ -119,3 +119,20 @@ def test_solo_rescales_wait_for_the_previous_pv(stats_tmem):
     same_up_to_row_sum_order(solo, two, f"spiky stats_tmem={stats_tmem}")
     o_ref, l_ref = oracle.attention(q, k, v, 1 / math.sqrt(128), True)
     check(solo[0], solo[1], o_ref, l_ref, f"spiky stats_tmem={stats_tmem}")
+
+
+@pytest.mark.parametrize("shape", [(4, 32, 8, 1, 16384), (2, 8, 8, 1024, 1024), (1, 32, 8, 1, 4096)],
+                         ids=lambda s: "B%dH%dKV%dNq%dNk%d" % s)
+def test_split_query_matches_the_call(shape):
+    """fa_fwd_kv_splits reports the key ranges a num_splits=0 call uses (with the task
+    size the library picks): the call with that count given explicitly is bit-identical."""
+    import torch
+    B, H, Hkv, Nq, Nk = shape
+    q, k, v = fa_inputs.make_qkv(B, Nq, H, 128, seed=8100 + B + Nq, Nkv=Nk, Hkv=Hkv)
+    qd, kd, vd = dev(q), dev(k), dev(v)
+    n = fa.num_splits(B, H, Hkv, Nq, Nk, 0, causal=True, d=128)
+    a = fa.fa_fwd(qd, kd, vd, causal=True, num_splits=0)
+    b = fa.fa_fwd(qd, kd, vd, causal=True, num_splits=n)
+    st, word = fa.last_device_status()
+    assert st == fa.FA_OK, hex(word)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
