@@ -1228,6 +1228,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           float a;
           if (p.stats_tmem) {
             tc_fence_after();
+            // acc_scale: column 0 of the tile's score tile; solo tasks: column 32 (WG0's half)
             a = __uint_as_float(tmem_ld1(tmem + lane_base + L::col_s(b) + (solo ? 32u : 0u)));
             tmem_wait_ld();
           } else {
