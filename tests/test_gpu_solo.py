@@ -136,3 +136,24 @@ def test_split_query_matches_the_call(shape):
     st, word = fa.last_device_status()
     assert st == fa.FA_OK, hex(word)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_solo_fp16(d):
+    """fp16 inputs through the solo kernel (P in fp16, tau capped at 15), grouped heads."""
+    import torch
+    q, k, v = fa_inputs.make_qkv(1, 333, 8, d, seed=8200 + d, Hkv=2, dtype="f16")
+    to = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.float16).cuda()
+    out = {}
+    for solo in (1, 0):
+        fa.set_option("solo_tiles", solo)
+        try:
+            o, lse = fa.fa_fwd(to(q), to(k), to(v), causal=True)
+            st, word = fa.last_device_status()
+        finally:
+            fa.set_option("solo_tiles", -1)
+        assert st == fa.FA_OK, hex(word)
+        out[solo] = (o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64))
+    same_up_to_row_sum_order(out[1], out[0], f"fp16 d={d}")
+    o_ref, l_ref = oracle.attention(q, k, v, 1 / math.sqrt(d), True, dtype="f16")
+    check(out[1][0], out[1][1], o_ref, l_ref, f"fp16 d={d}")
