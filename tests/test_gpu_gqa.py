@@ -33,6 +33,15 @@ def cuda():
     fa.set_option("persistent", -1)
 
 
+@pytest.fixture(params=["two_tile", "auto"], autouse=True)
+def task_shape(request):
+    """Every test twice: with two-tile tasks forced, and with the library's choice
+    (small shapes then run as solo tasks)."""
+    fa.set_option("solo_tiles", 0 if request.param == "two_tile" else -1)
+    yield request.param
+    fa.set_option("solo_tiles", -1)
+
+
 def tdtype(dtype):
     import torch
     return torch.float16 if dtype == "f16" else torch.bfloat16

@@ -37,6 +37,15 @@ def cuda():
     fa.set_option("stats_tmem", 1)
 
 
+@pytest.fixture(params=["two_tile", "auto"], autouse=True)
+def task_shape(request):
+    """Every test twice: with two-tile tasks forced, and with the library's choice
+    (small shapes then run as solo tasks)."""
+    fa.set_option("solo_tiles", 0 if request.param == "two_tile" else -1)
+    yield request.param
+    fa.set_option("solo_tiles", -1)
+
+
 def dev(bits):
     import torch
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
