@@ -71,6 +71,8 @@ def library() -> ctypes.CDLL:
     """Load (building first if needed) the in-tree libfa_gb300.so, or its tracing
     build libfa_gb300_trace.so when the environment sets FA_GB300_TRACE=1."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             path = _build.build(trace=os.environ.get("FA_GB300_TRACE", "0") == "1")
@@ -144,8 +146,8 @@ def fa_fwd(q, k, v, *, scale: float | None = None, causal: bool = False, out=Non
     defaults to 1/sqrt(d). num_splits > 1 cuts the keys into ranges computed in
     parallel and merged through their LSE (0: the library decides)."""
     torch = _torch()
-    code = _dtype_code(q)
-    _need(q, "q", q.dtype, 4)
+    _need(q, "q", (torch.bfloat16, torch.float16), 4)
+    code = FA_DTYPE_FP16 if q.dtype == torch.float16 else FA_DTYPE_BF16
     B, N, H, d = q.shape
     Nk, Hkv = (k.shape[1], k.shape[2]) if isinstance(k, torch.Tensor) and k.dim() == 4 else (N, H)
     for name, t in (("k", k), ("v", v)):
