@@ -54,7 +54,8 @@ namespace fa {
 constexpr int kBlockM = 128;          // rows of one Q tile
 constexpr int kBlockN = 128;          // keys of one K/V block
 constexpr int kTaskRows = 2 * kBlockM;
-constexpr int kSplitP = 64;           // P is handed to the PV MMA in two column halves
+constexpr int kSplitP = 96;           // two-tile tasks hand P to the PV MMA as keys [0, 96) and [96, 128)
+constexpr int kSoloSplitP = 64;       // solo tasks: one half per softmax warpgroup
 constexpr int kThreads = 512;
 constexpr uint32_t kTmemCols = 512;
 
@@ -469,8 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       mbar_init(bar(L::bQFull + i), 1);
       mbar_init(bar(L::bQEmpty + i), 1);
       mbar_init(bar(L::bSFull + i), 1);
-      mbar_init(bar(L::bPO + i), 2 * kBlockM);      // P[:, :64] stored (softmax WG) + O ready (WG2)
-      mbar_init(bar(L::bP2 + i), kBlockM);          // P[:, 64:] stored (softmax WG)
+      mbar_init(bar(L::bPO + i), 2 * kBlockM);      // first part of P stored (softmax) + O ready (WG2)
+      mbar_init(bar(L::bP2 + i), kBlockM);          // the rest of P stored (softmax)
       mbar_init(bar(L::bCorrFull + i), kBlockM);
       mbar_init(bar(L::bCorrEmpty + i), kBlockM);
       mbar_init(bar(L::bOFinal + i), 1);
@@ -689,12 +690,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
               po_par ^= 1u << b;
               tc_fence_after();
               // P of keys 0-63 in columns [0, 32) of the score tile, of keys 64-127 in [64, 96)
-              if (leader) issue_pv<D, 0, kSplitP, F16>(O0, b ? S1 : S0, Vd + vs * kStageStep, i > 0);
+              if (leader) issue_pv<D, 0, kSoloSplitP, F16>(O0, b ? S1 : S0, Vd + vs * kStageStep, i > 0);
               if (!w.wait(bar(L::bP2 + b), (p2_par >> b) & 1, L::bP2 + b, j)) { ok = false; break; }
               p2_par ^= 1u << b;
               tc_fence_after();
               if (leader) {
-                issue_pv<D, kSplitP, kBlockN, F16>(O0, (b ? S1 : S0) + 32, Vd + vs * kStageStep, true);
+                issue_pv<D, kSoloSplitP, kBlockN, F16>(O0, (b ? S1 : S0) + 32, Vd + vs * kStageStep, true);
                 mma_commit(bar(L::bKVEmpty + vs));
                 mma_commit(bar(L::bPVDone));                         // O holds blocks 0 .. i
                 if (i == nb - 1) mma_commit(bar(L::bOFinal + 0));
@@ -1109,7 +1110,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
 #pragma unroll
-          for (int g = h * 4; g < h * 4 + 4; ++g) {
+          for (int g = (h ? kSplitP / 16 : 0); g < (h ? kBlockN / 16 : kSplitP / 16); ++g) {
             if (EMU && g < emu) {
 #pragma unroll
               for (int e = 0; e < 16; e += 2) {
@@ -1130,8 +1131,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
               }
             }
           }
-          // this half of P over the upper half of S_t (all of S was read above)
-          tmem_st32(tP + h * 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[h * 32]));
+          // this part of P (keys [0, 96), then [96, 128)) over the upper half of S_t (all of S was read above)
+          static_assert(kSplitP == 96, "P is stored as 48 + 16 columns");
+          if (h == 0) {
+            tmem_st32(tP, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+            tmem_st16(tP + 32, *reinterpret_cast<const uint32_t(*)[16]>(&pk[32]));
+          } else {
+            tmem_st16(tP + 48, *reinterpret_cast<const uint32_t(*)[16]>(&pk[48]));
+          }
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(bar(h == 0 ? L::bPO + t : L::bP2 + t));
