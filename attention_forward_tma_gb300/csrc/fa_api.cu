@@ -194,6 +194,19 @@ int task_rows_fixed(int B, int H_kv, int N_q, int gshift, int sm_count) {
   return (t256 < sm_count && t128 <= sm_count) ? fa::kBlockM : fa::kTaskRows;
 }
 
+// Varlen: the same rule on an upper bound of the work tiles, H_kv * (ceil(total_q * G / rows)
+// + num_seqs) (a sequence adds at most one partial tile).
+long long varlen_tiles(long long total_q, int num_seqs, int H_kv, int gshift, int rows) {
+  return (long long)H_kv * (((total_q << gshift) + rows - 1) / rows + num_seqs);
+}
+int task_rows_varlen(long long total_q, int num_seqs, int H_kv, int gshift, int sm_count) {
+  if (g_opt.solo == 0 || g_opt.emu_groups > 0) return fa::kTaskRows;
+  if (g_opt.solo == 1) return fa::kBlockM;
+  return (varlen_tiles(total_q, num_seqs, H_kv, gshift, fa::kTaskRows) < sm_count &&
+          varlen_tiles(total_q, num_seqs, H_kv, gshift, fa::kBlockM) <= sm_count)
+             ? fa::kBlockM : fa::kTaskRows;
+}
+
 int choose_splits(int requested, long long base_tasks, int key_blocks, int sm_count) {
   const int most = key_blocks < 1 ? 1 : (key_blocks < kMaxSplits ? key_blocks : kMaxSplits);
   if (requested > 0) return requested < most ? requested : most;
@@ -317,7 +330,7 @@ int grid_for(const fa::FwdParams& p, const DevInfo* dev, int n_tasks) {
 namespace fa {
 constexpr int kSchedBuckets = 4096;
 
-// One CTA: enumerate the (sequence, 256-row block, key range) work tiles, bucket
+// One CTA: enumerate the (sequence, rows-row block, key range) work tiles, bucket
 // them by their number of K/V blocks, and write them longest first, each
 // followed by all Hkv K/V heads ("FlashAttention-4（下）" (argus lesson 7),
 // section "6. LPT 调度": sort work tiles by their cost, write a virtual -> actual
@@ -327,19 +340,19 @@ constexpr int kSchedBuckets = 4096;
 // write the rows' empty result.
 __global__ void __launch_bounds__(1024) fa_varlen_schedule_kernel(const int* cu_q, const int* cu_k, int num_seqs,
                                                                   int Hkv, int gshift, int causal, int splits,
-                                                                  int capacity, int4* tasks, int* count) {
+                                                                  int rows, int capacity, int4* tasks, int* count) {
   __shared__ int hist[kSchedBuckets];
   __shared__ int total_tiles;
   for (int i = threadIdx.x; i < kSchedBuckets; i += blockDim.x) hist[i] = 0;
   if (threadIdx.x == 0) total_tiles = 0;
   __syncthreads();
   auto cost_of = [&](int m, int Lq, int Lk, int sp) {
-    const KRange r = key_range(m * kTaskRows, kTaskRows, Lq, Lk, gshift, causal != 0, splits, sp);
+    const KRange r = key_range(m * rows, rows, Lq, Lk, gshift, causal != 0, splits, sp);
     return min(r.hi - r.lo, kSchedBuckets - 1);
   };
   for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
     const int Lq = max(cu_q[s + 1] - cu_q[s], 0), Lk = max(cu_k[s + 1] - cu_k[s], 0);
-    const int nm = ((Lq << gshift) + kTaskRows - 1) / kTaskRows;
+    const int nm = ((Lq << gshift) + rows - 1) / rows;
     for (int m = 0; m < nm; ++m)
       for (int sp = 0; sp < splits; ++sp) atomicAdd(&hist[cost_of(m, Lq, Lk, sp)], 1);
     atomicAdd(&total_tiles, nm * splits);
@@ -360,7 +373,7 @@ __global__ void __launch_bounds__(1024) fa_varlen_schedule_kernel(const int* cu_
   __syncthreads();
   for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
     const int Lq = max(cu_q[s + 1] - cu_q[s], 0), Lk = max(cu_k[s + 1] - cu_k[s], 0);
-    const int nm = ((Lq << gshift) + kTaskRows - 1) / kTaskRows;
+    const int nm = ((Lq << gshift) + rows - 1) / rows;
     for (int m = 0; m < nm; ++m) {
       for (int sp = 0; sp < splits; ++sp) {
         const int c = cost_of(m, Lq, Lk, sp);
@@ -703,14 +716,14 @@ int varlen_check(const void* q, const void* k, const void* v, void* o, float* ls
 // varlen call whose task list lives in tasks[0, cap) with its count at *count.
 int varlen_launch(DevInfo* dev, const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_q,
                   const int* cu_k, int num_seqs, int total_q, int total_k, int H, int H_kv, int gshift, int d,
-                  float scale, int causal, bool f16, int splits, const Partials* parts, int4* tasks, int* count,
-                  int cap, cudaStream_t s) {
+                  float scale, int causal, bool f16, int splits, int rows, const Partials* parts, int4* tasks,
+                  int* count, int cap, cudaStream_t s) {
   fa::FwdParams p;
   std::memset(&p, 0, sizeof p);
   int st = make_maps(p, q, k, v, o, total_q, total_k, H, H_kv, d, f16);
   if (st != FA_OK) return st;
-  fa::fa_varlen_schedule_kernel<<<1, 1024, 0, s>>>(cu_q, cu_k, num_seqs, H_kv, gshift, causal, splits, cap, tasks,
-                                                   count);
+  fa::fa_varlen_schedule_kernel<<<1, 1024, 0, s>>>(cu_q, cu_k, num_seqs, H_kv, gshift, causal, splits, rows, cap,
+                                                   tasks, count);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   p.o = static_cast<uint16_t*>(o);
   p.lse = lse;
@@ -724,7 +737,7 @@ int varlen_launch(DevInfo* dev, const void* q, const void* k, const void* v, voi
   p.total_tokens = total_q;
   p.num_tasks = cap;
   p.varlen = 1;
-  p.task_rows = fa::kTaskRows;
+  p.task_rows = rows;
   p.splits = splits;
   if (splits > 1) {
     p.o_part = parts->o_part;
@@ -753,6 +766,8 @@ int fa_fwd_varlen_kv(const void* q, const void* k, const void* v, void* o, float
   if (st != FA_OK) return st;
   DevInfo* dev = nullptr;
   if ((st = device_info(&dev)) != FA_OK) return st;
+  const int rows = task_rows_varlen(total_q, num_seqs, H_kv, gshift, dev->sm_count);
+  base = varlen_tiles(total_q, num_seqs, H_kv, gshift, rows);
   const int splits = choose_splits(num_splits, base, (max_seqlen_kv + fa::kBlockN - 1) / fa::kBlockN,
                                    dev->sm_count);
   const long long cap = base * splits;
@@ -766,7 +781,7 @@ int fa_fwd_varlen_kv(const void* q, const void* k, const void* v, void* o, float
   int4* tasks = static_cast<int4*>(ws.base);
   int* count = reinterpret_cast<int*>(static_cast<char*>(ws.base) + (size_t)cap * sizeof(int4));
   st = varlen_launch(dev, q, k, v, o, lse, cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv, H, H_kv, gshift,
-                     d, scale, causal, f16, splits, &ws, tasks, count, (int)cap, s);
+                     d, scale, causal, f16, splits, rows, &ws, tasks, count, (int)cap, s);
   const int fst = ws.release(s);
   return st != FA_OK ? st : fst;
 }
@@ -812,7 +827,7 @@ int fa_fwd_varlen_kv_splits(int num_seqs, int total_q, int max_seqlen_kv, int H,
   DevInfo* dev = nullptr;
   if ((st = device_info(&dev)) != FA_OK) return st;
   const long long base =
-      (long long)H_kv * ((((long long)total_q << gshift) + fa::kTaskRows - 1) / fa::kTaskRows + num_seqs);
+      varlen_tiles(total_q, num_seqs, H_kv, gshift, task_rows_varlen(total_q, num_seqs, H_kv, gshift, dev->sm_count));
   *splits = choose_splits(num_splits, base, (max_seqlen_kv + fa::kBlockN - 1) / fa::kBlockN, dev->sm_count);
   return FA_OK;
 }
@@ -868,7 +883,8 @@ int fa_varlen_schedule(const int* cu_seqlens_q, const int* cu_seqlens_kv, int nu
   DevInfo* dev = nullptr;
   if ((st = device_info(&dev)) != FA_OK) return st;
   fa::fa_varlen_schedule_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(
-      cu_seqlens_q, cu_seqlens_kv, num_seqs, H_kv, gshift, causal, splits, capacity, static_cast<int4*>(tasks), count);
+      cu_seqlens_q, cu_seqlens_kv, num_seqs, H_kv, gshift, causal, splits, fa::kTaskRows, capacity,
+      static_cast<int4*>(tasks), count);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -883,12 +899,14 @@ int fa_fwd_varlen_noalloc(const void* q, const void* k, const void* v, void* o, 
   if (cap > kNoAllocMaxTasks) return FA_ERR_CAPACITY;
   DevInfo* dev = nullptr;
   if ((st = device_info(&dev)) != FA_OK) return st;
+  const int rows = task_rows_varlen(total_tokens, num_seqs, H, gshift, dev->sm_count);
+  cap = varlen_tiles(total_tokens, num_seqs, H, gshift, rows);   // solo only while this is at most the SM count
   int4* scratch = nullptr;
   if ((st = noalloc_scratch(&scratch)) != FA_OK) return st;
   int4* tasks = scratch;
   int* count = reinterpret_cast<int*>(scratch + kNoAllocMaxTasks);
   return varlen_launch(dev, q, k, v, o, lse, cu_seqlens, cu_seqlens, num_seqs, total_tokens, total_tokens, H, H,
-                       gshift, d, scale, causal, false, 1, nullptr, tasks, count, (int)cap,
+                       gshift, d, scale, causal, false, 1, rows, nullptr, tasks, count, (int)cap,
                        static_cast<cudaStream_t>(stream));
 }
 

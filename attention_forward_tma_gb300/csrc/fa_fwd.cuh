@@ -203,7 +203,7 @@ __device__ __forceinline__ bool get_task(const FwdParams& p, bool causal, int id
     const int4 e = p.tasks[idx];
     const int s0 = p.cu_seqlens[e.x], s1 = p.cu_seqlens[e.x + 1];
     const int k0 = p.cu_seqlens_k[e.x], k1 = p.cu_seqlens_k[e.x + 1];
-    t.kvh = e.y & 0xffff; t.split = e.y >> 16; t.row0 = e.z * kTaskRows; t.rows = kTaskRows;
+    t.kvh = e.y & 0xffff; t.split = e.y >> 16; t.row0 = e.z * ROWS; t.rows = ROWS;
     t.tok0 = s0; t.len = s1 - s0;
     t.tok0k = k0; t.lenk = k1 - k0;
     t.lse_base = (t.kvh << p.gshift) * p.total_tokens + s0;

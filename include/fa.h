@@ -325,8 +325,8 @@ int fa_last_device_status(void* stream, unsigned long long* detail);
  *                            (instead of two Q tiles sharing each K/V block). -1 = the
  *                            library's choice (default: when the 256-row tasks leave SMs
  *                            idle and the 128-row ones fit in one wave, e.g. decoding and
- *                            small batches), 0 = never, 1 = always. Varlen calls always
- *                            use two-tile tasks.
+ *                            small batches; for varlen calls the rule takes an upper bound
+ *                            of the work tiles), 0 = never, 1 = always.
  * The forward variants compute the same result as the default path.
  * Returns FA_OK or FA_ERR_INVALID_ARG.
  */

@@ -157,3 +157,44 @@ def test_solo_fp16(d):
     same_up_to_row_sum_order(out[1], out[0], f"fp16 d={d}")
     o_ref, l_ref = oracle.attention(q, k, v, 1 / math.sqrt(d), True, dtype="f16")
     check(out[1][0], out[1][1], o_ref, l_ref, f"fp16 d={d}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("lq,lk", [([7, 0, 129, 300, 1, 520], None), ([1, 1, 1, 1], [700, 1, 129, 4096])],
+                         ids=["self", "decode"])
+def test_solo_varlen(lq, lk, causal):
+    """Packed batches through solo tasks (the schedule kernel cuts 128-row tiles):
+    self-attention with empty and one-row sequences, and decoding (one query row per
+    sequence against its own key length), against two-tile tasks and the oracle."""
+    import torch
+    H, Hkv, d = 8, 2, 128
+    lk = lq if lk is None else lk
+    rng = np.random.default_rng(sum(lq) + 3 * sum(lk))
+    cu_q = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(lk)]).astype(np.int32)
+    q = fa_inputs.f32_to_bits(rng.standard_normal((int(cu_q[-1]), H, d), dtype=np.float32), "bf16")
+    k = fa_inputs.f32_to_bits(rng.standard_normal((int(cu_k[-1]), Hkv, d), dtype=np.float32), "bf16")
+    v = fa_inputs.f32_to_bits(rng.standard_normal((int(cu_k[-1]), Hkv, d), dtype=np.float32), "bf16")
+    cq, ck = torch.from_numpy(cu_q).cuda(), torch.from_numpy(cu_k).cuda()
+    out = {}
+    for solo in (1, 0):
+        fa.set_option("solo_tiles", solo)
+        try:
+            o, lse = fa.fa_fwd_varlen(dev(q), dev(k), dev(v), cq, max(lq), causal=causal, cu_seqlens_k=ck,
+                                      max_seqlen_k=max(lk), num_splits=0)
+            st, word = fa.last_device_status()
+        finally:
+            fa.set_option("solo_tiles", -1)
+        assert st == fa.FA_OK, hex(word)
+        out[solo] = (host(o), host(lse))
+    same_up_to_row_sum_order(out[1], out[0], f"varlen {lq} {lk}")
+    o_ref = np.zeros((int(cu_q[-1]), H, d))
+    l_ref = np.full((H, int(cu_q[-1])), -np.inf)
+    for s in range(len(lq)):
+        a, b, c, e = int(cu_q[s]), int(cu_q[s + 1]), int(cu_k[s]), int(cu_k[s + 1])
+        if b == a:
+            continue
+        os_, ls_ = oracle.attention(q[None, a:b], k[None, c:e], v[None, c:e], 1 / math.sqrt(d), causal)
+        o_ref[a:b] = os_[0]
+        l_ref[:, a:b] = ls_[0]
+    check(out[1][0], out[1][1], o_ref, l_ref, f"varlen {lq} {lk} causal={causal}")
