@@ -93,7 +93,7 @@ struct FwdParams {
   int num_tasks;                 // fixed length: exact; varlen: upper bound (grid sizing)
   int num_m;                     // fixed length: task_rows-row blocks of packed rows per (b, kv head)
   int task_rows;                 // packed rows per task: 256 (two Q tiles) or 128 (solo: one Q tile whose
-                                 // score tile alternates between S_0 and S_1; fixed length only)
+                                 // score tile alternates between S_0 and S_1)
   int lpt_group;                 // causal fixed length: (b, kv head) pairs per L2 section
   int varlen;
   float scale_log2;              // scale * log2(e)
@@ -195,7 +195,7 @@ __device__ __forceinline__ int packed_pos(const Task& t, int row, int gshift) {
   return (t.row0 + row) >> gshift;
 }
 
-// ROWS: packed rows per fixed-length task (256, or 128 in a solo kernel).
+// ROWS: packed rows per task (256, or 128 in a solo kernel).
 template <int ROWS>
 __device__ __forceinline__ bool get_task(const FwdParams& p, bool causal, int idx, Task& t) {
   if (p.varlen) {
@@ -437,11 +437,11 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
 }
 
 // ------------------------------------------------------------------ the kernel
-// SOLO: fixed-length tasks of one 128-row Q tile whose score tile alternates between
+// SOLO: tasks of one 128-row Q tile whose score tile alternates between
 // S_0 and S_1 (the host launches it when p.task_rows == 128).
 template <int D, bool CAUSAL, bool EMU, bool F16, bool SOLO = false>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
-  constexpr int kRows = SOLO ? kBlockM : kTaskRows;   // packed rows per fixed-length task
+  constexpr int kRows = SOLO ? kBlockM : kTaskRows;   // packed rows per task
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
