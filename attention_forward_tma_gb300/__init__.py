@@ -16,7 +16,7 @@ import threading
 
 from . import _build
 
-__all__ = ["fa_fwd", "fa_fwd_varlen", "fa_bwd", "fa_bwd_varlen", "lse_combine", "num_splits", "num_splits_varlen", "FaError", "set_option", "last_device_status", "library",
+__all__ = ["fa_fwd", "fa_fwd_varlen", "fa_fwd_kv_partial", "fa_bwd", "fa_bwd_varlen", "lse_combine", "num_splits", "num_splits_varlen", "FaError", "set_option", "last_device_status", "library",
            "release_cached_memory",
            "FA_DTYPE_BF16", "FA_DTYPE_FP16",
            "selftest_mma_tile", "selftest_exp2", "selftest_wait_timeout", "varlen_schedule",
@@ -38,6 +38,7 @@ _SIGNATURES = {
     "fa_fwd_varlen_kv": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _ci,
                          _ci, _vp],
     "fa_lse_combine": [_vp, _vp, _ci, _ci, _ci, _ci, _ci, _vp, _vp, _ci, _vp],
+    "fa_fwd_kv_partial": [_vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _ci, _vp],
     "fa_bwd": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _ci, _vp],
     "fa_bwd_varlen": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _ci,
                       _cf, _ci, _ci, _vp],
@@ -295,6 +296,38 @@ def fa_bwd_varlen(q, k, v, o, dout, lse, cu_seqlens, max_seqlen: int, *, cu_seql
                                    max_seqlen_k, H, Hkv, d, scale, int(bool(causal)), code,
                                    _stream_handle(stream, q.device)), "fa_bwd_varlen")
     return dq, dk, dv
+
+
+def fa_fwd_kv_partial(q, k, v, kv_offset: int, n_kv_total: int, *, scale: float | None = None,
+                      causal: bool = False, o_part=None, lse_part=None, stream=None):
+    """One key shard of a longer sequence: q [B, N_q, H, d]; k, v [B, N_kv, H_kv, d] hold keys
+    [kv_offset, kv_offset + N_kv) of a sequence of n_kv_total keys (bf16 or fp16; a causal
+    mask is the full sequence's bottom-right one). Returns (o_part fp32 [B, N_q, H, d],
+    lse_part fp32 [B, H, N_q]): the output normalised over this shard's keys and its LSE
+    (0 and -inf for rows that see none of them), to be merged with lse_combine."""
+    torch = _torch()
+    code = _dtype_code(q)
+    _need(q, "q", q.dtype, 4)
+    B, Nq, H, d = q.shape
+    for name, t in (("k", k), ("v", v)):
+        _need(t, name, q.dtype, 4)
+    Nk, Hkv = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, Nk, Hkv, d) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError(f"k and v must have shape {(B, Nk, Hkv, d)}")
+    if o_part is None:
+        o_part = torch.empty((B, Nq, H, d), dtype=torch.float32, device=q.device)
+    if lse_part is None:
+        lse_part = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    _need(o_part, "o_part", torch.float32, 4)
+    _need(lse_part, "lse_part", torch.float32, 3)
+    if tuple(o_part.shape) != (B, Nq, H, d) or tuple(lse_part.shape) != (B, H, Nq):
+        raise ValueError("o_part / lse_part have the wrong shape")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    _check(library().fa_fwd_kv_partial(q.data_ptr(), k.data_ptr(), v.data_ptr(), o_part.data_ptr(),
+                                       lse_part.data_ptr(), B, H, Hkv, Nq, Nk, int(n_kv_total), int(kv_offset), d,
+                                       scale, int(bool(causal)), code, _stream_handle(stream, q.device)),
+           "fa_fwd_kv_partial")
+    return o_part, lse_part
 
 
 def lse_combine(o_parts, lse_parts, *, out=None, lse=None, return_lse: bool = True, dtype=None, stream=None):

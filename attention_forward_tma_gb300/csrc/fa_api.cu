@@ -338,16 +338,53 @@ constexpr int kSchedBuckets = 4096;
 // sequence of Lq query rows has Lq << gshift packed rows, and row r of a block
 // sits at position r >> gshift. Tiles without keys (cost 0) are listed too: they
 // write the rows' empty result.
+//
+// The offsets are checked first (the varlen design reads per-sequence offsets
+// from cu_seqlens, "FlashAttention-4（下）" section "6. LPT 调度"): cu_q[0] =
+// cu_k[0] = 0, both non-decreasing, and, where the argument is >= 0,
+// cu_q[num_seqs] = total_q, cu_k[num_seqs] = total_k and every query length
+// <= max_q. On a violation the kernel lists no tile (*count = 0, so the attention
+// kernel and the merge write nothing) and records FA_ERR_INVALID_ARG | role 7 << 8 |
+// (first offending index) << 32 in the device status word.
+constexpr uint32_t kRoleSchedule = 7;
+constexpr unsigned long long kStatusInvalid = 1;  // == FA_ERR_INVALID_ARG
+
+__device__ __forceinline__ bool cu_entry_ok(const int* cu, int s, int num_seqs, int total, int max_len) {
+  const int a = cu[s], b = cu[s + 1];
+  if (b < a) return false;
+  if (s == 0 && a != 0) return false;
+  if (s == num_seqs - 1 && total >= 0 && b != total) return false;
+  return max_len < 0 || b - a <= max_len;
+}
+
 __global__ void __launch_bounds__(1024) fa_varlen_schedule_kernel(const int* cu_q, const int* cu_k, int num_seqs,
                                                                   int Hkv, int gshift, int causal, int splits,
-                                                                  int rows, int capacity, int4* tasks, int* count) {
+                                                                  int rows, int capacity, int4* tasks, int* count,
+                                                                  int total_q, int total_k, int max_q) {
   __shared__ int hist[kSchedBuckets];
   __shared__ int total_tiles;
+  __shared__ int first_bad;
   for (int i = threadIdx.x; i < kSchedBuckets; i += blockDim.x) hist[i] = 0;
-  if (threadIdx.x == 0) total_tiles = 0;
+  if (threadIdx.x == 0) {
+    total_tiles = 0;
+    first_bad = INT_MAX;
+  }
   __syncthreads();
+  for (int s = threadIdx.x; s < num_seqs; s += blockDim.x)
+    if (!cu_entry_ok(cu_q, s, num_seqs, total_q, max_q) || !cu_entry_ok(cu_k, s, num_seqs, total_k, -1))
+      atomicMin(&first_bad, s);
+  __syncthreads();
+  if (first_bad != INT_MAX) {
+    if (threadIdx.x == 0) {
+      *count = 0;
+      atomicCAS(&g_fa_status, 0ull,
+                kStatusInvalid | ((unsigned long long)kRoleSchedule << 8) |
+                    ((unsigned long long)(uint32_t)first_bad << 32));
+    }
+    return;
+  }
   auto cost_of = [&](int m, int Lq, int Lk, int sp) {
-    const KRange r = key_range(m * rows, rows, Lq, Lk, gshift, causal != 0, splits, sp);
+    const KRange r = key_range(m * rows, rows, Lk - Lq, Lk, gshift, causal != 0, splits, sp);
     return min(r.hi - r.lo, kSchedBuckets - 1);
   };
   for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
@@ -400,7 +437,10 @@ template <int D, bool F16>
 __global__ void __launch_bounds__(256) fa_combine_kernel(const float* __restrict__ o_part,
                                                          const float* __restrict__ lse_part, int parts,
                                                          long long o_stride, long long lse_stride, int rows, int H,
-                                                         int nl, uint16_t* __restrict__ o, float* __restrict__ lse) {
+                                                         int nl, uint16_t* __restrict__ o, float* __restrict__ lse,
+                                                         const int* __restrict__ task_count) {
+  // a varlen call whose schedule kernel rejected cu_seqlens listed no tile: write nothing
+  if (task_count != nullptr && *task_count == 0) return;
   constexpr int E = D / 32;   // floats per lane
   const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (w >= (long long)rows * H) return;
@@ -442,20 +482,71 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const float* __restrict
 
 namespace {
 int launch_combine(const float* o_part, const float* lse_part, int parts, long long o_stride, long long lse_stride,
-                   int rows, int H, int nl, int d, bool f16, void* o, float* lse, cudaStream_t s) {
+                   int rows, int H, int nl, int d, bool f16, void* o, float* lse, cudaStream_t s,
+                   const int* task_count = nullptr) {
   const long long warps = (long long)rows * H;
   const long long blocks = (warps + 7) / 8;
   if (blocks > INT_MAX) return FA_ERR_INVALID_ARG;
   uint16_t* out = static_cast<uint16_t*>(o);
   const int g = (int)blocks;
   if (d == 128) {
-    if (f16) fa::fa_combine_kernel<128, true><<<g, 256, 0, s>>>(o_part, lse_part, parts, o_stride, lse_stride, rows, H, nl, out, lse);
-    else fa::fa_combine_kernel<128, false><<<g, 256, 0, s>>>(o_part, lse_part, parts, o_stride, lse_stride, rows, H, nl, out, lse);
+    if (f16) fa::fa_combine_kernel<128, true><<<g, 256, 0, s>>>(o_part, lse_part, parts, o_stride, lse_stride, rows, H, nl, out, lse, task_count);
+    else fa::fa_combine_kernel<128, false><<<g, 256, 0, s>>>(o_part, lse_part, parts, o_stride, lse_stride, rows, H, nl, out, lse, task_count);
   } else {
-    if (f16) fa::fa_combine_kernel<64, true><<<g, 256, 0, s>>>(o_part, lse_part, parts, o_stride, lse_stride, rows, H, nl, out, lse);
-    else fa::fa_combine_kernel<64, false><<<g, 256, 0, s>>>(o_part, lse_part, parts, o_stride, lse_stride, rows, H, nl, out, lse);
+    if (f16) fa::fa_combine_kernel<64, true><<<g, 256, 0, s>>>(o_part, lse_part, parts, o_stride, lse_stride, rows, H, nl, out, lse, task_count);
+    else fa::fa_combine_kernel<64, false><<<g, 256, 0, s>>>(o_part, lse_part, parts, o_stride, lse_stride, rows, H, nl, out, lse, task_count);
   }
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+}  // namespace
+
+// ------------------------------------------------------------------ fixed-length parameters
+namespace {
+// Argument checks and kernel parameters of a fixed-length call (everything but the
+// outputs): maps of q, k, v and o (o only for the TMA store of full 16-bit tiles),
+// task shape and count, key splits, L2 sections.
+int fixed_params(fa::FwdParams& p, DevInfo** devp, const void* q, const void* k, const void* v, const void* o,
+                 int B, int H, int H_kv, int N_q, int N_kv, int d, float scale, int causal, int dtype,
+                 int num_splits) {
+  if (!q || !k || !v) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return FA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || H_kv <= 0 || N_q <= 0 || N_kv <= 0 || num_splits < 0) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_INVALID_ARG;
+  int gshift = 0;
+  int st = check_heads(H, H_kv, &gshift);
+  if (st != FA_OK) return st;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long tokens = (long long)B * N_q, tokens_k = (long long)B * N_kv;
+  if (tokens * H > INT_MAX || tokens_k * H_kv > INT_MAX) return FA_ERR_INVALID_ARG;  // 32-bit row indexing
+  DevInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != FA_OK) return st;
+  *devp = dev;
+  const bool f16 = dtype == FA_DTYPE_FP16;
+  std::memset(&p, 0, sizeof p);
+  if ((st = make_maps(p, q, k, v, const_cast<void*>(o), tokens, tokens_k, H, H_kv, d, f16)) != FA_OK) return st;
+  p.B = B; p.H = H; p.N = N_q; p.Nk = N_kv;
+  p.Hkv = H_kv;
+  p.gshift = gshift;
+  p.total_tokens = (int)tokens;
+  // tasks of task_rows packed rows; a (b, kv head) has N_q * G rows
+  p.task_rows = task_rows_fixed(B, H_kv, N_q, gshift, dev->sm_count);
+  p.num_m = (int)((((long long)N_q << gshift) + p.task_rows - 1) / p.task_rows);
+  const long long base_tasks = (long long)B * H_kv * p.num_m;
+  p.splits = choose_splits_fixed(num_splits, B, H, H_kv, p.num_m, p.task_rows, N_q, N_kv, d, gshift, causal != 0,
+                                 dev->sm_count);
+  const long long ntask = base_tasks * p.splits;
+  if (ntask > INT_MAX) return FA_ERR_INVALID_ARG;
+  p.num_tasks = (int)ntask;
+  const long long kv_bytes = 4LL * N_kv * d;                    // K + V of one (b, kv head)
+  long long group = (dev->l2_bytes / 2) / (kv_bytes > 0 ? kv_bytes : 1);
+  if (group < 1) group = 1;
+  if (group > (long long)B * H_kv) group = (long long)B * H_kv;
+  p.lpt_group = (int)group;
+  p.varlen = 0;
+  fill_common(p, scale, f16);
+  return FA_OK;
 }
 }  // namespace
 
@@ -615,55 +706,23 @@ int fa_set_option(int option, double value) {
 
 int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N_q,
               int N_kv, int d, float scale, int causal, int dtype, int num_splits, void* stream) {
-  if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || (lse && !aligned(lse, 4)))
-    return FA_ERR_INVALID_ARG;
-  if (B <= 0 || H <= 0 || H_kv <= 0 || N_q <= 0 || N_kv <= 0 || num_splits < 0) return FA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
-  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_INVALID_ARG;
-  int gshift = 0;
-  int st = check_heads(H, H_kv, &gshift);
-  if (st != FA_OK) return st;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  const long long tokens = (long long)B * N_q, tokens_k = (long long)B * N_kv;
-  if (tokens * H > INT_MAX || tokens_k * H_kv > INT_MAX) return FA_ERR_INVALID_ARG;  // 32-bit row indexing
-  DevInfo* dev = nullptr;
-  if ((st = device_info(&dev)) != FA_OK) return st;
-  const bool f16 = dtype == FA_DTYPE_FP16;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-
+  if (!o || !aligned(o, 16) || (lse && !aligned(lse, 4))) return FA_ERR_INVALID_ARG;
   fa::FwdParams p;
-  std::memset(&p, 0, sizeof p);
-  if ((st = make_maps(p, q, k, v, o, tokens, tokens_k, H, H_kv, d, f16)) != FA_OK) return st;
+  DevInfo* dev = nullptr;
+  int st = fixed_params(p, &dev, q, k, v, o, B, H, H_kv, N_q, N_kv, d, scale, causal, dtype, num_splits);
+  if (st != FA_OK) return st;
   p.o = static_cast<uint16_t*>(o);
   p.lse = lse;
-  p.B = B; p.H = H; p.N = N_q; p.Nk = N_kv;
-  p.Hkv = H_kv;
-  p.gshift = gshift;
-  p.total_tokens = (int)tokens;
-  // tasks of task_rows packed rows; a (b, kv head) has N_q * G rows
-  p.task_rows = task_rows_fixed(B, H_kv, N_q, gshift, dev->sm_count);
-  p.num_m = (int)((((long long)N_q << gshift) + p.task_rows - 1) / p.task_rows);
-  const long long base_tasks = (long long)B * H_kv * p.num_m;
-  p.splits = choose_splits_fixed(num_splits, B, H, H_kv, p.num_m, p.task_rows, N_q, N_kv, d, gshift, causal != 0,
-                                 dev->sm_count);
-  const long long ntask = base_tasks * p.splits;
-  if (ntask > INT_MAX) return FA_ERR_INVALID_ARG;
-  p.num_tasks = (int)ntask;
-  const long long kv_bytes = 4LL * N_kv * d;                    // K + V of one (b, kv head)
-  long long group = (dev->l2_bytes / 2) / (kv_bytes > 0 ? kv_bytes : 1);
-  if (group < 1) group = 1;
-  if (group > (long long)B * H_kv) group = (long long)B * H_kv;
-  p.lpt_group = (int)group;
-  p.varlen = 0;
-  fill_common(p, scale, f16);
+  const bool f16 = dtype == FA_DTYPE_FP16;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int grid = grid_for(p, dev, p.num_tasks);
   if (p.splits == 1) return dispatch(dev, p, d, causal != 0, f16, grid, s);
 
   // split keys: partial results in a temporary buffer, then the merge
+  const long long tokens = (long long)B * N_q;
   Partials ws;
   if ((st = ws.alloc(p.splits, tokens * H, d, 0, s)) != FA_OK) return st;
+  p.part_out = 1;
   p.o_part = ws.o_part;
   p.lse_part = ws.lse_part;
   p.lse_split_stride = tokens * H;
@@ -673,6 +732,27 @@ int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, 
                         o, lse, s);
   const int fst = ws.release(s);
   return st != FA_OK ? st : fst;
+}
+
+int fa_fwd_kv_partial(const void* q, const void* k, const void* v, float* o_part, float* lse_part, int B, int H,
+                      int H_kv, int N_q, int N_kv, int N_kv_total, int kv_offset, int d, float scale, int causal,
+                      int dtype, void* stream) {
+  if (!o_part || !lse_part || !aligned(o_part, 16) || !aligned(lse_part, 4)) return FA_ERR_INVALID_ARG;
+  if (N_kv <= 0 || kv_offset < 0 || N_kv_total < N_kv || (long long)kv_offset + N_kv > N_kv_total)
+    return FA_ERR_INVALID_ARG;
+  fa::FwdParams p;
+  DevInfo* dev = nullptr;
+  // The O tensor map is built over q and never used: partial rows are written as fp32
+  // by per-row stores, not by the TMA store of 16-bit tiles.
+  int st = fixed_params(p, &dev, q, k, v, q, B, H, H_kv, N_q, N_kv, d, scale, causal, dtype, 1);
+  if (st != FA_OK) return st;
+  p.part_out = 1;
+  p.o_part = o_part;
+  p.lse_part = lse_part;
+  p.lse_split_stride = 0;
+  p.diag_shift = N_kv_total - kv_offset - N_kv;   // keys of the sequence after this shard
+  const bool f16 = dtype == FA_DTYPE_FP16;
+  return dispatch(dev, p, d, causal != 0, f16, grid_for(p, dev, p.num_tasks), static_cast<cudaStream_t>(stream));
 }
 
 int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
@@ -715,7 +795,7 @@ int varlen_check(const void* q, const void* k, const void* v, void* o, float* ls
 // Maps, schedule kernel, attention kernel (and with splits > 1 the merge) of a
 // varlen call whose task list lives in tasks[0, cap) with its count at *count.
 int varlen_launch(DevInfo* dev, const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_q,
-                  const int* cu_k, int num_seqs, int total_q, int total_k, int H, int H_kv, int gshift, int d,
+                  const int* cu_k, int num_seqs, int total_q, int total_k, int max_q, int H, int H_kv, int gshift, int d,
                   float scale, int causal, bool f16, int splits, int rows, const Partials* parts, int4* tasks,
                   int* count, int cap, cudaStream_t s) {
   fa::FwdParams p;
@@ -723,7 +803,7 @@ int varlen_launch(DevInfo* dev, const void* q, const void* k, const void* v, voi
   int st = make_maps(p, q, k, v, o, total_q, total_k, H, H_kv, d, f16);
   if (st != FA_OK) return st;
   fa::fa_varlen_schedule_kernel<<<1, 1024, 0, s>>>(cu_q, cu_k, num_seqs, H_kv, gshift, causal, splits, rows, cap,
-                                                   tasks, count);
+                                                   tasks, count, total_q, total_k, max_q);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   p.o = static_cast<uint16_t*>(o);
   p.lse = lse;
@@ -740,6 +820,7 @@ int varlen_launch(DevInfo* dev, const void* q, const void* k, const void* v, voi
   p.task_rows = rows;
   p.splits = splits;
   if (splits > 1) {
+    p.part_out = 1;
     p.o_part = parts->o_part;
     p.lse_part = parts->lse_part;
     p.lse_split_stride = (long long)total_q * H;
@@ -749,7 +830,7 @@ int varlen_launch(DevInfo* dev, const void* q, const void* k, const void* v, voi
   st = dispatch(dev, p, d, causal != 0, f16, grid, s);
   if (st != FA_OK || splits == 1) return st;
   return launch_combine(parts->o_part, parts->lse_part, splits, (long long)total_q * H * d, (long long)total_q * H,
-                        total_q, H, total_q, d, f16, o, lse, s);
+                        total_q, H, total_q, d, f16, o, lse, s, count);
 }
 }  // namespace
 
@@ -780,7 +861,8 @@ int fa_fwd_varlen_kv(const void* q, const void* k, const void* v, void* o, float
   if ((st = ws.alloc(splits > 1 ? splits : 0, (long long)total_q * H, d, list_bytes, s)) != FA_OK) return st;
   int4* tasks = static_cast<int4*>(ws.base);
   int* count = reinterpret_cast<int*>(static_cast<char*>(ws.base) + (size_t)cap * sizeof(int4));
-  st = varlen_launch(dev, q, k, v, o, lse, cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv, H, H_kv, gshift,
+  st = varlen_launch(dev, q, k, v, o, lse, cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv, max_seqlen_q,
+                     H, H_kv, gshift,
                      d, scale, causal, f16, splits, rows, &ws, tasks, count, (int)cap, s);
   const int fst = ws.release(s);
   return st != FA_OK ? st : fst;
@@ -884,7 +966,7 @@ int fa_varlen_schedule(const int* cu_seqlens_q, const int* cu_seqlens_kv, int nu
   if ((st = device_info(&dev)) != FA_OK) return st;
   fa::fa_varlen_schedule_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(
       cu_seqlens_q, cu_seqlens_kv, num_seqs, H_kv, gshift, causal, splits, fa::kTaskRows, capacity,
-      static_cast<int4*>(tasks), count);
+      static_cast<int4*>(tasks), count, -1, -1, -1);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -896,16 +978,23 @@ int fa_fwd_varlen_noalloc(const void* q, const void* k, const void* v, void* o, 
   int st = varlen_check(q, k, v, o, lse, cu_seqlens, cu_seqlens, num_seqs, total_tokens, total_tokens, max_seqlen,
                         max_seqlen, H, H, d, scale, causal, FA_DTYPE_BF16, 1, &gshift, &cap);
   if (st != FA_OK) return st;
+  // Refuse before touching the device when the tile bound of 256-row tasks, or of 128-row
+  // tasks if FA_OPT_SOLO_TILES forces them, is already too large for the array.
   if (cap > kNoAllocMaxTasks) return FA_ERR_CAPACITY;
+  if (g_opt.solo == 1 && varlen_tiles(total_tokens, num_seqs, H, gshift, fa::kBlockM) > kNoAllocMaxTasks)
+    return FA_ERR_CAPACITY;
   DevInfo* dev = nullptr;
   if ((st = device_info(&dev)) != FA_OK) return st;
+  // The schedule kernel writes up to `cap` tiles: check the bound of the row count chosen.
   const int rows = task_rows_varlen(total_tokens, num_seqs, H, gshift, dev->sm_count);
-  cap = varlen_tiles(total_tokens, num_seqs, H, gshift, rows);   // solo only while this is at most the SM count
+  cap = varlen_tiles(total_tokens, num_seqs, H, gshift, rows);
+  if (cap > kNoAllocMaxTasks) return FA_ERR_CAPACITY;
   int4* scratch = nullptr;
   if ((st = noalloc_scratch(&scratch)) != FA_OK) return st;
   int4* tasks = scratch;
   int* count = reinterpret_cast<int*>(scratch + kNoAllocMaxTasks);
-  return varlen_launch(dev, q, k, v, o, lse, cu_seqlens, cu_seqlens, num_seqs, total_tokens, total_tokens, H, H,
+  return varlen_launch(dev, q, k, v, o, lse, cu_seqlens, cu_seqlens, num_seqs, total_tokens, total_tokens,
+                       max_seqlen, H, H,
                        gshift, d, scale, causal, false, 1, rows, nullptr, tasks, count, (int)cap,
                        static_cast<cudaStream_t>(stream));
 }

@@ -39,6 +39,7 @@
 // Every wait is bounded as in the forward kernel.
 #pragma once
 
+#include <climits>
 #include <cuda_fp16.h>
 
 #include "fa_fwd.cuh"
@@ -76,6 +77,8 @@ struct BwdParams {
   int* sem;
   int ntiles;
   int* task_counter;         // zero on entry: tasks claimed beyond the first gridDim.x
+  const int* cu_ok;          // variable length: 1 if cu_q / cu_k passed fa_bwd_check_cu_kernel (else
+                             // every kernel of the call returns at once); null for fixed length
 };
 
 template <int D>
@@ -126,7 +129,9 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint16_t* __restr
                                                          const float* __restrict__ lse, float* __restrict__ lse2,
                                                          float* __restrict__ dsum, float* __restrict__ dq_acc,
                                                          long long tokens, const int* __restrict__ cu_q, int B,
-                                                         int H, int gshift, int Nq, int mpad) {
+                                                         int H, int gshift, int Nq, int mpad,
+                                                         const int* __restrict__ cu_ok) {
+  if (cu_ok != nullptr && *cu_ok == 0) return;
   constexpr int kLanes = D / 8;                // lanes per row: 16-byte loads of 8 elements
   constexpr int kRowsPerWarp = 32 / kLanes;
   const int lane = threadIdx.x & 31;
@@ -179,11 +184,41 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint16_t* __restr
 // dQ (16-bit) from the fp32 accumulator, 4 elements per thread.
 template <bool F16>
 __global__ void __launch_bounds__(256) fa_bwd_post_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq,
-                                                          long long n4) {
+                                                          long long n4, const int* __restrict__ cu_ok) {
+  if (cu_ok != nullptr && *cu_ok == 0) return;
   const long long i = (long long)blockIdx.x * 256 + threadIdx.x;
   if (i >= n4) return;
   const float4 x = acc[i];
   dq[i] = make_uint2(pack_16x2<F16>(x.x, x.y), pack_16x2<F16>(x.z, x.w));
+}
+
+// Check of the sequence offsets of a variable-length backward call, one CTA:
+// cu_q[0] = cu_k[0] = 0, both non-decreasing, cu_q[B] = total_q, cu_k[B] = total_k,
+// every query length <= max_q and every key length <= max_k (the grid and the packed
+// LSE / D rows are sized by the longest sequences). *ok = 1 if all hold; else *ok
+// stays 0 and FA_ERR_INVALID_ARG | 7 << 8 | (first offending sequence) << 32 is
+// recorded in the device status word.
+__global__ void __launch_bounds__(1024) fa_bwd_check_cu_kernel(const int* __restrict__ cu_q,
+                                                               const int* __restrict__ cu_k, int B, int total_q,
+                                                               int total_k, int max_q, int max_k, int* ok) {
+  __shared__ int first_bad;
+  if (threadIdx.x == 0) first_bad = INT_MAX;
+  __syncthreads();
+  auto entry_ok = [&](const int* cu, int s, int total, int max_len) {
+    const int a = cu[s], b = cu[s + 1];
+    return b >= a && (s != 0 || a == 0) && (s != B - 1 || b == total) && b - a <= max_len;
+  };
+  for (int s = threadIdx.x; s < B; s += blockDim.x)
+    if (!entry_ok(cu_q, s, total_q, max_q) || !entry_ok(cu_k, s, total_k, max_k)) atomicMin(&first_bad, s);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (first_bad == INT_MAX) {
+      *ok = 1;
+    } else {
+      *ok = 0;
+      atomicCAS(&g_fa_status, 0ull, 1ull | (7ull << 8) | ((unsigned long long)(uint32_t)first_bad << 32));
+    }
+  }
 }
 
 // ------------------------------------------------------------------ tasks
@@ -256,6 +291,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
     if (threadIdx.x == 0) atomicCAS(&g_fa_status, 0ull, kStatusUnsupported);
     return;
   }
+  // rejected sequence offsets (variable length): nothing to compute, nothing written
+  if (p.cu_ok != nullptr && *p.cu_ok == 0) return;
   const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sQ = sbase + L::kQ, sDO = sbase + L::kDO,
                  sDS = sbase + L::kDS;
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * (uint32_t)i; };

@@ -67,29 +67,29 @@ struct Shape {
 
 template <int D, bool F>
 int pre_post(bool post, const void* o, const void* dout, const float* lse, float* lse2, float* dsum,
-             float* dq_acc, void* dq, const Shape& sh, int mpad, cudaStream_t s) {
+             float* dq_acc, void* dq, const Shape& sh, int mpad, const int* cu_ok, cudaStream_t s) {
   const long long rows = sh.tokens_q * sh.H;
   if (rows == 0) return FA_OK;
   if (!post) {
     const long long rows_per_block = 8LL * (32 / (D / 8));
     fa::fa_bwd_pre_kernel<D, F><<<(unsigned)((rows + rows_per_block - 1) / rows_per_block), 256, 0, s>>>(
         static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, lse2, dsum, dq_acc, sh.tokens_q,
-        sh.cu_q, sh.B, sh.H, sh.gshift, sh.N_q, mpad);
+        sh.cu_q, sh.B, sh.H, sh.gshift, sh.N_q, mpad, cu_ok);
   } else {
     const long long n4 = rows * D / 4;
     fa::fa_bwd_post_kernel<F><<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(
-        reinterpret_cast<const float4*>(dq_acc), static_cast<uint2*>(dq), n4);
+        reinterpret_cast<const float4*>(dq_acc), static_cast<uint2*>(dq), n4, cu_ok);
   }
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int pre_post_any(bool post, bool f16, const void* o, const void* dout, const float* lse, float* lse2, float* dsum,
-                 float* dq_acc, void* dq, const Shape& sh, int mpad, cudaStream_t s) {
+                 float* dq_acc, void* dq, const Shape& sh, int mpad, const int* cu_ok, cudaStream_t s) {
   if (sh.d == 128)
-    return f16 ? pre_post<128, true>(post, o, dout, lse, lse2, dsum, dq_acc, dq, sh, mpad, s)
-               : pre_post<128, false>(post, o, dout, lse, lse2, dsum, dq_acc, dq, sh, mpad, s);
-  return f16 ? pre_post<64, true>(post, o, dout, lse, lse2, dsum, dq_acc, dq, sh, mpad, s)
-             : pre_post<64, false>(post, o, dout, lse, lse2, dsum, dq_acc, dq, sh, mpad, s);
+    return f16 ? pre_post<128, true>(post, o, dout, lse, lse2, dsum, dq_acc, dq, sh, mpad, cu_ok, s)
+               : pre_post<128, false>(post, o, dout, lse, lse2, dsum, dq_acc, dq, sh, mpad, cu_ok, s);
+  return f16 ? pre_post<64, true>(post, o, dout, lse, lse2, dsum, dq_acc, dq, sh, mpad, cu_ok, s)
+             : pre_post<64, false>(post, o, dout, lse, lse2, dsum, dq_acc, dq, sh, mpad, cu_ok, s);
 }
 
 int device_check() {
@@ -139,8 +139,15 @@ int bwd_run(const void* q, const void* k, const void* v, const void* o, const vo
   float* dsum = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes + vec_bytes);
   int* sem = det ? reinterpret_cast<int*>(static_cast<char*>(ws) + acc_bytes + 2 * vec_bytes) : nullptr;
   int* counter = reinterpret_cast<int*>(static_cast<char*>(ws) + acc_bytes + 2 * vec_bytes + sem_bytes - 256);
+  // variable length: the check kernel's verdict on the sequence offsets, next to the counter
+  int* cu_ok = sh.cu_q != nullptr ? counter + 1 : nullptr;
   if (cudaMemsetAsync(lse2, 0, 2 * vec_bytes + sem_bytes, s) != cudaSuccess) st = FA_ERR_CUDA;
-  if (st == FA_OK) st = pre_post_any(false, f16, o, dout, lse, lse2, dsum, dq_acc, nullptr, sh, (int)mpad, s);
+  if (st == FA_OK && cu_ok != nullptr) {
+    fa::fa_bwd_check_cu_kernel<<<1, 1024, 0, s>>>(sh.cu_q, sh.cu_k, sh.B, (int)sh.tokens_q, (int)sh.tokens_k,
+                                                  sh.N_q, sh.N_kv, cu_ok);
+    if (cudaGetLastError() != cudaSuccess) st = FA_ERR_CUDA;
+  }
+  if (st == FA_OK) st = pre_post_any(false, f16, o, dout, lse, lse2, dsum, dq_acc, nullptr, sh, (int)mpad, cu_ok, s);
   if (st == FA_OK && sh.tokens_q > 0) st = fa_host::make_map_f32(&p.tm_dq, dq_acc, sh.tokens_q, sh.H, d, G);
   if (st == FA_OK && sh.tokens_q > 0 && sh.tokens_k > 0 && nkb > 0) {
     p.lse2 = lse2;
@@ -167,6 +174,7 @@ int bwd_run(const void* q, const void* k, const void* v, const void* o, const vo
     p.sem = sem;
     p.ntiles = ntiles;
     p.task_counter = counter;
+    p.cu_ok = cu_ok;
     fa_host::trace_target(&p.trace, &p.trace_ctas);
     // persistent CTAs, one per SM, claiming tasks in order (FA_OPT_PERSISTENT = 0: one
     // CTA per task)
@@ -182,7 +190,8 @@ int bwd_run(const void* q, const void* k, const void* v, const void* o, const vo
     else
       st = f16 ? launch_c<64, true>(p, grid, causal != 0, s) : launch_c<64, false>(p, grid, causal != 0, s);
   }
-  if (st == FA_OK) st = pre_post_any(true, f16, nullptr, nullptr, nullptr, nullptr, nullptr, dq_acc, dq, sh, (int)mpad, s);
+  if (st == FA_OK)
+    st = pre_post_any(true, f16, nullptr, nullptr, nullptr, nullptr, nullptr, dq_acc, dq, sh, (int)mpad, cu_ok, s);
   if (cudaFreeAsync(ws, s) != cudaSuccess && st == FA_OK) st = FA_ERR_CUDA;
   return st;
 }

@@ -81,6 +81,10 @@ struct FwdParams {
   float* lse_part;               // [splits, LSE layout]
   long long lse_split_stride;    // elements between the splits of lse_part
   int splits;
+  int part_out;                  // 1: write o_part / lse_part (splits > 1, or one key shard of a longer
+                                 // sequence whose partial result another call or device merges)
+  int diag_shift;                // fixed length: keys of the sequence after the last key given (a key
+                                 // shard's causal diagonal stays the full sequence's); else 0
   const int* cu_seqlens;         // varlen only: query rows of each sequence
   const int* cu_seqlens_k;       // varlen only: key rows of each sequence
   const int4* tasks;             // varlen only: {seq, kv head | split << 16, m_block, cost}, longest first
@@ -185,6 +189,7 @@ struct Task {
   int kvh, tok0, len;      // K/V head, first query row of the sequence, its length
   int row0, rows;          // the task's packed rows [row0, row0 + rows) of the sequence (rows 256 or 128)
   int tok0k, lenk;         // first key row of the sequence, its number of keys
+  int off;                 // causal offset: position i sees keys j <= i + off
   int split;               // key range (splits > 1)
   int lse_base;            // lse index of position 0 of query head kvh * G
   int lse_hstride;         // lse distance between consecutive query heads
@@ -205,7 +210,7 @@ __device__ __forceinline__ bool get_task(const FwdParams& p, bool causal, int id
     const int k0 = p.cu_seqlens_k[e.x], k1 = p.cu_seqlens_k[e.x + 1];
     t.kvh = e.y & 0xffff; t.split = e.y >> 16; t.row0 = e.z * ROWS; t.rows = ROWS;
     t.tok0 = s0; t.len = s1 - s0;
-    t.tok0k = k0; t.lenk = k1 - k0;
+    t.tok0k = k0; t.lenk = k1 - k0; t.off = t.lenk - t.len;
     t.lse_base = (t.kvh << p.gshift) * p.total_tokens + s0;
     t.lse_hstride = p.total_tokens;
     return true;
@@ -231,7 +236,7 @@ __device__ __forceinline__ bool get_task(const FwdParams& p, bool causal, int id
   }
   const int b = bh / p.Hkv;
   t.kvh = bh - b * p.Hkv; t.row0 = m * ROWS; t.rows = ROWS; t.tok0 = b * p.N; t.len = p.N;
-  t.tok0k = b * p.Nk; t.lenk = p.Nk;
+  t.tok0k = b * p.Nk; t.lenk = p.Nk; t.off = p.Nk - p.N + p.diag_shift;
   t.lse_base = (b * p.H + (t.kvh << p.gshift)) * p.N;
   t.lse_hstride = p.N;
   return true;
@@ -246,8 +251,9 @@ __device__ __forceinline__ bool task_one_tile(const Task& t, int gshift) {
 }
 
 // Causal offset: query position i sees keys j <= i + off, with off = N_kv - N_q
-// (bottom-right alignment, "Flash Attention 4", section "Causal Mask").
-__device__ __forceinline__ int task_off(const Task& t) { return t.lenk - t.len; }
+// (bottom-right alignment, "Flash Attention 4", section "Causal Mask"); a key shard
+// adds the keys that follow it in the full sequence.
+__device__ __forceinline__ int task_off(const Task& t) { return t.off; }
 
 // K/V blocks [lo, hi) a task visits, from hi - 1 down to lo. Causal work stops
 // at the last key the bottom row of the task may see; with splits > 1 the
@@ -256,11 +262,12 @@ __device__ __forceinline__ int task_off(const Task& t) { return t.lenk - t.len; 
 struct KRange {
   int lo, hi;
 };
-// The same for the packed rows [row0, row0 + rows) of a sequence with lenq query and lenk key rows.
-__device__ __forceinline__ KRange key_range(int row0, int rows, int lenq, int lenk, int gshift, bool causal,
+// The same for the packed rows [row0, row0 + rows) of a sequence with lenk key rows and
+// causal offset off.
+__device__ __forceinline__ KRange key_range(int row0, int rows, int off, int lenk, int gshift, bool causal,
                                             int splits, int split) {
   int kmax = lenk;
-  if (causal) kmax = min(((row0 + rows - 1) >> gshift) + (lenk - lenq) + 1, lenk);
+  if (causal) kmax = min(((row0 + rows - 1) >> gshift) + off + 1, lenk);
   const int nb = kmax > 0 ? (kmax + kBlockN - 1) / kBlockN : 0;
   if (splits == 1) return {0, nb};
   const int per = ((lenk + kBlockN - 1) / kBlockN + splits - 1) / splits;
@@ -268,7 +275,7 @@ __device__ __forceinline__ KRange key_range(int row0, int rows, int lenq, int le
   return {lo, max(lo, min(lo + per, nb))};
 }
 __device__ __forceinline__ KRange task_range(const FwdParams& p, const Task& t, bool causal) {
-  return key_range(t.row0, t.rows, t.len, t.lenk, p.gshift, causal, p.splits, t.split);
+  return key_range(t.row0, t.rows, t.off, t.lenk, p.gshift, causal, p.splits, t.split);
 }
 
 // ------------------------------------------------------------------ task ring
@@ -360,6 +367,26 @@ __device__ __forceinline__ uint32_t pack_16x2_u64(uint64_t v) {
   unpack2(v, lo, hi);
   return pack_16x2<F16>(lo, hi);
 }
+// Rounding error of one weight as the PV product sees it: round(p) - p, with round the
+// conversion to the 16-bit type of P (round to nearest even). Exact in fp32.
+template <bool F16>
+__device__ __forceinline__ float p_rounding_error(float p) {
+  const uint32_t h = pack_16x2<F16>(p, 0.f) & 0xffffu;
+  float r;
+  if constexpr (F16) {
+    asm("{\n\t.reg .f16 t;\n\tmov.b16 t, %1;\n\tcvt.f32.f16 %0, t;\n\t}" : "=f"(r) : "h"((unsigned short)h));
+  } else {
+    r = __uint_as_float(h << 16);
+  }
+  return r - p;
+}
+// The same weight computed as the exponential loop computes the block maximum's:
+// exp2(m * sl2 - ref * sl2) with one fused multiply-add and the hardware ex2.
+__device__ __forceinline__ float p_of_score(float m, float sl2, float bias) {
+  float x;
+  asm("fma.rn.ftz.f32 %0, %1, %2, %3;" : "=f"(x) : "f"(m), "f"(sl2), "f"(bias));
+  return ex2_approx(x);
+}
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float m;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
@@ -405,6 +432,15 @@ __device__ __forceinline__ uint64_t exp2_poly2(uint64_t x2) {
   unpack2(r, r0, r1);
   return pack2(__int_as_float(__float_as_int(q0) + (__float_as_int(r0) << 23)),
                __int_as_float(__float_as_int(q1) + (__float_as_int(r1) << 23)));
+}
+
+// The block maximum's weight as an emulated column computes it (the pair path, low lane).
+__device__ __forceinline__ float p_of_score_poly(float m, float sl2, float bias) {
+  float x;
+  asm("fma.rn.ftz.f32 %0, %1, %2, %3;" : "=f"(x) : "f"(m), "f"(sl2), "f"(bias));
+  float lo, hi;
+  unpack2(exp2_poly2(pack2(x, x)), lo, hi);
+  return lo;
 }
 
 // ------------------------------------------------------------------ MMA issue helpers
@@ -851,7 +887,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       auto store_lse = [&](float v) {
         if (pos < tk.len && tk.tok0 + pos < p.total_tokens) {
           const int li = tk.lse_base + (r & ((1 << p.gshift) - 1)) * tk.lse_hstride + pos;
-          if (p.splits > 1) p.lse_part[tk.split * p.lse_split_stride + li] = v;
+          if (p.part_out) p.lse_part[tk.split * p.lse_split_stride + li] = v;
           else if (p.lse != nullptr) p.lse[li] = v;
         }
       };
@@ -874,6 +910,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         const int tp0 = packed_pos(tk, 0, p.gshift);   // both warpgroups: the rows of Q tile 0
         const int row_limit = CAUSAL ? min(tp0 + (r >> p.gshift) + off + 1, tk.lenk) : tk.lenk;  // keys [0, row_limit)
         float row_max = -INFINITY, row_sum = 0.f;
+        float row_corr = 0.f;   // rounding errors of the blocks' largest weights (as in two-tile tasks)
         for (int i = 0; i < nb; ++i) {
           const int j = kr.hi - 1 - i, b = i & 1;
           const uint32_t tS = tmem + lane_base + L::col_s(b);
@@ -946,6 +983,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             tr.rec(kEvMail, j);
           }
           const float ref_safe = ref == -INFINITY ? 0.f : ref;
+          // the block maximum's weight, whichever half holds it (both warpgroups compute it;
+          // WG0 hands the normaliser to WG2)
+          row_corr = row_corr * acc + p_rounding_error<F16>(p_of_score(blk_max, sl2, -ref_safe * sl2));
           const uint64_t scale2 = pack2(sl2, sl2);
           const uint64_t bias2 = pack2(-ref_safe * sl2, -ref_safe * sl2);
           uint64_t sum2a = 0, sum2b = 0;
@@ -976,10 +1016,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         if (!w.wait(bar(L::bRowSum), rs_par & 1, L::bRowSum, -1)) { ok = false; break; }
         rs_par ^= 1u;
         row_sum += ysum[r];
-        // final statistics to WG2 (row_sum), LSE straight to global memory
+        // final statistics to WG2 (the normaliser of O), LSE straight to global memory
         if (!w.wait(bar(L::bCorrEmpty + 0), (ce_par & 1) ^ 1, L::bCorrEmpty + 0, -1)) { ok = false; break; }
         ce_par ^= 1u;
-        mail[r] = row_sum;
+        mail[r] = row_sum + row_corr;
         mbar_arrive(bar(p.stats_tmem ? L::bStats + 0 : L::bCorrFull + 0));
         tr.rec(kEvStats, -1);
         const float ref_safe = row_max == -INFINITY ? 0.f : row_max;
@@ -1001,6 +1041,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       }
       const int row_limit = CAUSAL ? min(pos + off + 1, tk.lenk) : tk.lenk;  // keys [0, row_limit) visible
       float row_max = -INFINITY, row_sum = 0.f;
+      // O is normalised by row_sum + row_corr: row_corr adds, per key block, the 16-bit
+      // rounding error of the block's largest weight, so a row dominated by one key
+      // divides that key's rounded weight (the one PV multiplies) by itself. Without it a
+      // dominant weight 2^delta kept under the delayed-rescale rule (delta up to tau, not
+      // an integer) leaves its bf16 rounding, up to 2^-8 relative, in O: up to |v| * 2^-8.
+      // The LSE uses the fp32 row_sum, the exact denominator.
+      float row_corr = 0.f;
 #ifdef FA_TRACE
       uint32_t n_upd = 0, n_resc = 0;   // this row's later-block updates and O rescales
 #endif
@@ -1100,11 +1147,26 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         }
         if (stagger && !take_turn(j)) { ok = false; break; }
         const float ref_safe = ref == -INFINITY ? 0.f : ref;
-        const uint64_t scale2 = pack2(sl2, sl2);
-        const uint64_t bias2 = pack2(-ref_safe * sl2, -ref_safe * sl2);
         // P = exp2(S * sl2 - ref * sl2) -> 16-bit pairs; with EMU the first emu_groups
         // 16-column groups use the FMA polynomial (blocks without masked columns only)
         const int emu = (EMU && !need_mask) ? p.emu_groups : 0;
+        {
+          float pm = p_of_score(blk_max, sl2, -ref_safe * sl2);
+          if constexpr (EMU) {
+            // the block maximum's weight as its own column computes it: by the polynomial
+            // if the maximum lies in an emulated group
+            if (emu > 0) {
+              float mxe = -INFINITY;
+#pragma unroll
+              for (int c = 0; c < kBlockN; ++c)
+                if (c < emu * 16) mxe = fmaxf(mxe, s[c]);
+              if (mxe == blk_max) pm = p_of_score_poly(blk_max, sl2, -ref_safe * sl2);
+            }
+          }
+          row_corr = row_corr * acc + p_rounding_error<F16>(pm);
+        }
+        const uint64_t scale2 = pack2(sl2, sl2);
+        const uint64_t bias2 = pack2(-ref_safe * sl2, -ref_safe * sl2);
         uint64_t sum2a = 0, sum2b = 0;
         uint32_t pk[kBlockN / 2];
 #pragma unroll
@@ -1150,10 +1212,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         row_sum = row_sum * acc + (sa + sb);
       }
       if (!ok) break;
-      // final statistics to WG2 (row_sum), LSE straight to global memory
+      // final statistics to WG2 (the normaliser of O), LSE straight to global memory
       if (!w.wait(bar(L::bCorrEmpty + t), (ce_par & 1) ^ 1, L::bCorrEmpty + t, -1)) { ok = false; break; }
       ce_par ^= 1u;
-      mail[t * kBlockM + r] = row_sum;
+      mail[t * kBlockM + r] = row_sum + row_corr;
       // with acc_scale in tensor memory the per-block hand-offs have no empty barrier,
       // so the final one takes a barrier of its own: on corr_full it could complete a
       // second phase before WG2 has waited for the last block's
@@ -1208,10 +1270,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           const int head = (tk.kvh << p.gshift) + (r & ((1 << p.gshift) - 1));
           if (pos < tk.len && tk.tok0 + pos < p.total_tokens) {
             const size_t row = (size_t)(tk.tok0 + pos) * p.H + head;
-            uint4* dst = p.splits > 1
+            uint4* dst = p.part_out
                              ? reinterpret_cast<uint4*>(p.o_part + ((size_t)tk.split * p.total_tokens * p.H + row) * D)
                              : reinterpret_cast<uint4*>(p.o + row * D);
-            const int n16 = p.splits > 1 ? D / 4 : D / 8;   // 16-byte units per row
+            const int n16 = p.part_out ? D / 4 : D / 8;   // 16-byte units per row
 #pragma unroll 1
             for (int c = 0; c < n16; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
           }
@@ -1289,7 +1351,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         const int tile_pos0 = packed_pos(tk, t * kBlockM, p.gshift);   // sequence position of row 0
         const int tile_end = tile_pos0 + (kBlockM >> p.gshift);        // one past the tile's last position
         const uint32_t tO = tmem + lane_base + L::col_o(t);
-        const bool full_tile = p.splits == 1 && tile_end <= tk.len && tk.tok0 + tile_end <= p.total_tokens;
+        const bool full_tile = !p.part_out && tile_end <= tk.len && tk.tok0 + tile_end <= p.total_tokens;
         if (full_tile) {
           // Stage the tile in shared memory in the TMA's 128-byte-swizzled layout
           // (16-byte unit k of row r sits at unit k ^ (r % 8)), then one thread
@@ -1326,8 +1388,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             __syncwarp();
           }
           ++ost_n;
-        } else if (p.splits > 1) {
-          // one key range of a split task: normalised fp32 rows, merged later
+        } else if (p.part_out) {
+          // one key range of a split task (or a key shard): normalised fp32 rows, merged later
           const int pos = tile_pos0 + (r >> p.gshift);
           const int head = (tk.kvh << p.gshift) + (r & ((1 << p.gshift) - 1));
           const bool valid = pos < tk.len && tk.tok0 + pos < p.total_tokens;

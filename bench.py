@@ -147,30 +147,49 @@ def profiled_traffic(workload: str, which: str = "fwd"):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms while the benchmark runs;
+    each sample carries the host time it was read, so that a time window can be summarised."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    PERIOD_S = 0.02
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.samples = []   # (host time, sm MHz, max sm MHz, power W, reasons)
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(int(self.PERIOD_S * 1000))], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            t_end = time.perf_counter() + 10.0      # wait (bounded) for the first sample
+            while not self.samples and time.perf_counter() < t_end and self.proc.poll() is None:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm, smax = float(parts[0]), float(parts[1])
+            except ValueError:
+                continue
+            try:
+                power = float(parts[2])
+            except ValueError:
+                power = None
+            reasons = {n for n, v in zip(self.NAMES, parts[3:7]) if v.lower() == "active"}
+            self.samples.append((time.perf_counter(), sm, smax, power, reasons))
 
     def __exit__(self, *exc):
         if self.proc:
@@ -181,25 +200,17 @@ class ClockSampler:
                 self.proc.kill()
             self.thread.join(timeout=2)
 
-    def summary(self):
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 7:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                smax.append(float(parts[1]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[3:7]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+    def summary(self, t0: float, t1: float):
+        """Samples read in [t0 - period, t1 + period] (a short region still gets the samples around it)."""
+        win = [x for x in self.samples if t0 - self.PERIOD_S <= x[0] <= t1 + self.PERIOD_S]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "window_s": round(t1 - t0, 4)}
+        reasons = set().union(*(x[4] for x in win))
+        powers = [x[3] for x in win if x[3] is not None]
+        return {"sm_mhz": statistics.median(x[1] for x in win), "sm_max_mhz": max(x[2] for x in win),
+                "reasons": sorted(reasons), "samples": len(win), "window_s": round(t1 - t0, 4),
+                "power_w_max": max(powers) if powers else None}
 
 
 def workload_flops(w, x=None):
@@ -288,6 +299,42 @@ def cpu_baseline_bwd(w, x):
                       f"head(s) of {w.name} (fp64 NumPy, full matrices per head), {dt:.1f} s"}
 
 
+def workload_config(w, x, l2_bytes: int, bwd: bool = False):
+    """The JSON line's "config", the same for both arms: the workload, its sizes, input
+    recipe (scale, seed), FLOPs per step and how the timing treats L2."""
+    if w.varlen:
+        T = int(x["cu_seqlens"][-1])
+        in_bytes = 2 * (2 * T * w.H + 2 * T * w.Hkv) * w.d
+    else:
+        in_bytes = 2 * (2 * w.B * w.N * w.H + 2 * w.B * w.Nk * w.Hkv) * w.d
+    flops = workload_flops(w, x) * (2.5 if bwd else 1.0)
+    cfg = {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.Hkv, "N": w.N, "d": w.d, "causal": w.causal,
+           "inputs": w.dtype, "scale": w.scale, "seed": w.seed,
+           "l2": ("inputs larger than L2 (Q+K+V+O = %.0f MiB), no flush" % (in_bytes / 2 ** 20))
+           if in_bytes > l2_bytes else
+           ("inputs smaller than L2 (Q+K+V+O = %.1f MiB): 256 MiB written between steps, value from the "
+            "per-step events" % (in_bytes / 2 ** 20)),
+           "flops_per_step": flops}
+    if bwd:
+        cfg["pass"] = "backward (FLOPs = 2.5 x the forward count)"
+    if w.Nk != w.N:
+        cfg["N_kv"] = w.Nk
+    if w.varlen:
+        cfg["lengths"] = [int(L) for L in x["lengths"]]
+    return cfg, in_bytes
+
+
+def l2_size_bytes(index: int = 0) -> int:
+    """The GPU's L2 size (a property query, no work on the GPU); GB300's if no GPU is visible."""
+    try:
+        import torch
+        if torch.cuda.is_available():
+            return int(torch.cuda.get_device_properties(index).L2_cache_size)
+    except Exception:
+        pass
+    return 126 << 20
+
+
 # --------------------------------------------------------------------------- the reference arm
 def run_reference(a, dist):
     w = fa_inputs.WORKLOADS[a.workload]
@@ -312,8 +359,7 @@ def run_reference(a, dist):
         run_oracle_rows(w, x, samples[i][0], threads)
     dt = time.perf_counter() - t0
     value = flops / dt / 1e12
-    cfg = {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.Hkv, "N": w.N, "d": w.d, "causal": w.causal,
-           "inputs": w.dtype}
+    cfg, _ = workload_config(w, x, l2_size_bytes(dist.local))
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "impl": "reference", "n_gpus": a.gpus,
             "steps": a.steps, "warmup": a.warmup, "ms_per_step": dt / a.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
@@ -384,6 +430,7 @@ def run_ours(a, dist):
         launches_per_step = 1 + (1 if splits > 1 else 0)   # attention (, merge)
 
     stream = torch.cuda.current_stream(dev)
+    clocks = ClockSampler(dist.local).__enter__()
     for _ in range(a.warmup):
         step(stream)
     torch.cuda.synchronize(dev)
@@ -395,23 +442,24 @@ def run_ours(a, dist):
     # 256 MiB buffer is written between steps (outside the per-step events) and
     # the value comes from the per-step events alone.
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
-    in_bytes = (2 * q.numel() + k.numel() + v.numel()) * 2
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if in_bytes <= l2_bytes else None
+    cfg, in_bytes = workload_config(w, x, l2_bytes, bwd)
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = flush_buf if in_bytes <= l2_bytes else None
 
     # timed region: K steps, per-launch CUDA events on the launching stream
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
     dist.barrier()
     torch.cuda.synchronize(dev)
-    with ClockSampler(dist.local) as clocks:
-        t0 = time.perf_counter()
-        for i in range(a.steps):
-            if flush is not None:
-                flush.fill_(i & 0xff)
-            ev[i][0].record(stream)
-            step(stream)
-            ev[i][1].record(stream)
-        torch.cuda.synchronize(dev)
-        wall = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    for i in range(a.steps):
+        if flush is not None:
+            flush.fill_(i & 0xff)
+        ev[i][0].record(stream)
+        step(stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.perf_counter()
+    wall = t1 - t0
     dist.barrier()
     st, word = fa.last_device_status(stream)
     if st != fa.FA_OK:
@@ -421,6 +469,36 @@ def run_ours(a, dist):
     region_s = dist.max(region_ms / 1e3)
     value = dist.world * flops * a.steps / region_s / 1e12
     avg_launch_s = sum(per_launch_ms) / len(per_launch_ms) / 1e3
+    clk = clocks.summary(t0, t1)
+
+    # sustained: at least 50 launches over at least 0.5 s, median per-launch time, with L2
+    # left warm (back to back) and with 256 MiB written between launches (L2 flushed);
+    # each with the clocks sampled over its own window
+    n_sus = int(min(max(50, math.ceil(0.5 / max(avg_launch_s, 1e-6))), 20000))
+
+    def sustained(flushed: bool):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_sus)]
+        torch.cuda.synchronize(dev)
+        s0 = time.perf_counter()
+        for i in range(n_sus):
+            if flushed:
+                flush_buf.fill_(i & 0xff)
+            evs[i][0].record(stream)
+            step(stream)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        s1 = time.perf_counter()
+        ms = sorted(e0.elapsed_time(e1) for e0, e1 in evs)
+        med = statistics.median(ms)
+        return {"value": flops / (med / 1e3) / 1e12, "unit": "TFLOP/s", "median_launch_ms": med,
+                "p10_launch_ms": ms[len(ms) // 10], "p90_launch_ms": ms[(9 * len(ms)) // 10], "launches": n_sus,
+                "seconds": round(s1 - s0, 3), "clocks": clocks.summary(s0, s1)}
+
+    sus = {"warm_l2": sustained(False), "flushed_l2": sustained(True)}
+    st, word = fa.last_device_status(stream)
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device status {st} ({word:#x}) in the sustained runs")
+    clocks.__exit__(None, None, None)
 
     # end to end through the public API with host buffers (pinned), copies inside the region
     n_e2e = max(1, min(a.e2e_steps, a.steps))
@@ -489,8 +567,7 @@ def run_ours(a, dist):
         return
     peak, peak_sust, hbm, peak_src = measured_peaks()
     props = torch.cuda.get_device_properties(dev)
-    clk = clocks.summary()
-    max_mhz = clk["sm_max_mhz"] or 2070.0
+    max_mhz = clk["sm_max_mhz"] or sus["warm_l2"]["clocks"]["sm_max_mhz"] or 2070.0
     theoretical = props.multi_processor_count * FLOP_PER_CLK_PER_SM * max_mhz * 1e6 / 1e12
     traffic = profiled_traffic(w.name, a.which)
     # the bound follows the arithmetic intensity: below the ridge of the measured
@@ -510,18 +587,19 @@ def run_ours(a, dist):
     roof.update({"kernel": ("fa_bwd_kernel (+ preprocessing, dQ conversion)" if bwd else
                             "fa_fwd_kernel" + (" + fa_combine_kernel" if splits > 1 else "")),
                  "avg_launch_ms": avg_launch_s * 1e3, "min_launch_ms": min(per_launch_ms), "wall_s": wall})
-    cfg = {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.Hkv, "N": w.N, "d": w.d, "causal": w.causal,
-           "scale": w.scale, "seed": w.seed,
-           "l2": ("inputs larger than L2 (Q+K+V+O = %.0f MiB), no flush" % (in_bytes / 2 ** 20)) if flush is None
-           else ("inputs smaller than L2 (Q+K+V+O = %.1f MiB): 256 MiB written between steps, value from the "
-                 "per-step events" % (in_bytes / 2 ** 20)),
-           "flops_per_step": flops, "key_splits": splits}
-    if bwd:
-        cfg["pass"] = "backward (FLOPs = 2.5 x the forward count)"
-    if w.Nk != w.N:
-        cfg["N_kv"] = w.Nk
-    if w.varlen:
-        cfg["lengths"] = [int(L) for L in x["lengths"]]
+    # the sustained roofline: the median launch of the mode that matches the value's L2
+    # policy, against the sustained (power-capped) measured peak
+    sus_main = sus["warm_l2"] if flush is None else sus["flushed_l2"]
+    med_s = sus_main["median_launch_ms"] / 1e3
+    if roof["bound"] == "hbm":
+        sus["roofline"] = {"bound": "hbm", "achieved": nbytes / med_s / 1e9, "peak": hbm, "unit": "GB/s",
+                           "frac": nbytes / med_s / 1e9 / hbm, "mode": "warm_l2" if flush is None else "flushed_l2",
+                           "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"}
+    else:
+        sus["roofline"] = {"bound": "tensor", "achieved": flops / med_s / 1e12, "peak": peak_sust,
+                           "unit": "TFLOP/s", "frac": flops / med_s / 1e12 / peak_sust,
+                           "mode": "warm_l2" if flush is None else "flushed_l2",
+                           "peak_source": f"{peak_src} bf16 sustained (MEASURED_PEAKS.json bf16_tflops_sustained)"}
     line = {
         "metric": METRIC_BWD if bwd else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": dist.world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": region_s / a.steps * 1e3, "higher_is_better": True,
@@ -535,6 +613,8 @@ def run_ours(a, dist):
                 "overlap": "step i+1's copies in | step i's kernels | step i-1's copies out, three streams"},
         "gpu_launches": launches_per_step * a.steps,
         "clocks": clk,
+        "key_splits": splits,
+        "sustained": sus,
     }
     if not a.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_bwd(w, x) if bwd else cpu_baseline(w, x)

@@ -114,6 +114,34 @@ int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse,
               int num_splits, void* stream);
 
 /*
+ * One key shard of a longer sequence ("context" sharding of the keys, for example
+ * over several GPUs): the attention of every query row over keys
+ * [kv_offset, kv_offset + N_kv) of a sequence of N_kv_total keys, written as a
+ * partial result for a later merge through the LSE (fa_lse_combine; the two-round
+ * example of "FlashAttention：一次前向计算" merges the results of two key blocks
+ * through a common reference, and "Flash Attention 4", section "重缩放与结果写回",
+ * defines each part's LSE).
+ *   q            : [B, N_q, H, d]        k, v : [B, N_kv, H_kv, d], the shard's keys
+ *                  (dtype elements, device; H_kv, G and dtype as for fa_fwd_gqa)
+ *   o_part       : fp32 [B, N_q, H, d] (device, written): the output normalised over
+ *                  this shard's keys; 0 for a row that sees none of them
+ *   lse_part     : fp32 [B, H, N_q] (device, written): natural-log LSE over this
+ *                  shard's keys; -inf for a row that sees none of them
+ *   N_kv_total   : keys of the whole sequence; kv_offset >= 0 and
+ *                  kv_offset + N_kv <= N_kv_total (else FA_ERR_INVALID_ARG)
+ *   causal       : 1 = the full sequence's bottom-right mask: query i sees global key
+ *                  j <= i + N_kv_total - N_q, i.e. shard key jl <= i + N_kv_total - N_q
+ *                  - kv_offset
+ * Merging the shards of all ranges with fa_lse_combine (num_parts = number of
+ * shards, parts stacked in the order of the o_parts / lse_parts layout) gives the
+ * result of fa_fwd_kv over the whole sequence. No temporary memory; no key splits
+ * inside the call. Other arguments and errors as for fa_fwd_kv.
+ */
+int fa_fwd_kv_partial(const void* q, const void* k, const void* v, float* o_part, float* lse_part,
+                      int B, int H, int H_kv, int N_q, int N_kv, int N_kv_total, int kv_offset, int d,
+                      float scale, int causal, int dtype, void* stream);
+
+/*
  * Variable-length (packed) attention forward: sequence s owns the rows
  * [cu_seqlens[s], cu_seqlens[s+1]) of q, k, v and o; each sequence attends only
  * to itself (self-attention, causal mask aligned per sequence).
@@ -129,8 +157,13 @@ int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse,
  * temporary device buffer taken from the library's stream-ordered memory pool
  * (cudaMallocFromPoolAsync / cudaFreeAsync on `stream`; the pool keeps its memory
  * between calls).
- * The contents of cu_seqlens are trusted (they are on the device): lengths
- * above max_seqlen or a total other than total_tokens are not detected.
+ * The schedule kernel checks cu_seqlens on the device before it lists any tile
+ * (cu_seqlens[0] = 0, non-decreasing, cu_seqlens[num_seqs] = total_tokens, every
+ * length <= max_seqlen). If a rule is broken it lists no tile, so nothing is
+ * written to o or lse, and fa_last_device_status returns FA_ERR_INVALID_ARG
+ * (detail: 7 << 8 | the first offending sequence << 32). The general entry point
+ * fa_fwd_varlen_kv checks cu_seqlens_kv the same way against total_kv (its key
+ * lengths are not bounded by max_seqlen_kv, which only guides num_splits = 0).
  */
 int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                   const int* cu_seqlens, int num_seqs, int total_tokens, int max_seqlen,
@@ -207,8 +240,10 @@ int fa_lse_combine(const float* o_parts, const float* lse_parts, int num_parts, 
  * It allocates nothing. Its work-tile list lives in a fixed array of this
  * library (2 MiB + 16 bytes of device memory, taken on every GPU that loads
  * the library and kept until the process exits), so:
- *  - the problem must satisfy H * (ceil(total_tokens / 256) + num_seqs) <= 131072
- *    (tiles of 256 query rows of one head), else it returns FA_ERR_CAPACITY
+ *  - the problem must satisfy H * (ceil(total_tokens / R) + num_seqs) <= 131072,
+ *    R the query rows per work tile: 256, or 128 when the library runs one-tile
+ *    tasks (FA_OPT_SOLO_TILES = 1 forces them; the automatic choice takes them only
+ *    for problems of at most one tile per SM), else it returns FA_ERR_CAPACITY
  *    and enqueues nothing;
  *  - all calls on a device share that array: calls whose work overlaps on the
  *    GPU (for example on two streams at once) race and may return wrong
@@ -255,9 +290,13 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
  *                    (dtype elements, device; dq, dk, dv written)
  *   lse            : fp32 [H, total_q], the LSE that fa_fwd_varlen* wrote
  *   cu_seqlens_q, cu_seqlens_kv : device int32 [num_seqs + 1], non-decreasing, starting
- *                    at 0 and ending at total_q / total_kv (not checked on the host);
- *                    empty sequences are allowed (a query row without keys gets dQ = 0,
- *                    a key without queries dK = dV = 0)
+ *                    at 0 and ending at total_q / total_kv, every length at most
+ *                    max_seqlen_q / max_seqlen_kv; empty sequences are allowed (a query
+ *                    row without keys gets dQ = 0, a key without queries dK = dV = 0).
+ *                    A one-block kernel checks the arrays on the device before any other
+ *                    work: if they break a rule, the call writes nothing to dq, dk, dv and
+ *                    fa_last_device_status returns FA_ERR_INVALID_ARG (detail: 7 << 8 |
+ *                    the first offending sequence << 32)
  *   max_seqlen_q, max_seqlen_kv : the longest sequence's lengths (upper bounds suffice;
  *                    they size the grid and the packed-row buffers)
  *   other arguments as for fa_bwd. Errors: as fa_bwd, plus FA_ERR_INVALID_ARG for null
@@ -275,9 +314,12 @@ const char* fa_error_string(int status);
 
 /*
  * Synchronizes `stream`, then returns and clears the device-side status word of
- * the current device: FA_OK, or FA_ERR_TIMEOUT if a kernel of this library gave
- * up on a wait since the last call (FA_ERR_CUDA if the synchronization failed).
- * If `detail` is not NULL it receives the raw word (role, barrier, block).
+ * the current device: FA_OK; FA_ERR_TIMEOUT if a kernel of this library gave up
+ * on a wait since the last call; FA_ERR_INVALID_ARG if a varlen call's device-side
+ * check rejected its cu_seqlens (FA_ERR_CUDA if the synchronization failed).
+ * If `detail` is not NULL it receives the raw word: code | role << 8 | barrier << 16
+ * | block << 32 (role 7 = the cu_seqlens check, its "block" the first offending
+ * sequence).
  */
 int fa_last_device_status(void* stream, unsigned long long* detail);
 

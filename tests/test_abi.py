@@ -150,6 +150,31 @@ def varlen_kv(**kw):
                                                              "causal", "dtype", "splits", "stream")])
 
 
+def kv_partial(**kw):
+    args = dict(q=16, k=16, v=16, o=16, l=16, B=1, H=8, Hkv=2, Nq=100, Nk=1000, Nt=4000, off=1000, d=128,
+                scale=0.125, causal=1, dtype=0, stream=NULL)
+    args.update(kw)
+    return fa.library().fa_fwd_kv_partial(*[args[n] for n in ("q", "k", "v", "o", "l", "B", "H", "Hkv", "Nq", "Nk",
+                                                              "Nt", "off", "d", "scale", "causal", "dtype",
+                                                              "stream")])
+
+
+@pytest.mark.parametrize("kw", [dict(off=-1), dict(off=3001), dict(Nt=999), dict(Nk=0), dict(o=NULL), dict(l=NULL),
+                                dict(o=8), dict(l=2), dict(Nq=0), dict(Hkv=3), dict(causal=2), dict(dtype=4),
+                                dict(scale=0.0), dict(k=NULL)])
+def test_kv_partial_rejects_invalid_arguments(kw):
+    assert kv_partial(**kw) == fa.FA_ERR_INVALID_ARG
+
+
+def test_kv_partial_head_dim_and_no_device():
+    assert kv_partial(d=96) == fa.FA_ERR_UNSUPPORTED
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        assert kv_partial() == fa.FA_ERR_NO_DEVICE
+        assert kv_partial(off=3000) == fa.FA_ERR_NO_DEVICE       # the last shard: ends at the last key
+        assert kv_partial(causal=0, off=0, Nt=1000) == fa.FA_ERR_NO_DEVICE
+
+
 def combine(**kw):
     args = dict(o=16, l=16, P=3, B=1, N=10, H=4, d=128, out=16, lse=NULL, dtype=0, stream=NULL)
     args.update(kw)

@@ -1,0 +1,90 @@
+"""Full-size parity: the three large workloads, every output element against the oracle.
+
+The CUDA path (through the C ABI, in the launch configuration the benchmark times)
+runs B4 H16 N4096 d128 causal, B1 H32 N16384 d128 causal with spiky scores, and the
+packed batch of 8 sequences of 512..8192 tokens (H16 d128 causal); the fp64 oracle
+computes the same problems in full on the host's cores, and every element of O and
+every LSE value is compared: max-abs O <= 2e-2 and LSE <= 1e-3, for bf16 inputs. The
+method reaches the plain definition of attention exactly up to rounding ("Flash
+Attention 4", section "算法结构": the result equals standard attention), so the
+whole output is checked, not a sample of rows.
+
+Each test also reports the error against the oracle rounded to bf16 (round to
+nearest even), which separates the kernel's own error from the output rounding.
+"""
+import numpy as np
+import pytest
+
+import attention_forward_tma_gb300 as fa
+import fa_inputs
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+TOL_O = 2e-2
+TOL_LSE = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    fa.library()
+    fa.set_option("solo_tiles", -1)
+    yield torch
+
+
+def dev(bits):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def bf16_host(t):
+    import torch
+    return fa_inputs.bf16_bits_to_f32(t.view(torch.int16).cpu().numpy().view(np.uint16)).astype(np.float64)
+
+
+def compare(name, o, lse, o_ref, lse_ref):
+    assert np.isfinite(o).all(), f"{name}: non-finite output"
+    err_o = float(np.abs(o - o_ref).max())
+    o_ref16 = fa_inputs.bf16_bits_to_f32(fa_inputs.f32_to_bf16_bits(o_ref.astype(np.float32))).astype(np.float64)
+    err_o16 = float(np.abs(o - o_ref16).max())
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isfinite(lse), fin), f"{name}: LSE finiteness differs"
+    err_l = float(np.abs(lse[fin] - lse_ref[fin]).max())
+    print(f"\n{name}: {o.size} O elements, {lse.size} LSE values; max|O - oracle| = {err_o:.3e}, "
+          f"max|O - bf16(oracle)| = {err_o16:.3e}, max|LSE - oracle| = {err_l:.3e}")
+    assert err_o <= TOL_O, f"{name}: max |O - oracle| = {err_o}"
+    assert err_l <= TOL_LSE, f"{name}: max |LSE - oracle| = {err_l}"
+
+
+@pytest.mark.parametrize("name", ["c3_b4h16n4096d128_causal", "c4_b1h32n16384d128_causal_spiky"])
+def test_fixed_length_workload_every_element(name):
+    import torch
+    w = fa_inputs.WORKLOADS[name]
+    x = fa_inputs.make_workload(w)
+    q, k, v = dev(x["q"]), dev(x["k"]), dev(x["v"])
+    o = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((w.B, w.H, w.N), float("nan"), dtype=torch.float32, device="cuda")
+    fa.fa_fwd(q, k, v, scale=w.scale, causal=w.causal, out=o, lse=lse)
+    st, word = fa.last_device_status()
+    assert st == fa.FA_OK, hex(word)
+    o_gpu, l_gpu = bf16_host(o), lse.cpu().numpy().astype(np.float64)
+    del q, k, v, o, lse
+    o_ref, l_ref = oracle.attention(x["q"], x["k"], x["v"], w.scale, w.causal)
+    compare(name, o_gpu, l_gpu, o_ref, l_ref)
+
+
+def test_varlen_workload_every_element():
+    import torch
+    w = fa_inputs.WORKLOADS["c5_varlen8_h16d128_causal"]
+    x = fa_inputs.make_workload(w)
+    cu = x["cu_seqlens"]
+    o, l = fa.fa_fwd_varlen(dev(x["q"]), dev(x["k"]), dev(x["v"]), torch.from_numpy(cu).cuda(),
+                            int(x["lengths"].max()), scale=w.scale, causal=True)
+    st, word = fa.last_device_status()
+    assert st == fa.FA_OK, hex(word)
+    o_gpu, l_gpu = bf16_host(o), l.cpu().numpy().astype(np.float64)
+    del o, l
+    o_ref, l_ref = oracle.attention_varlen(x["q"], x["k"], x["v"], cu, w.scale, True)
+    compare("c5_varlen8_h16d128_causal", o_gpu, l_gpu, o_ref, l_ref)

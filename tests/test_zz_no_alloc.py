@@ -4,11 +4,12 @@ Some callers cannot allocate device memory when they call attention: a server
 that gave all GPU memory to its own pool at start-up, or a latency-critical
 loop that must not run allocator calls. fa_fwd_varlen_noalloc serves them by
 keeping its work-tile list in a fixed array inside the library. These tests
-call it through the C ABI (ctypes) and check that it returns what
-fa_fwd_varlen (which takes a temporary buffer from the stream-ordered
-allocator) returns, on two calls in a row with different problems, so stale
-contents of the shared array from the first call cannot leak into the second.
-This file is named to be collected last.
+call it through the C ABI (ctypes) on two calls in a row with different
+problems, so stale contents of the shared array from the first call cannot leak
+into the second, and check each result against the fp64 oracle (O <= 2e-2,
+LSE <= 1e-3 max-abs) and, bit for bit, against fa_fwd_varlen, which runs the
+same schedule and kernel from a temporary buffer of the stream-ordered
+allocator. This file is named to be collected last.
 """
 import ctypes
 
@@ -17,6 +18,7 @@ import pytest
 
 import attention_forward_tma_gb300 as fa
 import fa_inputs
+import oracle
 
 TOL_O = 2e-2
 TOL_LSE = 1e-3
@@ -30,6 +32,20 @@ def test_noalloc_rejects_problems_beyond_its_fixed_capacity():
     assert "scratch" in fa.error_string(st)
 
 
+def test_noalloc_capacity_counts_one_tile_tasks_when_forced():
+    """With one-tile (128-row) tasks forced, 16 heads x (2^20 / 128 + 1) = 131088 tiles
+    exceed the array although 16 x (2^20 / 256 + 1) = 65552 would fit: refused."""
+    lib = fa.library()
+    T = 1 << 20
+    assert 16 * (T // 128 + 1) > 131072 >= 16 * (T // 256 + 1)
+    fa.set_option("solo_tiles", 1)
+    try:
+        st = lib.fa_fwd_varlen_noalloc(256, 256, 256, 256, None, 256, 1, T, T, 16, 128, 0.088, 1, None)
+    finally:
+        fa.set_option("solo_tiles", -1)
+    assert st == fa.FA_ERR_CAPACITY
+
+
 def _run(entry, q, k, v, cu, maxL, H, d, causal):
     import torch
     T = q.shape[0]
@@ -41,12 +57,11 @@ def _run(entry, q, k, v, cu, maxL, H, d, causal):
     assert st == fa.FA_OK, fa.error_string(st)
     st, word = fa.last_device_status()
     assert st == fa.FA_OK, hex(word)
-    o32 = fa_inputs.bf16_bits_to_f32(o.view(torch.int16).cpu().numpy().view(np.uint16))
-    return o32.astype(np.float64), lse.cpu().numpy().astype(np.float64)
+    return o.view(torch.int16).cpu().numpy().view(np.uint16), lse.cpu().numpy()
 
 
 @pytest.mark.gpu
-def test_noalloc_matches_allocating_entry_point_on_two_calls():
+def test_noalloc_matches_oracle_and_allocating_entry_point_on_two_calls():
     import torch
     assert torch.cuda.is_available()
     lib = fa.library()
@@ -60,10 +75,16 @@ def test_noalloc_matches_allocating_entry_point_on_two_calls():
         _, cu, q, k, v = fa_inputs.make_varlen_from_lengths(lengths, H, d, seed)
         qd, kd, vd, cud = dev(q), dev(k), dev(v), torch.from_numpy(cu).cuda()
         maxL = max(lengths)
-        o_ref, l_ref = _run(lib.fa_fwd_varlen, qd, kd, vd, cud, maxL, H, d, causal)
         o_new, l_new = _run(lib.fa_fwd_varlen_noalloc, qd, kd, vd, cud, maxL, H, d, causal)
-        assert np.isfinite(o_new).all()
-        assert np.abs(o_new - o_ref).max() <= TOL_O
-        fin = np.isfinite(l_ref)
+        o_ref, l_ref = _run(lib.fa_fwd_varlen, qd, kd, vd, cud, maxL, H, d, causal)
+        # the same schedule and kernel as the allocating call: the same bits
+        assert np.array_equal(o_new, o_ref)
+        assert np.array_equal(l_new.view(np.uint32), l_ref.view(np.uint32))
+        # and the oracle's values within the forward tolerances
+        o_or, l_or = oracle.attention_varlen(q, k, v, cu, 1.0 / d ** 0.5, causal)
+        o64 = fa_inputs.bf16_bits_to_f32(o_new).astype(np.float64)
+        assert np.isfinite(o64).all()
+        assert np.abs(o64 - o_or).max() <= TOL_O
+        fin = np.isfinite(l_or)
         assert np.array_equal(np.isfinite(l_new), fin)
-        assert np.abs(l_new[fin] - l_ref[fin]).max() <= TOL_LSE
+        assert np.abs(l_new[fin].astype(np.float64) - l_or[fin]).max() <= TOL_LSE
