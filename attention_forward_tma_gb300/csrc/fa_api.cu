@@ -364,10 +364,12 @@ __global__ void __launch_bounds__(1024) fa_varlen_schedule_kernel(const int* cu_
   __shared__ int hist[kSchedBuckets];
   __shared__ int total_tiles;
   __shared__ int first_bad;
+  __shared__ int max_cost;
   for (int i = threadIdx.x; i < kSchedBuckets; i += blockDim.x) hist[i] = 0;
   if (threadIdx.x == 0) {
     total_tiles = 0;
     first_bad = INT_MAX;
+    max_cost = 0;
   }
   __syncthreads();
   for (int s = threadIdx.x; s < num_seqs; s += blockDim.x)
@@ -387,19 +389,28 @@ __global__ void __launch_bounds__(1024) fa_varlen_schedule_kernel(const int* cu_
     const KRange r = key_range(m * rows, rows, Lk - Lq, Lk, gshift, causal != 0, splits, sp);
     return min(r.hi - r.lo, kSchedBuckets - 1);
   };
-  for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
+  // one warp per sequence, its lanes over the sequence's row blocks
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  int my_max = 0, my_tiles = 0;
+  for (int s = warp; s < num_seqs; s += nwarps) {
     const int Lq = max(cu_q[s + 1] - cu_q[s], 0), Lk = max(cu_k[s + 1] - cu_k[s], 0);
     const int nm = ((Lq << gshift) + rows - 1) / rows;
-    for (int m = 0; m < nm; ++m)
-      for (int sp = 0; sp < splits; ++sp) atomicAdd(&hist[cost_of(m, Lq, Lk, sp)], 1);
-    atomicAdd(&total_tiles, nm * splits);
+    for (int m = lane; m < nm; m += 32)
+      for (int sp = 0; sp < splits; ++sp) {
+        const int c = cost_of(m, Lq, Lk, sp);
+        atomicAdd(&hist[c], 1);
+        my_max = max(my_max, c);
+        ++my_tiles;
+      }
   }
+  atomicMax(&max_cost, my_max);
+  atomicAdd(&total_tiles, my_tiles);
   __syncthreads();
   if (threadIdx.x == 0) {
-    // exclusive scan from the most expensive bucket down: hist[c] becomes the
-    // first slot of bucket c
+    // exclusive scan from the most expensive bucket present down: hist[c] becomes
+    // the first slot of bucket c
     int run = 0;
-    for (int c = kSchedBuckets - 1; c >= 0; --c) {
+    for (int c = max_cost; c >= 0; --c) {
       const int n = hist[c];
       hist[c] = run;
       run += n;
@@ -408,10 +419,10 @@ __global__ void __launch_bounds__(1024) fa_varlen_schedule_kernel(const int* cu_
     *count = (int)(n_tasks < capacity ? n_tasks : capacity);
   }
   __syncthreads();
-  for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
+  for (int s = warp; s < num_seqs; s += nwarps) {
     const int Lq = max(cu_q[s + 1] - cu_q[s], 0), Lk = max(cu_k[s + 1] - cu_k[s], 0);
     const int nm = ((Lq << gshift) + rows - 1) / rows;
-    for (int m = 0; m < nm; ++m) {
+    for (int m = lane; m < nm; m += 32) {
       for (int sp = 0; sp < splits; ++sp) {
         const int c = cost_of(m, Lq, Lk, sp);
         const int slot = atomicAdd(&hist[c], 1);
