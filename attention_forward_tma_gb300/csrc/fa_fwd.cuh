@@ -112,12 +112,14 @@ struct FwdParams {
 };
 
 // ------------------------------------------------------------------ tracing (FA_TRACE builds)
-// A tracing build stamps clock64 at every hand-off of the pipeline for the first
-// trace_ctas CTAs: one leader thread per role writes (clock, event code, block)
-// pairs into trace[(cta * kTraceRoles + role) * kTraceSlots ...]; slot 0 holds
-// the event count. Normal builds compile the stamps away.
+// A tracing build stamps the SM clock at every hand-off of the pipeline for the
+// first trace_ctas CTAs: one leader thread per role writes one 64-bit word per
+// event, (32-bit clock << 32) | (event code << 24) | (block & 0xffffff), into
+// trace[(cta * kTraceRoles + role) * kTraceSlots + n]; the buffer starts zeroed,
+// so the first zero word ends a role's events. One clock read and one store per
+// event keep the stamps' own cost small. Normal builds compile the stamps away.
 constexpr int kTraceRoles = 5;      // producer, MMA, softmax 0, softmax 1, correction
-constexpr int kTraceSlots = 8192;   // 64-bit words per role: count + 2 per event
+constexpr int kTraceSlots = 8192;   // 64-bit words (events) per role
 enum : uint32_t {
   kEvQ0 = 1, kEvK = 2, kEvQ1 = 3, kEvV = 4,
   kEvS0 = 10, kEvS1 = 11, kEvPO0 = 12, kEvPV0a = 13, kEvP20 = 14, kEvPV0b = 15, kEvPO1 = 16,
@@ -141,10 +143,10 @@ struct Tracer {
     init(p.trace, p.trace_ctas, role, leader);
   }
   __device__ __forceinline__ void rec(uint32_t code, int blk) {
-    if (buf != nullptr && 2 * n + 2 < (uint32_t)kTraceSlots) {
-      buf[1 + 2 * n] = clock64();
-      buf[2 + 2 * n] = ((unsigned long long)code << 32) | (uint32_t)blk;
-      buf[0] = ++n;
+    if (buf != nullptr && n < (uint32_t)kTraceSlots) {
+      uint32_t c;
+      asm volatile("mov.u32 %0, %%clock;" : "=r"(c));
+      buf[n++] = ((unsigned long long)c << 32) | (code << 24) | ((uint32_t)blk & 0xffffffu);
     }
   }
 #else

@@ -6,7 +6,8 @@ Runs one attention forward (or backward) of a synthetic workload with clock
 stamps at every hand-off of the pipeline (TMA issue, MMA issue, softmax phases,
 correction and epilogue; for the backward: Q/dO loads, the five products, the
 P and dS phases and the dQ reduce) for the first N CTAs, then prints per-role
-cycle statistics. Stamps are SM clock cycles (clock64) of the CTA's own SM.
+cycle statistics. Stamps are SM clock cycles (the 32-bit clock, unwrapped) of the
+CTA's own SM.
 """
 from __future__ import annotations
 
@@ -62,15 +63,21 @@ def capture(run, ctas: int = 2):
     for c in range(ctas):
         out[c] = {}
         for r in range(roles.value):
-            n = int(raw[c, r, 0])
             ev = []
-            for i in range(n):
-                clk = int(raw[c, r, 1 + 2 * i])
-                word = int(raw[c, r, 2 + 2 * i])
-                code, blk = word >> 32, word & 0xFFFFFFFF
-                if blk >= 1 << 31:
-                    blk -= 1 << 32
-                ev.append((clk, EVENTS.get(code, str(code)), blk))
+            high = 0          # the 32-bit clock wraps every 2^32 cycles: unwrap in order
+            last = None
+            for word in raw[c, r]:
+                word = int(word)
+                if word == 0:
+                    break
+                clk = word >> 32
+                if last is not None and clk < last:
+                    high += 1 << 32
+                last = clk
+                code, blk = (word >> 24) & 0xFF, word & 0xFFFFFF
+                if blk >= 1 << 23:
+                    blk -= 1 << 24
+                ev.append((high + clk, EVENTS.get(code, str(code)), blk))
             out[c][ROLES[r]] = ev
     return out
 
