@@ -360,11 +360,13 @@ __device__ __forceinline__ bool cu_entry_ok(const int* cu, int s, int num_seqs, 
 __global__ void __launch_bounds__(1024) fa_varlen_schedule_kernel(const int* cu_q, const int* cu_k, int num_seqs,
                                                                   int Hkv, int gshift, int causal, int splits,
                                                                   int rows, int capacity, int4* tasks, int* count,
-                                                                  int total_q, int total_k, int max_q) {
+                                                                  int total_q, int total_k, int max_q,
+                                                                  long long section_bytes, int kv_row_bytes) {
   __shared__ int hist[kSchedBuckets];
   __shared__ int total_tiles;
   __shared__ int first_bad;
   __shared__ int max_cost;
+  __shared__ long long sec_bytes;
   for (int i = threadIdx.x; i < kSchedBuckets; i += blockDim.x) hist[i] = 0;
   if (threadIdx.x == 0) {
     total_tiles = 0;
@@ -397,22 +399,53 @@ __global__ void __launch_bounds__(1024) fa_varlen_schedule_kernel(const int* cu_
     const int nm = ((Lq << gshift) + rows - 1) / rows;
     for (int m = lane; m < nm; m += 32)
       for (int sp = 0; sp < splits; ++sp) {
-        const int c = cost_of(m, Lq, Lk, sp);
-        atomicAdd(&hist[c], 1);
-        my_max = max(my_max, c);
+        my_max = max(my_max, cost_of(m, Lq, Lk, sp));
         ++my_tiles;
       }
   }
   atomicMax(&max_cost, my_max);
   atomicAdd(&total_tiles, my_tiles);
   __syncthreads();
+  // L2 sections: consecutive sequences whose K and V (all K/V heads) fill about
+  // section_bytes form one section (a sequence belongs to the section where its keys
+  // start, so no scan is needed: cu_k is the prefix); the tiles are listed section by
+  // section, longest first inside each, so the CTAs running at once share one
+  // section's K/V in L2. Sort key = section * (max_cost + 1) + (max_cost - cost); the
+  // sections grow until the keys fit in the histogram. section_bytes = 0: one section.
+  const int nc = max_cost + 1;
   if (threadIdx.x == 0) {
-    // exclusive scan from the most expensive bucket present down: hist[c] becomes
-    // the first slot of bucket c
+    const long long all = (long long)total_k * kv_row_bytes;
+    long long b = section_bytes > 0 ? section_bytes : all + 1;
+    if (b < 1) b = 1;
+    long long nsec = all / b + 1;
+    if (nsec * nc > kSchedBuckets) {
+      b *= (nsec * nc + kSchedBuckets - 1) / kSchedBuckets;
+      nsec = all / b + 1;
+      while (nsec * nc > kSchedBuckets) {   // integer rounding: grow until it fits
+        b += b / 8 + 1;
+        nsec = all / b + 1;
+      }
+    }
+    sec_bytes = b;
+  }
+  __syncthreads();
+  const long long sb = sec_bytes;
+  auto key_of = [&](int s, int c) { return (int)(((long long)cu_k[s] * kv_row_bytes) / sb) * nc + (max_cost - c); };
+  for (int s = warp; s < num_seqs; s += nwarps) {
+    const int Lq = max(cu_q[s + 1] - cu_q[s], 0), Lk = max(cu_k[s + 1] - cu_k[s], 0);
+    const int nm = ((Lq << gshift) + rows - 1) / rows;
+    for (int m = lane; m < nm; m += 32)
+      for (int sp = 0; sp < splits; ++sp) atomicAdd(&hist[key_of(s, cost_of(m, Lq, Lk, sp))], 1);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // exclusive scan in key order: hist[k] becomes the first slot of key k
+    const long long all = (long long)total_k * kv_row_bytes;
+    const int nkeys = (int)(all / sb + 1) * nc;
     int run = 0;
-    for (int c = max_cost; c >= 0; --c) {
-      const int n = hist[c];
-      hist[c] = run;
+    for (int k = 0; k < nkeys; ++k) {
+      const int n = hist[k];
+      hist[k] = run;
       run += n;
     }
     const long long n_tasks = (long long)total_tiles * Hkv;
@@ -425,7 +458,7 @@ __global__ void __launch_bounds__(1024) fa_varlen_schedule_kernel(const int* cu_
     for (int m = lane; m < nm; m += 32) {
       for (int sp = 0; sp < splits; ++sp) {
         const int c = cost_of(m, Lq, Lk, sp);
-        const int slot = atomicAdd(&hist[c], 1);
+        const int slot = atomicAdd(&hist[key_of(s, c)], 1);
         for (int h = 0; h < Hkv; ++h) {
           const long long ti = (long long)slot * Hkv + h;
           if (ti < capacity) tasks[ti] = make_int4(s, h | (sp << 16), m, c);
@@ -817,8 +850,10 @@ int varlen_launch(DevInfo* dev, const void* q, const void* k, const void* v, voi
   std::memset(&p, 0, sizeof p);
   int st = make_maps(p, q, k, v, o, total_q, total_k, H, H_kv, d, f16);
   if (st != FA_OK) return st;
+  // L2 sections of a quarter of L2 of K/V, as for fixed-length causal work
   fa::fa_varlen_schedule_kernel<<<1, 1024, 0, s>>>(cu_q, cu_k, num_seqs, H_kv, gshift, causal, splits, rows, cap,
-                                                   tasks, count, total_q, total_k, max_q);
+                                                   tasks, count, total_q, total_k, max_q, dev->l2_bytes / 4,
+                                                   H_kv * 4 * d);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   p.o = static_cast<uint16_t*>(o);
   p.lse = lse;
@@ -981,7 +1016,7 @@ int fa_varlen_schedule(const int* cu_seqlens_q, const int* cu_seqlens_kv, int nu
   if ((st = device_info(&dev)) != FA_OK) return st;
   fa::fa_varlen_schedule_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(
       cu_seqlens_q, cu_seqlens_kv, num_seqs, H_kv, gshift, causal, splits, fa::kTaskRows, capacity,
-      static_cast<int4*>(tasks), count, -1, -1, -1);
+      static_cast<int4*>(tasks), count, -1, -1, -1, 0, 0);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
