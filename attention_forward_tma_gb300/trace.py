@@ -162,6 +162,65 @@ def _cross(ea, a, eb, b, shift=0):
     return [clk - ta[blk - shift] for clk, name, blk in eb if name == b and blk - shift in ta]
 
 
+# tcgen05.mma M128 N128 K16 (bf16/fp16 in, fp32 accumulate) measured on a GB300 by a
+# one-warp issue probe: 71 cycles with both operands in shared memory, 68 with A in
+# tensor memory. Products per group of the forward's MMA warp: QK^T is 8 K16 steps
+# over d = 128, PV 6 + 2 steps over the 96 + 32 columns of P.
+MMA_CYCLES = 71.0
+FWD_GROUP_MMAS = {"S0": 8, "S1": 8, "PV0a": 6, "PV1a": 6, "PV0b": 2, "PV1b": 2}
+FWD_WAITS = ("PO0", "PO1", "P2_0", "P2_1", "KVfull_K", "KVfull_V")
+
+
+def pipe_model(roles, mma_cycles: float = MMA_CYCLES, group_mmas=None) -> dict:
+    """Tensor-pipe occupancy of one CTA from its MMA warp's stamps (forward, d = 128).
+
+    Each issue group (IssueBegin ... the group's end stamp) is taken to enter the pipe
+    at its IssueBegin stamp, or when the pipe finishes the previous group if that is
+    later, and to keep it busy for (its MMAs) x mma_cycles. Time the pipe spends idle
+    before a group is charged to the wait the MMA warp passed just before that group
+    ("issue" when it passed none: the commit and bookkeeping between two groups)."""
+    group_mmas = group_mmas or FWD_GROUP_MMAS
+    ev = roles["mma"]
+    free = t_first = None
+    busy = 0.0
+    idle, issue = {}, {}
+    last_wait = None
+    for i, (clk, name, _) in enumerate(ev):
+        if name in FWD_WAITS:
+            last_wait = name
+        if name != "IssueBegin":
+            continue
+        j = i + 1
+        while j < len(ev) and ev[j][1] not in group_mmas:
+            j += 1
+        if j == len(ev):
+            break
+        n = group_mmas[ev[j][1]]
+        issue.setdefault(ev[j][1], []).append(ev[j][0] - clk)
+        if free is None:
+            free = t_first = clk
+        if clk > free:
+            idle.setdefault(last_wait or "issue", []).append(clk - free)
+            free = clk
+        free += n * mma_cycles
+        busy += n * mma_cycles
+        last_wait = None
+    span = (free - t_first) if free is not None else 0.0
+    return {"span": span, "busy": busy, "idle": idle, "issue": issue}
+
+
+def timeline(roles, start: int = 0, count: int = 60):
+    """The CTA's stamps of every role merged in clock order: `count` of them from the
+    `start`-th stamp of the MMA warp on, as (cycles since that stamp, role, event, block)."""
+    merged = sorted((clk, role, name, blk) for role, ev in roles.items() for clk, name, blk in ev)
+    mma = roles["mma"]
+    if not mma:
+        return []
+    t0 = mma[min(start, len(mma) - 1)][0]
+    out = [(clk - t0, role, name, blk) for clk, role, name, blk in merged if clk >= t0]
+    return out[:count]
+
+
 def _fmt(v):
     if isinstance(v, list):
         if not v:
@@ -176,6 +235,10 @@ def main():
     ap.add_argument("--ctas", type=int, default=2)
     ap.add_argument("--json", default=None)
     ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"])
+    ap.add_argument("--timeline", type=int, default=0, metavar="N",
+                    help="print N merged stamps of CTA 0 from its MMA warp's 200th stamp on")
+    ap.add_argument("--pipe", action="store_true",
+                    help="forward: modelled tensor-pipe occupancy and idle time by the preceding wait")
     a = ap.parse_args()
     sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
     import numpy as np
@@ -215,6 +278,23 @@ def main():
         print(f"CTA {c}")
         for key, val in d.items():
             print(f"  {key:28s} {_fmt(val)}")
+    if a.pipe and a.which == "fwd":
+        for c in tr:
+            m = pipe_model(tr[c])
+            if not m["span"]:
+                continue
+            print(f"CTA {c}: tensor pipe busy {m['busy']:.0f} of {m['span']:.0f} cycles "
+                  f"({100 * m['busy'] / m['span']:.1f} %, {MMA_CYCLES:.0f} cycles per MMA)")
+            for name, v in sorted(m["idle"].items(), key=lambda kv: -sum(kv[1])):
+                print(f"  idle after {name:9s} {100 * sum(v) / m['span']:5.1f} % of the span "
+                      f"(n={len(v)}, median {statistics.median(v):.0f} cycles)")
+            for name, v in m["issue"].items():
+                print(f"  issue of {name:5s} median {statistics.median(v):.0f} cycles "
+                      f"({FWD_GROUP_MMAS[name]} MMAs)")
+    if a.timeline:
+        print(f"CTA 0 timeline (cycles from the MMA warp's 200th stamp):")
+        for dt, role, name, blk in timeline(tr[0], 200, a.timeline):
+            print(f"  {dt:8d}  {role:10s} {name:10s} {blk}")
 
 
 if __name__ == "__main__":
