@@ -508,8 +508,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       mbar_init(bar(L::bQFull + i), 1);
       mbar_init(bar(L::bQEmpty + i), 1);
       mbar_init(bar(L::bSFull + i), 1);
-      mbar_init(bar(L::bPO + i), 2 * kBlockM);      // first part of P stored (softmax) + O ready (WG2)
-      mbar_init(bar(L::bP2 + i), kBlockM);          // the rest of P stored (softmax)
+      // two-tile tasks: first part of P stored (softmax) + O ready (WG2); solo tasks: both
+      // warpgroups' halves of P stored + O ready
+      mbar_init(bar(L::bPO + i), (SOLO ? 3 : 2) * kBlockM);
+      mbar_init(bar(L::bP2 + i), kBlockM);          // two-tile tasks: the rest of P stored (softmax)
       mbar_init(bar(L::bCorrFull + i), kBlockM);
       mbar_init(bar(L::bCorrEmpty + i), kBlockM);
       mbar_init(bar(L::bOFinal + i), 1);
@@ -724,15 +726,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
               const uint32_t c = (c0 + 2u * (uint32_t)i + 1u) % (2u * L::kStages);
               const uint32_t vs = c % L::kStages;
               if (!w.wait(bar(L::bKVFull + vs), c / L::kStages, L::bKVFull + vs, j)) { ok = false; break; }
+              // both halves of P (the warpgroups finish within ~150 cycles of each other)
+              // and O: one wait
               if (!w.wait(bar(L::bPO + b), (po_par >> b) & 1, L::bPO + b, j)) { ok = false; break; }
               po_par ^= 1u << b;
               tc_fence_after();
               // P of keys 0-63 in columns [0, 32) of the score tile, of keys 64-127 in [64, 96)
-              if (leader) issue_pv<D, 0, kSoloSplitP, F16>(O0, b ? S1 : S0, Vd + vs * kStageStep, i > 0);
-              if (!w.wait(bar(L::bP2 + b), (p2_par >> b) & 1, L::bP2 + b, j)) { ok = false; break; }
-              p2_par ^= 1u << b;
-              tc_fence_after();
               if (leader) {
+                issue_pv<D, 0, kSoloSplitP, F16>(O0, b ? S1 : S0, Vd + vs * kStageStep, i > 0);
                 issue_pv<D, kSoloSplitP, kBlockN, F16>(O0, (b ? S1 : S0) + 32, Vd + vs * kStageStep, true);
                 mma_commit(bar(L::bKVEmpty + vs));
                 mma_commit(bar(L::bPVDone));                         // O holds blocks 0 .. i
@@ -901,6 +902,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         // keeps the row sum of its own columns, and WG1 hands its sum to WG0 at the end.
         // P of WG0's keys goes to columns [0, 32) of the score tile and WG1's to
         // [64, 96) (columns each has itself read); WG0 passes acc_scale in column 32.
+        // Both warpgroups announce their half on p_o[b], which WG2's O arrival completes.
         float* xm = reinterpret_cast<float*>(smem + L::kQOff + L::kTileBytes);   // [2 blocks][2 halves][128]
         float* ysum = xm + 4 * kBlockM;                                          // [128] WG1's row sums
         if (kr.hi <= kr.lo) {   // no key for any row of the task: LSE = -inf (O = 0 is written by WG2)
@@ -1003,7 +1005,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           tmem_st32(tS + (t == 0 ? 0 : 64), pk);
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(bar(t == 0 ? L::bPO + b : L::bP2 + b));
+          mbar_arrive(bar(L::bPO + b));
           tr.rec(t == 0 ? kEvHalf1 : kEvHalf2, j);
           float sa, sb;
           unpack2(add2(sum2a, sum2b), sa, sb);

@@ -236,7 +236,8 @@ def main():
     ap.add_argument("--json", default=None)
     ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"])
     ap.add_argument("--timeline", type=int, default=0, metavar="N",
-                    help="print N merged stamps of CTA 0 from its MMA warp's 200th stamp on")
+                    help="print N merged stamps of CTA 0 from its MMA warp's --timeline-from-th stamp on")
+    ap.add_argument("--timeline-from", type=int, default=200, metavar="I")
     ap.add_argument("--pipe", action="store_true",
                     help="forward: modelled tensor-pipe occupancy and idle time by the preceding wait")
     a = ap.parse_args()
@@ -292,8 +293,8 @@ def main():
                 print(f"  issue of {name:5s} median {statistics.median(v):.0f} cycles "
                       f"({FWD_GROUP_MMAS[name]} MMAs)")
     if a.timeline:
-        print(f"CTA 0 timeline (cycles from the MMA warp's 200th stamp):")
-        for dt, role, name, blk in timeline(tr[0], 200, a.timeline):
+        print(f"CTA 0 timeline (cycles from the MMA warp's stamp {a.timeline_from}):")
+        for dt, role, name, blk in timeline(tr[0], a.timeline_from, a.timeline):
             print(f"  {dt:8d}  {role:10s} {name:10s} {blk}")
 
 
