@@ -468,23 +468,34 @@ def run_ours(a, dist):
         reg_ms = ev[0][0].elapsed_time(ev[-1][1]) if flush is None else sum(per_ms)
         return per_ms, reg_ms, t0, t1
 
+    graph = None
     if flush is None:
         # timed region: the K steps captured once in a CUDA graph (each call captures
         # after one eager call per shape) and replayed, bracketed by events on the
-        # launching stream; the same K steps launched eagerly are reported beside it
-        side = torch.cuda.Stream(dev)
-        side.wait_stream(stream)
-        with torch.cuda.stream(side):
-            step(side)
-        stream.wait_stream(side)
-        torch.cuda.synchronize(dev)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            cap = torch.cuda.current_stream(dev)
-            for _ in range(a.steps):
-                step(cap)
-        graph.replay()
-        torch.cuda.synchronize(dev)
+        # launching stream; the same K steps launched eagerly are reported beside it.
+        # Should capture fail, the eager region is the value (stated in `timing`).
+        try:
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                step(side)
+            stream.wait_stream(side)
+            torch.cuda.synchronize(dev)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                cap = torch.cuda.current_stream(dev)
+                for _ in range(a.steps):
+                    step(cap)
+            graph.replay()
+            torch.cuda.synchronize(dev)
+        except RuntimeError as e:
+            print(f"bench: CUDA graph capture failed ({e}); timing eager launches", file=sys.stderr)
+            graph = None
+            torch.cuda.synchronize(dev)
+        # every rank takes the same path (the paths differ in their barriers)
+        if dist.max(0.0 if graph is not None else 1.0) != 0.0:
+            graph = None
+    if graph is not None:
         g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         dist.barrier()
         torch.cuda.synchronize(dev)
@@ -508,7 +519,8 @@ def run_ours(a, dist):
         avg_launch_s = region_ms / a.steps / 1e3
     else:
         per_launch_ms, region_ms, t0, t1 = eager_steps()
-        timing = "K eager launches, 256 MiB written between steps outside the per-step events"
+        timing = ("K eager launches, 256 MiB written between steps outside the per-step events"
+                  if flush is not None else "K eager launches, events around each step (graph capture failed)")
         eager = None
         avg_launch_s = sum(per_launch_ms) / len(per_launch_ms) / 1e3
     wall = t1 - t0
