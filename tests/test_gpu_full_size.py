@@ -1,10 +1,13 @@
-"""Full-size parity: the three large workloads, every output element against the oracle.
+"""Full-size parity: the large workloads, every output element against the oracle.
 
 The CUDA path (through the C ABI, in the launch configuration the benchmark times)
 runs B4 H16 N4096 d128 causal, B1 H32 N16384 d128 causal with spiky scores, and the
-packed batch of 8 sequences of 512..8192 tokens (H16 d128 causal); the fp64 oracle
-computes the same problems in full on the host's cores, and every element of O and
-every LSE value is compared: max-abs O <= 2e-2 and LSE <= 1e-3, for bf16 inputs. The
+packed batch of 8 sequences of 512..8192 tokens (H16 d128 causal); beyond them the
+grouped-query B4 H32/8 N4096 causal, the grouped-query packed batch in fp16 (H32/4) and
+decoding (B8 H32/8, one query row against 32768 keys, the library's key splits and
+merge). The fp64 oracle computes the same problems in full on the host's cores, and
+every element of O and every LSE value is compared: max-abs O <= 2e-2 and LSE <= 1e-3,
+for bf16 and fp16 inputs. The
 method reaches the plain definition of attention exactly up to rounding ("Flash
 Attention 4", section "算法结构": the result equals standard attention), so the
 whole output is checked, not a sample of rows.
@@ -44,16 +47,31 @@ def bf16_host(t):
     return fa_inputs.bf16_bits_to_f32(t.view(torch.int16).cpu().numpy().view(np.uint16)).astype(np.float64)
 
 
-def compare(name, o, lse, o_ref, lse_ref):
+def dev_as(bits, dtype):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
+        torch.float16 if dtype == "f16" else torch.bfloat16).cuda()
+
+
+def host_as(t, dtype):
+    if dtype == "f16":
+        return t.float().cpu().numpy().astype(np.float64)
+    return bf16_host(t)
+
+
+def compare(name, o, lse, o_ref, lse_ref, dtype="bf16"):
     assert np.isfinite(o).all(), f"{name}: non-finite output"
     err_o = float(np.abs(o - o_ref).max())
-    o_ref16 = fa_inputs.bf16_bits_to_f32(fa_inputs.f32_to_bf16_bits(o_ref.astype(np.float32))).astype(np.float64)
+    if dtype == "f16":
+        o_ref16 = o_ref.astype(np.float16).astype(np.float64)
+    else:
+        o_ref16 = fa_inputs.bf16_bits_to_f32(fa_inputs.f32_to_bf16_bits(o_ref.astype(np.float32))).astype(np.float64)
     err_o16 = float(np.abs(o - o_ref16).max())
     fin = np.isfinite(lse_ref)
     assert np.array_equal(np.isfinite(lse), fin), f"{name}: LSE finiteness differs"
     err_l = float(np.abs(lse[fin] - lse_ref[fin]).max())
     print(f"\n{name}: {o.size} O elements, {lse.size} LSE values; max|O - oracle| = {err_o:.3e}, "
-          f"max|O - bf16(oracle)| = {err_o16:.3e}, max|LSE - oracle| = {err_l:.3e}")
+          f"max|O - {dtype}(oracle)| = {err_o16:.3e}, max|LSE - oracle| = {err_l:.3e}")
     assert err_o <= TOL_O, f"{name}: max |O - oracle| = {err_o}"
     assert err_l <= TOL_LSE, f"{name}: max |LSE - oracle| = {err_l}"
 
@@ -88,3 +106,37 @@ def test_varlen_workload_every_element():
     del o, l
     o_ref, l_ref = oracle.attention_varlen(x["q"], x["k"], x["v"], cu, w.scale, True)
     compare("c5_varlen8_h16d128_causal", o_gpu, l_gpu, o_ref, l_ref)
+
+
+@pytest.mark.parametrize("name", ["g2_gqa_b4h32kv8n4096d128_causal", "d1_decode_b8h32kv8nq1nk32768d128"])
+def test_grouped_and_decoding_workloads_every_element(name):
+    """Grouped-query heads (G = 4 packed into each tile) and decoding (one query row,
+    the library's choice of key splits merged by the LSE combine)."""
+    import torch
+    w = fa_inputs.WORKLOADS[name]
+    x = fa_inputs.make_workload(w)
+    q, k, v = dev_as(x["q"], w.dtype), dev_as(x["k"], w.dtype), dev_as(x["v"], w.dtype)
+    o = torch.full(q.shape, float("nan"), dtype=q.dtype, device="cuda")
+    lse = torch.full((w.B, w.H, w.N), float("nan"), dtype=torch.float32, device="cuda")
+    fa.fa_fwd(q, k, v, scale=w.scale, causal=w.causal, out=o, lse=lse, num_splits=w.splits)
+    st, word = fa.last_device_status()
+    assert st == fa.FA_OK, hex(word)
+    o_gpu, l_gpu = host_as(o, w.dtype), lse.cpu().numpy().astype(np.float64)
+    del q, k, v, o, lse
+    o_ref, l_ref = oracle.attention(x["q"], x["k"], x["v"], w.scale, w.causal, dtype=w.dtype)
+    compare(name, o_gpu, l_gpu, o_ref, l_ref, w.dtype)
+
+
+def test_grouped_varlen_fp16_workload_every_element():
+    import torch
+    w = fa_inputs.WORKLOADS["g3_gqa_varlen8_h32kv4d128_causal_f16"]
+    x = fa_inputs.make_workload(w)
+    cu = x["cu_seqlens"]
+    o, l = fa.fa_fwd_varlen(dev_as(x["q"], w.dtype), dev_as(x["k"], w.dtype), dev_as(x["v"], w.dtype),
+                            torch.from_numpy(cu).cuda(), int(x["lengths"].max()), scale=w.scale, causal=True)
+    st, word = fa.last_device_status()
+    assert st == fa.FA_OK, hex(word)
+    o_gpu, l_gpu = host_as(o, w.dtype), l.cpu().numpy().astype(np.float64)
+    del o, l
+    o_ref, l_ref = oracle.attention_varlen(x["q"], x["k"], x["v"], cu, w.scale, True, dtype=w.dtype)
+    compare(w.name, o_gpu, l_gpu, o_ref, l_ref, w.dtype)
