@@ -218,6 +218,15 @@ def test_backward_full_size_one_head_group(name, b, kvh):
         assert np.isfinite(g).all()
 
 
+def test_backward_full_size_every_element():
+    """c3 (B4 H16 N4096 d128 causal) through the kernel in bench.py's launch
+    configuration: every element of dQ, dK and dV against the fp64 oracle."""
+    w, x, do = _full_inputs("c3_b4h16n4096d128_causal")
+    got = run_bwd(x["q"], x["k"], x["v"], do, w.causal, w.dtype, scale=w.scale)
+    ref = oracle.attention_backward(x["q"], x["k"], x["v"], do, w.scale, w.causal, dtype=w.dtype)
+    check(got, ref, f"c3 full: {got[0].size} dQ, {got[1].size} dK and {got[2].size} dV elements")
+
+
 def test_backward_full_size_varlen_one_sequence():
     import torch
     w, x, do = _full_inputs("c5_varlen8_h16d128_causal")
