@@ -388,7 +388,9 @@ __global__ void __launch_bounds__(1024) fa_varlen_schedule_kernel(const int* cu_
     return;
   }
   auto cost_of = [&](int m, int Lq, int Lk, int sp) {
-    const KRange r = key_range(m * rows, rows, Lk - Lq, Lk, gshift, causal != 0, splits, sp);
+    int row0, nrows;
+    varlen_block_rows(m, Lq << gshift, rows, causal != 0, row0, nrows);
+    const KRange r = key_range(row0, nrows, Lk - Lq, Lk, gshift, causal != 0, splits, sp);
     return min(r.hi - r.lo, kSchedBuckets - 1);
   };
   // one warp per sequence, its lanes over the sequence's row blocks

@@ -230,10 +230,31 @@ def test_varlen_elementwise(lengths, causal):
     check(o, lse, o_ref, l_ref, f"varlen {lengths}")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_short_last_blocks(causal):
+    """Sequences whose last 256-row block holds 128 rows or fewer (with causal masking the
+    row blocks then move down by 128 rows): remainders of 1, 44, 128 and 129 rows,
+    sequences of one tile, and one long sequence with a full last block."""
+    lengths = [257, 300, 640, 385, 129, 1, 128, 384, 2000]
+    (q, k, v, cu), o, lse = run_varlen(lengths, 2, 128, causal, seed=77)
+    o_ref, l_ref = oracle.attention_varlen(q, k, v, cu, 1 / math.sqrt(128), causal)
+    check(o, lse, o_ref, l_ref, f"varlen short last blocks causal={causal}")
+
+
 def test_varlen_d64():
     (q, k, v, cu), o, lse = run_varlen([200, 77, 513], 2, 64, True, seed=9)
     o_ref, l_ref = oracle.attention_varlen(q, k, v, cu, 1 / 8, True)
     check(o, lse, o_ref, l_ref, "varlen d64")
+
+
+def block_rows(m, P, causal, R=256):
+    """Packed rows (row0, rows) of varlen row block m of a sequence with P packed rows:
+    with causal masking and a last block of 128 rows or fewer, the blocks move down by
+    128 rows, so that the one short block is the first."""
+    rem = P % R
+    if causal and P > 128 and 0 < rem <= 128:
+        return (0, 128) if m == 0 else (m * R - 128, R)
+    return m * R, R
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -254,7 +275,8 @@ def test_varlen_schedule_is_complete_and_longest_first(causal):
     cost = t[:, 3]
     assert (np.diff(cost) <= 0).all()
     for s, h, m, c in t:
-        kmax = min(m * 256 + 256, lengths[s]) if causal else lengths[s]
+        row0, rows = block_rows(m, lengths[s], causal)
+        kmax = min(row0 + rows, lengths[s]) if causal else lengths[s]
         assert c == (kmax + 127) // 128
 
 
