@@ -279,7 +279,23 @@ int launch_fwd(DevInfo* dev, const fa::FwdParams& p, int grid, cudaStream_t stre
     }
     if (dev->attr_status[di][ci][ei][fi][si] != FA_OK) return dev->attr_status[di][ci][ei][fi][si];
   }
-  kern<<<grid, fa::kThreads, L::kSmemAlloc, stream>>>(p);
+  // A grid of one wave (latency-bound work) is launched with programmatic stream
+  // serialization: its prologue (barriers, tensor memory, tensor-map prefetch) runs
+  // while the previous kernel in the stream finishes, and it waits for that kernel
+  // (griddepcontrol.wait) before touching global memory. Measured, CUDA graphs of 20
+  // calls: B1 H1 N256 d64 6.95 -> 5.92 us, B2 H8 N1024 13.5 -> 13.15 us; larger grids
+  // gained nothing (B4 H16 N4096 causal 0.9 % slower), so they keep the plain launch.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(fa::kThreads);
+  cfg.dynamicSmemBytes = L::kSmemAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = grid <= dev->sm_count ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return FA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -362,6 +378,7 @@ __global__ void __launch_bounds__(1024) fa_varlen_schedule_kernel(const int* cu_
                                                                   int rows, int capacity, int4* tasks, int* count,
                                                                   int total_q, int total_k, int max_q,
                                                                   long long section_bytes, int kv_row_bytes) {
+  griddep_launch_dependents();   // an attention grid of one wave may start its prologue now
   __shared__ int hist[kSchedBuckets];
   __shared__ int total_tiles;
   __shared__ int first_bad;

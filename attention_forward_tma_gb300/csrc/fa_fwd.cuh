@@ -567,6 +567,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Launched with programmatic stream serialization, everything above may overlap
+  // the previous kernel in the stream; global memory is touched only from here on.
+  griddep_wait();
 
   // consumers: the k-th task of this CTA from the ring (warp-uniform; -1 = done)
   auto take_task = [&](Waiter& w, int k) -> int {
@@ -667,7 +670,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           mbar_arrive(bar(L::bTaskFull + slot));
         }
         __syncwarp();
-        if (idx < 0) break;
+        if (idx < 0) {
+          // no task left to claim (none of the grid's CTAs waits to launch): the next
+          // kernel in the stream may start its prologue on the SMs this grid frees
+          if (leader) griddep_launch_dependents();
+          break;
+        }
         get_task<kRows>(p, CAUSAL, idx, tk);
         const KRange kr = task_range(p, tk, CAUSAL);
         if (kr.hi <= kr.lo) continue;   // no key to attend to: nothing to load

@@ -56,6 +56,12 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on have
+// completed and their writes are visible (a no-op without such a dependency), and
+// let the dependent grid launch once every CTA of this one has signalled or exited.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // One lane of a converged warp returns true (the same lane on every call).
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred;
