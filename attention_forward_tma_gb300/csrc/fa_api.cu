@@ -135,7 +135,9 @@ int choose_splits_fixed(int requested, int B, int H, int H_kv, int num_m, int ta
   for (int m = 0; m < num_m; ++m) {
     long long kmax = N_kv;
     if (causal) {
-      const long long last = ((long long)m * task_rows + task_rows - 1) >> gshift;
+      int row0, rows;
+      fa::varlen_block_rows(m, N_q << gshift, task_rows, true, row0, rows);
+      const long long last = ((long long)row0 + rows - 1) >> gshift;
       kmax = std::min<long long>(last + (N_kv - N_q) + 1, N_kv);
     }
     nb[m] = kmax > 0 ? (int)((kmax + fa::kBlockN - 1) / fa::kBlockN) : 0;

@@ -202,13 +202,13 @@ __device__ __forceinline__ int packed_pos(const Task& t, int row, int gshift) {
   return (t.row0 + row) >> gshift;
 }
 
-// Packed rows [row0, row0 + rows) of row block m of a causal varlen sequence with P
-// packed rows, blocks of R rows. When the last block would hold kBlockM rows or fewer
+// Packed rows [row0, row0 + rows) of row block m of a causal sequence (varlen or fixed
+// length) with P packed rows, blocks of R rows. When the last block would hold kBlockM rows or fewer
 // (a task of one Q tile at the end of the sequence, where causal rows see the most
 // keys), the blocks move down by kBlockM rows: block 0 is rows [0, kBlockM), the one
 // short block, where causal rows see the fewest keys, and block m > 0 starts at
 // m R - kBlockM. The number of blocks, ceil(P / R), is the same either way.
-__device__ __forceinline__ void varlen_block_rows(int m, int P, int R, bool causal, int& row0, int& rows) {
+__host__ __device__ __forceinline__ void varlen_block_rows(int m, int P, int R, bool causal, int& row0, int& rows) {
   const int rem = P % R;
   if (causal && R == 2 * kBlockM && P > kBlockM && rem > 0 && rem <= kBlockM) {
     row0 = m == 0 ? 0 : m * R - kBlockM;
@@ -255,7 +255,8 @@ __device__ __forceinline__ bool get_task(const FwdParams& p, bool causal, int id
     m = idx - bh * p.num_m;
   }
   const int b = bh / p.Hkv;
-  t.kvh = bh - b * p.Hkv; t.row0 = m * ROWS; t.rows = ROWS; t.tok0 = b * p.N; t.len = p.N;
+  t.kvh = bh - b * p.Hkv; t.tok0 = b * p.N; t.len = p.N;
+  varlen_block_rows(m, p.N << p.gshift, ROWS, causal, t.row0, t.rows);   // the same row blocks as a sequence
   t.tok0k = b * p.Nk; t.lenk = p.Nk; t.off = p.Nk - p.N + p.diag_shift;
   t.lse_base = (b * p.H + (t.kvh << p.gshift)) * p.N;
   t.lse_hstride = p.N;

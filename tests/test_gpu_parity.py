@@ -241,6 +241,23 @@ def test_varlen_short_last_blocks(causal):
     check(o, lse, o_ref, l_ref, f"varlen short last blocks causal={causal}")
 
 
+@pytest.mark.parametrize("N,Nk,H,Hkv,splits", [(300, 300, 2, 2, 1), (1100, 1100, 4, 1, 1), (4100, 4100, 2, 2, 1),
+                                               (385, 700, 8, 2, 1), (1100, 1100, 2, 2, 3)], ids=str)
+def test_fixed_length_short_last_blocks(N, Nk, H, Hkv, splits):
+    """Causal fixed-length problems whose last 256-row block holds 128 packed rows or
+    fewer (the row blocks then move down by 128 rows), with grouped heads, N_q != N_kv
+    and key splits: every element against the oracle."""
+    import torch
+    q, k, v = fa_inputs.make_qkv(1, N, H, 128, seed=N + H, Hkv=Hkv, Nkv=Nk)
+    out = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    l = torch.full((1, H, N), float("nan"), dtype=torch.float32, device="cuda")
+    fa.fa_fwd(dev(q), dev(k), dev(v), causal=True, out=out, lse=l, num_splits=splits)
+    st, word = fa.last_device_status()
+    assert st == fa.FA_OK, hex(word)
+    o_ref, l_ref = oracle.attention(q, k, v, 1 / math.sqrt(128), True)
+    check(host(out), host(l), o_ref, l_ref, f"N={N} N_kv={Nk} H={H}/{Hkv} splits={splits}")
+
+
 def test_varlen_d64():
     (q, k, v, cu), o, lse = run_varlen([200, 77, 513], 2, 64, True, seed=9)
     o_ref, l_ref = oracle.attention_varlen(q, k, v, cu, 1 / 8, True)
