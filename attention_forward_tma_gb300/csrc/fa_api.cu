@@ -135,9 +135,7 @@ int choose_splits_fixed(int requested, int B, int H, int H_kv, int num_m, int ta
   for (int m = 0; m < num_m; ++m) {
     long long kmax = N_kv;
     if (causal) {
-      int row0, rows;
-      fa::varlen_block_rows(m, N_q << gshift, task_rows, true, row0, rows);
-      const long long last = ((long long)row0 + rows - 1) >> gshift;
+      const long long last = ((long long)m * task_rows + task_rows - 1) >> gshift;
       kmax = std::min<long long>(last + (N_kv - N_q) + 1, N_kv);
     }
     nb[m] = kmax > 0 ? (int)((kmax + fa::kBlockN - 1) / fa::kBlockN) : 0;
@@ -407,9 +405,7 @@ __global__ void __launch_bounds__(1024) fa_varlen_schedule_kernel(const int* cu_
     return;
   }
   auto cost_of = [&](int m, int Lq, int Lk, int sp) {
-    int row0, nrows;
-    varlen_block_rows(m, Lq << gshift, rows, causal != 0, row0, nrows);
-    const KRange r = key_range(row0, nrows, Lk - Lq, Lk, gshift, causal != 0, splits, sp);
+    const KRange r = key_range(m * rows, rows, Lk - Lq, Lk, gshift, causal != 0, splits, sp);
     return min(r.hi - r.lo, kSchedBuckets - 1);
   };
   // one warp per sequence, its lanes over the sequence's row blocks

@@ -202,23 +202,6 @@ __device__ __forceinline__ int packed_pos(const Task& t, int row, int gshift) {
   return (t.row0 + row) >> gshift;
 }
 
-// Packed rows [row0, row0 + rows) of row block m of a causal sequence (varlen or fixed
-// length) with P packed rows, blocks of R rows. When the last block would hold kBlockM rows or fewer
-// (a task of one Q tile at the end of the sequence, where causal rows see the most
-// keys), the blocks move down by kBlockM rows: block 0 is rows [0, kBlockM), the one
-// short block, where causal rows see the fewest keys, and block m > 0 starts at
-// m R - kBlockM. The number of blocks, ceil(P / R), is the same either way.
-__host__ __device__ __forceinline__ void varlen_block_rows(int m, int P, int R, bool causal, int& row0, int& rows) {
-  const int rem = P % R;
-  if (causal && R == 2 * kBlockM && P > kBlockM && rem > 0 && rem <= kBlockM) {
-    row0 = m == 0 ? 0 : m * R - kBlockM;
-    rows = m == 0 ? kBlockM : R;
-  } else {
-    row0 = m * R;
-    rows = R;
-  }
-}
-
 // ROWS: packed rows per task (256, or 128 in a solo kernel).
 template <int ROWS>
 __device__ __forceinline__ bool get_task(const FwdParams& p, bool causal, int idx, Task& t) {
@@ -227,9 +210,8 @@ __device__ __forceinline__ bool get_task(const FwdParams& p, bool causal, int id
     const int4 e = p.tasks[idx];
     const int s0 = p.cu_seqlens[e.x], s1 = p.cu_seqlens[e.x + 1];
     const int k0 = p.cu_seqlens_k[e.x], k1 = p.cu_seqlens_k[e.x + 1];
-    t.kvh = e.y & 0xffff; t.split = e.y >> 16;
+    t.kvh = e.y & 0xffff; t.split = e.y >> 16; t.row0 = e.z * ROWS; t.rows = ROWS;
     t.tok0 = s0; t.len = s1 - s0;
-    varlen_block_rows(e.z, t.len << p.gshift, ROWS, causal, t.row0, t.rows);
     t.tok0k = k0; t.lenk = k1 - k0; t.off = t.lenk - t.len;
     t.lse_base = (t.kvh << p.gshift) * p.total_tokens + s0;
     t.lse_hstride = p.total_tokens;
@@ -255,8 +237,7 @@ __device__ __forceinline__ bool get_task(const FwdParams& p, bool causal, int id
     m = idx - bh * p.num_m;
   }
   const int b = bh / p.Hkv;
-  t.kvh = bh - b * p.Hkv; t.tok0 = b * p.N; t.len = p.N;
-  varlen_block_rows(m, p.N << p.gshift, ROWS, causal, t.row0, t.rows);   // the same row blocks as a sequence
+  t.kvh = bh - b * p.Hkv; t.row0 = m * ROWS; t.rows = ROWS; t.tok0 = b * p.N; t.len = p.N;
   t.tok0k = b * p.Nk; t.lenk = p.Nk; t.off = p.Nk - p.N + p.diag_shift;
   t.lse_base = (b * p.H + (t.kvh << p.gshift)) * p.N;
   t.lse_hstride = p.N;

@@ -181,16 +181,6 @@ def test_gqa_varlen_elementwise(lengths, H, Hkv, causal, dtype):
     check(host(out), host(lse), o_ref, l_ref, f"varlen gqa {lengths} {dtype}")
 
 
-def block_rows(m, P, causal, R=256):
-    """Packed rows (row0, rows) of varlen row block m of a sequence with P packed rows:
-    with causal masking and a last block of 128 rows or fewer, the blocks move down by
-    128 rows, so that the one short block is the first."""
-    rem = P % R
-    if causal and P > 128 and 0 < rem <= 128:
-        return (0, 128) if m == 0 else (m * R - 128, R)
-    return m * R, R
-
-
 @pytest.mark.parametrize("group", [2, 4, 128])
 def test_gqa_varlen_schedule_covers_packed_rows(group):
     import torch
@@ -204,8 +194,7 @@ def test_gqa_varlen_schedule_covers_packed_rows(group):
     assert n == len(want) and {tuple(x[:3]) for x in t} == want
     assert (np.diff(t[:, 3]) <= 0).all()
     for s, h, m, c in t:
-        row0, rows = block_rows(m, lengths[s] * group, True)
-        last_pos = (row0 + rows - 1) // group        # the task's last packed row's position
+        last_pos = (m * 256 + 255) // group          # the task's last packed row's position
         assert c == (min(last_pos + 1, lengths[s]) + 127) // 128
 
 

@@ -232,9 +232,9 @@ def test_varlen_elementwise(lengths, causal):
 
 @pytest.mark.parametrize("causal", [False, True])
 def test_varlen_short_last_blocks(causal):
-    """Sequences whose last 256-row block holds 128 rows or fewer (with causal masking the
-    row blocks then move down by 128 rows): remainders of 1, 44, 128 and 129 rows,
-    sequences of one tile, and one long sequence with a full last block."""
+    """Sequences whose last 256-row block holds 128 rows or fewer (a task of one Q tile
+    at the sequence's end): remainders of 1, 44, 128 and 129 rows, sequences of one
+    tile, and one long sequence with a full last block."""
     lengths = [257, 300, 640, 385, 129, 1, 128, 384, 2000]
     (q, k, v, cu), o, lse = run_varlen(lengths, 2, 128, causal, seed=77)
     o_ref, l_ref = oracle.attention_varlen(q, k, v, cu, 1 / math.sqrt(128), causal)
@@ -245,8 +245,8 @@ def test_varlen_short_last_blocks(causal):
                                                (385, 700, 8, 2, 1), (1100, 1100, 2, 2, 3)], ids=str)
 def test_fixed_length_short_last_blocks(N, Nk, H, Hkv, splits):
     """Causal fixed-length problems whose last 256-row block holds 128 packed rows or
-    fewer (the row blocks then move down by 128 rows), with grouped heads, N_q != N_kv
-    and key splits: every element against the oracle."""
+    fewer (a task of one Q tile), with grouped heads, N_q != N_kv and key splits: every
+    element against the oracle."""
     import torch
     q, k, v = fa_inputs.make_qkv(1, N, H, 128, seed=N + H, Hkv=Hkv, Nkv=Nk)
     out = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
@@ -262,16 +262,6 @@ def test_varlen_d64():
     (q, k, v, cu), o, lse = run_varlen([200, 77, 513], 2, 64, True, seed=9)
     o_ref, l_ref = oracle.attention_varlen(q, k, v, cu, 1 / 8, True)
     check(o, lse, o_ref, l_ref, "varlen d64")
-
-
-def block_rows(m, P, causal, R=256):
-    """Packed rows (row0, rows) of varlen row block m of a sequence with P packed rows:
-    with causal masking and a last block of 128 rows or fewer, the blocks move down by
-    128 rows, so that the one short block is the first."""
-    rem = P % R
-    if causal and P > 128 and 0 < rem <= 128:
-        return (0, 128) if m == 0 else (m * R - 128, R)
-    return m * R, R
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -292,8 +282,7 @@ def test_varlen_schedule_is_complete_and_longest_first(causal):
     cost = t[:, 3]
     assert (np.diff(cost) <= 0).all()
     for s, h, m, c in t:
-        row0, rows = block_rows(m, lengths[s], causal)
-        kmax = min(row0 + rows, lengths[s]) if causal else lengths[s]
+        kmax = min(m * 256 + 256, lengths[s]) if causal else lengths[s]
         assert c == (kmax + 127) // 128
 
 

@@ -183,16 +183,6 @@ def test_varlen_kv_elementwise(lq, lk, causal, splits):
     check(host(out), host(lse), o_ref, l_ref, f"varlen kv {lq} {lk}")
 
 
-def block_rows(m, P, causal, R=256):
-    """Packed rows (row0, rows) of varlen row block m of a sequence with P packed rows:
-    with causal masking and a last block of 128 rows or fewer, the blocks move down by
-    128 rows, so that the one short block is the first."""
-    rem = P % R
-    if causal and P > 128 and 0 < rem <= 128:
-        return (0, 128) if m == 0 else (m * R - 128, R)
-    return m * R, R
-
-
 @pytest.mark.parametrize("splits", [1, 4])
 def test_varlen_schedule_with_key_ranges(splits):
     import torch
@@ -208,8 +198,7 @@ def test_varlen_schedule_with_key_ranges(splits):
     for s, hs, m, c in t:
         sp = hs >> 16
         off = lk[s] - lq[s]
-        row0, rows = block_rows(m, lq[s] * 4, True)
-        kmax = min((row0 + rows - 1) // 4 + off + 1, lk[s])
+        kmax = min((m * 256 + 255) // 4 + off + 1, lk[s])
         nb = (kmax + 127) // 128 if kmax > 0 else 0
         per = -(-((lk[s] + 127) // 128) // splits)
         lo, hi = (0, nb) if splits == 1 else (sp * per, max(sp * per, min(sp * per + per, nb)))
