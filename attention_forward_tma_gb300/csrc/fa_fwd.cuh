@@ -32,8 +32,10 @@
 //   P_t = 16-bit (bf16 / fp16) pairs over columns [64,128) of S_t.
 //
 // Shared memory: Q tiles (2), a ring of K/V stages (K and V blocks alternate
-// through the same ring), mbarriers, and a 2x128 float mailbox that carries
-// acc_scale (and finally row_sum) from the softmax warpgroups to WG2.
+// through the same ring), the O staging tile of the TMA store, mbarriers, and a
+// 2x128 float mailbox that carries each row's final row_sum from the softmax
+// warpgroups to WG2 (acc_scale goes through column 0 of S_t, or through the
+// mailbox when the statistics option selects shared memory).
 //
 // Every wait is bounded: after FwdParams::timeout_ns a waiter records
 // FA_ERR_TIMEOUT in g_fa_status, raises a CTA-wide abort flag and unwinds;
