@@ -295,7 +295,9 @@ int launch_fwd(DevInfo* dev, const fa::FwdParams& p, int grid, cudaStream_t stre
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = grid <= dev->sm_count ? 1 : 0;
-  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return FA_ERR_CUDA;
+  fa::FwdParams q = p;
+  q.pdl = cfg.numAttrs;
+  if (cudaLaunchKernelEx(&cfg, kern, q) != cudaSuccess) return FA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
